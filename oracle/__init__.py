@@ -1,0 +1,204 @@
+"""CPU oracle for the 4-bit block formats -- TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline
+leg may import this package.  It shares no code with the CUDA library in
+``bit_block_quantized_gb300``: the scalar decoders and the f64 GEMV live in
+``q4_oracle.c`` (plain C, built with ``-ffp-contract=off``), the bit packers and
+the repack-through-the-logical-matrix route in ``packing.py`` (numpy).
+
+Citations name the source page and its section:
+  [FBTC] "Four Bits, Three Contracts"; [W4K] "Why 4-Bit Quantization Is King";
+  [BPA] "Bit Packing Architecture, in depth"; [MUS7] "Muser book, Chapter 7".
+Every function is pinned by ``tests/test_oracle_pins.py``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+from . import packing  # noqa: F401  (re-exported)
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "q4_oracle.c")
+_LIB = os.path.join(_HERE, "_build", "liborc.so")
+_lock = threading.Lock()
+_lib = None
+
+FMT = {"nvfp4": 1, "mxfp4": 2, "q4k": 3, "q40": 4, "gptq": 5, "awq": 6,
+       "nvfp4_splithalf": 7, "logical": 8}
+
+
+def build(force: bool = False) -> str:
+    """Compile q4_oracle.c with the host C compiler (no CUDA involved)."""
+    os.makedirs(os.path.dirname(_LIB), exist_ok=True)
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        subprocess.check_call(["gcc", "-O2", "-std=c11", "-fPIC", "-shared",
+                               "-ffp-contract=off", "-fno-fast-math",
+                               "-o", tmp, _SRC, "-lm"])
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+class _Tensor(ctypes.Structure):
+    _fields_ = [("fmt", ctypes.c_int32), ("group", ctypes.c_int32),
+                ("N", ctypes.c_int64), ("K", ctypes.c_int64),
+                ("w", ctypes.c_void_p), ("scales", ctypes.c_void_p),
+                ("zeros", ctypes.c_void_p), ("g_idx", ctypes.c_void_p),
+                ("scale2", ctypes.c_float)]
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            lib.orc_e2m1.restype = ctypes.c_float
+            lib.orc_e2m1.argtypes = [ctypes.c_uint]
+            lib.orc_e4m3fn.restype = ctypes.c_int
+            lib.orc_e4m3fn.argtypes = [ctypes.c_uint, ctypes.POINTER(ctypes.c_float)]
+            lib.orc_e8m0.restype = ctypes.c_int
+            lib.orc_e8m0.argtypes = [ctypes.c_uint, ctypes.POINTER(ctypes.c_float)]
+            lib.orc_half.restype = ctypes.c_float
+            lib.orc_half.argtypes = [ctypes.c_uint16]
+            lib.orc_bf16.restype = ctypes.c_float
+            lib.orc_bf16.argtypes = [ctypes.c_uint16]
+            lib.orc_round_bf16.restype = ctypes.c_uint16
+            lib.orc_round_bf16.argtypes = [ctypes.c_float]
+            lib.orc_dequant_rows.restype = ctypes.c_int
+            lib.orc_dequant_rows.argtypes = [ctypes.POINTER(_Tensor), ctypes.c_int64,
+                                             ctypes.c_int64, ctypes.c_void_p]
+            lib.orc_gemv_rows.restype = ctypes.c_int
+            lib.orc_gemv_rows.argtypes = [ctypes.POINTER(_Tensor), ctypes.c_void_p, ctypes.c_int64,
+                                          ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p,
+                                          ctypes.c_void_p]
+            lib.orc_round_bf16_array.restype = None
+            lib.orc_round_bf16_array.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64]
+            lib.orc_count_nan_scales.restype = ctypes.c_int64
+            lib.orc_count_nan_scales.argtypes = [ctypes.c_int, ctypes.c_void_p, ctypes.c_int64]
+            _lib = lib
+    return _lib
+
+
+class OracleError(ValueError):
+    pass
+
+
+# ------------------------------------------------------------------ scalars
+
+def e2m1(code: int) -> float:
+    return float(_load().orc_e2m1(code))
+
+
+def e4m3fn(byte: int) -> float:
+    v = ctypes.c_float()
+    if _load().orc_e4m3fn(byte, ctypes.byref(v)):
+        raise OracleError(f"E4M3FN byte 0x{byte:02x} is a NaN encoding")
+    return float(v.value)
+
+
+def e8m0(byte: int) -> float:
+    v = ctypes.c_float()
+    if _load().orc_e8m0(byte, ctypes.byref(v)):
+        raise OracleError(f"E8M0 byte 0x{byte:02x} is a NaN encoding")
+    return float(v.value)
+
+
+def half(bits: int) -> float:
+    return float(_load().orc_half(bits))
+
+
+def bf16(bits: int) -> float:
+    return float(_load().orc_bf16(bits))
+
+
+def round_bf16(x: np.ndarray) -> np.ndarray:
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    out = np.empty(x.shape, dtype=np.uint16)
+    _load().orc_round_bf16_array(x.ctypes.data, out.ctypes.data, x.size)
+    return out
+
+
+def bf16_bits_to_f32(bits: np.ndarray) -> np.ndarray:
+    """Widen bfloat16 bit patterns to f32 exactly (bf16 is the top half of f32)."""
+    return (np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32)
+
+
+# ------------------------------------------------------------------ tensors
+
+class Tensor:
+    """A packed weight tensor as host numpy arrays, in one of the formats.
+
+    ``w``: payload bytes (any integer dtype, read as little-endian bytes);
+    ``scales``: scale tensor bytes; ``zeros``: qzeros / logical zeros;
+    ``g_idx``: optional int32 [K]; ``scale2``: NVFP4 tensor scale.
+    """
+
+    def __init__(self, fmt, N, K, w, scales=None, zeros=None, g_idx=None, group=128,
+                 scale2=1.0):
+        self.fmt = FMT[fmt] if isinstance(fmt, str) else int(fmt)
+        self.N, self.K, self.group, self.scale2 = int(N), int(K), int(group), float(scale2)
+        self.w = np.ascontiguousarray(w)
+        self.scales = None if scales is None else np.ascontiguousarray(scales)
+        self.zeros = None if zeros is None else np.ascontiguousarray(zeros)
+        self.g_idx = None if g_idx is None else np.ascontiguousarray(g_idx, dtype=np.int32)
+
+    def _c(self) -> _Tensor:
+        p = lambda a: None if a is None else a.ctypes.data  # noqa: E731
+        return _Tensor(self.fmt, self.group, self.N, self.K, p(self.w), p(self.scales),
+                       p(self.zeros), p(self.g_idx), self.scale2)
+
+
+def dequant(t: Tensor, rows=None) -> np.ndarray:
+    """f32 [len(rows)][K] (all rows if ``rows`` is None) by the pinned rule."""
+    lib = _load()
+    ct = _Tensor.from_buffer_copy(t._c())
+    if rows is None:
+        out = np.empty((t.N, t.K), dtype=np.float32)
+        rc = lib.orc_dequant_rows(ctypes.byref(ct), 0, t.N, out.ctypes.data)
+    else:
+        rows = list(rows)
+        out = np.empty((len(rows), t.K), dtype=np.float32)
+        rc = 0
+        for i, n in enumerate(rows):
+            rc = rc or lib.orc_dequant_rows(ctypes.byref(ct), int(n), 1, out[i].ctypes.data)
+    if rc == 1:
+        raise OracleError("a scale byte is a NaN encoding")
+    if rc:
+        raise OracleError(f"unknown format {t.fmt}")
+    return out
+
+
+def gemv(t: Tensor, x: np.ndarray, rows=None):
+    """(y, bound): y[m][i] = sum_k w_hat[rows[i]][k] x[m][k] in f64, and
+    bound[m][i] = sum_k |w_hat||x|.  ``x`` is f32 [M][K] (or [K])."""
+    x = np.ascontiguousarray(np.atleast_2d(x), dtype=np.float32)
+    M = x.shape[0]
+    assert x.shape[1] == t.K
+    rows = np.arange(t.N, dtype=np.int64) if rows is None else np.asarray(rows, dtype=np.int64)
+    rows = np.ascontiguousarray(rows)
+    y = np.empty((M, rows.size), dtype=np.float64)
+    bound = np.empty((M, rows.size), dtype=np.float64)
+    ct = _Tensor.from_buffer_copy(t._c())
+    rc = _load().orc_gemv_rows(ctypes.byref(ct), x.ctypes.data, M, rows.ctypes.data, rows.size,
+                               y.ctypes.data, bound.ctypes.data)
+    if rc == 1:
+        raise OracleError("a scale byte is a NaN encoding")
+    if rc:
+        raise OracleError(f"unknown format {t.fmt}")
+    return y, bound
+
+
+def count_nan_scales(fmt, scales: np.ndarray) -> int:
+    s = np.ascontiguousarray(scales, dtype=np.uint8)
+    f = FMT[fmt] if isinstance(fmt, str) else int(fmt)
+    return int(_load().orc_count_nan_scales(f, s.ctypes.data, s.size))
+
+
+def gemv_tolerance(bound: np.ndarray) -> np.ndarray:
+    """The GEMV acceptance bound: |y_gpu - y_ref| <= 1e-5 * sum|w_hat||x| + 1e-6."""
+    return 1e-5 * bound + 1e-6
