@@ -1,0 +1,439 @@
+"""Batch-1 NVFP4 decode-GEMV bench: weight-stream GB/s on the 4096x14336 MLP set.
+
+One step = the three projections of one decoder MLP in NVFP4 at batch 1
+(gate 14336x4096, up 14336x4096, down 4096x14336), each a fused decode-GEMV
+through the C ABI (q4_gemv).  The weights come from the seeded synthetic
+recipe (W ~ N(0,0.02) with U(0.5,2) row scales, NVFP4 per 16, bf16 x).
+
+L2 policy: inputs larger than L2 -- the step rotates through distinct copies
+of the weight set totalling >= max(1 GiB, 4 x L2), so no step finds its
+weights in the 129 MB L2.  The timed loop is one CUDA graph per rotation.
+
+Output: one JSON line (rank 0).  ``--impl reference`` times the CPU oracle on
+a bounded sample of the same workload instead.  Under torchrun (N > 1) every
+rank runs its own replica (the path has no exchange step: replicas only).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "weight-stream GB/s and % of GB300 HBM peak for batch-1 4-bit dequant-GEMV"
+WORKLOAD = "nvfp4_gemv_m1_mlp_4096x14336_set"
+SET = [("gate", 14336, 4096), ("up", 14336, 4096), ("down", 4096, 14336)]
+CONFIG_ID = 5          # seed block of this workload's synthetic draws
+NOMINAL_HBM_GBS = 7900.0
+FALLBACK_HBM_GBS = 6800.0
+DOMINANT = "gemv_rows_m1<NVFP4, bf16, R=4, TMAX=128> (gate/up, 14336x4096)"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100000)
+    ap.add_argument("--warmup", type=int, default=200)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--e2e-steps", type=int, default=2000)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0,
+                    help="target CPU time of the oracle baseline sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def measured_hbm_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def source_sha():
+    h = hashlib.sha256()
+    for rel in ("bit_block_quantized_gb300/csrc/gemv.cu", "bit_block_quantized_gb300/csrc/q4_internal.cuh"):
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic():
+    """DRAM bytes per launch of the dominant kernel from the committed ncu
+    summary, only if it was taken on the current kernel source."""
+    p = os.path.join(ROOT, "profiles", "gemv_rows_m1_nvfp4_14336x4096.md")
+    try:
+        text = open(p).read()
+    except OSError:
+        return None
+    m = re.search(r"traffic_bytes_per_launch:\s*(\d+)\s+source_sha:\s*([0-9a-f]+)", text)
+    if not m or m.group(2) != source_sha():
+        return None
+    return int(m.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons, sampled every 200 ms in the background."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.dev = device_index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"q4_clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((float(parts[1]), float(parts[2]), parts[5:9]))
+            except ValueError:
+                continue
+        try:
+            os.remove(self.path)
+        except OSError:
+            pass
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for _, _, r in rows for i, v in enumerate(r) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ---------------------------------------------------------------- our arm
+
+def build_workload(torch, q4, synth):
+    """Host NVFP4 tensors of the set + device copies rotating past L2."""
+    host = []
+    for i, (name, N, K) in enumerate(SET):
+        layer = synth.make_layer("nvfp4", N, K, config=CONFIG_ID, matrix=i, row_scale=True)
+        xbits, _ = synth.draw_x(1, K, config=CONFIG_ID, matrix=i)
+        host.append((name, N, K, layer, xbits))
+    set_bytes = sum(q4.q4_packed_bytes("nvfp4", N, K) for _, N, K in SET)
+    l2 = torch.cuda.get_device_properties(0).L2_cache_size
+    copies = int(np.ceil(max(1 << 30, 4 * l2) / set_bytes))
+    dev = []
+    for c in range(copies):
+        mats = []
+        for name, N, K, layer, xbits in host:
+            w = torch.from_numpy(layer["w"]).cuda()
+            s = torch.from_numpy(layer["scales"]).cuda()
+            mats.append((name, N, K, w, s, layer["scale2"]))
+        dev.append(mats)
+    xs = [torch.from_numpy(h[4].view(np.int16)).cuda().view(torch.bfloat16) for h in host]
+    ys = [torch.empty((1, N), dtype=torch.float32, device="cuda") for _, N, _ in SET]
+    return host, dev, xs, ys, set_bytes, copies, l2
+
+
+def run_ours(args, rank, world):
+    import torch
+
+    import bit_block_quantized_gb300 as q4
+    import synth
+    from bit_block_quantized_gb300 import build as q4build
+
+    q4build.build()
+    torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+    host, dev, xs, ys, set_bytes, copies, l2 = build_workload(torch, q4, synth)
+    auxes = [q4.make_aux(scale2=h[3]["scale2"], fmt="nvfp4") for h in host]
+    stream = torch.cuda.Stream()
+
+    def step(c, s):
+        for j, (name, N, K, w, sc, _) in enumerate(dev[c]):
+            q4.q4_gemv("nvfp4", w, sc, auxes[j], xs[j], ys[j], 1, N, K, stream=s)
+
+    # one graph per full rotation, plus single-step graphs for the remainder
+    with torch.cuda.stream(stream):
+        for c in range(copies):
+            step(c, stream)
+        torch.cuda.synchronize()
+        g_rot = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_rot, stream=stream):
+            for c in range(copies):
+                step(c, stream)
+        g_one = []
+        for c in range(copies):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                step(c, stream)
+            g_one.append(g)
+        # per-kernel graphs for the roofline of each projection
+        g_kern = []
+        for j in range(len(SET)):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for c in range(copies):
+                    name, N, K, w, sc, _ = dev[c][j]
+                    q4.q4_gemv("nvfp4", w, sc, auxes[j], xs[j], ys[j], 1, N, K, stream=stream)
+            g_kern.append(g)
+
+    def run_steps(n):
+        full, rem = divmod(n, copies)
+        for _ in range(full):
+            g_rot.replay()
+        for c in range(rem):
+            g_one[c].replay()
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+
+    with torch.cuda.stream(stream):
+        run_steps(args.warmup)
+        torch.cuda.synchronize()
+        barrier()
+        torch.cuda.synchronize()
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with ClockSampler(torch.cuda.current_device()) as clk:
+            start.record(stream)
+            run_steps(args.steps)
+            end.record(stream)
+            torch.cuda.synchronize()
+        barrier()
+        ms = start.elapsed_time(end)
+        # per-kernel average launch duration (same stream, inputs > L2)
+        kern_ms = []
+        reps = max(3, 2000 // copies)
+        for j in range(len(SET)):
+            g_kern[j].replay()
+            torch.cuda.synchronize()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for _ in range(reps):
+                g_kern[j].replay()
+            b.record(stream)
+            torch.cuda.synchronize()
+            kern_ms.append(a.elapsed_time(b) / (reps * copies))
+
+    if world > 1:
+        t = torch.tensor([ms], dtype=torch.float64, device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+
+    # end to end through the public API: pinned host x in, y out, every step
+    e2e = run_e2e(args, torch, q4, dev, auxes, host, stream)
+
+    if rank != 0:
+        return None
+    peak, peak_kind = measured_hbm_peak()
+    value = world * set_bytes * args.steps / (ms * 1e-3) / 1e9
+    gate_bytes = q4.q4_packed_bytes("nvfp4", 14336, 4096)
+    achieved = gate_bytes / (kern_ms[0] * 1e-3) / 1e9
+    per_kernel = {name: {"us_per_launch": round(kern_ms[j] * 1e3, 3),
+                         "GBps": round(q4.q4_packed_bytes("nvfp4", N, K) / (kern_ms[j] * 1e-3) / 1e9, 1)}
+                  for j, (name, N, K) in enumerate(SET)}
+    x_bytes = sum(K * 2 for _, _, K in SET)
+    y_bytes = sum(N * 4 for _, N, _ in SET)
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded W ~ N(0,0.02) x U(0.5,2) rows, NVFP4 per 16; x ~ N(0,1) bf16)",
+        "config": {"workload": WORKLOAD, "batch": 1,
+                   "matrices": [f"{n} {N}x{K}" for n, N, K in SET],
+                   "weight_bytes_per_step": set_bytes, "x_bytes_per_step": x_bytes,
+                   "y_bytes_per_step": y_bytes,
+                   "l2": f"inputs larger than L2: {copies} rotating copies of the set = "
+                         f"{copies * set_bytes / 1e9:.2f} GB (L2 {l2 / 1e6:.0f} MB)",
+                   "launch": "one CUDA graph per rotation; 3 q4_gemv launches per step",
+                   "parallelism": f"replicas x{world}"},
+        "pct_of_hbm_peak": {"measured": round(value / world / peak, 4),
+                            "nominal_7900": round(value / world / NOMINAL_HBM_GBS, 4)},
+        "per_kernel": per_kernel,
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
+                     "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
+                     else "fallback 6.8 TB/s",
+                     "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": profiled_traffic(),
+                     "kernel": DOMINANT, "algorithmic_bytes_per_launch": gate_bytes},
+        "e2e": e2e,
+        "gpu_launches": 3 * args.steps,
+        "clocks": clk.summary(),
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(args.cpu_seconds, host)
+    return line
+
+
+def run_e2e(args, torch, q4, dev, auxes, host, stream):
+    """Same metric through q4_gemv with host buffers: every step copies its x
+    from pinned host memory, runs the three projections, and reads y back."""
+    xs_h = [torch.from_numpy(h[4].view(np.int16)).view(torch.bfloat16).pin_memory() for h in host]
+    ys_h = [torch.empty((1, N), dtype=torch.float32).pin_memory() for _, N, _ in SET]
+    xs_d = [torch.empty_like(x, device="cuda") for x in xs_h]
+    ys_d = [torch.empty((1, N), dtype=torch.float32, device="cuda") for _, N, _ in SET]
+    copies = len(dev)
+    n = args.e2e_steps
+
+    def one(c):
+        for j, (name, N, K, w, sc, _) in enumerate(dev[c]):
+            xs_d[j].copy_(xs_h[j], non_blocking=True)
+            q4.q4_gemv("nvfp4", w, sc, auxes[j], xs_d[j], ys_d[j], 1, N, K, stream=stream)
+            ys_h[j].copy_(ys_d[j], non_blocking=True)
+        stream.synchronize()
+
+    with torch.cuda.stream(stream):
+        for c in range(min(copies, 20)):
+            one(c % copies)
+        t0 = time.perf_counter()
+        for i in range(n):
+            one(i % copies)
+        dt = time.perf_counter() - t0
+    set_bytes = sum(q4.q4_packed_bytes("nvfp4", N, K) for _, N, K in SET)
+    return {"value": round(set_bytes * n / dt / 1e9, 1), "unit": "GB/s",
+            "h2d_bytes_per_step": sum(K * 2 for _, _, K in SET),
+            "d2h_bytes_per_step": sum(N * 4 for _, N, _ in SET),
+            "steps": n, "ms_per_step": dt * 1e3 / n,
+            "note": "per step: pinned x H2D, 3 q4_gemv, y D2H, host sync (no graph)"}
+
+
+# --------------------------------------------------------- oracle on host
+
+def cpu_baseline(seconds, host=None, sample_rows=None):
+    """The CPU oracle as it stands (single thread, f64 accumulation), timed on
+    a bounded row sample of the same three matrices."""
+    import oracle
+    import synth
+    oracle.build()
+    if host is None:
+        host = []
+        for i, (name, N, K) in enumerate(SET):
+            layer = synth.make_layer("nvfp4", N, K, config=CONFIG_ID, matrix=i, row_scale=True)
+            xbits, _ = synth.draw_x(1, K, config=CONFIG_ID, matrix=i)
+            host.append((name, N, K, layer, xbits))
+    # calibrate: rows per second on a small probe, then size the sample
+    name, N, K, layer, xbits = host[0]
+    T = oracle.Tensor("nvfp4", N, K, layer["w"], layer["scales"], scale2=layer["scale2"])
+    xf = oracle.bf16_bits_to_f32(xbits)
+    t0 = time.perf_counter()
+    oracle.gemv(T, xf, rows=np.arange(64))
+    per_row_4096 = (time.perf_counter() - t0) / 64
+    if sample_rows is None:
+        frac = min(1.0, seconds / (per_row_4096 * (14336 + 14336 + 4096 * 3.5)))
+    else:
+        frac = sample_rows
+    bytes_done, t_total, rows_done = 0, 0.0, 0
+    for name, N, K, layer, xbits in host:
+        rows = np.arange(max(1, int(N * frac)))
+        T = oracle.Tensor("nvfp4", N, K, layer["w"], layer["scales"], scale2=layer["scale2"])
+        xf = oracle.bf16_bits_to_f32(xbits)
+        t0 = time.perf_counter()
+        oracle.gemv(T, xf, rows=rows)
+        t_total += time.perf_counter() - t0
+        bytes_done += rows.size * (K // 2 + K // 16)
+        rows_done += rows.size
+    return {"value": round(bytes_done / t_total / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"{rows_done} rows ({frac:.3%}) of each of the 3 set matrices, batch 1, "
+                      f"{t_total:.1f} s", "cpu": _cpu_name()}
+
+
+def _cpu_name():
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith(("model name", "cpu part")):
+                return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return os.uname().machine
+
+
+def run_reference(args, rank, world):
+    """The reference arm: the CPU oracle on the host cores, each step a bounded
+    sample of the same workload (rank 0 only)."""
+    if rank != 0:
+        return None
+    import synth
+    import oracle
+    oracle.build()
+    host = []
+    for i, (name, N, K) in enumerate(SET):
+        layer = synth.make_layer("nvfp4", N, K, config=CONFIG_ID, matrix=i, row_scale=True)
+        xbits, _ = synth.draw_x(1, K, config=CONFIG_ID, matrix=i)
+        host.append((name, N, K, layer, xbits))
+    # size each step's sample so that the whole run stays near a minute
+    rows_per_matrix = int(max(1, min(64, 60.0 / (max(args.steps, 1) * 0.65e-3))))
+    tensors = [(oracle.Tensor("nvfp4", N, K, l["w"], l["scales"], scale2=l["scale2"]),
+                oracle.bf16_bits_to_f32(xb), K) for _, N, K, l, xb in host]
+
+    def step():
+        b = 0
+        for T, xf, K in tensors:
+            oracle.gemv(T, xf, rows=np.arange(rows_per_matrix))
+            b += rows_per_matrix * (K // 2 + K // 16)
+        return b
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    total = sum(step() for _ in range(args.steps))
+    dt = time.perf_counter() - t0
+    value = total / dt / 1e9
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": dt * 1e3 / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "batch": 1,
+                       "sample_per_step": f"{rows_per_matrix} rows of each of the 3 set matrices"},
+            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": f"{rows_per_matrix} rows per matrix per step", "cpu": _cpu_name()},
+            "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main():
+    args = parse()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        args.warmup = min(args.warmup, 3)
+        line = run_reference(args, rank, world)
+    else:
+        if world > 1:
+            import torch
+            torch.distributed.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+        line = run_ours(args, rank, world)
+        if world > 1:
+            import torch
+            torch.distributed.destroy_process_group()
+    if line is not None:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,221 @@
+// dequant.cu -- q4_dequant kernels: packed tensor -> f32 or bf16 [N][K] by the
+// pinned per-format rule.  Write-bound (4 or 2 bytes out per weight), so each
+// kernel is organised for coalesced stores; the packed reads are small.
+#include "q4_internal.cuh"
+
+namespace q4 {
+namespace {
+
+template <typename OT> __device__ __forceinline__ void store16(OT *out, const float *v);
+
+template <> __device__ __forceinline__ void store16<float>(float *out, const float *v) {
+    float4 *o = reinterpret_cast<float4 *>(out);
+#pragma unroll
+    for (int i = 0; i < 4; i++) o[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+}
+
+template <>
+__device__ __forceinline__ void store16<__nv_bfloat16>(__nv_bfloat16 *out, const float *v) {
+    uint4 *o = reinterpret_cast<uint4 *>(out);
+    uint32_t p[8];
+#pragma unroll
+    for (int i = 0; i < 8; i++) {
+        __nv_bfloat162 b = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+        p[i] = *reinterpret_cast<uint32_t *>(&b);
+    }
+    o[0] = make_uint4(p[0], p[1], p[2], p[3]);
+    o[1] = make_uint4(p[4], p[5], p[6], p[7]);
+}
+
+template <typename OT> __device__ __forceinline__ OT to_out(float v);
+template <> __device__ __forceinline__ float to_out<float>(float v) { return v; }
+template <> __device__ __forceinline__ __nv_bfloat16 to_out<__nv_bfloat16>(float v) {
+    return __float2bfloat16_rn(v);
+}
+
+// NVFP4 / split-half NVFP4 / MXFP4: one thread per 16-value group (8 payload
+// bytes).  NVFP4 order (e2m1 * e4m3fn) * scale2 ([MUS7] 7.2): the first
+// product is exact, the second is the single rounding.
+template <int FMT, typename OT>
+__global__ void dequant_fp4(const uint8_t *__restrict__ w, const uint8_t *__restrict__ scales,
+                            float scale2, OT *__restrict__ out, int64_t ngroups) {
+    for (int64_t g = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; g < ngroups;
+         g += (int64_t)gridDim.x * blockDim.x) {
+        uint2 p = *reinterpret_cast<const uint2 *>(w + 8 * g);
+        float s = (FMT == Q4_MXFP4) ? e8m0_f32(scales[g >> 1]) : e4m3_f32(scales[g]);
+        uint32_t words[2] = {p.x, p.y};
+        float v[16];
+#pragma unroll
+        for (int b = 0; b < 8; b++) {
+            float2 c = e2m1x2_f32(words[b >> 2] >> (8 * (b & 3)));
+            if (FMT == Q4_NVFP4_SPLITHALF) {
+                v[b] = c.x;          // low nibble of byte b = lane b
+                v[b + 8] = c.y;      // high nibble = lane b + 8 ([W4K] section 5)
+            } else {
+                v[2 * b] = c.x;      // low nibble = even k
+                v[2 * b + 1] = c.y;
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < 16; i++) {
+            if (FMT == Q4_MXFP4) {
+                v[i] = __fmul_rn(v[i], s);
+            } else {
+                float prod = __fmul_rn(v[i], s);
+                v[i] = __fmul_rn(prod, scale2);
+            }
+        }
+        store16<OT>(out + 16 * g, v);
+    }
+}
+
+// Q4_K: one thread per (super-block, 64-chunk c, half h): 16 code bytes -> 32
+// weights at k = 64c+16h+i (low nibbles, sub-block 2c) and 64c+32+16h+i (high
+// nibbles, sub-block 2c+1) ([FBTC] sections 5-6).  w = fma(q, d*s, -dmin*m)
+// equals the pinned (d*s)*q - dmin*m: d*s*q is exact, one rounding.
+__device__ __forceinline__ uint32_t byte_of(uint4 hdr, int i) {
+    uint32_t word = i < 4 ? hdr.y : (i < 8 ? hdr.z : hdr.w);
+    return (word >> (8 * (i & 3))) & 0xffu;
+}
+
+__device__ __forceinline__ void q4k_scale_min(uint4 hdr, int j, float &sc, float &mn) {
+    uint32_t s, m;
+    if (j < 4) {
+        s = byte_of(hdr, j) & 63u;
+        m = byte_of(hdr, j + 4) & 63u;
+    } else {
+        s = (byte_of(hdr, j + 4) & 15u) | ((byte_of(hdr, j - 4) >> 6) << 4);
+        m = (byte_of(hdr, j + 4) >> 4) | ((byte_of(hdr, j) >> 6) << 4);
+    }
+    sc = (float)s;
+    mn = (float)m;
+}
+
+template <typename OT>
+__global__ void dequant_q4k(const uint8_t *__restrict__ w, OT *__restrict__ out, int64_t nunits) {
+    for (int64_t u = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; u < nunits;
+         u += (int64_t)gridDim.x * blockDim.x) {
+        int64_t blk = u >> 3;
+        int c = (int)((u >> 1) & 3), h = (int)(u & 1);
+        const uint8_t *b = w + blk * 144;
+        uint4 hdr = *reinterpret_cast<const uint4 *>(b);
+        uint4 qs = *reinterpret_cast<const uint4 *>(b + 16 + 32 * c + 16 * h);
+        float d = half_bits_f32(hdr.x), dmin = half_bits_f32(hdr.x >> 16);
+        float sc_lo, m_lo, sc_hi, m_hi;
+        q4k_scale_min(hdr, 2 * c, sc_lo, m_lo);
+        q4k_scale_min(hdr, 2 * c + 1, sc_hi, m_hi);
+        float step_lo = __fmul_rn(d, sc_lo), off_lo = __fmul_rn(dmin, m_lo);
+        float step_hi = __fmul_rn(d, sc_hi), off_hi = __fmul_rn(dmin, m_hi);
+        uint32_t words[4] = {qs.x, qs.y, qs.z, qs.w};
+        float lo[16], hi[16];
+#pragma unroll
+        for (int i = 0; i < 16; i++) {
+            uint32_t byte = (words[i >> 2] >> (8 * (i & 3))) & 0xffu;
+            lo[i] = __fmaf_rn((float)(byte & 15u), step_lo, -off_lo);
+            hi[i] = __fmaf_rn((float)(byte >> 4), step_hi, -off_hi);
+        }
+        OT *o = out + blk * 256 + 64 * c + 16 * h;
+        store16<OT>(o, lo);
+        store16<OT>(o + 32, hi);
+    }
+}
+
+// Q4_0: one thread per 18-byte block: fp16 d, byte j = element j (low) and
+// j+16 (high); w = d*(q-8), exact ([BPA] "Real layouts compared").
+template <typename OT>
+__global__ void dequant_q40(const uint8_t *__restrict__ w, OT *__restrict__ out, int64_t nblocks) {
+    for (int64_t bi = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; bi < nblocks;
+         bi += (int64_t)gridDim.x * blockDim.x) {
+        const uint16_t *b = reinterpret_cast<const uint16_t *>(w + bi * 18);
+        float d = half_bits_f32(b[0]);
+        float lo[16], hi[16];
+#pragma unroll
+        for (int j = 0; j < 8; j++) {
+            uint32_t two = b[1 + j];
+#pragma unroll
+            for (int e = 0; e < 2; e++) {
+                uint32_t byte = (two >> (8 * e)) & 0xffu;
+                lo[2 * j + e] = __fmul_rn(d, (float)((int)(byte & 15u) - 8));
+                hi[2 * j + e] = __fmul_rn(d, (float)((int)(byte >> 4) - 8));
+            }
+        }
+        store16<OT>(out + bi * 32, lo);
+        store16<OT>(out + bi * 32 + 16, hi);
+    }
+}
+
+// 64x64 tile, transposed through shared memory: reads run along n (the packed
+// axis), writes along k (the output row).
+template <int FMT, typename OT>
+__global__ void dequant_kmajor(Tensor t, OT *__restrict__ out) {
+    __shared__ float tile[64][65];
+    int64_t n0 = (int64_t)blockIdx.x * 64, k0 = (int64_t)blockIdx.y * 64;
+    int tx = threadIdx.x & 63, ty = threadIdx.x >> 6;  // 256 threads: 64 x 4
+    for (int kk = ty; kk < 64; kk += 4) {
+        int64_t n = n0 + tx, k = k0 + kk;
+        tile[kk][tx] = (n < t.N && k < t.K) ? elem_weight<FMT>(t, n, k) : 0.0f;
+    }
+    __syncthreads();
+    for (int nn = ty; nn < 64; nn += 4) {
+        int64_t n = n0 + nn, k = k0 + tx;
+        if (n < t.N && k < t.K) out[n * t.K + k] = to_out<OT>(tile[tx][nn]);
+    }
+}
+
+int grid_for(int64_t units, int threads) {
+    int64_t blocks = (units + threads - 1) / threads;
+    int64_t cap = (int64_t)sm_count() * 16;
+    return (int)(blocks < cap ? (blocks < 1 ? 1 : blocks) : cap);
+}
+
+template <typename OT> cudaError_t dispatch(const Tensor &t, OT *out, cudaStream_t s) {
+    const int T = 256;
+    switch (t.fmt) {
+    case Q4_NVFP4: {
+        int64_t n = t.N * t.K / 16;
+        dequant_fp4<Q4_NVFP4, OT><<<grid_for(n, T), T, 0, s>>>(t.w, t.scales, t.scale2, out, n);
+        break;
+    }
+    case Q4_NVFP4_SPLITHALF: {
+        int64_t n = t.N * t.K / 16;
+        dequant_fp4<Q4_NVFP4_SPLITHALF, OT><<<grid_for(n, T), T, 0, s>>>(t.w, t.scales, t.scale2, out, n);
+        break;
+    }
+    case Q4_MXFP4: {
+        int64_t n = t.N * t.K / 16;
+        dequant_fp4<Q4_MXFP4, OT><<<grid_for(n, T), T, 0, s>>>(t.w, t.scales, 1.0f, out, n);
+        break;
+    }
+    case Q4_Q4K: {
+        int64_t n = t.N * (t.K / 256) * 8;
+        dequant_q4k<OT><<<grid_for(n, T), T, 0, s>>>(t.w, out, n);
+        break;
+    }
+    case Q4_Q40: {
+        int64_t n = t.N * (t.K / 32);
+        dequant_q40<OT><<<grid_for(n, T), T, 0, s>>>(t.w, out, n);
+        break;
+    }
+    case Q4_GPTQ:
+    case Q4_AWQ:
+    case Q4_LOGICAL: {
+        dim3 grid((unsigned)((t.N + 63) / 64), (unsigned)((t.K + 63) / 64));
+        if (t.fmt == Q4_GPTQ) dequant_kmajor<Q4_GPTQ, OT><<<grid, 256, 0, s>>>(t, out);
+        else if (t.fmt == Q4_AWQ) dequant_kmajor<Q4_AWQ, OT><<<grid, 256, 0, s>>>(t, out);
+        else dequant_kmajor<Q4_LOGICAL, OT><<<grid, 256, 0, s>>>(t, out);
+        break;
+    }
+    default:
+        return cudaErrorInvalidValue;
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_dequant(const Tensor &t, void *out, q4_dtype out_dtype, cudaStream_t s) {
+    if (out_dtype == Q4_DT_BF16) return dispatch<__nv_bfloat16>(t, (__nv_bfloat16 *)out, s);
+    return dispatch<float>(t, (float *)out, s);
+}
+
+}  // namespace q4

@@ -1,0 +1,575 @@
+// gemv.cu -- fused 4-bit decode + matrix-vector product for batch 1..8
+// ([W4K] section 1: load packed bytes and scales, unpack, scale, multiply,
+// accumulate in a wider type -- no dequantized matrix is written).
+//
+// Row-major formats (NVFP4, MXFP4, Q4_0, Q4_K), batch 1: "slice-stationary"
+// threads.  A CTA has one thread per 32-weight slice of a row (K/32 threads,
+// rounded up to a warp); each thread keeps the 32 activations of its slice
+// in f32 registers for the whole kernel and walks over row tiles, streaming
+// 16 B of codes per row with 128-bit non-allocating loads, one tile ahead.
+// Per-row partial sums are reduced across the CTA with a transposed warp
+// shuffle (R rows in log2(R)+5-log2(R) shuffles) and one shared-memory pass.
+//
+// K-major formats (GPTQ, AWQ): lanes run along N (the packed axis, so loads
+// coalesce), warps and the CTAs of a thread-block cluster split K, and the
+// partial sums are combined in a fixed order through distributed shared
+// memory -- deterministic, with no global scratch.
+//
+// Anything else (M > 1 on row-major formats, K not a multiple of 32, act-order
+// g_idx) runs a general warp-per-row kernel over the per-element decoders.
+#include <cooperative_groups.h>
+
+#include "q4_internal.cuh"
+
+namespace cg = cooperative_groups;
+
+namespace q4 {
+namespace {
+
+// ----------------------------------------------------------- row slices
+template <int FMT> struct Slice;
+
+// NVFP4 slice s of row n: payload bytes [16s, 16s+16) = k 32s..32s+31, two
+// E4M3FN scales; (e2m1 * e4m3) per 16-group, scale2 once per row ([MUS7] 7.4.1
+// applies the block scale once per 16 and scale2 once per row as well).
+template <> struct Slice<Q4_NVFP4> {
+    struct Regs { uint4 p; uint32_t s; };
+    __device__ static int kpos(int s, int i) { return 32 * s + i; }
+    __device__ static void load(const Tensor &t, int64_t n, int s, Regs &r) {
+        r.p = ldg_stream16(t.w + n * (t.K >> 1) + 16 * s);
+        r.s = ldg_stream2(t.scales + n * (t.K >> 4) + 2 * s);
+    }
+    __device__ static float dot(const Regs &r, const float (&xs)[32]) {
+        const uint32_t wd[4] = {r.p.x, r.p.y, r.p.z, r.p.w};
+        float2 a0 = make_float2(0.f, 0.f), a1 = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int b = 0; b < 8; b++)
+            ffma2(a0, e2m1x2_f32(wd[b >> 2] >> (8 * (b & 3))), make_float2(xs[2 * b], xs[2 * b + 1]));
+#pragma unroll
+        for (int b = 8; b < 16; b++)
+            ffma2(a1, e2m1x2_f32(wd[b >> 2] >> (8 * (b & 3))), make_float2(xs[2 * b], xs[2 * b + 1]));
+        float2 sc = e4m3x2_f32(r.s);
+        return fmaf(a1.x + a1.y, sc.y, (a0.x + a0.y) * sc.x);
+    }
+    __device__ static float epilogue(float v, const Tensor &t) { return v * t.scale2; }
+};
+
+// MXFP4 slice: the same payload, one E8M0 scale for all 32 ([FBTC] section 3).
+template <> struct Slice<Q4_MXFP4> {
+    struct Regs { uint4 p; uint32_t s; };
+    __device__ static int kpos(int s, int i) { return 32 * s + i; }
+    __device__ static void load(const Tensor &t, int64_t n, int s, Regs &r) {
+        r.p = ldg_stream16(t.w + n * (t.K >> 1) + 16 * s);
+        r.s = ldg_stream1(t.scales + n * (t.K >> 5) + s);
+    }
+    __device__ static float dot(const Regs &r, const float (&xs)[32]) {
+        const uint32_t wd[4] = {r.p.x, r.p.y, r.p.z, r.p.w};
+        float2 a0 = make_float2(0.f, 0.f), a1 = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int b = 0; b < 16; b += 2) {
+            ffma2(a0, e2m1x2_f32(wd[b >> 2] >> (8 * (b & 3))), make_float2(xs[2 * b], xs[2 * b + 1]));
+            ffma2(a1, e2m1x2_f32(wd[(b + 1) >> 2] >> (8 * ((b + 1) & 3))),
+                  make_float2(xs[2 * b + 2], xs[2 * b + 3]));
+        }
+        return ((a0.x + a0.y) + (a1.x + a1.y)) * e8m0_f32(r.s);
+    }
+    __device__ static float epilogue(float v, const Tensor &) { return v; }
+};
+
+// Q4_0 slice = one 18-byte block: d * sum (q-8) x ([BPA] "Real layouts
+// compared").  Blocks are 2-byte aligned: four aligned words plus two u16.
+template <> struct Slice<Q4_Q40> {
+    struct Regs { uint32_t w0, w1, w2, w3, e14, e16; uint32_t odd; };
+    __device__ static int kpos(int s, int i) { return 32 * s + i; }
+    __device__ static void load(const Tensor &t, int64_t n, int s, Regs &r) {
+        int64_t o = (n * (t.K >> 5) + s) * 18;
+        const uint8_t *a = t.w + (o & ~(int64_t)3);
+        r.w0 = ldg_stream4(a);
+        r.w1 = ldg_stream4(a + 4);
+        r.w2 = ldg_stream4(a + 8);
+        r.w3 = ldg_stream4(a + 12);
+        r.e14 = ldg_stream2(t.w + o + 14);
+        r.e16 = ldg_stream2(t.w + o + 16);
+        r.odd = (uint32_t)(o & 2);
+    }
+    __device__ static float dot(const Regs &r, const float (&xs)[32]) {
+        uint32_t d, q[4];
+        if (r.odd) {   // block starts 2 bytes into w0
+            d = r.w0 >> 16;
+            q[0] = r.w1; q[1] = r.w2; q[2] = r.w3; q[3] = r.e14 | (r.e16 << 16);
+        } else {
+            d = r.w0 & 0xffffu;
+            q[0] = __funnelshift_r(r.w0, r.w1, 16);
+            q[1] = __funnelshift_r(r.w1, r.w2, 16);
+            q[2] = __funnelshift_r(r.w2, r.w3, 16);
+            q[3] = (r.w3 >> 16) | (r.e16 << 16);
+        }
+        float2 a0 = make_float2(0.f, 0.f), a1 = make_float2(0.f, 0.f);
+        const float m8 = 8388616.0f;   // 2^23 + 8: (2^23 + q) - m8 = q - 8 exactly
+#pragma unroll
+        for (int j = 0; j < 16; j += 2) {
+            uint32_t b0 = (q[j >> 2] >> (8 * (j & 3))) & 0xffu;
+            uint32_t b1 = (q[(j + 1) >> 2] >> (8 * ((j + 1) & 3))) & 0xffu;
+            ffma2(a0, make_float2(uint_minus(b0 & 15u, m8), uint_minus(b1 & 15u, m8)),
+                  make_float2(xs[j], xs[j + 1]));
+            ffma2(a1, make_float2(uint_minus(b0 >> 4, m8), uint_minus(b1 >> 4, m8)),
+                  make_float2(xs[16 + j], xs[17 + j]));
+        }
+        return ((a0.x + a0.y) + (a1.x + a1.y)) * half_bits_f32(d);
+    }
+    __device__ static float epilogue(float v, const Tensor &) { return v; }
+};
+
+// Q4_K slice s: super-block b = s/8, 64-chunk c = (s/2)%4, half h = s%2:
+// code bytes 32c+16h .. +16 feed k = 64c+16h+i (sub-block 2c, low nibbles)
+// and 64c+32+16h+i (sub-block 2c+1, high) ([FBTC] sections 5-6).  Each
+// weight is rebuilt as fma(q, d*s_j, -dmin*m_j) -- the oracle's single
+// rounding -- before it meets x.
+template <> struct Slice<Q4_Q4K> {
+    struct Regs { uint4 hdr; uint4 qs; };
+    __device__ static int kpos(int s, int i) {
+        int b = s >> 3, c = (s >> 1) & 3, h = s & 1;
+        return 256 * b + 64 * c + 16 * h + (i < 16 ? i : 16 + i);
+    }
+    __device__ static void load(const Tensor &t, int64_t n, int s, Regs &r) {
+        int b = s >> 3, c = (s >> 1) & 3, h = s & 1;
+        const uint8_t *blk = t.w + (n * (t.K >> 8) + b) * 144;
+        r.hdr = ldg_stream16(blk);
+        r.qs = ldg_stream16(blk + 16 + 32 * c + 16 * h);
+    }
+    __device__ static uint32_t meta_byte(const uint4 &h, int i) {
+        uint32_t w = i < 4 ? h.y : (i < 8 ? h.z : h.w);
+        return (w >> (8 * (i & 3))) & 0xffu;
+    }
+    __device__ static void scale_min(const uint4 &h, int j, float &sc, float &mn) {
+        uint32_t s, m;
+        if (j < 4) {
+            s = meta_byte(h, j) & 63u;
+            m = meta_byte(h, j + 4) & 63u;
+        } else {
+            s = (meta_byte(h, j + 4) & 15u) | ((meta_byte(h, j - 4) >> 6) << 4);
+            m = (meta_byte(h, j + 4) >> 4) | ((meta_byte(h, j) >> 6) << 4);
+        }
+        sc = (float)s;
+        mn = (float)m;
+    }
+    __device__ static float dot_c(const Regs &r, const float (&xs)[32], int c) {
+        float d = half_bits_f32(r.hdr.x), dmin = half_bits_f32(r.hdr.x >> 16);
+        float sl, ml, sh, mh;
+        scale_min(r.hdr, 2 * c, sl, ml);
+        scale_min(r.hdr, 2 * c + 1, sh, mh);
+        const float step_lo = __fmul_rn(d, sl), off_lo = -__fmul_rn(dmin, ml);
+        const float step_hi = __fmul_rn(d, sh), off_hi = -__fmul_rn(dmin, mh);
+        const uint32_t wd[4] = {r.qs.x, r.qs.y, r.qs.z, r.qs.w};
+        const float two23 = 8388608.0f;
+        float2 a0 = make_float2(0.f, 0.f), a1 = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int i = 0; i < 16; i += 2) {
+            uint32_t b0 = (wd[i >> 2] >> (8 * (i & 3))) & 0xffu;
+            uint32_t b1 = (wd[(i + 1) >> 2] >> (8 * ((i + 1) & 3))) & 0xffu;
+            float2 wl = make_float2(__fmaf_rn(uint_minus(b0 & 15u, two23), step_lo, off_lo),
+                                    __fmaf_rn(uint_minus(b1 & 15u, two23), step_lo, off_lo));
+            float2 wh = make_float2(__fmaf_rn(uint_minus(b0 >> 4, two23), step_hi, off_hi),
+                                    __fmaf_rn(uint_minus(b1 >> 4, two23), step_hi, off_hi));
+            ffma2(a0, wl, make_float2(xs[i], xs[i + 1]));
+            ffma2(a1, wh, make_float2(xs[16 + i], xs[17 + i]));
+        }
+        return (a0.x + a0.y) + (a1.x + a1.y);
+    }
+    __device__ static float epilogue(float v, const Tensor &) { return v; }
+};
+
+template <int FMT> struct SliceDot {
+    __device__ static float run(const typename Slice<FMT>::Regs &r, const float (&xs)[32], int) {
+        return Slice<FMT>::dot(r, xs);
+    }
+};
+template <> struct SliceDot<Q4_Q4K> {
+    __device__ static float run(const Slice<Q4_Q4K>::Regs &r, const float (&xs)[32], int s) {
+        return Slice<Q4_Q4K>::dot_c(r, xs, (s >> 1) & 3);
+    }
+};
+
+// Transposed warp reduction of R row partials: after it, lane L holds the
+// warp sum of row L / (32/R).
+template <int R> __device__ __forceinline__ float warp_reduce_rows(float (&v)[R], int lane) {
+    int cnt = R;
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) {
+        if (cnt > 1) {
+            const bool upper = (lane & off) != 0;
+            const int half = cnt >> 1;
+#pragma unroll
+            for (int i = 0; i < R / 2; i++) {
+                if (i < half) {
+                    float send = upper ? v[i] : v[i + half];
+                    float keep = upper ? v[i + half] : v[i];
+                    v[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+                }
+            }
+            cnt = half;
+        } else {
+            v[0] += __shfl_xor_sync(0xffffffffu, v[0], off);
+        }
+    }
+    return v[0];
+}
+
+template <int FMT, typename XT, int R, int TMAX>
+__global__ void __launch_bounds__(TMAX) gemv_rows_m1(Tensor t, const XT *__restrict__ x,
+                                                     float *__restrict__ y, int ntiles) {
+    using S = Slice<FMT>;
+    const int NS = (int)(t.K >> 5);
+    const int s = threadIdx.x;
+    const bool active = s < NS;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+
+    float xs[32];
+#pragma unroll
+    for (int i = 0; i < 32; i++) xs[i] = active ? x_to_f32<XT>(x[S::kpos(s, i)]) : 0.0f;
+
+    __shared__ float red[2][32][R];
+    typename S::Regs cur[R], nxt[R];
+    int tile = blockIdx.x;
+    if (tile < ntiles) {
+#pragma unroll
+        for (int r = 0; r < R; r++) {
+            int64_t n = (int64_t)tile * R + r;
+            if (active && n < t.N) S::load(t, n, s, cur[r]);
+        }
+    }
+    int buf = 0;
+    for (; tile < ntiles; tile += gridDim.x) {
+        const int nt = tile + gridDim.x;
+        if (nt < ntiles) {
+#pragma unroll
+            for (int r = 0; r < R; r++) {
+                int64_t n = (int64_t)nt * R + r;
+                if (active && n < t.N) S::load(t, n, s, nxt[r]);
+            }
+        }
+        float acc[R];
+#pragma unroll
+        for (int r = 0; r < R; r++) {
+            int64_t n = (int64_t)tile * R + r;
+            acc[r] = (active && n < t.N) ? SliceDot<FMT>::run(cur[r], xs, s) : 0.0f;
+        }
+        float v = warp_reduce_rows<R>(acc, lane);
+        if ((lane & (32 / R - 1)) == 0) red[buf][warp][lane / (32 / R)] = v;
+        __syncthreads();
+        if (threadIdx.x < R) {
+            int64_t n = (int64_t)tile * R + threadIdx.x;
+            if (n < t.N) {
+                float sum = 0.0f;
+                for (int w = 0; w < nwarps; w++) sum += red[buf][w][threadIdx.x];
+                y[n] = S::epilogue(sum, t);
+            }
+        }
+        buf ^= 1;
+#pragma unroll
+        for (int r = 0; r < R; r++) cur[r] = nxt[r];
+    }
+}
+
+// -------------------------------------------------- general shapes, any M
+// One warp per (row, batch chunk of up to 8): lanes stride over k, each
+// weight rebuilt by the pinned per-element rule, f32 accumulation.
+template <int FMT, typename XT>
+__global__ void __launch_bounds__(256) gemv_general(Tensor t, const XT *__restrict__ x,
+                                                    float *__restrict__ y, int64_t M) {
+    const int lane = threadIdx.x & 31;
+    const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
+    const int64_t mchunks = (M + 7) / 8;
+    for (int64_t item = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+         item < t.N * mchunks; item += warps) {
+        const int64_t n = item / mchunks, m0 = (item % mchunks) * 8;
+        const int mc = (int)((M - m0) < 8 ? (M - m0) : 8);
+        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        for (int64_t k = lane; k < t.K; k += 32) {
+            const float w = elem_weight<FMT>(t, n, k);
+#pragma unroll
+            for (int mm = 0; mm < 8; mm++)
+                if (mm < mc) acc[mm] = fmaf(w, x_to_f32<XT>(x[(m0 + mm) * t.K + k]), acc[mm]);
+        }
+#pragma unroll
+        for (int mm = 0; mm < 8; mm++) {
+#pragma unroll
+            for (int off = 16; off >= 1; off >>= 1) acc[mm] += __shfl_xor_sync(0xffffffffu, acc[mm], off);
+        }
+        if (lane == 0)
+            for (int mm = 0; mm < mc; mm++) y[(m0 + mm) * t.N + n] = acc[mm];
+    }
+}
+
+// ---------------------------------------------------- K-major (GPTQ, AWQ)
+// GPTQ: lane = one column n (qweight word (r, n) holds k 8r..8r+7); a warp
+//       covers 32 columns.  AWQ: lane = one word (k, c) = columns 8c..8c+7 in
+//       slot order; a warp covers 256 columns.
+// The 8 warps of a CTA split the CTA's K range into contiguous chunks; the
+// CS CTAs of a cluster (grid.y) split K.  Group scale and zero are loaded
+// once per group; sum (q - z) x is accumulated per group, then scaled.
+constexpr int KM_WARPS = 8;
+
+template <int FMT> struct KCols { static constexpr int value = (FMT == Q4_GPTQ) ? 1 : 8; };
+
+template <int FMT, typename XT, int MB>
+__global__ void __launch_bounds__(KM_WARPS * 32) gemv_kmajor(Tensor t, const XT *__restrict__ x,
+                                                             float *__restrict__ y, int M,
+                                                             int k_per_cta) {
+    constexpr int C = KCols<FMT>::value;        // columns per lane
+    constexpr int WCOLS = 32 * C;               // columns per warp (= per CTA)
+    extern __shared__ float smem[];             // x[MB][k_per_cta] then partials
+    float *xs = smem;
+    float *part = smem + MB * k_per_cta;        // [KM_WARPS][MB][WCOLS]
+
+    cg::cluster_group cluster = cg::this_cluster();
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int64_t N = t.N, K = t.K;
+    const int64_t col0 = (int64_t)blockIdx.x * WCOLS;
+    const int64_t k0 = (int64_t)blockIdx.y * k_per_cta;
+    const int64_t kn = (K - k0) < k_per_cta ? (K - k0) : k_per_cta;   // may be <= 0
+
+    for (int i = threadIdx.x; i < MB * k_per_cta; i += blockDim.x) {
+        int m = i / k_per_cta, kk = i % k_per_cta;
+        xs[i] = (m < M && kk < kn) ? x_to_f32<XT>(x[(int64_t)m * K + k0 + kk]) : 0.0f;
+    }
+    __syncthreads();
+
+    float acc[MB][C];
+#pragma unroll
+    for (int m = 0; m < MB; m++)
+#pragma unroll
+        for (int c = 0; c < C; c++) acc[m][c] = 0.0f;
+
+    const int G = t.group;
+    // this warp's contiguous k chunk, aligned to whole groups
+    const int groups_cta = (int)((kn + G - 1) / G);
+    const int g_per_warp = (groups_cta + KM_WARPS - 1) / KM_WARPS;
+    const int gw0 = warp * g_per_warp;
+    const int64_t cword = (FMT == Q4_GPTQ) ? (col0 + lane) : ((col0 >> 3) + lane);
+    const bool col_ok = (FMT == Q4_GPTQ) ? (cword < N) : (cword < (N >> 3));
+    const uint32_t *qw = reinterpret_cast<const uint32_t *>(t.w);
+    const uint32_t *qz = reinterpret_cast<const uint32_t *>(t.zeros);
+    const uint16_t *sc = reinterpret_cast<const uint16_t *>(t.scales);
+
+    for (int gl = gw0; gl < gw0 + g_per_warp && gl < groups_cta && col_ok; gl++) {
+        const int64_t kg0 = k0 + (int64_t)gl * G;                 // group start (absolute k)
+        const int64_t g = kg0 / G;
+        const int kcount = (int)((k0 + kn - kg0) < G ? (k0 + kn - kg0) : G);
+        float s[C], z[C];
+        if (FMT == Q4_GPTQ) {
+            s[0] = half_bits_f32(sc[g * N + cword]);
+            uint32_t zw = qz[g * (N >> 3) + (cword >> 3)];
+            z[0] = (float)(((zw >> (4 * (cword & 7))) & 15u) + 1u);
+        } else {
+            uint32_t zw = qz[g * (N >> 3) + cword];
+            const uint4 s4 = *reinterpret_cast<const uint4 *>(sc + g * N + 8 * cword);
+            const uint32_t sw[4] = {s4.x, s4.y, s4.z, s4.w};
+#pragma unroll
+            for (int p = 0; p < 8; p++) {            // slot p holds column order[p]
+                const int col = (p < 4) ? 2 * p : 2 * (p - 4) + 1;
+                z[col] = (float)((zw >> (4 * p)) & 15u);
+                s[col] = half_bits_f32(sw[col >> 1] >> (16 * (col & 1)));
+            }
+        }
+        float gacc[MB][C];
+#pragma unroll
+        for (int m = 0; m < MB; m++)
+#pragma unroll
+            for (int c = 0; c < C; c++) gacc[m][c] = 0.0f;
+        const float two23 = 8388608.0f;
+        if (FMT == Q4_GPTQ) {
+            const int64_t r0 = kg0 >> 3;
+            const int rows = kcount >> 3;
+#pragma unroll 4
+            for (int r = 0; r < rows; r++) {
+                const uint32_t word = ldg_stream4(qw + (r0 + r) * N + cword);
+                const float *xr = xs + (kg0 - k0) + 8 * r;
+#pragma unroll
+                for (int j = 0; j < 8; j++) {
+                    const float qmz = uint_minus((word >> (4 * j)) & 15u, two23) - z[0];
+#pragma unroll
+                    for (int m = 0; m < MB; m++) gacc[m][0] = fmaf(qmz, xr[m * k_per_cta + j], gacc[m][0]);
+                }
+            }
+        } else {
+#pragma unroll 4
+            for (int kk = 0; kk < kcount; kk++) {
+                const uint32_t word = ldg_stream4(qw + (kg0 + kk) * (N >> 3) + cword);
+                const float *xr = xs + (kg0 - k0) + kk;
+#pragma unroll
+                for (int p = 0; p < 8; p++) {
+                    const int col = (p < 4) ? 2 * p : 2 * (p - 4) + 1;
+                    const float qmz = uint_minus((word >> (4 * p)) & 15u, two23) - z[col];
+#pragma unroll
+                    for (int m = 0; m < MB; m++) gacc[m][col] = fmaf(qmz, xr[m * k_per_cta], gacc[m][col]);
+                }
+            }
+        }
+#pragma unroll
+        for (int m = 0; m < MB; m++)
+#pragma unroll
+            for (int c = 0; c < C; c++) acc[m][c] = fmaf(gacc[m][c], s[c], acc[m][c]);
+    }
+
+    // warp partials -> shared [warp][m][col]; warp-sum in fixed order
+#pragma unroll
+    for (int m = 0; m < MB; m++)
+#pragma unroll
+        for (int c = 0; c < C; c++) part[(warp * MB + m) * WCOLS + lane * C + c] = acc[m][c];
+    __syncthreads();
+    for (int i = threadIdx.x; i < MB * WCOLS; i += blockDim.x) {
+        float v = 0.0f;
+        for (int w = 0; w < KM_WARPS; w++) v += part[w * MB * WCOLS + i];
+        part[i] = v;                     // row 0 of `part` holds the CTA total
+    }
+    cluster.sync();
+    if (cluster.block_rank() == 0) {
+        const int cs = (int)cluster.num_blocks();
+        for (int i = threadIdx.x; i < MB * WCOLS; i += blockDim.x) {
+            float v = 0.0f;
+            for (int r = 0; r < cs; r++) v += cluster.map_shared_rank(part, r)[i];
+            const int m = i / WCOLS;
+            const int64_t n = col0 + (i % WCOLS);
+            if (m < M && n < N) y[(int64_t)m * N + n] = v;
+        }
+    }
+    cluster.sync();   // keep every CTA's shared memory alive until rank 0 has read it
+}
+
+// ---------------------------------------------------------------- launch
+// Resident CTAs per SM for (kernel, threads, smem), cached per device so that
+// calls made during stream capture issue no occupancy queries after warm-up.
+struct OccKey { const void *fn; int threads; size_t smem; int dev; };
+struct OccEntry { OccKey key; int blocks; };
+OccEntry g_occ[64];
+int g_occ_n = 0;
+
+template <typename Kern> int max_blocks(Kern k, int threads, size_t smem) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const void *fn = reinterpret_cast<const void *>(k);
+    for (int i = 0; i < g_occ_n; i++) {
+        const OccKey &o = g_occ[i].key;
+        if (o.fn == fn && o.threads == threads && o.smem == smem && o.dev == dev) return g_occ[i].blocks;
+    }
+    int b = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, k, threads, smem) != cudaSuccess || b < 1)
+        b = 1;
+    if (g_occ_n < 64) g_occ[g_occ_n++] = OccEntry{OccKey{fn, threads, smem, dev}, b};
+    return b;
+}
+
+template <int FMT, typename XT, int R, int TMAX>
+cudaError_t run_rows_m1(const Tensor &t, const XT *x, float *y, cudaStream_t s) {
+    const int NS = (int)(t.K >> 5);
+    const int threads = (NS + 31) / 32 * 32;
+    const int ntiles = (int)((t.N + R - 1) / R);
+    auto kern = gemv_rows_m1<FMT, XT, R, TMAX>;
+    const int bps = max_blocks(kern, threads, 0);
+    int grid = bps * sm_count();
+    if (grid > ntiles) grid = ntiles;
+    kern<<<grid, threads, 0, s>>>(t, x, y, ntiles);
+    return cudaGetLastError();
+}
+
+template <int FMT, typename XT>
+cudaError_t rows_m1(const Tensor &t, const XT *x, float *y, cudaStream_t s) {
+    const int NS = (int)(t.K >> 5);
+    if (NS <= 128) return run_rows_m1<FMT, XT, 4, 128>(t, x, y, s);
+    if (NS <= 256) return run_rows_m1<FMT, XT, 4, 256>(t, x, y, s);
+    if (NS <= 512) return run_rows_m1<FMT, XT, 4, 512>(t, x, y, s);
+    return run_rows_m1<FMT, XT, 2, 1024>(t, x, y, s);
+}
+
+template <int FMT, typename XT>
+cudaError_t general(const Tensor &t, const XT *x, float *y, int64_t M, cudaStream_t s) {
+    const int64_t items = t.N * ((M + 7) / 8);
+    int64_t blocks = (items + 7) / 8;
+    const int64_t cap = (int64_t)sm_count() * 8;
+    if (blocks > cap) blocks = cap;
+    gemv_general<FMT, XT><<<(unsigned)blocks, 256, 0, s>>>(t, x, y, M);
+    return cudaGetLastError();
+}
+
+template <int FMT, typename XT, int MB>
+cudaError_t kmajor_mb(const Tensor &t, const XT *x, float *y, int M, cudaStream_t s) {
+    constexpr int WCOLS = 32 * KCols<FMT>::value;
+    const int64_t G = t.group;
+    const int64_t groups = t.K / G;
+    // cluster size: split K so that roughly 4 CTAs per SM are in flight
+    const int64_t tiles = (t.N + WCOLS - 1) / WCOLS;
+    auto x_bytes = [&](int c) { return sizeof(float) * (size_t)MB * (size_t)(((groups + c - 1) / c) * G); };
+    int cs = 1;
+    while (cs < 8 && groups / (cs * 2) >= 1 &&
+           (tiles * cs < (int64_t)sm_count() * 4 || x_bytes(cs) > 96 * 1024))
+        cs *= 2;
+    const int64_t gpc = (groups + cs - 1) / cs;
+    const int k_per_cta = (int)(gpc * G);
+    const size_t smem = sizeof(float) * ((size_t)MB * k_per_cta + (size_t)KM_WARPS * MB * WCOLS);
+    auto kern = gemv_kmajor<FMT, XT, MB>;
+    if (smem > 48 * 1024) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)tiles, (unsigned)cs, 1);
+    cfg.blockDim = dim3(KM_WARPS * 32, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 1;
+    attr[0].val.clusterDim.y = (unsigned)cs;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, t, x, y, M, k_per_cta);
+}
+
+template <int FMT, typename XT>
+cudaError_t kmajor(const Tensor &t, const XT *x, float *y, int64_t M, cudaStream_t s) {
+    cudaError_t e = cudaSuccess;
+    for (int64_t m0 = 0; m0 < M && e == cudaSuccess; m0 += 8) {
+        const int mc = (int)((M - m0) < 8 ? (M - m0) : 8);
+        const XT *xm = x + m0 * t.K;
+        float *ym = y + m0 * t.N;
+        if (mc == 1) e = kmajor_mb<FMT, XT, 1>(t, xm, ym, mc, s);
+        else if (mc == 2) e = kmajor_mb<FMT, XT, 2>(t, xm, ym, mc, s);
+        else if (mc <= 4) e = kmajor_mb<FMT, XT, 4>(t, xm, ym, mc, s);
+        else e = kmajor_mb<FMT, XT, 8>(t, xm, ym, mc, s);
+    }
+    return e;
+}
+
+template <typename XT>
+cudaError_t dispatch(const Tensor &t, const XT *x, float *y, int64_t M, cudaStream_t s) {
+    const bool fast_rows = (M == 1) && (t.K % 32 == 0) && (t.K <= 32768);
+    switch (t.fmt) {
+    case Q4_NVFP4:
+        return fast_rows ? rows_m1<Q4_NVFP4, XT>(t, x, y, s) : general<Q4_NVFP4, XT>(t, x, y, M, s);
+    case Q4_MXFP4:
+        return fast_rows ? rows_m1<Q4_MXFP4, XT>(t, x, y, s) : general<Q4_MXFP4, XT>(t, x, y, M, s);
+    case Q4_Q40:
+        return fast_rows ? rows_m1<Q4_Q40, XT>(t, x, y, s) : general<Q4_Q40, XT>(t, x, y, M, s);
+    case Q4_Q4K:
+        return fast_rows ? rows_m1<Q4_Q4K, XT>(t, x, y, s) : general<Q4_Q4K, XT>(t, x, y, M, s);
+    case Q4_GPTQ:
+        if (t.g_idx == nullptr && t.group % 8 == 0) return kmajor<Q4_GPTQ, XT>(t, x, y, M, s);
+        return general<Q4_GPTQ, XT>(t, x, y, M, s);
+    case Q4_AWQ:
+        return kmajor<Q4_AWQ, XT>(t, x, y, M, s);
+    default:
+        return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_gemv(const Tensor &t, const void *x, q4_dtype x_dtype, float *y, int64_t M,
+                        cudaStream_t s) {
+    if (x_dtype == Q4_DT_BF16) return dispatch<__nv_bfloat16>(t, (const __nv_bfloat16 *)x, y, M, s);
+    return dispatch<float>(t, (const float *)x, y, M, s);
+}
+
+}  // namespace q4

@@ -1,0 +1,185 @@
+// q4_api.cu -- the extern "C" boundary of libq4.so: host-side argument checks
+// (nothing is launched on a bad argument), then dispatch to the kernels.
+#include <cmath>
+#include <cstdio>
+
+#include "q4_internal.cuh"
+
+namespace q4 {
+
+int sm_count() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1) return 1;
+    return n;
+}
+
+namespace {
+
+bool known(q4_fmt f) { return f >= Q4_NVFP4 && f <= Q4_LOGICAL; }
+bool aligned16(const void *p) { return p && (((uintptr_t)p) & 15u) == 0; }
+bool kmajor_fmt(q4_fmt f) { return f == Q4_GPTQ || f == Q4_AWQ || f == Q4_LOGICAL; }
+bool uses_scale_tensor(q4_fmt f) { return f != Q4_Q4K && f != Q4_Q40; }
+
+int group_of(const q4_aux *aux) { return (aux && aux->group > 0) ? aux->group : 128; }
+
+// Shape rules of each format (block / group multiples; [BPA] padding note).
+int check_dims(q4_fmt f, int64_t N, int64_t K, int group) {
+    if (N <= 0 || K <= 0) return Q4_EDIM;
+    switch (f) {
+    case Q4_NVFP4:
+    case Q4_NVFP4_SPLITHALF: return K % 16 ? Q4_EDIM : Q4_OK;
+    case Q4_MXFP4:
+    case Q4_Q40: return K % 32 ? Q4_EDIM : Q4_OK;
+    case Q4_Q4K: return K % 256 ? Q4_EDIM : Q4_OK;
+    case Q4_GPTQ: return (K % 8 || K % group || N % 8) ? Q4_EDIM : Q4_OK;
+    case Q4_AWQ:
+    case Q4_LOGICAL: return (K % group || N % 8) ? Q4_EDIM : Q4_OK;
+    default: return Q4_EINVAL;
+    }
+}
+
+// Common checks for a packed weight tensor; fills `t`.  The NVFP4 scale2
+// check comes last so a caller that does not read scale2 may ignore it.
+int make_tensor(q4_fmt f, const void *W, const void *scales, const q4_aux *aux, int64_t N, int64_t K,
+                Tensor &t, bool need_scale2 = true) {
+    if (!known(f)) return Q4_EINVAL;
+    const int group = group_of(aux);
+    int rc = check_dims(f, N, K, group);
+    if (rc) return rc;
+    if (!W) return Q4_EINVAL;
+    if (!aligned16(W)) return Q4_EALIGN;
+    if (uses_scale_tensor(f)) {
+        if (!scales) return Q4_EINVAL;
+        if (!aligned16(scales)) return Q4_EALIGN;
+    }
+    if (kmajor_fmt(f)) {
+        if (!aux || !aux->zeros) return Q4_EINVAL;
+        if (!aligned16(aux->zeros)) return Q4_EALIGN;
+    }
+    if (aux && aux->g_idx) {
+        if (f != Q4_GPTQ && f != Q4_LOGICAL) return Q4_EINVAL;
+        if (!aligned16(aux->g_idx)) return Q4_EALIGN;
+    }
+    t.fmt = f;
+    t.w = (const uint8_t *)W;
+    t.scales = (const uint8_t *)scales;
+    t.zeros = aux ? (const uint8_t *)aux->zeros : nullptr;
+    t.g_idx = aux ? aux->g_idx : nullptr;
+    t.group = group;
+    t.scale2 = aux ? aux->scale2 : 1.0f;
+    t.N = N;
+    t.K = K;
+    if (need_scale2 && (f == Q4_NVFP4 || f == Q4_NVFP4_SPLITHALF)) {
+        if (!aux) return Q4_EINVAL;
+        if (!std::isfinite(aux->scale2) || !(aux->scale2 > 0.0f)) return Q4_ESCALE2;
+    }
+    return Q4_OK;
+}
+
+q4_dtype default_x_dtype(q4_fmt f) { return (f == Q4_NVFP4 || f == Q4_MXFP4) ? Q4_DT_BF16 : Q4_DT_F32; }
+
+}  // namespace
+}  // namespace q4
+
+using namespace q4;
+
+extern "C" {
+
+int q4_gemv(q4_fmt fmt, const void *W_packed, const void *scales, const q4_aux *aux, const void *x, float *y,
+            int64_t M, int64_t N, int64_t K, void *stream) {
+    Tensor t;
+    int rc = make_tensor(fmt, W_packed, scales, aux, N, K, t);
+    if (rc) return rc;
+    if (M <= 0) return Q4_EDIM;
+    if (fmt == Q4_NVFP4_SPLITHALF || fmt == Q4_LOGICAL) return Q4_EUNSUPPORTED;
+    if (!x || !y) return Q4_EINVAL;
+    if (!aligned16(x) || !aligned16(y)) return Q4_EALIGN;
+    const q4_dtype xd = aux ? aux->x_dtype : default_x_dtype(fmt);
+    if (xd != Q4_DT_F32 && xd != Q4_DT_BF16) return Q4_EINVAL;
+    cudaStream_t s = (cudaStream_t)stream;
+    bool handled = false;
+    cudaError_t e = cudaSuccess;
+    if (M > 8) e = launch_gemm_tc(t, x, xd, y, M, s, &handled);
+    if (e == cudaSuccess && !handled) e = launch_gemv(t, x, xd, y, M, s);
+    return e == cudaSuccess ? Q4_OK : Q4_ECUDA;
+}
+
+int q4_dequant(q4_fmt fmt, const void *W_packed, const void *scales, const q4_aux *aux, void *out, int64_t N,
+               int64_t K, void *stream) {
+    Tensor t;
+    int rc = make_tensor(fmt, W_packed, scales, aux, N, K, t);
+    if (rc) return rc;
+    if (!out) return Q4_EINVAL;
+    if (!aligned16(out)) return Q4_EALIGN;
+    const q4_dtype od = aux ? aux->out_dtype : Q4_DT_F32;
+    if (od != Q4_DT_F32 && od != Q4_DT_BF16) return Q4_EINVAL;
+    return launch_dequant(t, out, od, (cudaStream_t)stream) == cudaSuccess ? Q4_OK : Q4_ECUDA;
+}
+
+int q4_repack(q4_fmt src, const void *src_w, const void *src_scales, const q4_aux *src_aux, q4_fmt dst,
+              void *dst_w, void *dst_scales, void *dst_zeros, int32_t *perm_out, int64_t N, int64_t K,
+              void *stream) {
+    Tensor t;
+    int rc = make_tensor(src, src_w, src_scales, src_aux, N, K, t, /*need_scale2=*/false);
+    if (rc) return rc;
+    if (!known(dst)) return Q4_EINVAL;
+    const int group = (src == Q4_Q40) ? 32 : t.group;
+    rc = check_dims(dst, N, K, group);
+    if (rc) return rc;
+    if (!dst_w || !dst_scales) return Q4_EINVAL;
+    if (!aligned16(dst_w) || !aligned16(dst_scales)) return Q4_EALIGN;
+    if (kmajor_fmt(dst)) {
+        if (!dst_zeros) return Q4_EINVAL;
+        if (!aligned16(dst_zeros)) return Q4_EALIGN;
+    }
+    if (perm_out && !aligned16(perm_out)) return Q4_EALIGN;
+    return launch_repack(src, t, dst, dst_w, dst_scales, dst_zeros, perm_out, (cudaStream_t)stream);
+}
+
+int q4_validate(q4_fmt fmt, const void *W_packed, const void *scales, const q4_aux *aux, int64_t N, int64_t K,
+                int64_t *d_bad_count, void *stream) {
+    Tensor t;
+    const int rc = make_tensor(fmt, W_packed, scales, aux, N, K, t);
+    if (rc && rc != Q4_ESCALE2) return rc;
+    if (!d_bad_count) return Q4_EINVAL;
+    if (!aligned16(d_bad_count)) return Q4_EALIGN;
+    const int v = run_validate(t, d_bad_count, (cudaStream_t)stream);
+    return v != Q4_OK ? v : rc;      // NaN scale bytes first, then a bad scale2
+}
+
+const char *q4_strerror(int status) {
+    switch (status) {
+    case Q4_OK: return "ok";
+    case Q4_EINVAL: return "invalid argument (null pointer, unknown format or dtype, missing aux field)";
+    case Q4_EDIM: return "invalid dimensions (non-positive, or not a multiple of the format's block/group)";
+    case Q4_EALIGN: return "a tensor pointer is not 16-byte aligned";
+    case Q4_ENAN: return "NaN scale encodings found";
+    case Q4_ESCALE2: return "NVFP4 scale2 must be finite and > 0";
+    case Q4_ECUDA: return "CUDA launch or copy failed";
+    case Q4_EUNSUPPORTED: return "format/operation pair not provided";
+    case Q4_ERANGE: return "a zero point cannot be stored in the target format";
+    case Q4_ETIMEOUT: return "a bounded device-side wait timed out";
+    default: return "unknown status";
+    }
+}
+
+size_t q4_packed_bytes(q4_fmt fmt, int64_t N, int64_t K) {
+    if (check_dims(fmt, N, K, 128) != Q4_OK) return 0;
+    const int64_t G = K / 128;
+    switch (fmt) {
+    case Q4_NVFP4:
+    case Q4_NVFP4_SPLITHALF: return (size_t)(N * K / 2 + N * K / 16 + 4);
+    case Q4_MXFP4: return (size_t)(N * K / 2 + N * K / 32);
+    case Q4_Q4K: return (size_t)(N * (K / 256) * 144);
+    case Q4_Q40: return (size_t)(N * (K / 32) * 18);
+    case Q4_GPTQ:
+    case Q4_AWQ: return (size_t)(N * K / 2 + G * N * 2 + G * (N / 8) * 4);
+    case Q4_LOGICAL: return (size_t)(N * K + G * N * 2 + G * N);
+    default: return 0;
+    }
+}
+
+const char *q4_version(void) { return "q4 0.1 sm_103a"; }
+
+}  // extern "C"

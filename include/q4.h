@@ -1,0 +1,167 @@
+/*
+ * q4.h -- C ABI of libq4.so: fused 4-bit weight decode + GEMV/GEMM, dequant,
+ * repack and validation for NVFP4, MXFP4, GGUF Q4_K and Q4_0, GPTQ and AWQ,
+ * on one NVIDIA GB300 (sm_103a).
+ *
+ * Sources, cited as "page title, section":
+ *   [FBTC] "Four Bits, Three Contracts" (shivasnotes.com/blog/6006)
+ *   [W4K]  "Why 4-Bit Quantization Is King" (shivasnotes.com/blog/5996)
+ *   [BPA]  "Bit Packing Architecture, in depth" (aicassindra.com quant_bit_packing)
+ *   [MUS7] "Muser book, Chapter 7 - NVFP4: the native lane" (highperformanceailab.com)
+ *
+ * Conventions for every entry point
+ *   - Logical weights W are [N out][K in]; activations x are [M][K] row-major;
+ *     outputs y are [M][N] row-major f32:  y[m][n] = sum_k w_hat[n][k] * x[m][k].
+ *   - Every pointer is a DEVICE pointer owned by the caller (e.g. allocated by
+ *     torch).  The library allocates no device memory and keeps no pointer
+ *     after a call returns.  Tensor base pointers must be 16-byte aligned
+ *     (Q4_EALIGN otherwise).
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Calls are
+ *     asynchronous on it unless documented as synchronous.
+ *   - Arguments are checked on the host before any launch; a non-zero status
+ *     means nothing was launched.  Padding to block/group multiples is the
+ *     caller's job ([BPA] "Endianness, views and padding").
+ *   - Scale bytes are NOT scanned for NaN encodings on every call: run
+ *     q4_validate once when the weights are loaded ([MUS7] 7.3 fail-closed
+ *     loader).  Results on unvalidated NaN scales are unspecified (no fault).
+ *
+ * Formats (byte layouts, little-endian)
+ *   Q4_NVFP4  payload u8 [N][K/2], low nibble = even k; E4M3FN scales u8
+ *             [N][K/16]; aux->scale2 f32 > 0.  w = (e2m1 * e4m3fn) * scale2,
+ *             never regrouped ([MUS7] 7.1-7.2).  K % 16 == 0.
+ *   Q4_MXFP4  payload as NVFP4; E8M0 scales u8 [N][K/32]; w = e2m1 * 2^(b-127)
+ *             ([FBTC] section 3).  K % 32 == 0.
+ *   Q4_Q4K    144-byte super-blocks [N][K/256]: fp16 d @0, fp16 dmin @2, 12 B of
+ *             6-bit scales/mins @4, 128 code bytes @16; w = d*s_j*q - dmin*m_j;
+ *             code byte 32c+l feeds k = 64c+l (low) and 64c+32+l (high)
+ *             ([FBTC] sections 5-6).  `scales` ignored.  K % 256 == 0.
+ *   Q4_Q40    18-byte blocks [N][K/32]: fp16 d, 16 code bytes, byte j = element
+ *             j (low) and j+16 (high); w = d*(q-8) ([BPA] "Real layouts
+ *             compared").  `scales` ignored.  K % 32 == 0.
+ *   Q4_GPTQ   qweight i32 [K/8][N] (row 8r+j at bits 4j); scales fp16
+ *             [K/G][N]; aux->zeros = qzeros i32 [K/G][N/8] (column n at bits
+ *             4*(n%8), stored zero-1); optional aux->g_idx i32 [K]; w =
+ *             scale*(q - zero) ([BPA]).  K % G == 0, N % 8 == 0.
+ *   Q4_AWQ    qweight i32 [K][N/8], slot p holds column 8c+{0,2,4,6,1,3,5,7}[p];
+ *             scales fp16 [K/G][N]; aux->zeros = qzeros i32 [K/G][N/8], same
+ *             interleave, no minus-one ([BPA]).  K % G == 0, N % 8 == 0.
+ *   Q4_NVFP4_SPLITHALF  NVFP4 with split-half nibble order in each 16-group:
+ *             low nibbles of its 8 bytes = lanes 0-7, high = lanes 8-15 ([W4K]
+ *             section 5).  Dequant and repack only.
+ *   Q4_LOGICAL  the logical matrix of [BPA] "Repacking between formats": u8
+ *             codes [K][N], fp16 scales [K/G][N], aux->zeros u8 [K/G][N];
+ *             w = scale*(q - zero).  Dequant and repack only.
+ */
+#ifndef Q4_H
+#define Q4_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    Q4_NVFP4 = 1,
+    Q4_MXFP4 = 2,
+    Q4_Q4K = 3,
+    Q4_Q40 = 4,
+    Q4_GPTQ = 5,
+    Q4_AWQ = 6,
+    Q4_NVFP4_SPLITHALF = 7,
+    Q4_LOGICAL = 8
+} q4_fmt;
+
+typedef enum { Q4_DT_F32 = 0, Q4_DT_BF16 = 1 } q4_dtype;
+
+/* Status codes. */
+enum {
+    Q4_OK = 0,
+    Q4_EINVAL = 1,       /* null pointer, unknown format/dtype, missing aux field */
+    Q4_EDIM = 2,         /* M, N or K <= 0, or not a multiple of the format's block/group */
+    Q4_EALIGN = 3,       /* a tensor pointer is not 16-byte aligned */
+    Q4_ENAN = 4,         /* q4_validate found NaN scale encodings */
+    Q4_ESCALE2 = 5,      /* NVFP4 scale2 not finite and > 0 ([MUS7] 7.2) */
+    Q4_ECUDA = 6,        /* a CUDA launch or copy failed */
+    Q4_EUNSUPPORTED = 7, /* format/operation pair not provided (e.g. GEMV on LOGICAL) */
+    Q4_ERANGE = 8,       /* a value cannot be represented in the target (repack zeros) */
+    Q4_ETIMEOUT = 9      /* a bounded device-side wait ran out (see q4_last_error) */
+};
+
+/* Per-call options.  Passing aux == NULL selects the defaults: x_dtype = bf16
+ * for NVFP4/MXFP4 and f32 for the others, group = 128, no g_idx, out_dtype =
+ * f32.  NVFP4 requires aux (for scale2); GPTQ/AWQ/LOGICAL require aux->zeros. */
+typedef struct {
+    float scale2;          /* NVFP4 per-tensor f32 scale; must be finite and > 0 */
+    const void *zeros;     /* GPTQ/AWQ qzeros i32, LOGICAL u8 zeros */
+    const int32_t *g_idx;  /* optional GPTQ/LOGICAL group of each k (values < K/group) */
+    int32_t group;         /* GPTQ/AWQ/LOGICAL group size along K; <= 0 means 128 */
+    q4_dtype x_dtype;      /* activation dtype for q4_gemv */
+    q4_dtype out_dtype;    /* q4_dequant output dtype (bf16 = nearest-even of the f32 w) */
+} q4_aux;
+
+/* y[M][N] (f32) = x[M][K] . W^T.  The fused decode + dot of [W4K] section 1:
+ * packed weights are streamed once from HBM, decoded in registers and
+ * accumulated in f32; no dequantized matrix is written.  M <= 8 runs the
+ * bandwidth-bound GEMV kernels; M >= 9 on NVFP4 and Q4_K runs the tcgen05
+ * tensor-core kernel (weights decoded to bf16 in shared memory, f32 TMEM
+ * accumulation; Q4_K weights are rounded to bf16 there).  Accuracy: within
+ * 1e-5 * sum_k |w_hat||x| + 1e-6 of the exact f64 sum of the pinned w_hat.
+ * Returns Q4_OK or a status; asynchronous on `stream`. */
+int q4_gemv(q4_fmt fmt, const void *W_packed, const void *scales, const q4_aux *aux,
+            const void *x, float *y, int64_t M, int64_t N, int64_t K, void *stream);
+
+/* out[N][K] = w_hat, f32 or bf16 per aux->out_dtype, by the pinned per-format
+ * rule ([MUS7] 7.2 for NVFP4; the per-format sections cited above).  Bit-exact
+ * with the definition.  Asynchronous on `stream`. */
+int q4_dequant(q4_fmt fmt, const void *W_packed, const void *scales, const q4_aux *aux,
+               void *out, int64_t N, int64_t K, void *stream);
+
+/* Repack through the logical matrix ([BPA] "Repacking between formats"):
+ * unpack along the source's axis and order, normalise zero points (GPTQ +1),
+ * resolve g_idx, pack along the target's.  Pairs provided:
+ *   {GPTQ, AWQ, Q40, LOGICAL} -> {GPTQ, AWQ, LOGICAL}  (Q40 -> group 32, zero 8)
+ *   NVFP4 <-> NVFP4_SPLITHALF                           (scales copied)
+ * Outputs: dst_w, dst_scales (fp16 or E4M3 bytes), dst_zeros (GPTQ/AWQ i32,
+ * LOGICAL u8; unused for NVFP4).  If src_aux->g_idx is not k/group (act-order),
+ * rows are reordered so groups are contiguous (stable by k), every group must
+ * hold exactly `group` rows (Q4_EDIM otherwise), and perm_out[K] (required)
+ * receives the source row of each target row; the same permutation must be
+ * applied to the layer's activations.  Otherwise perm_out may be NULL.
+ * A GPTQ target cannot store zero 0 and an AWQ target cannot store 16: such a
+ * tensor yields Q4_ERANGE after the call (the call then synchronizes on
+ * `stream` to read the flag).  The result is bit-exact: q4_dequant of the
+ * target equals q4_dequant of the source (with rows permuted if perm_out). */
+int q4_repack(q4_fmt src, const void *src_w, const void *src_scales, const q4_aux *src_aux,
+              q4_fmt dst, void *dst_w, void *dst_scales, void *dst_zeros, int32_t *perm_out,
+              int64_t N, int64_t K, void *stream);
+
+/* Fail-closed scan of the scale tensor ([MUS7] 7.3): counts NaN encodings
+ * (E4M3FN 0x7f/0xff for NVFP4; E8M0 0xff for MXFP4; fp16 NaN/Inf in the d,
+ * dmin of Q4_K/Q4_0 blocks and in GPTQ/AWQ scales) and checks NVFP4 scale2.
+ * d_bad_count: caller-owned device int64 that receives the count.
+ * SYNCHRONOUS on `stream`.  Returns Q4_OK, Q4_ENAN, Q4_ESCALE2 or a status. */
+int q4_validate(q4_fmt fmt, const void *W_packed, const void *scales, const q4_aux *aux,
+                int64_t N, int64_t K, int64_t *d_bad_count, void *stream);
+
+/* Sticky device-side error of the current device (e.g. Q4_ETIMEOUT from a
+ * bounded mbarrier wait in the tensor-core kernel); reading it clears it.
+ * Synchronizes the device. */
+int q4_last_error(void);
+
+/* Human-readable text of a status code (static storage). */
+const char *q4_strerror(int status);
+
+/* Bytes of the packed payload plus scale tensor (plus zeros for GPTQ/AWQ,
+ * plus 4 for NVFP4's scale2) for an N x K tensor with group 128: the
+ * algorithmic bytes a GEMV must stream.  0 for invalid sizes. */
+size_t q4_packed_bytes(q4_fmt fmt, int64_t N, int64_t K);
+
+/* Library version string. */
+const char *q4_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* Q4_H */

@@ -71,12 +71,15 @@ def draw_x(M, K, config=0, matrix=0, dtype="bf16"):
 
 def round_e2m1(r: np.ndarray) -> np.ndarray:
     """Nearest E2M1 code for values r (any sign), ties to the even code,
-    saturating at magnitude 6; negative values keep the sign bit."""
-    a = np.abs(r.astype(np.float64))
-    lo = np.searchsorted(_E2M1_MID, a, side="left")
-    hi = np.searchsorted(_E2M1_MID, a, side="right")
-    idx = np.where((lo != hi) & (lo % 2 == 1), hi, lo)
-    idx = np.minimum(idx, 7).astype(np.uint8)
+    saturating at magnitude 6; negative values keep the sign bit.
+    A value above midpoint i moves past grid point i; a value exactly on
+    midpoint i goes up only when i is odd (grid i+1 has the even code)."""
+    a = np.abs(np.asarray(r, dtype=np.float32))
+    idx = np.zeros(a.shape, dtype=np.uint8)
+    for i, mid in enumerate(_E2M1_MID.astype(np.float32)):
+        idx += a > mid
+        if i % 2 == 1:
+            idx += a == mid
     return idx | (np.signbit(r).astype(np.uint8) << 3)
 
 
@@ -122,10 +125,10 @@ def quantize_nvfp4(W: np.ndarray):
     s_val = (amax_g / np.float32(6.0)) / scale2
     sb = round_e4m3fn(s_val.astype(np.float32))
     den = (_e4m3_grid_value(sb).astype(np.float32) * scale2).astype(np.float32)
-    with np.errstate(divide="ignore", invalid="ignore"):
-        r = np.where(den[:, :, None] > 0, g / den[:, :, None], np.float32(0.0)).astype(np.float32)
-    codes = round_e2m1(r).reshape(N, K)
-    codes = np.where(np.repeat(den, 16, axis=1) > 0, codes, 0).astype(np.uint8)
+    safe = np.where(den > 0, den, np.float32(1.0)).astype(np.float32)
+    codes = round_e2m1(g / safe[:, :, None])
+    codes[den <= 0] = 0
+    codes = codes.reshape(N, K)
     return _pack_nibbles_even_odd(codes), sb, np.float32(scale2)
 
 
@@ -133,8 +136,8 @@ def quantize_mxfp4(W: np.ndarray):
     """-> (payload u8 [N][K/2], E8M0 scales u8 [N][K/32])."""
     W = np.asarray(W, dtype=np.float32)
     N, K = W.shape
-    g = W.reshape(N, K // 32, 32).astype(np.float64)
-    amax = np.abs(g).max(axis=2)
+    g = W.reshape(N, K // 32, 32)
+    amax = np.abs(g).max(axis=2).astype(np.float64)
     _, ex = np.frexp(np.where(amax > 0, amax, 1.0))
     e = np.clip(ex - 1 - 2, -127, 127)
     e = np.where(amax > 0, e, -127)
@@ -273,3 +276,44 @@ def random_bytes(shape, seed, exclude=()):
             b[bad] = rng.integers(0, 256, size=int(bad.sum()), dtype=np.uint8)
             bad = np.isin(b, list(exclude))
     return b
+
+
+def make_layer(fmt: str, N: int, K: int, config: int = 0, matrix: int = 0, outliers=False,
+               row_scale=False, group: int = 128, act_order: bool = False, W=None) -> dict:
+    """One packed weight tensor of ``fmt`` drawn by the recipe above.
+
+    Returns host arrays: ``w`` (payload), ``scales``, ``zeros``, ``g_idx``
+    (None unless act_order), plus ``scale2`` and ``group``; dtypes match the
+    byte layouts (uint8 bytes, uint16 fp16 bits, int32 words)."""
+    if W is None:
+        W = draw_weights(N, K, config, matrix, outliers=outliers, row_scale=row_scale)
+    out = {"fmt": fmt, "N": N, "K": K, "scale2": 1.0, "group": group, "zeros": None,
+           "g_idx": None, "scales": None}
+    if fmt in ("nvfp4", "nvfp4_splithalf"):
+        p, s, s2 = quantize_nvfp4(W)
+        if fmt == "nvfp4_splithalf":
+            codes = np.empty((N, K), np.uint8)
+            codes[:, 0::2], codes[:, 1::2] = p & 15, p >> 4
+            g = codes.reshape(N, K // 16, 16)
+            p = (g[:, :, :8] | (g[:, :, 8:] << 4)).reshape(N, K // 2).astype(np.uint8)
+        out.update(w=p, scales=s, scale2=float(s2))
+    elif fmt == "mxfp4":
+        p, s = quantize_mxfp4(W)
+        out.update(w=p, scales=s)
+    elif fmt == "q4k":
+        out.update(w=quantize_q4k(W))
+    elif fmt == "q40":
+        out.update(w=quantize_q40(W))
+    elif fmt in ("gptq", "awq", "logical"):
+        g_idx = act_order_g_idx(K, group, seed_for(config, matrix, "mask") + 7) if act_order else None
+        codes, sb, z = quantize_affine(W, group, g_idx=g_idx)
+        if fmt == "gptq":
+            w, s, zz = pack_gptq(codes, sb, z)
+        elif fmt == "awq":
+            w, s, zz = pack_awq(codes, sb, z)
+        else:
+            w, s, zz = codes, sb, z
+        out.update(w=w, scales=s, zeros=zz, g_idx=g_idx)
+    else:
+        raise ValueError(fmt)
+    return out

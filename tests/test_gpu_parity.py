@@ -1,0 +1,330 @@
+"""CUDA path vs the CPU oracle, through the C ABI.
+
+Dequant and repack: bit-exact.  GEMV: |y_gpu - y_ref| <= 1e-5 * sum|w||x| + 1e-6
+against the oracle's f64 accumulation of the pinned weights.  Shapes span
+several tiles with ragged tails; the full-size workloads are checked on
+sampled rows.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from oracle import packing
+
+from _helpers import aux_for, to_device, to_oracle, within_tolerance, x_device
+
+torch = pytest.importorskip("torch")
+q4 = pytest.importorskip("bit_block_quantized_gb300")
+
+pytestmark = pytest.mark.gpu
+
+ROW_FORMATS = ["nvfp4", "mxfp4", "q4k", "q40"]
+ALL_GEMV = ROW_FORMATS + ["gptq", "awq"]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from bit_block_quantized_gb300 import build
+    build.build()
+    q4.lib()
+
+
+def shape_for(fmt, small=True):
+    """(N, K) spanning several CTA tiles with ragged tails."""
+    return {"nvfp4": (37, 4128), "mxfp4": (41, 2080), "q4k": (29, 1536), "q40": (33, 2080),
+            "gptq": (264, 1152), "awq": (264, 1152), "nvfp4_splithalf": (19, 528),
+            "logical": (72, 384)}[fmt]
+
+
+def gpu_dequant(layer, out_dtype=torch.float32):
+    d = to_device(layer)
+    N, K = layer["N"], layer["K"]
+    out = torch.empty((N, K), dtype=out_dtype, device="cuda")
+    aux = aux_for(layer, d, out_dtype=out_dtype)
+    q4.q4_dequant(layer["fmt"], d["w"], d["scales"], aux, out, N, K)
+    torch.cuda.synchronize()
+    return out
+
+
+def gpu_gemv(layer, xdev, M):
+    d = to_device(layer)
+    N, K = layer["N"], layer["K"]
+    y = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
+    aux = aux_for(layer, d, x_dtype=xdev.dtype)
+    q4.q4_gemv(layer["fmt"], d["w"], d["scales"], aux, xdev, y, M, N, K)
+    torch.cuda.synchronize()
+    return y.cpu().numpy()
+
+
+def bits_equal(a, b):
+    return np.array_equal(np.asarray(a, np.float32).view(np.uint32), np.asarray(b, np.float32).view(np.uint32))
+
+
+# ----------------------------------------------------------------- dequant
+
+@pytest.mark.parametrize("fmt", ["nvfp4", "mxfp4", "q4k", "q40", "gptq", "awq", "nvfp4_splithalf",
+                                 "logical"])
+def test_dequant_bit_exact(fmt):
+    N, K = shape_for(fmt)
+    layer = synth.make_layer(fmt, N, K, config=20, matrix=1, outliers=True)
+    ref = oracle.dequant(to_oracle(layer))
+    got = gpu_dequant(layer).cpu().numpy()
+    assert bits_equal(got, ref)
+    got16 = gpu_dequant(layer, torch.bfloat16).view(torch.int16).cpu().numpy().view(np.uint16)
+    assert np.array_equal(got16, oracle.round_bf16(ref))
+
+
+def test_dequant_gptq_act_order_bit_exact():
+    layer = synth.make_layer("gptq", 64, 512, config=20, matrix=2, act_order=True)
+    assert bits_equal(gpu_dequant(layer).cpu().numpy(), oracle.dequant(to_oracle(layer)))
+
+
+def test_nvfp4_every_finite_e4m3_scale_and_code():
+    """All 254 finite E4M3FN bytes x all 16 E2M1 codes, bit-for-bit
+    (the exhaustive sweep of Muser book, Chapter 7, section 7.2)."""
+    scales = np.array([b for b in range(256) if b not in (0x7F, 0xFF)], np.uint8)
+    N = scales.size
+    row = np.frombuffer(bytes.fromhex("1032547698badcfe"), np.uint8)
+    for scale2 in (0.25, 1.0, 3.0e-5):
+        layer = {"fmt": "nvfp4", "N": N, "K": 16, "w": np.tile(row, (N, 1)), "scales": scales[:, None].copy(),
+                 "zeros": None, "g_idx": None, "group": 128, "scale2": scale2}
+        assert bits_equal(gpu_dequant(layer).cpu().numpy(), oracle.dequant(to_oracle(layer)))
+
+
+def test_mxfp4_every_e8m0_scale():
+    scales = np.arange(255, dtype=np.uint8)
+    row = np.tile(np.frombuffer(bytes.fromhex("1032547698badcfe"), np.uint8), 2)
+    layer = {"fmt": "mxfp4", "N": 255, "K": 32, "w": np.tile(row, (255, 1)), "scales": scales[:, None].copy(),
+             "zeros": None, "g_idx": None, "group": 128, "scale2": 1.0}
+    got = gpu_dequant(layer).cpu().numpy()
+    ref = oracle.dequant(to_oracle(layer))
+    assert bits_equal(got, ref)            # includes the +-inf overflow rows (b >= 253)
+
+
+@pytest.mark.parametrize("fmt", ["nvfp4", "mxfp4", "q4k", "q40", "nvfp4_splithalf"])
+def test_dequant_random_bytes(fmt):
+    """Uniform random payload bytes (every code), random valid scales and
+    block headers, bit-for-bit."""
+    N, K = 23, 512
+    rng = np.random.default_rng(11)
+    layer = {"fmt": fmt, "N": N, "K": K, "zeros": None, "g_idx": None, "group": 128, "scale2": 0.0371}
+    if fmt in ("nvfp4", "mxfp4", "nvfp4_splithalf"):
+        layer["w"] = synth.random_bytes((N, K // 2), 1)
+        nsc = K // 16 if fmt != "mxfp4" else K // 32
+        excl = (0x7F, 0xFF) if fmt != "mxfp4" else (0xFF, 0xFE, 0xFD)
+        layer["scales"] = synth.random_bytes((N, nsc), 2, exclude=excl)
+    elif fmt == "q4k":
+        b = synth.random_bytes((N, K // 256, 144), 3)
+        h = rng.uniform(-2, 2, (N, K // 256, 2)).astype(np.float16).view(np.uint8).reshape(N, K // 256, 4)
+        b[:, :, :4] = h
+        layer["w"], layer["scales"] = b, None
+    else:
+        b = synth.random_bytes((N, K // 32, 18), 4)
+        b[:, :, :2] = rng.uniform(-2, 2, (N, K // 32)).astype(np.float16).view(np.uint8).reshape(N, K // 32, 2)
+        layer["w"], layer["scales"] = b, None
+    assert bits_equal(gpu_dequant(layer).cpu().numpy(), oracle.dequant(to_oracle(layer)))
+
+
+# -------------------------------------------------------------------- GEMV
+
+def check_gemv(layer, M, config=20, xdtype="bf16", rows=None):
+    K = layer["K"]
+    xbits, xf = synth.draw_x(M, K, config=config, matrix=5, dtype=xdtype)
+    y = gpu_gemv(layer, x_device(xbits), M)
+    ref, bound = oracle.gemv(to_oracle(layer), xf, rows=rows)
+    if rows is not None:
+        y = y[:, rows]
+    ok, worst = within_tolerance(y, ref, bound)
+    assert ok, f"worst error / tolerance = {worst}"
+    return worst
+
+
+@pytest.mark.parametrize("fmt", ALL_GEMV)
+def test_gemv_batch1(fmt):
+    N, K = shape_for(fmt)
+    layer = synth.make_layer(fmt, N, K, config=21, matrix=1, outliers=True)
+    check_gemv(layer, 1)
+    check_gemv(layer, 1, xdtype="f32")
+
+
+@pytest.mark.parametrize("fmt", ALL_GEMV)
+@pytest.mark.parametrize("M", [2, 4, 8])
+def test_gemv_small_batch(fmt, M):
+    N, K = shape_for(fmt)
+    layer = synth.make_layer(fmt, N, K, config=22, matrix=M, row_scale=True)
+    check_gemv(layer, M)
+
+
+def test_gemv_general_paths():
+    # NVFP4 with K % 32 == 16 and act-order GPTQ take the general kernel.
+    check_gemv(synth.make_layer("nvfp4", 21, 1040, config=23, matrix=1), 1)
+    check_gemv(synth.make_layer("gptq", 40, 512, config=23, matrix=2, act_order=True), 1)
+    check_gemv(synth.make_layer("gptq", 40, 512, config=23, matrix=3, act_order=True), 3)
+    check_gemv(synth.make_layer("nvfp4", 5, 16, config=23, matrix=4), 1)
+
+
+@pytest.mark.parametrize("fmt", ALL_GEMV)
+def test_gemv_random_bytes_edge(fmt):
+    """Random codes everywhere; single row; the all-zero x gives exactly 0."""
+    N, K = (8, 256) if fmt in ("gptq", "awq") else (1, 512)
+    layer = synth.make_layer(fmt, N, K, config=24, matrix=1)
+    check_gemv(layer, 1)
+    d = to_device(layer)
+    y = torch.full((1, N), 7.0, device="cuda")
+    xz = torch.zeros((1, K), dtype=torch.bfloat16, device="cuda")
+    q4.q4_gemv(fmt, d["w"], d["scales"], aux_for(layer, d, x_dtype=torch.bfloat16), xz, y, 1, N, K)
+    torch.cuda.synchronize()
+    assert torch.all(y == 0)
+
+
+def test_gemv_one_hot_gives_exact_column():
+    layer = synth.make_layer("nvfp4", 64, 4096, config=25, matrix=1)
+    ref = oracle.dequant(to_oracle(layer))
+    for k in (0, 17, 4095):
+        x = torch.zeros((1, 4096), dtype=torch.bfloat16, device="cuda")
+        x[0, k] = 1.0
+        y = gpu_gemv(layer, x, 1)[0]
+        assert bits_equal(y, ref[:, k])
+
+
+# Full-size workloads (the decode-GEMV study's layer shapes), sampled rows.
+FULL = [
+    ("nvfp4", 1024, 4096, dict(), 0),                        # NVFP4 1024 x 4096
+    ("q4k", 4096, 4096, dict(), 1),                          # Q4_K 4096 x 4096
+    ("mxfp4", 4096, 11008, dict(outliers=True), 2),          # MXFP4 4096 x 11008
+    ("q40", 4096, 11008, dict(outliers=True), 2),            # Q4_0 4096 x 11008
+    ("gptq", 4096, 11008, dict(outliers=True), 2),
+    ("awq", 4096, 11008, dict(outliers=True), 2),
+    ("nvfp4", 14336, 4096, dict(row_scale=True), 5),         # MLP gate/up of the 4096x14336 set
+    ("nvfp4", 4096, 14336, dict(row_scale=True), 5),         # MLP down
+]
+
+
+@pytest.mark.parametrize("fmt,N,K,kw,config", FULL)
+def test_gemv_full_size_sampled_rows(fmt, N, K, kw, config):
+    layer = synth.make_layer(fmt, N, K, config=config, matrix=0, **kw)
+    rows = np.unique(np.concatenate([[0, 1, N - 1], np.random.default_rng(config).integers(0, N, 40)]))
+    for M in (1, 4):
+        check_gemv(layer, M, config=config, rows=rows)
+
+
+# ------------------------------------------------------------------ repack
+
+def gpu_repack(layer, dst, perm=False):
+    N, K = layer["N"], layer["K"]
+    d = to_device(layer)
+    group = 32 if layer["fmt"] == "q40" else layer["group"]
+    if dst == "gptq":
+        w = torch.empty((K // 8, N), dtype=torch.int32, device="cuda")
+        z = torch.empty((K // group, N // 8), dtype=torch.int32, device="cuda")
+    elif dst == "awq":
+        w = torch.empty((K, N // 8), dtype=torch.int32, device="cuda")
+        z = torch.empty((K // group, N // 8), dtype=torch.int32, device="cuda")
+    elif dst == "logical":
+        w = torch.empty((K, N), dtype=torch.uint8, device="cuda")
+        z = torch.empty((K // group, N), dtype=torch.uint8, device="cuda")
+    else:
+        w = torch.empty((N, K // 2), dtype=torch.uint8, device="cuda")
+        z = None
+    if dst in ("nvfp4", "nvfp4_splithalf"):
+        s = torch.empty((N, K // 16), dtype=torch.uint8, device="cuda")
+    else:
+        s = torch.empty((K // group, N), dtype=torch.int16, device="cuda")
+    p = torch.empty((K,), dtype=torch.int32, device="cuda") if perm else None
+    rc = q4.q4_repack(layer["fmt"], d["w"], d["scales"], aux_for(layer, d), dst, w, s, z, p, N, K,
+                      check=False)
+    torch.cuda.synchronize()
+    out = [w.cpu().numpy(), s.cpu().numpy(), None if z is None else z.cpu().numpy(),
+           None if p is None else p.cpu().numpy()]
+    return rc, out
+
+
+@pytest.mark.parametrize("src,dst", [("gptq", "awq"), ("awq", "gptq"), ("gptq", "logical"),
+                                     ("logical", "gptq"), ("awq", "logical"), ("q40", "gptq"),
+                                     ("q40", "awq"), ("q40", "logical"), ("gptq", "gptq"),
+                                     ("nvfp4", "nvfp4_splithalf"), ("nvfp4_splithalf", "nvfp4")])
+def test_repack_bit_exact(src, dst):
+    N, K = (72, 512) if src != "q40" else (40, 512)
+    layer = synth.make_layer(src, N, K, config=26, matrix=1, outliers=True)
+    rc, (w, s, z, _) = gpu_repack(layer, dst)
+    assert rc == q4.Q4_OK
+    ew, es, ez, eperm = packing.repack(src, dst, N, K, layer["w"], layer["scales"], layer["zeros"],
+                                       layer["group"])
+    assert eperm is None
+    assert np.array_equal(w.view(np.uint8), np.ascontiguousarray(ew).view(np.uint8))
+    assert np.array_equal(s.view(np.uint8), np.ascontiguousarray(es).view(np.uint8))
+    if ez is not None:
+        assert np.array_equal(z.view(np.uint8), np.ascontiguousarray(ez).view(np.uint8))
+    # the target dequantizes to the same weights, bit for bit (on the GPU too)
+    tgt = dict(layer, fmt=dst, w=w, scales=s, zeros=z, group=32 if src == "q40" else layer["group"])
+    if s.dtype == np.int16:
+        tgt["scales"] = s.view(np.uint16)
+    assert bits_equal(gpu_dequant(tgt).cpu().numpy(), oracle.dequant(to_oracle(layer)))
+
+
+def test_repack_act_order_to_awq():
+    N, K = 48, 1024
+    layer = synth.make_layer("gptq", N, K, config=27, matrix=1, act_order=True)
+    rc, (w, s, z, perm) = gpu_repack(layer, "awq", perm=True)
+    assert rc == q4.Q4_OK
+    ew, es, ez, eperm = packing.repack("gptq", "awq", N, K, layer["w"], layer["scales"], layer["zeros"],
+                                       layer["group"], g_idx=layer["g_idx"])
+    assert np.array_equal(perm, eperm)
+    assert np.array_equal(w, ew) and np.array_equal(s.view(np.uint16), es) and np.array_equal(z, ez)
+
+
+def test_repack_rejections():
+    # a non-trivial g_idx without perm_out, and a zero the target cannot hold
+    layer = synth.make_layer("gptq", 16, 512, config=28, matrix=1, act_order=True)
+    rc, _ = gpu_repack(layer, "awq", perm=False)
+    assert rc == q4.Q4_EINVAL
+    lg = synth.make_layer("logical", 16, 256, config=28, matrix=2)
+    lg["zeros"] = lg["zeros"].copy()
+    lg["zeros"][0, 3] = 0
+    rc, _ = gpu_repack(lg, "gptq")
+    assert rc == q4.Q4_ERANGE
+    lg["zeros"][0, 3] = 16
+    rc, _ = gpu_repack(lg, "awq")
+    assert rc == q4.Q4_ERANGE
+    rc, _ = gpu_repack(lg, "gptq")
+    assert rc == q4.Q4_OK
+
+
+# ---------------------------------------------------------------- validate
+
+@pytest.mark.parametrize("fmt", ["nvfp4", "mxfp4", "q4k", "q40", "gptq", "awq"])
+def test_validate_counts_nan_scales(fmt):
+    N, K = shape_for(fmt)
+    layer = synth.make_layer(fmt, N, K, config=29, matrix=1)
+    cnt = torch.zeros(2, dtype=torch.int64, device="cuda")
+
+    def run(lay):
+        d = to_device(lay)
+        return q4.q4_validate(fmt, d["w"], d["scales"], aux_for(lay, d), N, K, cnt)
+    assert run(layer) == q4.Q4_OK and int(cnt[0]) == 0
+    bad = dict(layer)
+    if fmt in ("nvfp4", "mxfp4"):
+        s = layer["scales"].copy()
+        s.flat[[0, 5, s.size - 1]] = 0xFF
+        if fmt == "nvfp4":
+            s.flat[7] = 0x7F
+        bad["scales"] = s
+        want = 4 if fmt == "nvfp4" else 3
+        assert oracle.count_nan_scales(fmt, s) == want
+    elif fmt in ("q4k", "q40"):
+        w = layer["w"].copy()
+        w[0, 0, 0:2] = np.array([np.float16(np.nan)]).view(np.uint8)
+        w[-1, -1, 0:2] = np.array([np.float16(np.inf)]).view(np.uint8)
+        bad["w"] = w
+        want = 2
+    else:
+        s = layer["scales"].copy()
+        s.flat[[1, 9]] = np.array([np.float16(np.nan)]).view(np.uint16)[0]
+        bad["scales"] = s
+        want = 2
+    assert run(bad) == q4.Q4_ENAN and int(cnt[0]) == want
+    if fmt == "nvfp4":
+        d = to_device(layer)
+        assert q4.q4_validate(fmt, d["w"], d["scales"], q4.make_aux(scale2=float("nan"), fmt=fmt),
+                              N, K, cnt) == q4.Q4_ESCALE2
