@@ -36,7 +36,7 @@ SET = [("gate", 14336, 4096), ("up", 14336, 4096), ("down", 4096, 14336)]
 CONFIG_ID = 5          # seed block of this workload's synthetic draws
 NOMINAL_HBM_GBS = 7900.0
 FALLBACK_HBM_GBS = 6800.0
-DOMINANT = "gemv_rows_m1<NVFP4, bf16, R=4, TMAX=128> (gate/up, 14336x4096)"
+DOMINANT = "gemv_mma_nvfp4<bf16, MT=1> (gate/up, 14336x4096)"
 
 
 def parse():
@@ -63,7 +63,7 @@ def measured_hbm_peak():
 
 def source_sha():
     h = hashlib.sha256()
-    for rel in ("bit_block_quantized_gb300/csrc/gemv.cu", "bit_block_quantized_gb300/csrc/q4_internal.cuh"):
+    for rel in ("bit_block_quantized_gb300/csrc/gemv_mma.cu", "bit_block_quantized_gb300/csrc/q4_internal.cuh"):
         with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -72,7 +72,7 @@ def source_sha():
 def profiled_traffic():
     """DRAM bytes per launch of the dominant kernel from the committed ncu
     summary, only if it was taken on the current kernel source."""
-    p = os.path.join(ROOT, "profiles", "gemv_rows_m1_nvfp4_14336x4096.md")
+    p = os.path.join(ROOT, "profiles", "gemv_mma_nvfp4_14336x4096.md")
     try:
         text = open(p).read()
     except OSError:

@@ -13,13 +13,16 @@ cudaError_t launch_gemm_tc(const Tensor &, const void *, q4_dtype, float *, int6
     return cudaSuccess;
 }
 
+int gemv_read_and_clear_error();
+
 int read_and_clear_device_error() {
     int v = 0;
     const int zero = 0;
     if (cudaDeviceSynchronize() != cudaSuccess) return Q4_ECUDA;
     if (cudaMemcpyFromSymbol(&v, g_device_error, sizeof(v)) != cudaSuccess) return Q4_ECUDA;
     if (cudaMemcpyToSymbol(g_device_error, &zero, sizeof(zero)) != cudaSuccess) return Q4_ECUDA;
-    return v;
+    const int g = gemv_read_and_clear_error();
+    return v ? v : g;
 }
 
 }  // namespace q4

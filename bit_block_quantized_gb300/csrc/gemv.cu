@@ -19,6 +19,8 @@
 // g_idx) runs a general warp-per-row kernel over the per-element decoders.
 #include <cooperative_groups.h>
 
+#include <type_traits>
+
 #include "q4_internal.cuh"
 
 namespace cg = cooperative_groups;
@@ -39,6 +41,12 @@ template <> struct Slice<Q4_NVFP4> {
         r.p = ldg_stream16(t.w + n * (t.K >> 1) + 16 * s);
         r.s = ldg_stream2(t.scales + n * (t.K >> 4) + 2 * s);
     }
+    __device__ static void lds(const uint8_t *prow, const uint8_t *srow, int s, Regs &r) {
+        r.p = *reinterpret_cast<const uint4 *>(prow + 16 * s);
+        r.s = *reinterpret_cast<const uint16_t *>(srow + 2 * s);
+    }
+    static int64_t row_bytes(int64_t K) { return K / 2; }
+    static int64_t scale_row_bytes(int64_t K) { return K / 16; }
     __device__ static float dot(const Regs &r, const float (&xs)[32]) {
         const uint32_t wd[4] = {r.p.x, r.p.y, r.p.z, r.p.w};
         float2 a0 = make_float2(0.f, 0.f), a1 = make_float2(0.f, 0.f);
@@ -51,6 +59,25 @@ template <> struct Slice<Q4_NVFP4> {
         float2 sc = e4m3x2_f32(r.s);
         return fmaf(a1.x + a1.y, sc.y, (a0.x + a0.y) * sc.x);
     }
+    // x as 16 f16x2 (scaled by an exact power of two): one hardware E2M1 pair
+    // convert per byte and one mixed f16*f16+f32 FMA per weight.
+    __device__ static float dot16(const Regs &r, const uint32_t (&xh)[16]) {
+        uint32_t h[16];
+        e2m1x8_h2(r.p.x, h[0], h[1], h[2], h[3]);
+        e2m1x8_h2(r.p.y, h[4], h[5], h[6], h[7]);
+        e2m1x8_h2(r.p.z, h[8], h[9], h[10], h[11]);
+        e2m1x8_h2(r.p.w, h[12], h[13], h[14], h[15]);
+        float a0 = 0.f, a1 = 0.f, b0 = 0.f, b1 = 0.f;
+#pragma unroll
+        for (int j = 0; j < 8; j++) {
+            a0 = fma_f16_f32<0>(h[j], xh[j], a0);
+            a1 = fma_f16_f32<1>(h[j], xh[j], a1);
+            b0 = fma_f16_f32<0>(h[8 + j], xh[8 + j], b0);
+            b1 = fma_f16_f32<1>(h[8 + j], xh[8 + j], b1);
+        }
+        const float2 sc = e4m3x2_f32(r.s);
+        return fmaf(b0 + b1, sc.y, (a0 + a1) * sc.x);
+    }
     __device__ static float epilogue(float v, const Tensor &t) { return v * t.scale2; }
 };
 
@@ -62,6 +89,12 @@ template <> struct Slice<Q4_MXFP4> {
         r.p = ldg_stream16(t.w + n * (t.K >> 1) + 16 * s);
         r.s = ldg_stream1(t.scales + n * (t.K >> 5) + s);
     }
+    __device__ static void lds(const uint8_t *prow, const uint8_t *srow, int s, Regs &r) {
+        r.p = *reinterpret_cast<const uint4 *>(prow + 16 * s);
+        r.s = srow[s];
+    }
+    static int64_t row_bytes(int64_t K) { return K / 2; }
+    static int64_t scale_row_bytes(int64_t K) { return K / 32; }
     __device__ static float dot(const Regs &r, const float (&xs)[32]) {
         const uint32_t wd[4] = {r.p.x, r.p.y, r.p.z, r.p.w};
         float2 a0 = make_float2(0.f, 0.f), a1 = make_float2(0.f, 0.f);
@@ -72,6 +105,22 @@ template <> struct Slice<Q4_MXFP4> {
                   make_float2(xs[2 * b + 2], xs[2 * b + 3]));
         }
         return ((a0.x + a0.y) + (a1.x + a1.y)) * e8m0_f32(r.s);
+    }
+    __device__ static float dot16(const Regs &r, const uint32_t (&xh)[16]) {
+        uint32_t h[16];
+        e2m1x8_h2(r.p.x, h[0], h[1], h[2], h[3]);
+        e2m1x8_h2(r.p.y, h[4], h[5], h[6], h[7]);
+        e2m1x8_h2(r.p.z, h[8], h[9], h[10], h[11]);
+        e2m1x8_h2(r.p.w, h[12], h[13], h[14], h[15]);
+        float a0 = 0.f, a1 = 0.f, b0 = 0.f, b1 = 0.f;
+#pragma unroll
+        for (int j = 0; j < 8; j++) {
+            a0 = fma_f16_f32<0>(h[j], xh[j], a0);
+            a1 = fma_f16_f32<1>(h[j], xh[j], a1);
+            b0 = fma_f16_f32<0>(h[8 + j], xh[8 + j], b0);
+            b1 = fma_f16_f32<1>(h[8 + j], xh[8 + j], b1);
+        }
+        return ((a0 + a1) + (b0 + b1)) * e8m0_f32(r.s);
     }
     __device__ static float epilogue(float v, const Tensor &) { return v; }
 };
@@ -92,6 +141,18 @@ template <> struct Slice<Q4_Q40> {
         r.e16 = ldg_stream2(t.w + o + 16);
         r.odd = (uint32_t)(o & 2);
     }
+    __device__ static void lds(const uint8_t *prow, const uint8_t *, int s, Regs &r) {
+        const uint16_t *b = reinterpret_cast<const uint16_t *>(prow + 18 * s);
+        r.w0 = b[0] | ((uint32_t)b[1] << 16);
+        r.w1 = b[2] | ((uint32_t)b[3] << 16);
+        r.w2 = b[4] | ((uint32_t)b[5] << 16);
+        r.w3 = b[6] | ((uint32_t)b[7] << 16);
+        r.e16 = b[8];
+        r.e14 = 0;
+        r.odd = 0;
+    }
+    static int64_t row_bytes(int64_t K) { return K / 32 * 18; }
+    static int64_t scale_row_bytes(int64_t) { return 0; }
     __device__ static float dot(const Regs &r, const float (&xs)[32]) {
         uint32_t d, q[4];
         if (r.odd) {   // block starts 2 bytes into w0
@@ -137,6 +198,14 @@ template <> struct Slice<Q4_Q4K> {
         r.hdr = ldg_stream16(blk);
         r.qs = ldg_stream16(blk + 16 + 32 * c + 16 * h);
     }
+    __device__ static void lds(const uint8_t *prow, const uint8_t *, int s, Regs &r) {
+        int b = s >> 3, c = (s >> 1) & 3, h = s & 1;
+        const uint8_t *blk = prow + b * 144;
+        r.hdr = *reinterpret_cast<const uint4 *>(blk);
+        r.qs = *reinterpret_cast<const uint4 *>(blk + 16 + 32 * c + 16 * h);
+    }
+    static int64_t row_bytes(int64_t K) { return K / 256 * 144; }
+    static int64_t scale_row_bytes(int64_t) { return 0; }
     __device__ static uint32_t meta_byte(const uint4 &h, int i) {
         uint32_t w = i < 4 ? h.y : (i < 8 ? h.z : h.w);
         return (w >> (8 * (i & 3))) & 0xffu;
@@ -268,6 +337,174 @@ __global__ void __launch_bounds__(TMAX) gemv_rows_m1(Tensor t, const XT *__restr
         buf ^= 1;
 #pragma unroll
         for (int r = 0; r < R; r++) cur[r] = nxt[r];
+    }
+}
+
+template <int FMT, typename XT> struct UseF16 { static constexpr bool value = false; };
+template <> struct UseF16<Q4_NVFP4, __nv_bfloat16> { static constexpr bool value = true; };
+template <> struct UseF16<Q4_MXFP4, __nv_bfloat16> { static constexpr bool value = true; };
+
+template <int FMT, typename XT, bool F16> struct SliceRun {
+    template <int A, int B>
+    __device__ static float run(const typename Slice<FMT>::Regs &r, const float (&xs)[A], const uint32_t (&)[B],
+                                float, bool, const XT *, int s) {
+        return SliceDot<FMT>::run(r, reinterpret_cast<const float(&)[32]>(xs), s);
+    }
+};
+template <int FMT, typename XT> struct SliceRun<FMT, XT, true> {
+    template <int A, int B>
+    __device__ static float run(const typename Slice<FMT>::Regs &r, const float (&)[A], const uint32_t (&xh)[B],
+                                float xinv, bool exact16, const XT *x, int s) {
+        if (exact16) return Slice<FMT>::dot16(r, reinterpret_cast<const uint32_t(&)[16]>(xh)) * xinv;
+        float xs[32];
+#pragma unroll
+        for (int i = 0; i < 32; i++) xs[i] = x_to_f32<XT>(x[Slice<FMT>::kpos(s, i)]);
+        return Slice<FMT>::dot(r, xs);
+    }
+};
+
+// ------------------------------------------- batch 1, bulk-copy pipeline
+// The same slice-stationary consumers, fed by a dedicated producer warp that
+// streams whole row tiles (payload rows, then scale rows: contiguous in HBM)
+// into a ring of shared-memory stages with 1-D bulk copies (TMA engine,
+// completion on an mbarrier).  Many KB stay in flight per SM independent of
+// the consumers' registers.  The per-tile cross-warp reduction goes through a
+// per-stage "done" mbarrier that only warp 0 waits on, so the other warps run
+// ahead.  Every wait is bounded: on timeout the kernel records Q4_ETIMEOUT,
+// drains the copies it issued and returns.
+__device__ int g_gemv_error;
+
+template <int FMT, typename XT, int R>
+__global__ void __launch_bounds__(1024) gemv_rows_tma(Tensor t, const XT *__restrict__ x,
+                                                      float *__restrict__ y, int ntiles, int tiles_per_cta,
+                                                      int stages, uint32_t prb, uint32_t srb) {
+    using S = Slice<FMT>;
+    extern __shared__ __align__(128) uint8_t tma_smem[];
+    uint8_t *smem = tma_smem;
+    const uint32_t stage_bytes = (uint32_t)R * (prb + srb);
+    const int nwc = (int)(blockDim.x >> 5) - 1;        // consumer warps
+    const int rows_cta = tiles_per_cta * R;
+    uint8_t *data = smem;
+    float *red = reinterpret_cast<float *>(smem + (size_t)stages * stage_bytes);   // [nwc][rows_cta]
+    uint64_t *bars = reinterpret_cast<uint64_t *>(red + ((nwc * rows_cta + 1) & ~1));
+    uint64_t *full = bars, *empty = bars + stages;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int tile0 = blockIdx.x * tiles_per_cta;
+    const int tile1 = min(ntiles, tile0 + tiles_per_cta);
+
+    if (threadIdx.x == 0) {
+        for (int st = 0; st < stages; st++) {
+            mbar_init(&full[st], 1);
+            mbar_init(&empty[st], nwc);
+        }
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    if (warp == nwc) {                                   // producer warp
+        if (lane == 0) {
+            int it = 0;
+            for (int tile = tile0; tile < tile1; ++tile, ++it) {
+                const int st = it % stages, u = it / stages;
+                if (u > 0 && !mbar_wait_bounded(&empty[st], (u - 1) & 1)) {
+                    atomicExch(&g_gemv_error, Q4_ETIMEOUT);
+                    break;
+                }
+                const int64_t n0 = (int64_t)tile * R;
+                const uint32_t rows = (uint32_t)((t.N - n0) < R ? (t.N - n0) : R);
+                uint8_t *pb = data + (size_t)st * stage_bytes;
+                mbar_arrive_expect_tx(&full[st], rows * (prb + srb));
+                bulk_g2s(pb, t.w + n0 * prb, rows * prb, &full[st]);
+                if (srb) bulk_g2s(pb + (size_t)R * prb, t.scales + n0 * srb, rows * srb, &full[st]);
+            }
+            // never leave with a copy in flight into this CTA's shared memory
+            for (int j = (it > stages ? it - stages : 0); j < it; j++)
+                if (!mbar_wait_bounded(&full[j % stages], (j / stages) & 1))
+                    atomicExch(&g_gemv_error, Q4_ETIMEOUT);
+        }
+        return;
+    }
+
+    const int NS = (int)(t.K >> 5);
+    const int s = threadIdx.x;
+    const bool active = s < NS;
+    constexpr bool F16 = UseF16<FMT, XT>::value;
+    // Activations of this thread's slice: f32 registers, or (bf16 input on the
+    // FP4 formats) f16x2 registers holding x * 2^e exactly, e chosen from the
+    // slice's largest magnitude; if any value would not survive exactly the
+    // thread computes in f32 from x re-read from memory (same result).
+    float xs[F16 ? 1 : 32];
+    uint32_t xh[F16 ? 16 : 1];
+    float xinv = 1.0f;
+    bool exact16 = true;
+    if (F16) {
+        float tmp[32];
+        float amax = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 32; i++) {
+            tmp[i] = active ? x_to_f32<XT>(x[S::kpos(s, i)]) : 0.0f;
+            amax = fmaxf(amax, fabsf(tmp[i]));
+        }
+        const int e = (int)((__float_as_uint(amax) >> 23) & 255u) - 127;   // amax in [2^e, 2^(e+1))
+        float scale = 1.0f;
+        if (amax > 0.0f) {
+            if (e < -100 || e > 100) exact16 = false;
+            else {
+                scale = __uint_as_float((uint32_t)(127 + 12 - e) << 23);      // max |x * scale| < 2^13
+                xinv = __uint_as_float((uint32_t)(127 - 12 + e) << 23);
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < 16; j++) {
+            const float v0 = tmp[2 * j] * scale, v1 = tmp[2 * j + 1] * scale;
+            const __half2 hh = __floats2half2_rn(v0, v1);
+            const float2 back = __half22float2(hh);
+            exact16 = exact16 && back.x == v0 && back.y == v1;
+            xh[j] = *reinterpret_cast<const uint32_t *>(&hh);
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < 32; i++) xs[(F16 ? 0 : i)] = active ? x_to_f32<XT>(x[S::kpos(s, i)]) : 0.0f;
+    }
+
+    // Consumers never wait on one another inside the loop: each warp leaves
+    // its per-row partial sums in shared memory and releases the stage.
+    int it = 0;
+    for (int tile = tile0; tile < tile1; ++tile, ++it) {
+        const int st = it % stages;
+        const uint32_t ph = (uint32_t)(it / stages) & 1u;
+        if (!mbar_wait_bounded(&full[st], ph)) {
+            atomicExch(&g_gemv_error, Q4_ETIMEOUT);
+            break;
+        }
+        const uint8_t *pb = data + (size_t)st * stage_bytes;
+        const uint8_t *sb = pb + (size_t)R * prb;
+        float acc[R];
+#pragma unroll
+        for (int r = 0; r < R; r++) {
+            const int64_t n = (int64_t)tile * R + r;
+            acc[r] = 0.0f;
+            if (active && n < t.N) {
+                typename S::Regs rg;
+                S::lds(pb + r * prb, sb + r * srb, s, rg);
+                acc[r] = SliceRun<FMT, XT, F16>::run(rg, xs, xh, xinv, exact16, x, s);
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[st]);     // the stage's bytes are no longer needed
+        const float v = warp_reduce_rows<R>(acc, lane);
+        if ((lane & (32 / R - 1)) == 0) red[warp * rows_cta + it * R + lane / (32 / R)] = v;
+    }
+    // one barrier among the consumer warps, then a fixed-order sum per row
+    asm volatile("bar.sync 1, %0;" ::"r"(nwc * 32) : "memory");
+    const int64_t row0 = (int64_t)tile0 * R;
+    for (int i = threadIdx.x; i < rows_cta; i += nwc * 32) {
+        const int64_t n = row0 + i;
+        if (n < t.N && (tile0 + i / R) < tile1) {
+            float sum = 0.0f;
+            for (int w = 0; w < nwc; w++) sum += red[w * rows_cta + i];
+            y[n] = S::epilogue(sum, t);
+        }
     }
 }
 
@@ -482,6 +719,58 @@ cudaError_t rows_m1(const Tensor &t, const XT *x, float *y, cudaStream_t s) {
     return run_rows_m1<FMT, XT, 2, 1024>(t, x, y, s);
 }
 
+template <int FMT, typename XT, int R>
+cudaError_t run_rows_tma(const Tensor &t, const XT *x, float *y, cudaStream_t s) {
+    using S = Slice<FMT>;
+    const int NS = (int)(t.K >> 5);
+    const int threads = (NS + 31) / 32 * 32 + 32;
+    const int nwc = threads / 32 - 1;
+    const uint32_t prb = (uint32_t)S::row_bytes(t.K), srb = (uint32_t)S::scale_row_bytes(t.K);
+    const uint32_t stage_bytes = (uint32_t)R * (prb + srb);
+    int stages = (int)(28 * 1024 / stage_bytes);
+    stages = stages < 3 ? 3 : (stages > 8 ? 8 : stages);
+    auto kern = gemv_rows_tma<FMT, XT, R>;
+    static bool attr_set[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (!attr_set[dev & 63]) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+        if (e != cudaSuccess) return e;
+        attr_set[dev & 63] = true;
+    }
+    const int ntiles = (int)((t.N + R - 1) / R);
+    auto smem_for = [&](int tpc) {
+        return (size_t)stages * stage_bytes + sizeof(float) * (size_t)((nwc * tpc * R + 1) & ~1) +
+               2 * (size_t)stages * sizeof(uint64_t);
+    };
+    // occupancy with a nominal partial-sum area, then balance contiguous tile ranges
+    const int bps = max_blocks(kern, threads, smem_for(16));
+    int grid = bps * sm_count();
+    if (grid > ntiles) grid = ntiles;
+    const int tpc = (ntiles + grid - 1) / grid;
+    grid = (ntiles + tpc - 1) / tpc;
+    if (smem_for(tpc) > 190 * 1024) return rows_m1<FMT, XT>(t, x, y, s);   // very tall matrices
+    kern<<<grid, threads, smem_for(tpc), s>>>(t, x, y, ntiles, tpc, stages, prb, srb);
+    return cudaGetLastError();
+}
+
+template <int FMT, typename XT>
+bool tma_ok(const Tensor &t) {
+    using S = Slice<FMT>;
+    const int64_t NS = t.K >> 5;
+    return t.K % 32 == 0 && NS <= 992 && S::row_bytes(t.K) % 16 == 0 && S::scale_row_bytes(t.K) % 16 == 0 &&
+           (((uintptr_t)t.w | (uintptr_t)t.scales) & 15) == 0;
+}
+
+template <int FMT, typename XT>
+cudaError_t rows_batch1(const Tensor &t, const XT *x, float *y, cudaStream_t s) {
+    if (tma_ok<FMT, XT>(t)) {
+        if ((t.K >> 5) <= 256) return run_rows_tma<FMT, XT, 4>(t, x, y, s);
+        return run_rows_tma<FMT, XT, 2>(t, x, y, s);
+    }
+    return rows_m1<FMT, XT>(t, x, y, s);
+}
+
 template <int FMT, typename XT>
 cudaError_t general(const Tensor &t, const XT *x, float *y, int64_t M, cudaStream_t s) {
     const int64_t items = t.N * ((M + 7) / 8);
@@ -544,16 +833,18 @@ cudaError_t kmajor(const Tensor &t, const XT *x, float *y, int64_t M, cudaStream
 
 template <typename XT>
 cudaError_t dispatch(const Tensor &t, const XT *x, float *y, int64_t M, cudaStream_t s) {
+    if (std::is_same<XT, __nv_bfloat16>::value && gemv_mma_eligible(t, M))
+        return launch_gemv_mma(t, x, Q4_DT_BF16, y, M, s);
     const bool fast_rows = (M == 1) && (t.K % 32 == 0) && (t.K <= 32768);
     switch (t.fmt) {
     case Q4_NVFP4:
-        return fast_rows ? rows_m1<Q4_NVFP4, XT>(t, x, y, s) : general<Q4_NVFP4, XT>(t, x, y, M, s);
+        return fast_rows ? rows_batch1<Q4_NVFP4, XT>(t, x, y, s) : general<Q4_NVFP4, XT>(t, x, y, M, s);
     case Q4_MXFP4:
-        return fast_rows ? rows_m1<Q4_MXFP4, XT>(t, x, y, s) : general<Q4_MXFP4, XT>(t, x, y, M, s);
+        return fast_rows ? rows_batch1<Q4_MXFP4, XT>(t, x, y, s) : general<Q4_MXFP4, XT>(t, x, y, M, s);
     case Q4_Q40:
-        return fast_rows ? rows_m1<Q4_Q40, XT>(t, x, y, s) : general<Q4_Q40, XT>(t, x, y, M, s);
+        return fast_rows ? rows_batch1<Q4_Q40, XT>(t, x, y, s) : general<Q4_Q40, XT>(t, x, y, M, s);
     case Q4_Q4K:
-        return fast_rows ? rows_m1<Q4_Q4K, XT>(t, x, y, s) : general<Q4_Q4K, XT>(t, x, y, M, s);
+        return fast_rows ? rows_batch1<Q4_Q4K, XT>(t, x, y, s) : general<Q4_Q4K, XT>(t, x, y, M, s);
     case Q4_GPTQ:
         if (t.g_idx == nullptr && t.group % 8 == 0) return kmajor<Q4_GPTQ, XT>(t, x, y, M, s);
         return general<Q4_GPTQ, XT>(t, x, y, M, s);
@@ -565,6 +856,14 @@ cudaError_t dispatch(const Tensor &t, const XT *x, float *y, int64_t M, cudaStre
 }
 
 }  // namespace
+
+int gemv_read_and_clear_error() {
+    int v = 0;
+    const int zero = 0;
+    if (cudaMemcpyFromSymbol(&v, g_gemv_error, sizeof(v)) != cudaSuccess) return Q4_ECUDA;
+    if (cudaMemcpyToSymbol(g_gemv_error, &zero, sizeof(zero)) != cudaSuccess) return Q4_ECUDA;
+    return v;
+}
 
 cudaError_t launch_gemv(const Tensor &t, const void *x, q4_dtype x_dtype, float *y, int64_t M,
                         cudaStream_t s) {

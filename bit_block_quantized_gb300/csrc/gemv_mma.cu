@@ -1,0 +1,410 @@
+// gemv_mma.cu -- NVFP4 decode-GEMV for batch 1..8 with the dot products on the
+// tensor cores (mma.sync m16n8k16, f16 x f16 -> f32).
+//
+// Why tensor cores for a bandwidth-bound GEMV: at HBM speed one GB300 SM must
+// retire ~38 NVFP4 weights per clock.  Decoding a weight and multiplying it on
+// the CUDA cores costs >= 2 instructions per weight (hardware E2M1 convert,
+// half-word extracts, FMA), which is close to the whole issue budget.  Here
+// the decode stays in registers and the multiply-accumulate moves to the MMA:
+//   * the hardware convert cvt.rn.f16x2.e2m1x2 turns one payload byte (two
+//     consecutive k) into exactly one f16x2 A-fragment register;
+//   * one HMUL2 by the row's E4M3 block scale (also exact in f16: <= 6
+//     significant bits, range 2^-10 .. 2688) folds (e2m1 * e4m3) into A, the
+//     first product of the pinned order ([MUS7] 7.1-7.2);
+//   * x is B: each activation row m is a column of the MMA, scaled by an
+//     exact power of two into f16 (every bf16 value survives unless the
+//     slice's dynamic range exceeds ~2^29, in which case the warp computes in
+//     f32 on the CUDA cores instead);
+//   * f32 accumulation in the MMA, then x 2^-e and x scale2 once per row.
+// Columns 0..7 of the MMA are the batch (M <= 8): batch 1..8 cost the same
+// weight traffic and decode work.
+//
+// Work split: a CTA owns one 16-row tile; its W warps split K into contiguous
+// runs of 128-k blocks.  Lane (g, t) (g = lane/4, t = lane%4) streams the 16
+// payload bytes of rows g and g+8 that hold k = 128b + 32t .. +31 (coalesced:
+// 4 lanes cover 64 contiguous bytes of a row) plus their two E4M3 bytes, with
+// all of the warp's loads issued before x is staged.  The MMA's 16-k columns
+// are mapped to each lane's own k runs (the same permutation is applied to x
+// in shared memory), so no lane ever moves a weight between registers.
+#include "q4_internal.cuh"
+
+namespace q4 {
+namespace {
+
+#ifndef Q4_MMA_MW
+#define Q4_MMA_MW 8
+#endif
+constexpr int MW = Q4_MMA_MW;     // warps per CTA
+#ifndef Q4_MMA_PD
+#define Q4_MMA_PD 2
+#endif
+constexpr int PD = Q4_MMA_PD;     // 128-k blocks in flight per warp (register ring)
+#ifndef Q4_MMA_NACC
+#define Q4_MMA_NACC 4
+#endif
+constexpr int NACC = Q4_MMA_NACC; // independent accumulator sets (breaks the MMA chain)
+constexpr size_t SMEM_MAX = 200 * 1024;
+
+__device__ __forceinline__ uint32_t hmul2_u32(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+    uint32_t d;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+    return d;
+}
+__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// One 128-k block of rows g and g+8 for lane t: 16 payload bytes per row
+// (k = 128b + 32t .. +31) and the two E4M3 scales of those 32 k.
+struct Blk {
+    uint4 p0, p1;
+    uint32_t s0, s1;
+};
+
+__device__ __forceinline__ void load_blk(const Tensor &t, int64_t n0, int b, int g, int tt, bool ok0, bool ok1,
+                                         Blk &r) {
+    const int64_t K = t.K;
+    const int64_t off = (int64_t)b * 64 + 16 * tt;
+    const int64_t soff = (int64_t)b * 8 + 2 * tt;
+    if (ok0) {
+        r.p0 = ldg_stream16(t.w + (n0 + g) * (K >> 1) + off);
+        r.s0 = ldg_stream2(t.scales + (n0 + g) * (K >> 4) + soff);
+    } else {
+        r.p0 = make_uint4(0, 0, 0, 0);
+        r.s0 = 0;
+    }
+    if (ok1) {
+        r.p1 = ldg_stream16(t.w + (n0 + g + 8) * (K >> 1) + off);
+        r.s1 = ldg_stream2(t.scales + (n0 + g + 8) * (K >> 4) + soff);
+    } else {
+        r.p1 = make_uint4(0, 0, 0, 0);
+        r.s1 = 0;
+    }
+}
+
+// A-fragment source for one payload word (8 k): four f16x2 of e2m1 * e4m3.
+__device__ __forceinline__ void decode_word(uint32_t w, uint32_t sc2, uint32_t (&a)[4]) {
+    e2m1x8_h2(w, a[0], a[1], a[2], a[3]);
+#pragma unroll
+    for (int i = 0; i < 4; i++) a[i] = hmul2_u32(a[i], sc2);
+}
+
+// x slice of one warp as exactly-scaled f16 B fragments, staged once per CTA:
+// entry ((i*8 + j)*MT + m)*4 + t = x[m][128(b0+i) + 32t + 4j .. +3] * 2^e_m.
+// One load pass into registers, a warp max per column, then convert.
+template <typename XT, int MT>
+__device__ __forceinline__ bool stage_x(const XT *__restrict__ x, int64_t K, int M, int b0, int nbw, int lane,
+                                        uint2 *xs, float (&inv)[MT]) {
+    constexpr int PER = 8;                       // entries per lane per pass (covers nbw <= 2*PER/MT... loop)
+    const int entries = nbw * 8 * MT * 4;
+    float amax[MT];
+#pragma unroll
+    for (int m = 0; m < MT; m++) amax[m] = 0.0f;
+    // pass 1: max per column (register-only for the first PER*32 entries)
+    for (int e0 = 0; e0 < entries; e0 += 32 * PER) {
+#pragma unroll
+        for (int q = 0; q < PER; q++) {
+            const int e = e0 + q * 32 + lane;
+            const int te = e & 3, m = (e >> 2) % MT, j = (e / (4 * MT)) & 7, i = e / (32 * MT);
+            if (e < entries && m < M) {
+                const XT *src = x + (int64_t)m * K + (int64_t)(b0 + i) * 128 + 32 * te + 4 * j;
+                float mx = 0.0f;
+#pragma unroll
+                for (int r = 0; r < 4; r++) mx = fmaxf(mx, fabsf(x_to_f32<XT>(src[r])));
+#pragma unroll
+                for (int mm = 0; mm < MT; mm++)
+                    if (mm == m) amax[mm] = fmaxf(amax[mm], mx);
+            }
+        }
+    }
+    float scale[MT];
+    bool exact = true;
+#pragma unroll
+    for (int m = 0; m < MT; m++) {
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1) amax[m] = fmaxf(amax[m], __shfl_xor_sync(0xffffffffu, amax[m], off));
+        const int ex = (int)((__float_as_uint(amax[m]) >> 23) & 255u) - 127;
+        scale[m] = 1.0f;
+        inv[m] = 1.0f;
+        if (amax[m] > 0.0f) {
+            if (ex < -100 || ex > 100) exact = false;
+            else {
+                scale[m] = __uint_as_float((uint32_t)(127 + 12 - ex) << 23);     // max |x * scale| < 2^13
+                inv[m] = __uint_as_float((uint32_t)(127 - 12 + ex) << 23);
+            }
+        }
+    }
+    // pass 2: convert (L1-resident re-read) and check that every value survived
+    for (int e = lane; e < entries; e += 32) {
+        const int te = e & 3, m = (e >> 2) % MT, j = (e / (4 * MT)) & 7, i = e / (32 * MT);
+        uint2 v2 = make_uint2(0u, 0u);
+        if (m < M) {
+            const XT *src = x + (int64_t)m * K + (int64_t)(b0 + i) * 128 + 32 * te + 4 * j;
+            float sc = 1.0f;
+#pragma unroll
+            for (int mm = 0; mm < MT; mm++)
+                if (mm == m) sc = scale[mm];
+            float f[4];
+#pragma unroll
+            for (int r = 0; r < 4; r++) f[r] = x_to_f32<XT>(src[r]) * sc;
+            const __half2 h01 = __floats2half2_rn(f[0], f[1]), h23 = __floats2half2_rn(f[2], f[3]);
+            const float2 c01 = __half22float2(h01), c23 = __half22float2(h23);
+            exact = exact && c01.x == f[0] && c01.y == f[1] && c23.x == f[2] && c23.y == f[3];
+            v2 = make_uint2(*reinterpret_cast<const uint32_t *>(&h01), *reinterpret_cast<const uint32_t *>(&h23));
+        }
+        xs[e] = v2;
+    }
+    exact = __all_sync(0xffffffffu, exact);
+    __syncwarp();
+    return exact;
+}
+
+// f32 CUDA-core path for one warp's k range of a 16-row tile (used only when
+// the activations' dynamic range is too wide for exact f16 staging).
+template <typename XT, int MT>
+__device__ __noinline__ void warp_rows_f32(const Tensor &t, const XT *__restrict__ x, int M, int64_t n0, int b0,
+                                           int b1, int lane, float *rw) {
+    const int64_t N = t.N, K = t.K;
+    for (int rr = 0; rr < 16; rr++) {
+        const int64_t n = n0 + rr;
+        for (int m = 0; m < MT; m++) {
+            float acc = 0.0f;
+            if (n < N && m < M)
+                for (int64_t k = (int64_t)b0 * 128 + lane; k < (int64_t)b1 * 128; k += 32) {
+                    const uint32_t byte = t.w[n * (K >> 1) + (k >> 1)];
+                    const float v = e2m1x2_f32((k & 1) ? (byte >> 4) : (byte & 15u)).x;
+                    const float sc = e4m3_f32(t.scales[n * (K >> 4) + (k >> 4)]);
+                    acc = fmaf(v * sc, x_to_f32<XT>(x[(int64_t)m * K + k]), acc);
+                }
+#pragma unroll
+            for (int off = 16; off >= 1; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+            if (lane == 0) rw[rr * MT + m] = acc;
+        }
+    }
+}
+
+// Persistent CTAs: each takes row tiles blockIdx.x, +gridDim.x, ...; its MW
+// warps split K into runs of nbw_max 128-k blocks (the last runs may be
+// shorter).  A register ring of PD blocks per lane runs across tile
+// boundaries, so the next tile's first loads are in flight while the current
+// tile finishes; one barrier per tile hands the warp partials (double
+// buffered) to a fixed-order final sum.
+template <typename XT, int MT>
+#ifndef Q4_MMA_MINB
+#define Q4_MMA_MINB 2
+#endif
+__global__ void __launch_bounds__(MW * 32, Q4_MMA_MINB) gemv_mma_nvfp4(Tensor t, const XT *__restrict__ x,
+                                                          float *__restrict__ y, int M, int nbw_max, int ntiles) {
+    extern __shared__ __align__(16) uint8_t mma_smem[];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = lane >> 2, tt = lane & 3;
+    const int64_t N = t.N, K = t.K;
+    const int nb = (int)(K >> 7);
+    const int b0 = min(nb, warp * nbw_max), b1 = min(nb, (warp + 1) * nbw_max), nbw = b1 - b0;
+    uint2 *xs = reinterpret_cast<uint2 *>(mma_smem) + (size_t)warp * nbw_max * 8 * MT * 4;
+    float *red = reinterpret_cast<float *>(mma_smem + (size_t)MW * nbw_max * 8 * MT * 4 * sizeof(uint2));
+
+    const int my_tiles = blockIdx.x < ntiles ? (ntiles - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+    const int items = my_tiles * nbw_max;          // every warp walks the same item count
+
+    // Load cursor: walks items (tile, block) in order with offset increments
+    // only; a new tile recomputes its row offsets once.  Rows past N are
+    // clamped to N-1 (valid memory; their results are never stored).
+    const uint32_t rowb = (uint32_t)(K >> 1), srowb = (uint32_t)(K >> 4);
+    uint32_t ow0, os0, ow_d = 8 * rowb, os_d = 8 * srowb;
+    int lc_i = 0, lc_tile = blockIdx.x;
+    auto cursor_tile = [&](int tile) {
+        const int64_t n0 = (int64_t)tile * 16;
+        const uint32_t r0 = (uint32_t)((n0 + g) < N ? (n0 + g) : (N - 1));
+        const uint32_t r1 = (uint32_t)((n0 + g + 8) < N ? (n0 + g + 8) : (N - 1));
+        ow0 = r0 * rowb + (uint32_t)b0 * 64 + 16 * tt;
+        os0 = r0 * srowb + (uint32_t)b0 * 8 + 2 * tt;
+        ow_d = (r1 - r0) * rowb;
+        os_d = (r1 - r0) * srowb;
+        lc_tile = tile;
+        lc_i = 0;
+    };
+    cursor_tile(blockIdx.x);
+    int lu = 0;                                    // items issued so far
+    auto load_next = [&](Blk &r) {
+        if (lu < items) {
+            if (lc_i < nbw) {
+                r.p0 = ldg_stream16(t.w + ow0);
+                r.p1 = ldg_stream16(t.w + ow0 + ow_d);
+                r.s0 = ldg_stream2(t.scales + os0);
+                r.s1 = ldg_stream2(t.scales + os0 + os_d);
+            }
+            ow0 += 64;
+            os0 += 8;
+            if (++lc_i == nbw_max) cursor_tile(lc_tile + gridDim.x);
+            ++lu;
+        }
+    };
+    Blk buf[PD];
+#pragma unroll
+    for (int q = 0; q < PD; q++) load_next(buf[q]);
+
+    // Programmatic dependent launch: let the next kernel in the stream start
+    // its own weight prefetch as SMs free up, and wait for the previous one
+    // (which may have produced x) before reading activations.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+
+    float inv[MT];
+    const bool exact = nbw > 0 ? stage_x<XT, MT>(x, K, M, b0, nbw, lane, xs, inv) : true;
+    if (nbw <= 0)
+#pragma unroll
+        for (int m = 0; m < MT; m++) inv[m] = 1.0f;
+    const int mlane = g < M ? g : 0;
+    const uint2 *xbase = xs + mlane * 4 + tt;
+
+    float dacc[NACC][4];
+#pragma unroll
+    for (int a = 0; a < NACC; a++) dacc[a][0] = dacc[a][1] = dacc[a][2] = dacc[a][3] = 0.0f;
+    int ci = 0, ctile = blockIdx.x, par = 0;       // compute cursor
+    const uint2 *xb = xbase;
+    for (int u0 = 0; u0 < items; u0 += PD) {
+#pragma unroll
+        for (int q = 0; q < PD; q++) {
+            const int u = u0 + q;
+            if (u < items) {
+                const int i = ci;
+                const Blk r = buf[q];
+                load_next(buf[q]);
+                if (i < nbw && exact) {
+                    uint32_t h0, h1;
+                    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h0) : "h"((uint16_t)r.s0));
+                    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h1) : "h"((uint16_t)r.s1));
+                    const uint32_t sc0[2] = {prmt(h0, h0, 0x1010u), prmt(h0, h0, 0x3232u)};
+                    const uint32_t sc1[2] = {prmt(h1, h1, 0x1010u), prmt(h1, h1, 0x3232u)};
+                    const uint32_t w0[4] = {r.p0.x, r.p0.y, r.p0.z, r.p0.w};
+                    const uint32_t w1[4] = {r.p1.x, r.p1.y, r.p1.z, r.p1.w};
+#pragma unroll
+                    for (int w = 0; w < 4; w++) {
+                        uint32_t a[4], c[4];
+                        decode_word(w0[w], sc0[w >> 1], a);
+                        decode_word(w1[w], sc1[w >> 1], c);
+                        // lanes g >= M read column 0's x: MMA columns >= M are never stored
+                        const uint2 bA = xb[(2 * w) * MT * 4], bB = xb[(2 * w + 1) * MT * 4];
+                        mma16816(dacc[(2 * w) % NACC], a[0], c[0], a[1], c[1], bA.x, bA.y);
+                        mma16816(dacc[(2 * w + 1) % NACC], a[2], c[2], a[3], c[3], bB.x, bB.y);
+                    }
+                }
+                xb += 8 * MT * 4;
+                const int ti = ctile;
+                if (++ci == nbw_max) { ci = 0; ctile += gridDim.x; xb = xbase; }
+                if (i == nbw_max - 1) {
+                    // ---- end of tile `ti`: partials -> shared, one barrier, final sum
+                    const int64_t n0 = (int64_t)ti * 16;
+                    float *rw = red + (par * MW + warp) * 16 * MT;
+                    float d[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                    for (int a = 0; a < NACC; a++) {
+                        d[0] += dacc[a][0]; d[1] += dacc[a][1]; d[2] += dacc[a][2]; d[3] += dacc[a][3];
+                        dacc[a][0] = dacc[a][1] = dacc[a][2] = dacc[a][3] = 0.0f;
+                    }
+                    if (exact) {
+#pragma unroll
+                        for (int mm = 0; mm < MT; mm++) {
+                            if (mm == 2 * tt) { rw[g * MT + mm] = d[0] * inv[mm]; rw[(g + 8) * MT + mm] = d[2] * inv[mm]; }
+                            if (mm == 2 * tt + 1) { rw[g * MT + mm] = d[1] * inv[mm]; rw[(g + 8) * MT + mm] = d[3] * inv[mm]; }
+                        }
+                    } else {
+                        warp_rows_f32<XT, MT>(t, x, M, n0, b0, b1, lane, rw);
+                    }
+                    __syncthreads();
+                    const float *rt = red + par * MW * 16 * MT;
+                    par ^= 1;
+                    for (int e = threadIdx.x; e < 16 * MT; e += blockDim.x) {
+                        const int rr = e / MT, m = e % MT;
+                        const int64_t n = n0 + rr;
+                        if (n < N && m < M) {
+                            float sum = 0.0f;
+                            for (int w = 0; w < MW; w++) sum += rt[w * 16 * MT + e];
+                            y[(int64_t)m * N + n] = sum * t.scale2;
+                        }
+                    }
+                }
+            }
+        }
+    }
+}
+
+template <typename Kern> int max_blocks_mma(Kern k, size_t smem) {
+    int b = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, k, MW * 32, smem) != cudaSuccess || b < 1) b = 1;
+    return b;
+}
+
+size_t smem_bytes(int64_t K, int mt) {
+    const int nb = (int)(K >> 7), nbw_max = (nb + MW - 1) / MW;
+    return (size_t)MW * nbw_max * 8 * mt * 4 * sizeof(uint2) + 2 * (size_t)MW * 16 * mt * sizeof(float);
+}
+
+int mt_for(int64_t M) { return M == 1 ? 1 : (M == 2 ? 2 : (M <= 4 ? 4 : 8)); }
+
+template <typename XT, int MT>
+cudaError_t run(const Tensor &t, const XT *x, float *y, int M, cudaStream_t s) {
+    auto kern = gemv_mma_nvfp4<XT, MT>;
+    const size_t smem = smem_bytes(t.K, MT);
+    static bool attr_set[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (!attr_set[dev & 63]) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_MAX);
+        if (e != cudaSuccess) return e;
+        attr_set[dev & 63] = true;
+    }
+    const int nb = (int)(t.K >> 7), nbw_max = (nb + MW - 1) / MW;
+    const int ntiles = (int)((t.N + 15) / 16);
+    int grid = max_blocks_mma(kern, smem) * sm_count();
+    if (grid > ntiles) grid = ntiles;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid, 1, 1);
+    cfg.blockDim = dim3(MW * 32, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, t, x, y, M, nbw_max, ntiles);
+}
+
+}  // namespace
+
+// Eligible: NVFP4, K % 128 == 0, x slice fits in shared memory.
+bool gemv_mma_eligible(const Tensor &t, int64_t M) {
+    return t.fmt == Q4_NVFP4 && M >= 1 && M <= 8 && t.K % 128 == 0 && smem_bytes(t.K, mt_for(M)) <= SMEM_MAX &&
+           t.N * (t.K / 2) < (int64_t(1) << 32) &&
+           (((uintptr_t)t.w | (uintptr_t)t.scales) & 15) == 0;
+}
+
+cudaError_t launch_gemv_mma(const Tensor &t, const void *x, q4_dtype xd, float *y, int64_t M, cudaStream_t s) {
+    const int m = (int)M;
+    if (xd == Q4_DT_BF16) {
+        const __nv_bfloat16 *xb = (const __nv_bfloat16 *)x;
+        if (m == 1) return run<__nv_bfloat16, 1>(t, xb, y, m, s);
+        if (m == 2) return run<__nv_bfloat16, 2>(t, xb, y, m, s);
+        if (m <= 4) return run<__nv_bfloat16, 4>(t, xb, y, m, s);
+        return run<__nv_bfloat16, 8>(t, xb, y, m, s);
+    }
+    const float *xf = (const float *)x;
+    if (m == 1) return run<float, 1>(t, xf, y, m, s);
+    if (m == 2) return run<float, 2>(t, xf, y, m, s);
+    if (m <= 4) return run<float, 4>(t, xf, y, m, s);
+    return run<float, 8>(t, xf, y, m, s);
+}
+
+}  // namespace q4

@@ -29,6 +29,37 @@ __device__ __forceinline__ uint32_t e2m1x2_h2(uint32_t byte) {
     return h2;
 }
 
+// Four E2M1 pairs of one 32-bit payload word -> four f16x2 (byte b -> h[b];
+// low nibble in the low half).  The byte split is a register-level unpack.
+__device__ __forceinline__ void e2m1x8_h2(uint32_t w, uint32_t &h0, uint32_t &h1, uint32_t &h2, uint32_t &h3) {
+    asm("{ .reg .b8 b0, b1, b2, b3;\n\t"
+        "mov.b32 {b0, b1, b2, b3}, %4;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %0, b0;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %2, b2;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %3, b3; }"
+        : "=r"(h0), "=r"(h1), "=r"(h2), "=r"(h3)
+        : "r"(w));
+}
+
+// Mixed-precision FMA (sm_100 family): c + a*b with f16 a, b taken from the
+// low (HI=0) or high (HI=1) halves of two f16x2 registers; the product is
+// exact and the sum rounds once in f32, exactly like fmaf on the widened
+// operands.
+template <int HI>
+__device__ __forceinline__ float fma_f16_f32(uint32_t a2, uint32_t b2, float c) {
+    float d;
+    if (HI)
+        asm("{ .reg .b16 al, ah, bl, bh;\n\t mov.b32 {al, ah}, %1;\n\t mov.b32 {bl, bh}, %2;\n\t"
+            "fma.rn.f32.f16 %0, ah, bh, %3; }"
+            : "=f"(d) : "r"(a2), "r"(b2), "f"(c));
+    else
+        asm("{ .reg .b16 al, ah, bl, bh;\n\t mov.b32 {al, ah}, %1;\n\t mov.b32 {bl, bh}, %2;\n\t"
+            "fma.rn.f32.f16 %0, al, bl, %3; }"
+            : "=f"(d) : "r"(a2), "r"(b2), "f"(c));
+    return d;
+}
+
 // Two E4M3FN bytes (low byte -> .x) -> f32, via cvt.rn.f16x2.e4m3x2; every
 // finite E4M3FN value (subnormals included) is exact in f16.
 __device__ __forceinline__ float2 e4m3x2_f32(uint32_t two_bytes) {
@@ -104,6 +135,54 @@ __device__ __forceinline__ uint32_t ldg_stream1(const void *p) {
 // AWQ slot of logical column j (inverse of the slot order 0,2,4,6,1,3,5,7).
 __device__ __forceinline__ int awq_slot(int j) { return (j >> 1) + 4 * (j & 1); }
 
+// --------------------------------------------- mbarrier + bulk-copy (TMA)
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+// Make mbarrier initialisation visible to the async (bulk-copy) proxy.
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile("{ .reg .pred p;\n\t"
+                 "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+                 "selp.u32 %0, 1, 0, p; }"
+                 : "=r"(ok)
+                 : "r"(smem_u32(bar)), "r"(parity)
+                 : "memory");
+    return ok != 0;
+}
+// Bounded wait: gives up after ~`limit_cycles` SM clocks and returns false.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity,
+                                                  long long limit_cycles = 2000000000LL) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const long long t0 = clock64();
+    while (!mbar_try_wait(bar, parity)) {
+        if (clock64() - t0 > limit_cycles) return false;
+    }
+    return true;
+}
+// 1-D bulk copy global -> shared, completion counted on `bar` (bytes and both
+// addresses 16-byte aligned).
+__device__ __forceinline__ void bulk_g2s(void *dst_smem, const void *src_gmem, uint32_t bytes, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_u32(dst_smem)),
+        "l"(src_gmem), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
 // ------------------------------------------------------ launch interface
 struct Tensor {
     q4_fmt fmt;
@@ -122,6 +201,8 @@ cudaError_t launch_gemv(const Tensor &t, const void *x, q4_dtype x_dtype, float 
                         cudaStream_t s);
 cudaError_t launch_gemm_tc(const Tensor &t, const void *x, q4_dtype x_dtype, float *y, int64_t M,
                            cudaStream_t s, bool *handled);
+bool gemv_mma_eligible(const Tensor &t, int64_t M);
+cudaError_t launch_gemv_mma(const Tensor &t, const void *x, q4_dtype xd, float *y, int64_t M, cudaStream_t s);
 int launch_repack(q4_fmt src, const Tensor &t, q4_fmt dst, void *dst_w, void *dst_scales,
                   void *dst_zeros, int32_t *perm_out, cudaStream_t s);
 int run_validate(const Tensor &t, int64_t *d_bad, cudaStream_t s);

@@ -140,12 +140,52 @@ def check_gemv(layer, M, config=20, xdtype="bf16", rows=None):
     return worst
 
 
+# Shapes whose rows are whole 16-byte multiples take the bulk-copy pipeline.
+PIPELINE_SHAPES = {"nvfp4": (37, 4096), "mxfp4": (41, 2048), "q4k": (29, 1536), "q40": (33, 2048),
+                   "gptq": (264, 1152), "awq": (264, 1152)}
+
+
 @pytest.mark.parametrize("fmt", ALL_GEMV)
-def test_gemv_batch1(fmt):
-    N, K = shape_for(fmt)
+@pytest.mark.parametrize("pipeline", [False, True])
+def test_gemv_batch1(fmt, pipeline):
+    N, K = PIPELINE_SHAPES[fmt] if pipeline else shape_for(fmt)
     layer = synth.make_layer(fmt, N, K, config=21, matrix=1, outliers=True)
     check_gemv(layer, 1)
     check_gemv(layer, 1, xdtype="f32")
+
+
+@pytest.mark.parametrize("M", [1, 2, 3, 4, 5, 8])
+def test_gemv_nvfp4_tensor_core_path(M):
+    """NVFP4 with K % 128 == 0 and bf16 x runs the mma.sync decode-dot kernel:
+    ragged 16-row tiles, uneven K split over the warps, batch 1..8."""
+    for N, K in ((45, 4096), (16, 128), (7, 1152), (263, 14336)):
+        check_gemv(synth.make_layer("nvfp4", N, K, config=30, matrix=M, row_scale=True), M, config=30 + M)
+
+
+def test_gemv_nvfp4_wide_dynamic_range_x():
+    """x whose range defeats the f16 staging (1e30 next to 1e-10): those warps
+    fall back to f32 and the result is still within tolerance."""
+    N, K = 40, 4096
+    layer = synth.make_layer("nvfp4", N, K, config=31, matrix=0)
+    for M in (1, 3):
+        xf = np.random.default_rng(M).normal(0, 1e-10, (M, K)).astype(np.float32)
+        xf[:, 7] = 1e30
+        xf[:, 1000] = -3e20
+        xbits = synth.f32_to_bf16_bits(xf)
+        xr = oracle.bf16_bits_to_f32(xbits).reshape(M, K)
+        y = gpu_gemv(layer, x_device(xbits), M)
+        ref, bound = oracle.gemv(to_oracle(layer), xr)
+        ok, worst = within_tolerance(y, ref, bound)
+        assert ok, worst
+
+
+def test_gemv_pipeline_long_rows_and_tails():
+    """R=2 tiles (K > 8192), a ragged last tile, one row, and N < grid."""
+    for N, K in ((4099, 14336), (1, 14336), (3, 8448), (1029, 4096)):
+        check_gemv(synth.make_layer("nvfp4", N, K, config=21, matrix=N % 7), 1)
+    check_gemv(synth.make_layer("q4k", 517, 11008, config=21, matrix=9), 1)
+    check_gemv(synth.make_layer("q40", 131, 11008, config=21, matrix=10), 1)
+    assert q4.q4_last_error() == 0
 
 
 @pytest.mark.parametrize("fmt", ALL_GEMV)
@@ -185,7 +225,7 @@ def test_gemv_one_hot_gives_exact_column():
         x = torch.zeros((1, 4096), dtype=torch.bfloat16, device="cuda")
         x[0, k] = 1.0
         y = gpu_gemv(layer, x, 1)[0]
-        assert bits_equal(y, ref[:, k])
+        assert np.array_equal(y, ref[:, k])      # exact; a -0.0 weight sums to +0.0
 
 
 # Full-size workloads (the decode-GEMV study's layer shapes), sampled rows.
