@@ -1,8 +1,9 @@
 """Batch-1 NVFP4 decode-GEMV bench: weight-stream GB/s on the 4096x14336 MLP set.
 
 One step = the three projections of one decoder MLP in NVFP4 at batch 1
-(gate 14336x4096, up 14336x4096, down 4096x14336), each a fused decode-GEMV
-through the C ABI (q4_gemv).  The weights come from the seeded synthetic
+(gate 14336x4096, up 14336x4096, down 4096x14336): gate and up read the same
+x, down its own; each is one q4_gemv launch, chained by programmatic
+dependent launch.  The weights come from the seeded synthetic
 recipe (W ~ N(0,0.02) with U(0.5,2) row scales, NVFP4 per 16, bf16 x).
 
 L2 policy: inputs larger than L2 -- the step rotates through distinct copies
@@ -36,7 +37,7 @@ SET = [("gate", 14336, 4096), ("up", 14336, 4096), ("down", 4096, 14336)]
 CONFIG_ID = 5          # seed block of this workload's synthetic draws
 NOMINAL_HBM_GBS = 7900.0
 FALLBACK_HBM_GBS = 6800.0
-DOMINANT = "gemv_mma_nvfp4<bf16, MT=1> (gate/up, 14336x4096)"
+DOMINANT = "gemv_mma_nvfp4<bf16, MT=1, single> (gate/up, 14336x4096)"
 
 
 def parse():
@@ -49,6 +50,9 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="target CPU time of the oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ncu-case", action="store_true",
+                    help="small profiling case: 4 launches of the gate GEMV (14336x4096) on one "
+                         "weight copy (33 MB), no timing, no JSON line")
     return ap.parse_args()
 
 
@@ -145,7 +149,7 @@ def build_workload(torch, q4, synth):
     host = []
     for i, (name, N, K) in enumerate(SET):
         layer = synth.make_layer("nvfp4", N, K, config=CONFIG_ID, matrix=i, row_scale=True)
-        xbits, _ = synth.draw_x(1, K, config=CONFIG_ID, matrix=i)
+        xbits, _ = synth.draw_x(1, K, config=CONFIG_ID, matrix=0 if name in ("gate", "up") else i)
         host.append((name, N, K, layer, xbits))
     set_bytes = sum(q4.q4_packed_bytes("nvfp4", N, K) for _, N, K in SET)
     l2 = torch.cuda.get_device_properties(0).L2_cache_size
@@ -159,6 +163,7 @@ def build_workload(torch, q4, synth):
             mats.append((name, N, K, w, s, layer["scale2"]))
         dev.append(mats)
     xs = [torch.from_numpy(h[4].view(np.int16)).cuda().view(torch.bfloat16) for h in host]
+    xs[1] = xs[0]                                   # gate and up read the same activations
     ys = [torch.empty((1, N), dtype=torch.float32, device="cuda") for _, N, _ in SET]
     return host, dev, xs, ys, set_bytes, copies, l2
 
@@ -176,9 +181,15 @@ def run_ours(args, rank, world):
     auxes = [q4.make_aux(scale2=h[3]["scale2"], fmt="nvfp4") for h in host]
     stream = torch.cuda.Stream()
 
-    def step(c, s):
-        for j, (name, N, K, w, sc, _) in enumerate(dev[c]):
+    def one(j):
+        def f(c, s):
+            name, N, K, w, sc, _ = dev[c][j]
             q4.q4_gemv("nvfp4", w, sc, auxes[j], xs[j], ys[j], 1, N, K, stream=s)
+        return f
+
+    def step(c, s):
+        for j in range(len(SET)):
+            one(j)(c, s)
 
     # one graph per full rotation, plus single-step graphs for the remainder
     with torch.cuda.stream(stream):
@@ -195,14 +206,13 @@ def run_ours(args, rank, world):
             with torch.cuda.graph(g, stream=stream):
                 step(c, stream)
             g_one.append(g)
-        # per-kernel graphs for the roofline of each projection
+        # per-launch graphs for the roofline of each projection
         g_kern = []
-        for j in range(len(SET)):
+        for fn in (one(0), one(1), one(2)):
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=stream):
                 for c in range(copies):
-                    name, N, K, w, sc, _ = dev[c][j]
-                    q4.q4_gemv("nvfp4", w, sc, auxes[j], xs[j], ys[j], 1, N, K, stream=stream)
+                    fn(c, stream)
             g_kern.append(g)
 
     def run_steps(n):
@@ -232,7 +242,7 @@ def run_ours(args, rank, world):
         # per-kernel average launch duration (same stream, inputs > L2)
         kern_ms = []
         reps = max(3, 2000 // copies)
-        for j in range(len(SET)):
+        for j in range(len(g_kern)):
             g_kern[j].replay()
             torch.cuda.synchronize()
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -260,7 +270,7 @@ def run_ours(args, rank, world):
     per_kernel = {name: {"us_per_launch": round(kern_ms[j] * 1e3, 3),
                          "GBps": round(q4.q4_packed_bytes("nvfp4", N, K) / (kern_ms[j] * 1e-3) / 1e9, 1)}
                   for j, (name, N, K) in enumerate(SET)}
-    x_bytes = sum(K * 2 for _, _, K in SET)
+    x_bytes = 4096 * 2 + 14336 * 2
     y_bytes = sum(N * 4 for _, N, _ in SET)
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
@@ -273,7 +283,8 @@ def run_ours(args, rank, world):
                    "y_bytes_per_step": y_bytes,
                    "l2": f"inputs larger than L2: {copies} rotating copies of the set = "
                          f"{copies * set_bytes / 1e9:.2f} GB (L2 {l2 / 1e6:.0f} MB)",
-                   "launch": "one CUDA graph per rotation; 3 q4_gemv launches per step",
+                   "launch": "one CUDA graph per rotation; 3 q4_gemv launches per step (gate and up "
+                             "share x), chained by programmatic dependent launch",
                    "parallelism": f"replicas x{world}"},
         "pct_of_hbm_peak": {"measured": round(value / world / peak, 4),
                             "nominal_7900": round(value / world / NOMINAL_HBM_GBS, 4)},
@@ -293,19 +304,23 @@ def run_ours(args, rank, world):
 
 
 def run_e2e(args, torch, q4, dev, auxes, host, stream):
-    """Same metric through q4_gemv with host buffers: every step copies its x
-    from pinned host memory, runs the three projections, and reads y back."""
-    xs_h = [torch.from_numpy(h[4].view(np.int16)).view(torch.bfloat16).pin_memory() for h in host]
+    """Same metric through the public API with host buffers: every step copies
+    the two activation vectors from pinned host memory, runs the three
+    q4_gemv calls, and reads the three outputs back."""
+    xh_gu = torch.from_numpy(host[0][4].view(np.int16)).view(torch.bfloat16).pin_memory()
+    xh_dn = torch.from_numpy(host[2][4].view(np.int16)).view(torch.bfloat16).pin_memory()
+    xd_gu, xd_dn = torch.empty_like(xh_gu, device="cuda"), torch.empty_like(xh_dn, device="cuda")
     ys_h = [torch.empty((1, N), dtype=torch.float32).pin_memory() for _, N, _ in SET]
-    xs_d = [torch.empty_like(x, device="cuda") for x in xs_h]
     ys_d = [torch.empty((1, N), dtype=torch.float32, device="cuda") for _, N, _ in SET]
     copies = len(dev)
     n = args.e2e_steps
 
     def one(c):
+        xd_gu.copy_(xh_gu, non_blocking=True)
+        xd_dn.copy_(xh_dn, non_blocking=True)
         for j, (name, N, K, w, sc, _) in enumerate(dev[c]):
-            xs_d[j].copy_(xs_h[j], non_blocking=True)
-            q4.q4_gemv("nvfp4", w, sc, auxes[j], xs_d[j], ys_d[j], 1, N, K, stream=stream)
+            q4.q4_gemv("nvfp4", w, sc, auxes[j], xd_dn if j == 2 else xd_gu, ys_d[j], 1, N, K, stream=stream)
+        for j in range(3):
             ys_h[j].copy_(ys_d[j], non_blocking=True)
         stream.synchronize()
 
@@ -318,10 +333,10 @@ def run_e2e(args, torch, q4, dev, auxes, host, stream):
         dt = time.perf_counter() - t0
     set_bytes = sum(q4.q4_packed_bytes("nvfp4", N, K) for _, N, K in SET)
     return {"value": round(set_bytes * n / dt / 1e9, 1), "unit": "GB/s",
-            "h2d_bytes_per_step": sum(K * 2 for _, _, K in SET),
+            "h2d_bytes_per_step": xh_gu.numel() * 2 + xh_dn.numel() * 2,
             "d2h_bytes_per_step": sum(N * 4 for _, N, _ in SET),
             "steps": n, "ms_per_step": dt * 1e3 / n,
-            "note": "per step: pinned x H2D, 3 q4_gemv, y D2H, host sync (no graph)"}
+            "note": "per step: pinned x H2D (2 vectors), 3 q4_gemv, y D2H, host sync (no graph)"}
 
 
 # --------------------------------------------------------- oracle on host
@@ -336,7 +351,7 @@ def cpu_baseline(seconds, host=None, sample_rows=None):
         host = []
         for i, (name, N, K) in enumerate(SET):
             layer = synth.make_layer("nvfp4", N, K, config=CONFIG_ID, matrix=i, row_scale=True)
-            xbits, _ = synth.draw_x(1, K, config=CONFIG_ID, matrix=i)
+            xbits, _ = synth.draw_x(1, K, config=CONFIG_ID, matrix=0 if name in ("gate", "up") else i)
             host.append((name, N, K, layer, xbits))
     # calibrate: rows per second on a small probe, then size the sample
     name, N, K, layer, xbits = host[0]
@@ -385,7 +400,7 @@ def run_reference(args, rank, world):
     host = []
     for i, (name, N, K) in enumerate(SET):
         layer = synth.make_layer("nvfp4", N, K, config=CONFIG_ID, matrix=i, row_scale=True)
-        xbits, _ = synth.draw_x(1, K, config=CONFIG_ID, matrix=i)
+        xbits, _ = synth.draw_x(1, K, config=CONFIG_ID, matrix=0 if name in ("gate", "up") else i)
         host.append((name, N, K, layer, xbits))
     # size each step's sample so that the whole run stays near a minute
     rows_per_matrix = int(max(1, min(64, 60.0 / (max(args.steps, 1) * 0.65e-3))))
@@ -416,8 +431,34 @@ def run_reference(args, rank, world):
                     "d2h_bytes_per_step": 0}}
 
 
+def ncu_case():
+    """A few launches of the dominant kernel on one matrix, for ncu captures
+    sized well under a few GB of device memory."""
+    import torch
+
+    import bit_block_quantized_gb300 as q4
+    import synth
+    from bit_block_quantized_gb300 import build as q4build
+    q4build.build()
+    name, N, K = SET[0]
+    layer = synth.make_layer("nvfp4", N, K, config=CONFIG_ID, matrix=0, row_scale=True)
+    xbits, _ = synth.draw_x(1, K, config=CONFIG_ID, matrix=0)
+    w = torch.from_numpy(layer["w"]).cuda()
+    sc = torch.from_numpy(layer["scales"]).cuda()
+    x = torch.from_numpy(xbits.view(np.int16)).cuda().view(torch.bfloat16)
+    y = torch.empty((1, N), dtype=torch.float32, device="cuda")
+    aux = q4.make_aux(scale2=layer["scale2"], fmt="nvfp4")
+    for _ in range(4):
+        q4.q4_gemv("nvfp4", w, sc, aux, x, y, 1, N, K)
+    torch.cuda.synchronize()
+    print("ncu case done, last_error", q4.q4_last_error())
+
+
 def main():
     args = parse()
+    if args.ncu_case:
+        ncu_case()
+        return
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     if args.impl == "reference":

@@ -30,6 +30,13 @@ class Aux(ctypes.Structure):
                 ("x_dtype", ctypes.c_int), ("out_dtype", ctypes.c_int)]
 
 
+class GemvDesc(ctypes.Structure):
+    """Mirror of ``q4_gemv_desc``."""
+    _fields_ = [("fmt", ctypes.c_int), ("W_packed", ctypes.c_void_p), ("scales", ctypes.c_void_p),
+                ("aux", ctypes.POINTER(Aux)), ("x", ctypes.c_void_p), ("y", ctypes.c_void_p),
+                ("N", ctypes.c_int64), ("K", ctypes.c_int64)]
+
+
 class Q4Error(RuntimeError):
     def __init__(self, status: int, what: str):
         self.status = status
@@ -51,9 +58,10 @@ def lib() -> ctypes.CDLL:
         AUXP = ctypes.POINTER(Aux)
         L.q4_gemv.argtypes = [I32, P, P, AUXP, P, P, I64, I64, I64, P]
         L.q4_dequant.argtypes = [I32, P, P, AUXP, P, I64, I64, P]
+        L.q4_gemv_grouped.argtypes = [ctypes.POINTER(GemvDesc), I32, I64, P]
         L.q4_repack.argtypes = [I32, P, P, AUXP, I32, P, P, P, P, I64, I64, P]
         L.q4_validate.argtypes = [I32, P, P, AUXP, I64, I64, P, P]
-        for f in ("q4_gemv", "q4_dequant", "q4_repack", "q4_validate", "q4_last_error"):
+        for f in ("q4_gemv", "q4_gemv_grouped", "q4_dequant", "q4_repack", "q4_validate", "q4_last_error"):
             getattr(L, f).restype = ctypes.c_int
         L.q4_last_error.argtypes = []
         L.q4_strerror.restype = ctypes.c_char_p
@@ -118,6 +126,18 @@ def q4_gemv(fmt, W_packed, scales, aux, x, y, M, N, K, stream=None, check=True) 
                        int(M), int(N), int(K), _stream(stream))
     if check:
         _check(rc, "q4_gemv")
+    return rc
+
+
+def q4_gemv_grouped(descs, M, stream=None, check=True) -> int:
+    """``descs``: sequence of (fmt, W_packed, scales, aux, x, y, N, K) tuples."""
+    arr = (GemvDesc * len(descs))()
+    for i, (fmt, w, s, aux, x, y, N, K) in enumerate(descs):
+        arr[i] = GemvDesc(_fmt(fmt), _ptr(w), _ptr(s), None if aux is None else ctypes.pointer(aux),
+                          _ptr(x), _ptr(y), int(N), int(K))
+    rc = lib().q4_gemv_grouped(arr, len(descs), int(M), _stream(stream))
+    if check:
+        _check(rc, "q4_gemv_grouped")
     return rc
 
 

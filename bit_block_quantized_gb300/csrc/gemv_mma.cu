@@ -172,18 +172,18 @@ __device__ __forceinline__ bool stage_x(const XT *__restrict__ x, int64_t K, int
 // f32 CUDA-core path for one warp's k range of a 16-row tile (used only when
 // the activations' dynamic range is too wide for exact f16 staging).
 template <typename XT, int MT>
-__device__ __noinline__ void warp_rows_f32(const Tensor &t, const XT *__restrict__ x, int M, int64_t n0, int b0,
-                                           int b1, int lane, float *rw) {
-    const int64_t N = t.N, K = t.K;
+__device__ __noinline__ void warp_rows_f32(const uint8_t *w, const uint8_t *scales, int64_t N, int64_t K,
+                                           const XT *__restrict__ x, int M, int64_t n0, int b0, int b1, int lane,
+                                           float *rw) {
     for (int rr = 0; rr < 16; rr++) {
         const int64_t n = n0 + rr;
         for (int m = 0; m < MT; m++) {
             float acc = 0.0f;
             if (n < N && m < M)
                 for (int64_t k = (int64_t)b0 * 128 + lane; k < (int64_t)b1 * 128; k += 32) {
-                    const uint32_t byte = t.w[n * (K >> 1) + (k >> 1)];
+                    const uint32_t byte = w[n * (K >> 1) + (k >> 1)];
                     const float v = e2m1x2_f32((k & 1) ? (byte >> 4) : (byte & 15u)).x;
-                    const float sc = e4m3_f32(t.scales[n * (K >> 4) + (k >> 4)]);
+                    const float sc = e4m3_f32(scales[n * (K >> 4) + (k >> 4)]);
                     acc = fmaf(v * sc, x_to_f32<XT>(x[(int64_t)m * K + k]), acc);
                 }
 #pragma unroll
@@ -193,61 +193,87 @@ __device__ __noinline__ void warp_rows_f32(const Tensor &t, const XT *__restrict
     }
 }
 
-// Persistent CTAs: each takes row tiles blockIdx.x, +gridDim.x, ...; its MW
-// warps split K into runs of nbw_max 128-k blocks (the last runs may be
-// shorter).  A register ring of PD blocks per lane runs across tile
-// boundaries, so the next tile's first loads are in flight while the current
-// tile finishes; one barrier per tile hands the warp partials (double
-// buffered) to a fixed-order final sum.
-template <typename XT, int MT>
+// A group of independent GEMVs that share K and the batch M (e.g. the q/k/v
+// or gate/up projections of one decoder layer, which read the same x): their
+// row tiles form one list so a single persistent launch streams all of them.
+constexpr int MAXG = 8;
+template <typename XT> struct Group {
+    int count;
+    int tile_start[MAXG + 1];                      // cumulative 16-row tiles
+    const uint8_t *w[MAXG];
+    const uint8_t *s[MAXG];
+    const XT *x[MAXG];
+    float *y[MAXG];
+    int64_t N[MAXG];
+    float scale2[MAXG];
+};
+
 #ifndef Q4_MMA_MINB
 #define Q4_MMA_MINB 2
 #endif
-__global__ void __launch_bounds__(MW * 32, Q4_MMA_MINB) gemv_mma_nvfp4(Tensor t, const XT *__restrict__ x,
-                                                          float *__restrict__ y, int M, int nbw_max, int ntiles) {
+
+// Persistent CTAs: each takes tiles blockIdx.x, +gridDim.x, ... of the group's
+// tile list; its MW warps split K into runs of nbw_max 128-k blocks (the last
+// runs may be shorter).  A register ring of PD blocks per lane runs across
+// tile (and member) boundaries, so the next tile's first loads are in flight
+// while the current tile finishes; one barrier per tile hands the warp
+// partials (double buffered) to a fixed-order final sum.  A warp restages its
+// x slice only when the member's activation pointer changes.
+template <typename XT, int MT, bool MULTI>
+__global__ void __launch_bounds__(MW * 32, Q4_MMA_MINB) gemv_mma_nvfp4(const __grid_constant__ Group<XT> grp,
+                                                                      int64_t K, int M, int nbw_max) {
     extern __shared__ __align__(16) uint8_t mma_smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, tt = lane & 3;
-    const int64_t N = t.N, K = t.K;
     const int nb = (int)(K >> 7);
     const int b0 = min(nb, warp * nbw_max), b1 = min(nb, (warp + 1) * nbw_max), nbw = b1 - b0;
     uint2 *xs = reinterpret_cast<uint2 *>(mma_smem) + (size_t)warp * nbw_max * 8 * MT * 4;
     float *red = reinterpret_cast<float *>(mma_smem + (size_t)MW * nbw_max * 8 * MT * 4 * sizeof(uint2));
+    const int ntiles = MULTI ? grp.tile_start[grp.count] : grp.tile_start[1];
 
     const int my_tiles = blockIdx.x < ntiles ? (ntiles - 1 - blockIdx.x) / gridDim.x + 1 : 0;
     const int items = my_tiles * nbw_max;          // every warp walks the same item count
 
     // Load cursor: walks items (tile, block) in order with offset increments
     // only; a new tile recomputes its row offsets once.  Rows past N are
-    // clamped to N-1 (valid memory; their results are never stored).
-    const uint32_t rowb = (uint32_t)(K >> 1), srowb = (uint32_t)(K >> 4);
-    uint32_t ow0, os0, ow_d = 8 * rowb, os_d = 8 * srowb;
-    int lc_i = 0, lc_tile = blockIdx.x;
+    // clamped to N-1 (valid memory; their results are never stored).  Scale
+    // offsets are payload offsets / 8 (K/16 = (K/2)/8 bytes per row).
+    const uint32_t rowb = (uint32_t)(K >> 1);
+    const uint8_t *lw = grp.w[0], *ls = grp.s[0];
+    uint32_t ow0 = 0, ow_d = 0;
+    int lc_i = 0, lc_tile = blockIdx.x, lc_p = 0;
     auto cursor_tile = [&](int tile) {
-        const int64_t n0 = (int64_t)tile * 16;
-        const uint32_t r0 = (uint32_t)((n0 + g) < N ? (n0 + g) : (N - 1));
-        const uint32_t r1 = (uint32_t)((n0 + g + 8) < N ? (n0 + g + 8) : (N - 1));
-        ow0 = r0 * rowb + (uint32_t)b0 * 64 + 16 * tt;
-        os0 = r0 * srowb + (uint32_t)b0 * 8 + 2 * tt;
-        ow_d = (r1 - r0) * rowb;
-        os_d = (r1 - r0) * srowb;
         lc_tile = tile;
         lc_i = 0;
+        if (tile >= ntiles) return;
+        int64_t Np, n0;
+        if (MULTI) {
+            while (lc_p + 1 < grp.count && tile >= grp.tile_start[lc_p + 1]) lc_p++;
+            Np = grp.N[lc_p];
+            lw = grp.w[lc_p];
+            ls = grp.s[lc_p];
+            n0 = (int64_t)(tile - grp.tile_start[lc_p]) * 16;
+        } else {
+            Np = grp.N[0];
+            n0 = (int64_t)tile * 16;
+        }
+        const uint32_t r0 = (uint32_t)((n0 + g) < Np ? (n0 + g) : (Np - 1));
+        const uint32_t r1 = (uint32_t)((n0 + g + 8) < Np ? (n0 + g + 8) : (Np - 1));
+        ow0 = r0 * rowb + (uint32_t)b0 * 64 + 16 * tt;
+        ow_d = (r1 - r0) * rowb;
     };
     cursor_tile(blockIdx.x);
-    int lu = 0;                                    // items issued so far
     auto load_next = [&](Blk &r) {
-        if (lu < items) {
+        if (lc_tile < ntiles) {
             if (lc_i < nbw) {
-                r.p0 = ldg_stream16(t.w + ow0);
-                r.p1 = ldg_stream16(t.w + ow0 + ow_d);
-                r.s0 = ldg_stream2(t.scales + os0);
-                r.s1 = ldg_stream2(t.scales + os0 + os_d);
+                const uint8_t *bw = MULTI ? lw : grp.w[0], *bs = MULTI ? ls : grp.s[0];
+                r.p0 = ldg_stream16(bw + ow0);
+                r.p1 = ldg_stream16(bw + ow0 + ow_d);
+                r.s0 = ldg_stream2(bs + (ow0 >> 3));
+                r.s1 = ldg_stream2(bs + ((ow0 + ow_d) >> 3));
             }
             ow0 += 64;
-            os0 += 8;
             if (++lc_i == nbw_max) cursor_tile(lc_tile + gridDim.x);
-            ++lu;
         }
     };
     Blk buf[PD];
@@ -261,17 +287,17 @@ __global__ void __launch_bounds__(MW * 32, Q4_MMA_MINB) gemv_mma_nvfp4(Tensor t,
     asm volatile("griddepcontrol.wait;" ::: "memory");
 
     float inv[MT];
-    const bool exact = nbw > 0 ? stage_x<XT, MT>(x, K, M, b0, nbw, lane, xs, inv) : true;
-    if (nbw <= 0)
 #pragma unroll
-        for (int m = 0; m < MT; m++) inv[m] = 1.0f;
+    for (int m = 0; m < MT; m++) inv[m] = 1.0f;
+    bool exact = true;
+    int staged = -1;                                   // member whose x is in shared memory
     const int mlane = g < M ? g : 0;
     const uint2 *xbase = xs + mlane * 4 + tt;
 
     float dacc[NACC][4];
 #pragma unroll
     for (int a = 0; a < NACC; a++) dacc[a][0] = dacc[a][1] = dacc[a][2] = dacc[a][3] = 0.0f;
-    int ci = 0, ctile = blockIdx.x, par = 0;       // compute cursor
+    int ci = 0, ctile = blockIdx.x, cp = 0, par = 0;   // compute cursor
     const uint2 *xb = xbase;
     for (int u0 = 0; u0 < items; u0 += PD) {
 #pragma unroll
@@ -279,6 +305,18 @@ __global__ void __launch_bounds__(MW * 32, Q4_MMA_MINB) gemv_mma_nvfp4(Tensor t,
             const int u = u0 + q;
             if (u < items) {
                 const int i = ci;
+                if (i == 0) {                          // a new tile: its member's x staged?
+                    if (MULTI) {
+                        while (cp + 1 < grp.count && ctile >= grp.tile_start[cp + 1]) cp++;
+                        if (staged < 0 || grp.x[cp] != grp.x[staged]) {
+                            staged = cp;
+                            if (nbw > 0) exact = stage_x<XT, MT>(grp.x[cp], K, M, b0, nbw, lane, xs, inv);
+                        }
+                    } else if (staged < 0) {
+                        staged = 0;
+                        if (nbw > 0) exact = stage_x<XT, MT>(grp.x[0], K, M, b0, nbw, lane, xs, inv);
+                    }
+                }
                 const Blk r = buf[q];
                 load_next(buf[q]);
                 if (i < nbw && exact) {
@@ -305,7 +343,9 @@ __global__ void __launch_bounds__(MW * 32, Q4_MMA_MINB) gemv_mma_nvfp4(Tensor t,
                 if (++ci == nbw_max) { ci = 0; ctile += gridDim.x; xb = xbase; }
                 if (i == nbw_max - 1) {
                     // ---- end of tile `ti`: partials -> shared, one barrier, final sum
-                    const int64_t n0 = (int64_t)ti * 16;
+                    const int mb = MULTI ? cp : 0;
+                    const int64_t Np = grp.N[mb];
+                    const int64_t n0 = (int64_t)(ti - grp.tile_start[mb]) * 16;
                     float *rw = red + (par * MW + warp) * 16 * MT;
                     float d[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
@@ -320,18 +360,20 @@ __global__ void __launch_bounds__(MW * 32, Q4_MMA_MINB) gemv_mma_nvfp4(Tensor t,
                             if (mm == 2 * tt + 1) { rw[g * MT + mm] = d[1] * inv[mm]; rw[(g + 8) * MT + mm] = d[3] * inv[mm]; }
                         }
                     } else {
-                        warp_rows_f32<XT, MT>(t, x, M, n0, b0, b1, lane, rw);
+                        warp_rows_f32<XT, MT>(grp.w[mb], grp.s[mb], Np, K, grp.x[mb], M, n0, b0, b1, lane, rw);
                     }
                     __syncthreads();
                     const float *rt = red + par * MW * 16 * MT;
                     par ^= 1;
+                    float *yp = grp.y[mb];
+                    const float s2 = grp.scale2[mb];
                     for (int e = threadIdx.x; e < 16 * MT; e += blockDim.x) {
                         const int rr = e / MT, m = e % MT;
                         const int64_t n = n0 + rr;
-                        if (n < N && m < M) {
+                        if (n < Np && m < M) {
                             float sum = 0.0f;
                             for (int w = 0; w < MW; w++) sum += rt[w * 16 * MT + e];
-                            y[(int64_t)m * N + n] = sum * t.scale2;
+                            yp[(int64_t)m * Np + n] = sum * s2;
                         }
                     }
                 }
@@ -353,11 +395,12 @@ size_t smem_bytes(int64_t K, int mt) {
 
 int mt_for(int64_t M) { return M == 1 ? 1 : (M == 2 ? 2 : (M <= 4 ? 4 : 8)); }
 
-template <typename XT, int MT>
-cudaError_t run(const Tensor &t, const XT *x, float *y, int M, cudaStream_t s) {
-    auto kern = gemv_mma_nvfp4<XT, MT>;
-    const size_t smem = smem_bytes(t.K, MT);
+template <typename XT, int MT, bool MULTI>
+cudaError_t run_group(const Group<XT> &grp, int64_t K, int M, cudaStream_t s) {
+    auto kern = gemv_mma_nvfp4<XT, MT, MULTI>;
+    const size_t smem = smem_bytes(K, MT);
     static bool attr_set[64] = {};
+    static int bps_cache[64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
     if (!attr_set[dev & 63]) {
@@ -365,9 +408,11 @@ cudaError_t run(const Tensor &t, const XT *x, float *y, int M, cudaStream_t s) {
         if (e != cudaSuccess) return e;
         attr_set[dev & 63] = true;
     }
-    const int nb = (int)(t.K >> 7), nbw_max = (nb + MW - 1) / MW;
-    const int ntiles = (int)((t.N + 15) / 16);
-    int grid = max_blocks_mma(kern, smem) * sm_count();
+    const int nb = (int)(K >> 7), nbw_max = (nb + MW - 1) / MW;
+    const int ntiles = grp.tile_start[grp.count];
+    // occupancy measured once with the largest x area (smem only shrinks below it)
+    if (!bps_cache[dev & 63]) bps_cache[dev & 63] = max_blocks_mma(kern, smem);
+    int grid = bps_cache[dev & 63] * sm_count();
     if (grid > ntiles) grid = ntiles;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid, 1, 1);
@@ -379,7 +424,36 @@ cudaError_t run(const Tensor &t, const XT *x, float *y, int M, cudaStream_t s) {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, t, x, y, M, nbw_max, ntiles);
+    return cudaLaunchKernelEx(&cfg, kern, grp, K, M, nbw_max);
+}
+
+template <typename XT>
+cudaError_t launch_group_x(const Tensor *ts, const void *const *xs, float *const *ys, int count, int64_t M,
+                           cudaStream_t s) {
+    Group<XT> grp = {};
+    grp.count = count;
+    grp.tile_start[0] = 0;
+    for (int i = 0; i < count; i++) {
+        grp.w[i] = ts[i].w;
+        grp.s[i] = ts[i].scales;
+        grp.x[i] = (const XT *)xs[i];
+        grp.y[i] = ys[i];
+        grp.N[i] = ts[i].N;
+        grp.scale2[i] = ts[i].scale2;
+        grp.tile_start[i + 1] = grp.tile_start[i] + (int)((ts[i].N + 15) / 16);
+    }
+    const int64_t K = ts[0].K;
+    const int m = (int)M;
+    if (count > 1) {
+        if (m == 1) return run_group<XT, 1, true>(grp, K, m, s);
+        if (m == 2) return run_group<XT, 2, true>(grp, K, m, s);
+        if (m <= 4) return run_group<XT, 4, true>(grp, K, m, s);
+        return run_group<XT, 8, true>(grp, K, m, s);
+    }
+    if (m == 1) return run_group<XT, 1, false>(grp, K, m, s);
+    if (m == 2) return run_group<XT, 2, false>(grp, K, m, s);
+    if (m <= 4) return run_group<XT, 4, false>(grp, K, m, s);
+    return run_group<XT, 8, false>(grp, K, m, s);
 }
 
 }  // namespace
@@ -391,20 +465,16 @@ bool gemv_mma_eligible(const Tensor &t, int64_t M) {
            (((uintptr_t)t.w | (uintptr_t)t.scales) & 15) == 0;
 }
 
-cudaError_t launch_gemv_mma(const Tensor &t, const void *x, q4_dtype xd, float *y, int64_t M, cudaStream_t s) {
-    const int m = (int)M;
-    if (xd == Q4_DT_BF16) {
-        const __nv_bfloat16 *xb = (const __nv_bfloat16 *)x;
-        if (m == 1) return run<__nv_bfloat16, 1>(t, xb, y, m, s);
-        if (m == 2) return run<__nv_bfloat16, 2>(t, xb, y, m, s);
-        if (m <= 4) return run<__nv_bfloat16, 4>(t, xb, y, m, s);
-        return run<__nv_bfloat16, 8>(t, xb, y, m, s);
-    }
-    const float *xf = (const float *)x;
-    if (m == 1) return run<float, 1>(t, xf, y, m, s);
-    if (m == 2) return run<float, 2>(t, xf, y, m, s);
-    if (m <= 4) return run<float, 4>(t, xf, y, m, s);
-    return run<float, 8>(t, xf, y, m, s);
+// Several NVFP4 GEMVs with the same K and M in one launch (each eligible on
+// its own; count <= MAXG; bf16 activations).
+cudaError_t launch_gemv_mma_group(const Tensor *ts, const void *const *xs, float *const *ys, int count, int64_t M,
+                                  cudaStream_t s) {
+    if (count < 1 || count > MAXG) return cudaErrorInvalidValue;
+    return launch_group_x<__nv_bfloat16>(ts, xs, ys, count, M, s);
+}
+
+cudaError_t launch_gemv_mma(const Tensor &t, const void *x, q4_dtype, float *y, int64_t M, cudaStream_t s) {
+    return launch_gemv_mma_group(&t, &x, &y, 1, M, s);
 }
 
 }  // namespace q4

@@ -105,6 +105,41 @@ int q4_gemv(q4_fmt fmt, const void *W_packed, const void *scales, const q4_aux *
     return e == cudaSuccess ? Q4_OK : Q4_ECUDA;
 }
 
+int q4_gemv_grouped(const q4_gemv_desc *descs, int count, int64_t M, void *stream) {
+    if (!descs || count <= 0) return Q4_EINVAL;
+    if (M <= 0) return Q4_EDIM;
+    Tensor ts[8];
+    const void *xs[8];
+    float *ys[8];
+    bool one_launch = count <= 8;
+    for (int i = 0; i < count; i++) {          // check every member before launching any
+        const q4_gemv_desc &d = descs[i];
+        Tensor t;
+        const int rc = make_tensor(d.fmt, d.W_packed, d.scales, d.aux, d.N, d.K, t);
+        if (rc) return rc;
+        if (d.fmt == Q4_NVFP4_SPLITHALF || d.fmt == Q4_LOGICAL) return Q4_EUNSUPPORTED;
+        if (!d.x || !d.y) return Q4_EINVAL;
+        if (!aligned16(d.x) || !aligned16(d.y)) return Q4_EALIGN;
+        const q4_dtype xd = d.aux ? d.aux->x_dtype : default_x_dtype(d.fmt);
+        if (xd != Q4_DT_F32 && xd != Q4_DT_BF16) return Q4_EINVAL;
+        if (i < 8) {
+            ts[i] = t;
+            xs[i] = d.x;
+            ys[i] = d.y;
+        }
+        one_launch = one_launch && d.fmt == Q4_NVFP4 && xd == Q4_DT_BF16 && d.K == descs[0].K && M <= 8 &&
+                     gemv_mma_eligible(t, M);
+    }
+    if (one_launch)
+        return launch_gemv_mma_group(ts, xs, ys, count, M, (cudaStream_t)stream) == cudaSuccess ? Q4_OK : Q4_ECUDA;
+    for (int i = 0; i < count; i++) {
+        const q4_gemv_desc &d = descs[i];
+        const int rc = q4_gemv(d.fmt, d.W_packed, d.scales, d.aux, d.x, d.y, M, d.N, d.K, stream);
+        if (rc) return rc;
+    }
+    return Q4_OK;
+}
+
 int q4_dequant(q4_fmt fmt, const void *W_packed, const void *scales, const q4_aux *aux, void *out, int64_t N,
                int64_t K, void *stream) {
     Tensor t;

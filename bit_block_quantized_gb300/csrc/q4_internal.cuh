@@ -203,6 +203,8 @@ cudaError_t launch_gemm_tc(const Tensor &t, const void *x, q4_dtype x_dtype, flo
                            cudaStream_t s, bool *handled);
 bool gemv_mma_eligible(const Tensor &t, int64_t M);
 cudaError_t launch_gemv_mma(const Tensor &t, const void *x, q4_dtype xd, float *y, int64_t M, cudaStream_t s);
+cudaError_t launch_gemv_mma_group(const Tensor *ts, const void *const *xs, float *const *ys, int count, int64_t M,
+                                  cudaStream_t s);
 int launch_repack(q4_fmt src, const Tensor &t, q4_fmt dst, void *dst_w, void *dst_scales,
                   void *dst_zeros, int32_t *perm_out, cudaStream_t s);
 int run_validate(const Tensor &t, int64_t *d_bad, cudaStream_t s);

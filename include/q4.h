@@ -112,6 +112,29 @@ typedef struct {
 int q4_gemv(q4_fmt fmt, const void *W_packed, const void *scales, const q4_aux *aux,
             const void *x, float *y, int64_t M, int64_t N, int64_t K, void *stream);
 
+/* One GEMV of a group (see q4_gemv_grouped). */
+typedef struct {
+    q4_fmt fmt;
+    const void *W_packed;
+    const void *scales;
+    const q4_aux *aux;
+    const void *x;         /* [M][K] */
+    float *y;              /* [M][N] */
+    int64_t N, K;
+} q4_gemv_desc;
+
+/* Several independent GEMVs with the same batch M, e.g. the projections of
+ * one decoder layer that read the same activations (q/k/v, gate/up) -- the
+ * grouping the pages' decode path applies per layer ([W4K] section 7d: one
+ * token streams every weight once).  When every member is NVFP4 with bf16 x,
+ * all share K, count <= 8 and each takes the tensor-core path, the group runs
+ * as ONE persistent launch whose tile list spans all members (no launch gap
+ * or ramp between them); otherwise each member is issued as its own q4_gemv.
+ * Members must be independent: no y may alias another member's x or weights.
+ * Same checks, accuracy and stream semantics as q4_gemv; if any member is
+ * rejected nothing is launched. */
+int q4_gemv_grouped(const q4_gemv_desc *descs, int count, int64_t M, void *stream);
+
 /* out[N][K] = w_hat, f32 or bf16 per aux->out_dtype, by the pinned per-format
  * rule ([MUS7] 7.2 for NVFP4; the per-format sections cited above).  Bit-exact
  * with the definition.  Asynchronous on `stream`. */

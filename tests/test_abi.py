@@ -105,3 +105,8 @@ def test_host_side_rejections(lib):
     assert q4.q4_repack("gptq", A, B, q4.make_aux(zeros=C), "awq", B, C, D, None, 12, 256,
                         stream=0, check=False) == q4.Q4_EDIM
     assert q4.q4_validate("nvfp4", A, B, nv, 4, 64, 0, stream=0) == q4.Q4_EINVAL
+    good = ("nvfp4", A, B, nv, C, D, 64, 64)
+    assert q4.q4_gemv_grouped([good, ("nvfp4", A, B, nv, C, D + 4, 64, 64)], 1, stream=0,
+                              check=False) == q4.Q4_EALIGN      # nothing launched
+    assert q4.q4_gemv_grouped([good], 0, stream=0, check=False) == q4.Q4_EDIM
+    assert q4.q4_gemv_grouped([], 1, stream=0, check=False) == q4.Q4_EINVAL

@@ -179,6 +179,43 @@ def test_gemv_nvfp4_wide_dynamic_range_x():
         assert ok, worst
 
 
+@pytest.mark.parametrize("M", [1, 4])
+def test_gemv_grouped_matches_oracle(M):
+    """One launch over several NVFP4 members sharing K: shared and separate x,
+    ragged N per member; then a mixed-format group (issued member by member)."""
+    K = 2048
+    layers = [synth.make_layer("nvfp4", N, K, config=32, matrix=i, row_scale=True)
+              for i, N in enumerate((45, 16, 263, 7))]
+    xb0, xf0 = synth.draw_x(M, K, config=32, matrix=9)
+    xb1, xf1 = synth.draw_x(M, K, config=32, matrix=10)
+    xs = [(xb0, xf0), (xb0, xf0), (xb1, xf1), (xb0, xf0)]
+    devs = [to_device(L) for L in layers]
+    xd = {id(xb0): x_device(xb0), id(xb1): x_device(xb1)}
+    ys = [torch.full((M, L["N"]), float("nan"), device="cuda") for L in layers]
+    auxes = [aux_for(L, d, x_dtype=torch.bfloat16) for L, d in zip(layers, devs)]
+    descs = [("nvfp4", d["w"], d["scales"], a, xd[id(xb)], y, L["N"], K)
+             for L, d, a, (xb, _), y in zip(layers, devs, auxes, xs, ys)]
+    q4.q4_gemv_grouped(descs, M)
+    torch.cuda.synchronize()
+    for L, (_, xf), y in zip(layers, xs, ys):
+        ref, bound = oracle.gemv(to_oracle(L), xf)
+        ok, worst = within_tolerance(y.cpu().numpy(), ref, bound)
+        assert ok, worst
+    # mixed formats fall back to one q4_gemv per member
+    q = synth.make_layer("q4k", 20, K, config=32, matrix=7)
+    dq = to_device(q)
+    xq = x_device(xf0.astype(np.float32))
+    yq = torch.full((M, 20), float("nan"), device="cuda")
+    descs2 = [descs[0], ("q4k", dq["w"], None, aux_for(q, dq, x_dtype=torch.float32), xq, yq, 20, K)]
+    ys[0].fill_(float("nan"))
+    q4.q4_gemv_grouped(descs2, M)
+    torch.cuda.synchronize()
+    for L, xf, y in ((layers[0], xf0, ys[0]), (q, xf0, yq)):
+        ref, bound = oracle.gemv(to_oracle(L), xf)
+        ok, worst = within_tolerance(y.cpu().numpy(), ref, bound)
+        assert ok, worst
+
+
 def test_gemv_pipeline_long_rows_and_tails():
     """R=2 tiles (K > 8192), a ragged last tile, one row, and N < grid."""
     for N, K in ((4099, 14336), (1, 14336), (3, 8448), (1029, 4096)):
