@@ -61,6 +61,8 @@ def lib() -> ctypes.CDLL:
         L.q4_gemv_grouped.argtypes = [ctypes.POINTER(GemvDesc), I32, I64, P]
         L.q4_repack.argtypes = [I32, P, P, AUXP, I32, P, P, P, P, I64, I64, P]
         L.q4_validate.argtypes = [I32, P, P, AUXP, I64, I64, P, P]
+        L.q4_validate_noalloc.argtypes = [I32, P, P, AUXP, I64, I64, ctypes.POINTER(ctypes.c_int64), P]
+        L.q4_validate_noalloc.restype = ctypes.c_int
         for f in ("q4_gemv", "q4_gemv_grouped", "q4_dequant", "q4_repack", "q4_validate", "q4_last_error"):
             getattr(L, f).restype = ctypes.c_int
         L.q4_last_error.argtypes = []
@@ -163,6 +165,15 @@ def q4_validate(fmt, W_packed, scales, aux, N, K, d_bad_count, stream=None) -> i
     """Returns the status (Q4_OK, Q4_ENAN, Q4_ESCALE2, ...) without raising."""
     return lib().q4_validate(_fmt(fmt), _ptr(W_packed), _ptr(scales), _aux_ref(aux), int(N), int(K),
                              _ptr(d_bad_count), _stream(stream))
+
+
+def q4_validate_noalloc(fmt, W_packed, scales, aux, N, K, stream=None):
+    """The no-allocation scale scan: returns (status, count) with the count of
+    NaN/Inf scale encodings read back into host memory."""
+    n = ctypes.c_int64(-1)
+    rc = lib().q4_validate_noalloc(_fmt(fmt), _ptr(W_packed), _ptr(scales), _aux_ref(aux), int(N), int(K),
+                                   ctypes.byref(n), _stream(stream))
+    return rc, int(n.value)
 
 
 def q4_last_error() -> int:

@@ -168,6 +168,27 @@ int q4_repack(q4_fmt src, const void *src_w, const void *src_scales, const q4_au
 int q4_validate(q4_fmt fmt, const void *W_packed, const void *scales, const q4_aux *aux,
                 int64_t N, int64_t K, int64_t *d_bad_count, void *stream);
 
+/* q4_validate without any device allocation by the caller.  The pages have
+ * no counterpart; this exists for callers that cannot call cudaMalloc: a
+ * loader inside a serving process whose device memory is owned by a
+ * pre-sized pool or arena, a plugin handed tensors but no allocator, or code
+ * that must avoid cudaMalloc's implicit synchronisation.  Same checks and
+ * return codes as q4_validate; the count goes to a HOST int64 (`bad_count`,
+ * may be NULL).  Its scratch is a fixed per-device array inside libq4.so
+ * (Q4_VALIDATE_NOALLOC_MAX_CHUNKS x 8 B plus 8 B, held until the process
+ * exits), one partial count per chunk of 16384 scale entries, so a tensor
+ * may hold at most Q4_VALIDATE_NOALLOC_MAX_CHUNKS * 16384 scale entries
+ * (268,435,456; an NVFP4 tensor of up to 2^32 weights); larger ones get
+ * Q4_EDIM and nothing is launched.  The first call on a device looks up the
+ * scratch address once with that device current; make that first call
+ * before any stream capture.  Every call reuses the same array and overwrites
+ * what it reads, so calls that overlap on the GPU (two streams or two host
+ * threads) race and may report each other's counts.  SYNCHRONOUS on
+ * `stream`; allocates nothing. */
+#define Q4_VALIDATE_NOALLOC_MAX_CHUNKS 16384
+int q4_validate_noalloc(q4_fmt fmt, const void *W_packed, const void *scales, const q4_aux *aux,
+                        int64_t N, int64_t K, int64_t *bad_count, void *stream);
+
 /* Sticky device-side error of the current device (e.g. Q4_ETIMEOUT from a
  * bounded mbarrier wait in the tensor-core kernel); reading it clears it.
  * Synchronizes the device. */
