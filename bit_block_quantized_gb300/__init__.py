@@ -67,6 +67,7 @@ def lib() -> ctypes.CDLL:
             getattr(L, f).restype = ctypes.c_int
         L.q4_last_error.argtypes = []
         L.q4_strerror.restype = ctypes.c_char_p
+        L.q4_last_gemv_path.restype = ctypes.c_char_p
         L.q4_strerror.argtypes = [I32]
         L.q4_packed_bytes.restype = ctypes.c_size_t
         L.q4_packed_bytes.argtypes = [I32, I64, I64]
@@ -178,6 +179,11 @@ def q4_validate_noalloc(fmt, W_packed, scales, aux, N, K, stream=None):
 
 def q4_last_error() -> int:
     return lib().q4_last_error()
+
+
+def q4_last_gemv_path() -> str:
+    """Kernel family of this thread's latest q4_gemv / q4_gemv_grouped call."""
+    return lib().q4_last_gemv_path().decode()
 
 
 def strerror(status: int) -> str:

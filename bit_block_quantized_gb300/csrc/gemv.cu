@@ -765,9 +765,11 @@ bool tma_ok(const Tensor &t) {
 template <int FMT, typename XT>
 cudaError_t rows_batch1(const Tensor &t, const XT *x, float *y, cudaStream_t s) {
     if (tma_ok<FMT, XT>(t)) {
+        note_gemv_path("gemv_rows_tma");
         if ((t.K >> 5) <= 256) return run_rows_tma<FMT, XT, 4>(t, x, y, s);
         return run_rows_tma<FMT, XT, 2>(t, x, y, s);
     }
+    note_gemv_path("gemv_rows_m1");
     return rows_m1<FMT, XT>(t, x, y, s);
 }
 
@@ -777,6 +779,7 @@ cudaError_t general(const Tensor &t, const XT *x, float *y, int64_t M, cudaStrea
     int64_t blocks = (items + 7) / 8;
     const int64_t cap = (int64_t)sm_count() * 8;
     if (blocks > cap) blocks = cap;
+    note_gemv_path("gemv_general");
     gemv_general<FMT, XT><<<(unsigned)blocks, 256, 0, s>>>(t, x, y, M);
     return cudaGetLastError();
 }
@@ -818,6 +821,7 @@ cudaError_t kmajor_mb(const Tensor &t, const XT *x, float *y, int M, cudaStream_
 
 template <int FMT, typename XT>
 cudaError_t kmajor(const Tensor &t, const XT *x, float *y, int64_t M, cudaStream_t s) {
+    note_gemv_path("gemv_kmajor");
     cudaError_t e = cudaSuccess;
     for (int64_t m0 = 0; m0 < M && e == cudaSuccess; m0 += 8) {
         const int mc = (int)((M - m0) < 8 ? (M - m0) : 8);
@@ -833,8 +837,10 @@ cudaError_t kmajor(const Tensor &t, const XT *x, float *y, int64_t M, cudaStream
 
 template <typename XT>
 cudaError_t dispatch(const Tensor &t, const XT *x, float *y, int64_t M, cudaStream_t s) {
-    if (std::is_same<XT, __nv_bfloat16>::value && gemv_mma_eligible(t, M))
+    if (std::is_same<XT, __nv_bfloat16>::value && gemv_mma_eligible(t, M)) {
+        note_gemv_path("gemv_mma");
         return launch_gemv_mma(t, x, Q4_DT_BF16, y, M, s);
+    }
     const bool fast_rows = (M == 1) && (t.K % 32 == 0) && (t.K <= 32768);
     switch (t.fmt) {
     case Q4_NVFP4:

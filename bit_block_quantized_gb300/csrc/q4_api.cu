@@ -7,6 +7,12 @@
 
 namespace q4 {
 
+namespace {
+thread_local const char *g_last_path = "";
+}  // namespace
+
+void note_gemv_path(const char *name) { g_last_path = name; }
+
 int sm_count() {
     int dev = 0, n = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 1;
@@ -130,8 +136,10 @@ int q4_gemv_grouped(const q4_gemv_desc *descs, int count, int64_t M, void *strea
         one_launch = one_launch && d.fmt == Q4_NVFP4 && xd == Q4_DT_BF16 && d.K == descs[0].K && M <= 8 &&
                      gemv_mma_eligible(t, M);
     }
-    if (one_launch)
+    if (one_launch) {
+        note_gemv_path("gemv_mma_group");
         return launch_gemv_mma_group(ts, xs, ys, count, M, (cudaStream_t)stream) == cudaSuccess ? Q4_OK : Q4_ECUDA;
+    }
     for (int i = 0; i < count; i++) {
         const q4_gemv_desc &d = descs[i];
         const int rc = q4_gemv(d.fmt, d.W_packed, d.scales, d.aux, d.x, d.y, M, d.N, d.K, stream);
@@ -139,6 +147,8 @@ int q4_gemv_grouped(const q4_gemv_desc *descs, int count, int64_t M, void *strea
     }
     return Q4_OK;
 }
+
+const char *q4_last_gemv_path(void) { return q4::g_last_path; }
 
 int q4_dequant(q4_fmt fmt, const void *W_packed, const void *scales, const q4_aux *aux, void *out, int64_t N,
                int64_t K, void *stream) {

@@ -196,6 +196,9 @@ struct Tensor {
 };
 
 int sm_count();
+// Records, per host thread, which kernel family the latest q4_gemv /
+// q4_gemv_grouped call launched (read back by q4_last_gemv_path).
+void note_gemv_path(const char *name);
 cudaError_t launch_dequant(const Tensor &t, void *out, q4_dtype out_dtype, cudaStream_t s);
 cudaError_t launch_gemv(const Tensor &t, const void *x, q4_dtype x_dtype, float *y, int64_t M,
                         cudaStream_t s);

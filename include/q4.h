@@ -102,12 +102,18 @@ typedef struct {
 } q4_aux;
 
 /* y[M][N] (f32) = x[M][K] . W^T.  The fused decode + dot of [W4K] section 1:
- * packed weights are streamed once from HBM, decoded in registers and
- * accumulated in f32; no dequantized matrix is written.  M <= 8 runs the
- * bandwidth-bound GEMV kernels; M >= 9 on NVFP4 and Q4_K runs the tcgen05
- * tensor-core kernel (weights decoded to bf16 in shared memory, f32 TMEM
- * accumulation; Q4_K weights are rounded to bf16 there).  Accuracy: within
- * 1e-5 * sum_k |w_hat||x| + 1e-6 of the exact f64 sum of the pinned w_hat.
+ * packed weights are streamed once from HBM, decoded on chip and accumulated
+ * in f32; no dequantized matrix is written.  M <= 8 runs the bandwidth-bound
+ * GEMV kernels.  M >= 9 with bf16 x on NVFP4 or Q4_K (K % 256 == 0) runs the
+ * tcgen05 tensor-core kernel: weights decoded to bf16 straight into tensor
+ * memory, x tiles by TMA, f32 accumulation in TMEM, K split over a cluster
+ * and reduced in a fixed order (repeated calls agree bit for bit), batch in
+ * chunks of 128.  NVFP4's staged e2m1*e4m3 product is exact in bf16; Q4_K's
+ * f32 weight is rounded once to bf16 there, so its accuracy statement is
+ * against RNE_bf16(w_hat).  Other M >= 9 cases run the general GEMV kernel.
+ * Accuracy: within 1e-5 * sum_k |w||x| + 1e-6 of the exact f64 sum of the
+ * pinned w_hat (bf16-rounded for the Q4_K tensor-core case).  The tensor-core
+ * kernel's waits are bounded: a timeout is reported by q4_last_error.
  * Returns Q4_OK or a status; asynchronous on `stream`. */
 int q4_gemv(q4_fmt fmt, const void *W_packed, const void *scales, const q4_aux *aux,
             const void *x, float *y, int64_t M, int64_t N, int64_t K, void *stream);
@@ -193,6 +199,13 @@ int q4_validate_noalloc(q4_fmt fmt, const void *W_packed, const void *scales, co
  * bounded mbarrier wait in the tensor-core kernel); reading it clears it.
  * Synchronizes the device. */
 int q4_last_error(void);
+
+/* Name of the kernel family the calling host thread's latest q4_gemv or
+ * q4_gemv_grouped launched ("gemm_tc", "gemv_mma", "gemv_mma_group",
+ * "gemv_rows_tma", "gemv_rows_m1", "gemv_general", "gemv_kmajor"; "" before
+ * the first call).  A diagnostic with no counterpart in the pages: it lets a
+ * caller (and the tests) confirm which path a shape takes.  Static storage. */
+const char *q4_last_gemv_path(void);
 
 /* Human-readable text of a status code (static storage). */
 const char *q4_strerror(int status);

@@ -193,6 +193,21 @@ def gemv(t: Tensor, x: np.ndarray, rows=None):
     return y, bound
 
 
+def gemm_bf16_weights(t: Tensor, x: np.ndarray, rows=None):
+    """(y, bound) with every weight first rounded once to bf16.
+
+    The small-batch tensor-core path stages weight tiles as bf16.  NVFP4's
+    staged value v*dec(s) is exact there, but Q4_K's f32 weight
+    fl(q*d*sc - dmin*m) ([FBTC] sections 5-6) generally is not; the reading
+    for that path is w_bf16 = RNE_bf16(w_hat), then y = sum_k w_bf16 x in f64
+    and bound = sum_k |w_bf16||x|.  ``x`` is f32 [M][K]; the result is
+    [M][len(rows)] like :func:`gemv`."""
+    x = np.atleast_2d(np.asarray(x, dtype=np.float32)).astype(np.float64)
+    assert x.shape[1] == t.K
+    wb = bf16_bits_to_f32(round_bf16(dequant(t, rows))).astype(np.float64)
+    return x @ wb.T, np.abs(x) @ np.abs(wb).T
+
+
 def count_nan_scales(fmt, scales: np.ndarray) -> int:
     s = np.ascontiguousarray(scales, dtype=np.uint8)
     f = FMT[fmt] if isinstance(fmt, str) else int(fmt)

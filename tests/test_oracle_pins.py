@@ -455,3 +455,62 @@ def test_repack_act_order_permutation():
     assert np.all(np.diff(g_idx[perm]) >= 0)
     dst = oracle.dequant(oracle.Tensor("awq", N, K, aw, as_, az))
     assert np.array_equal(dst, src[:, perm])                    # same weights, K permuted
+
+
+# ------------------------------------------- bf16-staged weights (tensor-core GEMM)
+
+def _q4k_single_weight_block(d_bits):
+    """One Q4_K super-block whose only nonzero weight is k = 0 with
+    w_hat = d * sc_0 * q - dmin * m_0 = d (sc_0 = 1, m_0 = 0, q = 1, dmin = 0)."""
+    blk = np.zeros(144, np.uint8)
+    blk[0:2] = np.array([d_bits], np.uint16).view(np.uint8)
+    blk[4] = 1          # sc_0 = B[0] & 63
+    blk[16] = 0x01      # code byte 0, low nibble: k = 0
+    return oracle.Tensor("q4k", 1, 256, blk.reshape(1, 1, 144))
+
+
+@pytest.mark.parametrize("d, want", [
+    (1 + 2**-8 + 2**-10, 1 + 2**-7),   # above the midpoint: rounds up
+    (1 + 2**-8, 1.0),                  # exact tie, even neighbour below
+    (1 + 2**-7 + 2**-8, 1 + 2**-6),    # exact tie, even neighbour above
+    (1 + 2**-7, 1 + 2**-7),            # representable: unchanged
+])
+def test_bf16_weight_rounding_closed_form(d, want):
+    """bf16 keeps 8 significant bits: these f16 weights sit on, between and at
+    the midpoints of the bf16 grid near 1, so round-to-nearest-even is fixed
+    by hand."""
+    t = _q4k_single_weight_block(int(np.array([d], np.float16).view(np.uint16)[0]))
+    assert oracle.dequant(t)[0, 0] == np.float32(d)
+    x = np.zeros((2, 256), np.float32)
+    x[0, 0] = 1.0
+    x[1, 0] = -3.0
+    y, b = oracle.gemm_bf16_weights(t, x)
+    assert y[0, 0] == want and y[1, 0] == -3.0 * want
+    assert b[1, 0] == 3.0 * want
+
+
+def test_bf16_weights_equal_gemv_when_weights_are_bf16():
+    """NVFP4 with a power-of-two scale2: w_hat = v*dec(s)*2^j has <= 6
+    significant bits, so rounding to bf16 changes nothing and the result is
+    the independent f64 GEMV's."""
+    import synth
+    W = synth.draw_weights(24, 512, config=0, matrix=9)
+    p, s, _ = synth.quantize_nvfp4(W)
+    t = oracle.Tensor("nvfp4", 24, 512, p, s, scale2=0.25)
+    x = np.random.default_rng(4).normal(size=(3, 512)).astype(np.float32)
+    y, b = oracle.gemm_bf16_weights(t, x)
+    y0, b0 = oracle.gemv(t, x)
+    assert np.allclose(y, y0, rtol=1e-13, atol=1e-15) and np.allclose(b, b0, rtol=1e-13)
+
+
+def test_bf16_weights_against_torch_rounding():
+    """The rounding step agrees with torch's own float32 -> bfloat16 cast on a
+    random Q4_K tensor (rows subset included)."""
+    t = _random_tensor("q4k", 12, 512, 5)
+    x = np.random.default_rng(6).normal(size=(2, 512)).astype(np.float32)
+    Wt = torch.from_numpy(oracle.dequant(t)).to(torch.bfloat16).to(torch.float64).numpy()
+    ref = np.array([[math.fsum(Wt[n] * x[m].astype(np.float64)) for n in range(12)] for m in range(2)])
+    y, _ = oracle.gemm_bf16_weights(t, x)
+    assert np.allclose(y, ref, rtol=1e-12, atol=1e-14)
+    y2, _ = oracle.gemm_bf16_weights(t, x, rows=[7, 0])
+    assert np.allclose(y2, y[:, [7, 0]], rtol=1e-15, atol=0)
