@@ -53,6 +53,11 @@ def parse():
     ap.add_argument("--ncu-case", action="store_true",
                     help="small profiling case: 4 launches of the gate GEMV (14336x4096) on one "
                          "weight copy (33 MB), no timing, no JSON line")
+    ap.add_argument("--ncu-gemm-case", default=None, metavar="FMT:M",
+                    help="small profiling case of the tensor-core small-batch GEMM: 3 launches of "
+                         "FMT (nvfp4|q4k) at batch M on one 14336x4096 weight copy")
+    ap.add_argument("--no-small-m", action="store_true",
+                    help="skip the small-batch tensor-core GEMM measurements")
     return ap.parse_args()
 
 
@@ -298,6 +303,8 @@ def run_ours(args, rank, world):
         "gpu_launches": 3 * args.steps,
         "clocks": clk.summary(),
     }
+    if not args.no_small_m:
+        line["small_m_gemm"] = small_m_gemm(torch, q4, synth, peak)
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args.cpu_seconds, host)
     return line
@@ -431,6 +438,94 @@ def run_reference(args, rank, world):
                     "d2h_bytes_per_step": 0}}
 
 
+GEMM_SHAPE = (14336, 4096)
+GEMM_BATCHES = (16, 64, 128)
+
+
+def small_m_gemm(torch, q4, synth, peak_hbm):
+    """The small-batch tensor-core GEMM, Y[M][N] = X . W^T for M in 16/64/128
+    on the 14336 x 4096 layer, NVFP4 and Q4_K weights drawn like the 1024 x
+    4096 NVFP4 case (W ~ N(0, 0.02)), x ~ N(0, 1) bf16, f32 y.  Each launch
+    reads a different one of 6 weight copies (> L2); CUDA events on the
+    launching stream.  Reported per (format, M): microseconds per launch,
+    bytes moved (weights + x + y) per second, bf16 tensor TFLOP/s, and the
+    fractions of the measured HBM and bf16 peaks."""
+    N, K = GEMM_SHAPE
+    tflops_peak = None
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            tflops_peak = float(json.load(f)["bf16_tflops"])
+    except (OSError, KeyError, ValueError):
+        tflops_peak = 1900.0
+    out = []
+    stream = torch.cuda.Stream()
+    for fmt in ("nvfp4", "q4k"):
+        layer = synth.make_layer(fmt, N, K, config=4, matrix=0)
+        base = {k: (None if layer[k] is None else torch.from_numpy(
+            np.ascontiguousarray(layer[k]).view(np.int16) if layer[k].dtype == np.uint16
+            else np.ascontiguousarray(layer[k])).cuda()) for k in ("w", "scales")}
+        copies = [base] + [{k: (None if v is None else v.clone()) for k, v in base.items()} for _ in range(5)]
+        wbytes = q4.q4_packed_bytes(fmt, N, K)
+        aux = q4.make_aux(scale2=layer["scale2"], x_dtype=q4.Q4_DT_BF16, fmt=fmt)
+        for M in GEMM_BATCHES:
+            xb, _ = synth.draw_x(M, K, config=4, matrix=7)
+            x = torch.from_numpy(xb.view(np.int16)).cuda().view(torch.bfloat16)
+            y = torch.empty((M, N), dtype=torch.float32, device="cuda")
+            with torch.cuda.stream(stream):
+                def launch(i):
+                    c = copies[i % len(copies)]
+                    q4.q4_gemv(fmt, c["w"], c["scales"], aux, x, y, M, N, K, stream=stream)
+                for i in range(12):
+                    launch(i)
+                torch.cuda.synchronize()
+                reps = 120
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                for i in range(reps):
+                    launch(i)
+                b.record(stream)
+                torch.cuda.synchronize()
+            us = a.elapsed_time(b) * 1e3 / reps
+            moved = wbytes + M * K * 2 + M * N * 4
+            gbs = moved / us / 1e3
+            tf = 2.0 * M * N * K / us / 1e6
+            out.append({"fmt": fmt, "M": M, "us_per_launch": round(us, 2), "GBps": round(gbs, 1),
+                         "TFLOPs": round(tf, 1), "frac_hbm": round(gbs / peak_hbm, 4),
+                         "frac_bf16": round(tf / tflops_peak, 4), "path": q4.q4_last_gemv_path()})
+        del copies, base
+        torch.cuda.empty_cache()
+    return {"workload": f"small-batch GEMM M x {N} x {K}, NVFP4 and Q4_K (bf16 x, f32 y)",
+            "kernel": "gemm_tc_kernel (tcgen05.mma, A decoded into TMEM, x by TMA)",
+            "l2": "6 rotating weight copies, 198 MB > L2",
+            "peaks": {"hbm_GBps": peak_hbm, "bf16_TFLOPs": tflops_peak},
+            "entries": out}
+
+
+def ncu_gemm_case(spec):
+    """3 launches of the small-batch GEMM on one weight copy, for ncu."""
+    import torch
+
+    import bit_block_quantized_gb300 as q4
+    import synth
+    from bit_block_quantized_gb300 import build as q4build
+    q4build.build()
+    fmt, M = spec.split(":")
+    M = int(M)
+    N, K = GEMM_SHAPE
+    layer = synth.make_layer(fmt, N, K, config=4, matrix=0)
+    dev = {k: (None if layer[k] is None else torch.from_numpy(
+        np.ascontiguousarray(layer[k]).view(np.int16) if layer[k].dtype == np.uint16
+        else np.ascontiguousarray(layer[k])).cuda()) for k in ("w", "scales")}
+    xb, _ = synth.draw_x(M, K, config=4, matrix=7)
+    x = torch.from_numpy(xb.view(np.int16)).cuda().view(torch.bfloat16)
+    y = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    aux = q4.make_aux(scale2=layer["scale2"], x_dtype=q4.Q4_DT_BF16, fmt=fmt)
+    for _ in range(3):
+        q4.q4_gemv(fmt, dev["w"], dev["scales"], aux, x, y, M, N, K)
+    torch.cuda.synchronize()
+    print("ncu gemm case done:", q4.q4_last_gemv_path(), "last_error", q4.q4_last_error())
+
+
 def ncu_case():
     """A few launches of the dominant kernel on one matrix, for ncu captures
     sized well under a few GB of device memory."""
@@ -458,6 +553,9 @@ def main():
     args = parse()
     if args.ncu_case:
         ncu_case()
+        return
+    if args.ncu_gemm_case:
+        ncu_gemm_case(args.ncu_gemm_case)
         return
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

@@ -6,16 +6,20 @@
 // the batch, padded to 16, 32, 64 or 128 with zero rows by the TMA unit).
 // A is produced by CUDA cores, so it is written straight into tensor memory
 // (tcgen05.mma with A in TMEM): the decoded bf16 weights (4x the packed
-// bytes) never pass through shared memory, whose bandwidth would otherwise
-// cap the decode rate.  Roles per CTA (192 threads):
+// bytes) never pass through shared memory.  Roles per CTA (352 threads):
 //
-//   warps 0-3  decode: thread r streams weight row n0+r from HBM, decodes 64
-//              k per stage to bf16 pairs and stores them with tcgen05.st into
-//              lane r of a TMEM A stage; then the epilogue.
-//   warp 4     allocates TMEM; one thread issues tcgen05.mma and
-//              tcgen05.commit (which frees A/B stages and signals the end).
-//   warp 5     warms L2 with bulk prefetches of the CTA's weight slice, then
-//              one thread loads the X tiles by TMA (128-byte swizzle).
+//   warps 0-7  decode, as two warpgroups that split every 64-k stage in
+//              k halves: thread r of a warpgroup owns weight row n0+r (= TMEM
+//              lane r), reads its packed bytes from the shared-memory slot,
+//              decodes its 32 k to bf16 pairs and stores them with tcgen05.st
+//              into its 16 columns of a TMEM A stage.  Warps 0-3 run the
+//              epilogue.
+//   warp 8     allocates TMEM; one thread issues tcgen05.mma and
+//              tcgen05.commit (which frees A/X stages and signals the end).
+//   warp 9     one thread streams the weight slots by TMA (128 rows x 256 k:
+//              NVFP4 payload with a 128-byte swizzle plus its E4M3 scales,
+//              or the Q4_K super-blocks) into a ring of 2-4 slots.
+//   warp 10    one thread loads the X tiles by TMA (128-byte swizzle).
 //
 // K is split over the S CTAs of a thread-block cluster; their f32 partial
 // tiles are summed in rank order through distributed shared memory, so the
@@ -43,29 +47,36 @@ namespace {
 __device__ int g_device_error;
 
 constexpr int ROWS = 128;          // weight rows per CTA = MMA M = TMEM lanes
-constexpr int BK = 64;             // k per pipeline stage
+constexpr int BK = 64;             // k per pipeline (MMA) stage
 constexpr int A_COLS = BK / 2;     // TMEM columns per A stage (one bf16 pair per column)
-constexpr int THREADS = 192;
+constexpr int SLOT_K = 256;        // k per weight slot = 4 stages
+constexpr int PAYLOAD_BYTES = ROWS * 128;           // NVFP4: 128 rows x 128 payload bytes
+constexpr int SLOT_BYTES = PAYLOAD_BYTES + ROWS * 16;  // + 16 scale bytes a row; Q4_K: 128 x 144 B
+constexpr int DEC_WARPS = 8;
+constexpr int W_MMA = DEC_WARPS, W_TMA_W = DEC_WARPS + 1, W_TMA_X = DEC_WARPS + 2;
+constexpr int THREADS = (DEC_WARPS + 3) * 32;
 constexpr int TMEM_COLS = 256;     // two CTAs per SM share the 512 columns
 constexpr int SMEM_FLOOR = 80 * 1024;  // keeps a third CTA (which could get no TMEM) off the SM
-#ifndef Q4_TC_PD
-#define Q4_TC_PD 4
-#endif
-constexpr int PD = Q4_TC_PD;       // stages of weight bytes in registers per decode thread
-static_assert(PD % 4 == 0, "the Q4_K decoder needs the chunk index of a stage to be static");
+static_assert(SLOT_BYTES == ROWS * 144, "an NVFP4 slot and a Q4_K slot have the same size");
 
+// Both decode warpgroups work on every stage (each on half of its k range)
+// and every role walks the stage and slot rings in order, so each waiter on
+// a barrier sees all of its phases in turn -- mbarrier's parity test cannot
+// tell a phase from the one two uses later.
 template <int MB> struct Cfg {
     static constexpr int DCOLS = MB < 32 ? 32 : MB;           // accumulator columns
-    static constexpr int NS = (TMEM_COLS - DCOLS) / A_COLS;   // pipeline stages
+    static constexpr int NS = (TMEM_COLS - DCOLS) / A_COLS;   // A stages in TMEM = X stages
     static constexpr int B_BYTES = MB * BK * 2;               // one X tile: MB rows x 128 B
-    static constexpr int RING = NS * B_BYTES;
-    static constexpr int SMEM = (RING + 1024 > SMEM_FLOOR) ? RING + 1024 : SMEM_FLOOR;
-    static_assert(RING >= MB * ROWS * 4, "the f32 partial tile reuses the X ring");
+    static constexpr int XRING = NS * B_BYTES;
+    static constexpr int NW = MB <= 32 ? 4 : MB == 64 ? 3 : 2;  // weight slots in flight
+    static constexpr int WRING = NW * SLOT_BYTES;
+    static constexpr int USED = 1024 + WRING + XRING;
+    static constexpr int SMEM = USED > SMEM_FLOOR ? USED : SMEM_FLOOR;
+    static_assert(XRING >= MB * ROWS * 4, "the f32 partial tile reuses the X ring");
+    static_assert(2 * SMEM <= 227 * 1024, "two CTAs per SM");
 };
 
 struct TcArgs {
-    const uint8_t *w;   // packed weights (NVFP4 payload [N][K/2] or Q4_K blocks [N][K/256][144])
-    const uint8_t *s;   // NVFP4 E4M3 scales [N][K/16]; unused for Q4_K
     float *y;           // [M][N] f32 for this batch chunk
     int64_t N, K;
     int M;              // valid activation rows in this chunk (<= MB)
@@ -123,19 +134,14 @@ __device__ __forceinline__ void tma_2d(void *dst, const CUtensorMap *map, int c0
         "l"(map), "r"(c0), "r"(c1), "r"(smem_u32(bar))
         : "memory");
 }
-__device__ __forceinline__ void prefetch_l2(const void *p, uint32_t bytes) {
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
-}
 
-// 32 consecutive TMEM columns of this thread's lane <- v[0..31].
-__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32]) {
-    asm volatile("tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, "
-                 "%12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, "
-                 "%31, %32};" ::"r"(taddr),
+// 16 consecutive TMEM columns of this thread's lane <- v[0..15]; waits until
+// the stores are done.
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16]) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, "
+                 "%12, %13, %14, %15, %16};" ::"r"(taddr),
                  "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]),
-                 "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]),
-                 "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]),
-                 "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
+                 "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
                  : "memory");
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
@@ -154,11 +160,6 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
     uint32_t d;
     asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
-    return d;
-}
-__device__ __forceinline__ uint32_t bf16x2_mul(uint32_t a, uint32_t b) {
-    uint32_t d;
-    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
     return d;
 }
 // Two f32 -> bf16x2 (round to nearest even), `lo` in the low half.
@@ -203,50 +204,56 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity, vo
 }
 
 // ------------------------------------------------------------ NVFP4 decode
-struct NvStage {
-    uint4 a, b;   // 32 payload bytes: k0 .. k0+63 of one row
-    uint32_t s;   // their four E4M3 block scales
-};
-
-// Eight E2M1 codes of one payload word (byte j: k = 2j in the low nibble,
-// 2j+1 in the high nibble) times one block scale -> four bf16 pairs.
-// S = bf16x2 of (scale * 2^112).  The hardware convert gives the magnitude
-// codes as f16 whose low 9 bits are zero; shifted right by 3 each half is the
-// bf16 pattern of |v| * 2^-112 (a normal number).  The sign bits of the
-// nibbles (bits 3 and 7 of byte j) are placed at bits 15 and 31 by one byte
-// permute, and the bf16 multiply by S restores the exponent and applies the
-// block scale; every step is exact.
-__device__ __forceinline__ void nvfp4_word(uint32_t w, uint32_t S, uint32_t *o) {
-    uint32_t h0, h1, h2, h3;
-    e2m1x8_h2(w & 0x77777777u, h0, h1, h2, h3);
-    const uint32_t w4 = w << 4;
-    o[0] = bf16x2_mul((h0 >> 3) | (prmt(w, w4, 0x0040u) & 0x80008000u), S);
-    o[1] = bf16x2_mul((h1 >> 3) | (prmt(w, w4, 0x1050u) & 0x80008000u), S);
-    o[2] = bf16x2_mul((h2 >> 3) | (prmt(w, w4, 0x2060u) & 0x80008000u), S);
-    o[3] = bf16x2_mul((h3 >> 3) | (prmt(w, w4, 0x3070u) & 0x80008000u), S);
+__device__ __forceinline__ uint4 lds128(uint32_t saddr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(saddr));
+    return v;
 }
 
-__device__ __forceinline__ void nvfp4_stage(const NvStage &st, uint32_t (&o)[32]) {
-    const float k112 = 0x1p112f;
-    const float2 f01 = e4m3x2_f32(st.s & 0xffffu), f23 = e4m3x2_f32(st.s >> 16);
-    const uint32_t S0 = pack_bf16x2(f01.x * k112, f01.x * k112), S1 = pack_bf16x2(f01.y * k112, f01.y * k112);
-    const uint32_t S2 = pack_bf16x2(f23.x * k112, f23.x * k112), S3 = pack_bf16x2(f23.y * k112, f23.y * k112);
-    nvfp4_word(st.a.x, S0, o + 0);
-    nvfp4_word(st.a.y, S0, o + 4);
-    nvfp4_word(st.a.z, S1, o + 8);
-    nvfp4_word(st.a.w, S1, o + 12);
-    nvfp4_word(st.b.x, S2, o + 16);
-    nvfp4_word(st.b.y, S2, o + 20);
-    nvfp4_word(st.b.z, S3, o + 24);
-    nvfp4_word(st.b.w, S3, o + 28);
+// Eight E2M1 codes of one payload word (byte j: k = 2j in the low nibble,
+// 2j+1 in the high nibble) times one E4M3 block scale -> four bf16 pairs.
+// `s2` holds two scales as exact f16 (cvt.rn.f16x2.e4m3x2); HI picks which.
+// Per byte: the hardware convert gives both codes as exact f16, two
+// mixed-precision FMAs form v * scale in f32 (exact: <= 6 significant bits),
+// and one byte permute keeps the top halves of the two f32 -- their exact
+// bf16 patterns.  Two ALU and two FMA-pipe instructions per weight pair.
+#define Q4_NV_BYTE(B, OUT)                                                                                     \
+    "cvt.rn.f16x2.e2m1x2 h, " B ";\n\t"                                                                        \
+    "mov.b32 {c0, c1}, h;\n\t"                                                                                 \
+    "fma.rn.f32.f16 f0, c0, sc, 0f00000000;\n\t"                                                               \
+    "fma.rn.f32.f16 f1, c1, sc, 0f00000000;\n\t"                                                               \
+    "prmt.b32 " OUT ", f0, f1, 0x7632;\n\t"
+#define Q4_NV_WORD(SCALE_SEL)                                                                                  \
+    asm("{\n\t .reg .b8 b0, b1, b2, b3;\n\t .reg .b16 s_lo, s_hi, sc, c0, c1;\n\t .reg .b32 h, f0, f1;\n\t"     \
+        "mov.b32 {b0, b1, b2, b3}, %4;\n\t"                                                                    \
+        "mov.b32 {s_lo, s_hi}, %5;\n\t"                                                                        \
+        "mov.b16 sc, " SCALE_SEL ";\n\t" Q4_NV_BYTE("b0", "%0") Q4_NV_BYTE("b1", "%1") Q4_NV_BYTE("b2", "%2")   \
+            Q4_NV_BYTE("b3", "%3") "}"                                                                         \
+        : "=r"(o[0]), "=r"(o[1]), "=r"(o[2]), "=r"(o[3])                                                       \
+        : "r"(w), "r"(s2))
+template <int HI>
+__device__ __forceinline__ void nvfp4_word(uint32_t w, uint32_t s2, uint32_t *o) {
+    if constexpr (HI)
+        Q4_NV_WORD("s_hi");
+    else
+        Q4_NV_WORD("s_lo");
+}
+#undef Q4_NV_WORD
+#undef Q4_NV_BYTE
+
+// Half of a 64-k stage of one row: 16 payload bytes (32 codes, k = 32h ..
+// 32h+31 of the stage) and the two E4M3 scales of its 16-k groups (s2, the
+// low scale in the low byte) -> 16 bf16 pairs, column c holding k = 2c, 2c+1.
+__device__ __forceinline__ void nvfp4_half(uint4 p, uint32_t s2, uint32_t (&o)[16]) {
+    uint32_t sh;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(sh) : "h"((unsigned short)(s2 & 0xffffu)));
+    nvfp4_word<0>(p.x, sh, o + 0);
+    nvfp4_word<0>(p.y, sh, o + 4);
+    nvfp4_word<1>(p.z, sh, o + 8);
+    nvfp4_word<1>(p.w, sh, o + 12);
 }
 
 // ------------------------------------------------------------- Q4_K decode
-struct QkStage {
-    uint4 h;       // super-block header: fp16 d, fp16 dmin, 12 scale/min bytes
-    uint4 q0, q1;  // the 32 code bytes of one 64-weight chunk
-};
-
 // 6-bit scale and min of sub-block j from the 12 metadata bytes B0 (bytes
 // 0-3), B1 (4-7), B2 (8-11), [FBTC] section 6.
 __device__ __forceinline__ void q4k_sc_m(uint32_t B0, uint32_t B1, uint32_t B2, int j, uint32_t &sc, uint32_t &m) {
@@ -261,8 +268,9 @@ __device__ __forceinline__ void q4k_sc_m(uint32_t B0, uint32_t B1, uint32_t B2, 
 }
 
 // Four 4-bit codes (low nibble of each byte of L) -> two bf16 pairs of
-// fl(q*step - off): q is exact through the 2^23 + q construction, q*step is
-// exact (<= 21 significant bits), so the one FMA rounding is the pinned one.
+// RNE_bf16(fl(q*step - off)): q is exact through the 2^23 + q construction,
+// q*step is exact (<= 21 significant bits), so the one FMA rounding is the
+// pinned f32 one, and the pack rounds that once to bf16.
 __device__ __forceinline__ void q4k_quad(uint32_t L, float2 step, float2 noff, uint32_t *o) {
     const float2 m2 = make_float2(-8388608.0f, -8388608.0f);
     const float2 q01 = add2(make_float2(__uint_as_float(prmt(L, 0x4B000000u, 0x7440u)),
@@ -276,162 +284,154 @@ __device__ __forceinline__ void q4k_quad(uint32_t L, float2 step, float2 noff, u
     o[1] = pack_bf16x2(w23.x, w23.y);
 }
 
-// Chunk c of a super-block: code byte i holds k = 64c + i (low nibble,
-// sub-block 2c) and k = 64c + 32 + i (high nibble, sub-block 2c+1).  Output
-// column p holds k = 2p, 2p+1 of the chunk.
-__device__ __forceinline__ void q4k_stage(const QkStage &st, int c, uint32_t (&o)[32]) {
-    const float d = half_bits_f32(st.h.x), dmin = half_bits_f32(st.h.x >> 16);
-    uint32_t sc0, m0, sc1, m1;
-    q4k_sc_m(st.h.y, st.h.z, st.h.w, 2 * c, sc0, m0);
-    q4k_sc_m(st.h.y, st.h.z, st.h.w, 2 * c + 1, sc1, m1);
-    const float step0 = d * (float)sc0, off0 = dmin * (float)m0;
-    const float step1 = d * (float)sc1, off1 = dmin * (float)m1;
-    const float2 s0 = make_float2(step0, step0), n0 = make_float2(-off0, -off0);
-    const float2 s1 = make_float2(step1, step1), n1 = make_float2(-off1, -off1);
-    const uint32_t words[8] = {st.q0.x, st.q0.y, st.q0.z, st.q0.w, st.q1.x, st.q1.y, st.q1.z, st.q1.w};
+// Half HI of chunk c (k = 64c .. 64c+63) of a super-block with header h
+// (fp16 d, fp16 dmin, 12 metadata bytes): code byte i holds k = 64c + i in its
+// low nibble (sub-block 2c, HI = 0) and k = 64c + 32 + i in its high nibble
+// (sub-block 2c+1, HI = 1).  Output column p holds k = 2p, 2p+1 of the half.
+__device__ __forceinline__ void q4k_half(uint4 h, uint4 q0, uint4 q1, int c, int hi, uint32_t (&o)[16]) {
+    const float d = half_bits_f32(h.x), dmin = half_bits_f32(h.x >> 16);
+    uint32_t sc, m;
+    q4k_sc_m(h.y, h.z, h.w, 2 * c + hi, sc, m);
+    const float step = d * (float)sc, off = dmin * (float)m;   // both exact
+    const float2 s2 = make_float2(step, step), n2 = make_float2(-off, -off);
+    const uint32_t words[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+    const int shift = 4 * hi;
 #pragma unroll
-    for (int t = 0; t < 8; t++) {
-        const uint32_t w = words[t];
-        q4k_quad(w & 0x0F0F0F0Fu, s0, n0, o + 2 * t);             // k = 4t .. 4t+3
-        q4k_quad((w >> 4) & 0x0F0F0F0Fu, s1, n1, o + 16 + 2 * t); // k = 32 + 4t ..
-    }
+    for (int t = 0; t < 8; t++) q4k_quad((words[t] >> shift) & 0x0F0F0F0Fu, s2, n2, o + 2 * t);
 }
 
 // ------------------------------------------------------------ the kernel
-template <int FMT> struct StageOf;
-template <> struct StageOf<Q4_NVFP4> { using T = NvStage; };
-template <> struct StageOf<Q4_Q4K> { using T = QkStage; };
-
-template <int FMT>
-__device__ __forceinline__ void load_stage(const TcArgs &a, const uint8_t *wrow, const uint8_t *srow, int i,
-                                           typename StageOf<FMT>::T &st) {
-    if constexpr (FMT == Q4_NVFP4) {
-        st.a = ldg_stream16(wrow + 32 * i);
-        st.b = ldg_stream16(wrow + 32 * i + 16);
-        st.s = ldg_stream4(srow + 4 * i);
-    } else {
-        const uint8_t *blk = wrow + (i >> 2) * 144;
-        st.h = ldg_stream16(blk);
-        st.q0 = ldg_stream16(blk + 16 + 32 * (i & 3));
-        st.q1 = ldg_stream16(blk + 32 + 32 * (i & 3));
-    }
-}
+struct Maps {
+    CUtensorMap x;   // bf16 [rows][K], box 64 k x MB rows, 128-byte swizzle
+    CUtensorMap w;   // NVFP4 payload u8 [N][K/2] (box 128 x 128, 128-byte swizzle) or Q4_K u8 [N][K/256*144] (box 144 x 128)
+    CUtensorMap s;   // NVFP4 scales u8 [N][K/16], box 16 x 128 (unused for Q4_K)
+};
 
 template <int FMT, int MB>
 __global__ void __launch_bounds__(THREADS, 2)
-    gemm_tc_kernel(const __grid_constant__ TcArgs a, const __grid_constant__ CUtensorMap tmx) {
+    gemm_tc_kernel(const __grid_constant__ TcArgs a, const __grid_constant__ Maps maps) {
     using C = Cfg<MB>;
-    using Stage = typename StageOf<FMT>::T;
     extern __shared__ uint8_t smem_raw[];
-    __shared__ uint64_t full_bar[C::NS], empty_bar[C::NS], done_bar;
+    __shared__ uint64_t a_full[C::NS], a_empty[C::NS], w_full[C::NW], w_empty[C::NW], done_bar;
     __shared__ uint32_t tmem_base_s;
     __shared__ int abort_s;
 
-    uint8_t *xring = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    uint8_t *wring = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    uint8_t *xring = wring + C::WRING;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int tile = blockIdx.x / a.splits, rank = blockIdx.x % a.splits;
-    const int64_t n0 = (int64_t)tile * ROWS;
-    const int64_t kbeg = (int64_t)rank * a.k_per_cta;
-    const int nst = a.k_per_cta / BK;
+    const int n0 = tile * ROWS;
+    const int kbeg = rank * a.k_per_cta;
+    const int nst = a.k_per_cta / BK, nslots = a.k_per_cta / SLOT_K;
     volatile int *abort_flag = &abort_s;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::NS; s++) {
-            mbar_init(&full_bar[s], ROWS + 1);   // 128 decode threads + the TMA thread (with its bytes)
-            mbar_init(&empty_bar[s], 1);         // one tcgen05.commit
+            mbar_init(&a_full[s], 2 * ROWS + 1);   // the 256 decode threads + the X-tile thread
+            mbar_init(&a_empty[s], 1);         // one tcgen05.commit
+        }
+        for (int s = 0; s < C::NW; s++) {
+            mbar_init(&w_full[s], 1);          // the weight thread's arrive + its bytes
+            mbar_init(&w_empty[s], 2 * ROWS);      // the 256 decode threads that read the slot
         }
         mbar_init(&done_bar, 1);
         abort_s = 0;
         fence_mbar_init();
     }
-    if (warp == 4) tmem_alloc(&tmem_base_s);
+    if (warp == W_MMA) tmem_alloc(&tmem_base_s);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tbase = tmem_base_s;
     bool aborted = false;
 
-    if (warp < 4) {
+    if (warp < DEC_WARPS) {
         // ---------------------------------------------------------- decode
-        const int r = threadIdx.x;
-        const int64_t n = n0 + r;
-        const bool valid = n < a.N;
-        const uint8_t *wrow, *srow = nullptr;
-        if constexpr (FMT == Q4_NVFP4) {
-            wrow = a.w + (valid ? n : 0) * (a.K / 2) + kbeg / 2;
-            srow = a.s + (valid ? n : 0) * (a.K / 16) + kbeg / 16;
-        } else {
-            wrow = a.w + ((valid ? n : 0) * (a.K / 256) + kbeg / 256) * 144;
-        }
-        const uint32_t lane_base = tbase + ((uint32_t)(r & ~31) << 16) + C::DCOLS;
-        Stage ring[PD];
+        const int h = warp >> 2;                 // warpgroup: k half of every stage
+        const int r = threadIdx.x & (ROWS - 1);  // weight row in the tile = TMEM lane
+        const uint32_t lane_base = tbase + ((uint32_t)(r & ~31) << 16) + C::DCOLS + h * (A_COLS / 2);
+        for (int j = 0; j < nslots && !aborted; j++) {
+            const int wi = j % C::NW;
+            bool ok = wait_or_abort(&w_full[wi], (j / C::NW) & 1, abort_flag);
+            if (!__all_sync(0xffffffffu, ok)) {
+                aborted = true;
+                break;
+            }
+            const uint32_t slot = smem_u32(wring + wi * SLOT_BYTES);
+            uint4 meta;   // NVFP4: the row's 16 scale bytes; Q4_K: its super-block header
+            if constexpr (FMT == Q4_NVFP4)
+                meta = lds128(slot + PAYLOAD_BYTES + r * 16);
+            else
+                meta = lds128(slot + r * 144);
 #pragma unroll
-        for (int p = 0; p < PD; p++) {
-            ring[p] = Stage{};
-            if (valid && p < nst) load_stage<FMT>(a, wrow, srow, p, ring[p]);
-        }
-        for (int i0 = 0; i0 < nst && !aborted; i0 += PD) {
-#pragma unroll
-            for (int p = 0; p < PD; p++) {
-                const int i = i0 + p;
-                if (i < nst && !aborted) {
-                    const Stage cur = ring[p];
-                    if (valid && i + PD < nst) load_stage<FMT>(a, wrow, srow, i + PD, ring[p]);
-                    uint32_t o[32];
-                    if constexpr (FMT == Q4_NVFP4)
-                        nvfp4_stage(cur, o);
-                    else
-                        q4k_stage(cur, p & 3, o);   // kbeg % 256 == 0 and PD % 4 == 0: chunk = p % 4
-                    const int s = i % C::NS;
-                    bool ok = i < C::NS || wait_or_abort(&empty_bar[s], ((i / C::NS) & 1) ^ 1, abort_flag);
-                    ok = __all_sync(0xffffffffu, ok);   // tcgen05.st is warp-collective
-                    if (!ok) {
-                        aborted = true;
-                    } else {
-                        tc_fence_after();
-                        tmem_st32(lane_base + s * A_COLS, o);
-                        tc_fence_before();
-                        mbar_arrive(&full_bar[s]);
-                    }
+            for (int c = 0; c < 4; c++) {
+                const int i = 4 * j + c;
+                uint32_t o[16];
+                if constexpr (FMT == Q4_NVFP4) {
+                    // 16-byte chunk 2c+h of the row, at its 128-byte-swizzle position
+                    const uint4 p = lds128(slot + r * 128 + (((uint32_t)(2 * c + h) ^ (uint32_t)(r & 7)) << 4));
+                    const uint32_t s4 = c == 0 ? meta.x : c == 1 ? meta.y : c == 2 ? meta.z : meta.w;
+                    nvfp4_half(p, s4 >> (16 * h), o);
+                } else {
+                    const uint32_t blk = slot + r * 144 + 16 + 32 * c;
+                    q4k_half(meta, lds128(blk), lds128(blk + 16), c, h, o);
                 }
+                if (c == 3) mbar_arrive(&w_empty[wi]);   // the slot's bytes are all in registers
+                const int s = i % C::NS;
+                ok = i < C::NS || wait_or_abort(&a_empty[s], ((i / C::NS) & 1) ^ 1, abort_flag);
+                if (!__all_sync(0xffffffffu, ok)) {   // tcgen05.st is warp-collective
+                    aborted = true;
+                    break;
+                }
+                tc_fence_after();
+                tmem_st16(lane_base + s * A_COLS, o);
+                tc_fence_before();
+                mbar_arrive(&a_full[s]);
             }
         }
-    } else if (warp == 4) {
+    } else if (warp == W_MMA) {
         // ------------------------------------------------------------ MMA
         if (lane == 0) {
             constexpr uint32_t idesc = idesc_bf16<MB>();
             for (int i = 0; i < nst; i++) {
                 const int s = i % C::NS;
-                if (!wait_or_abort(&full_bar[s], (i / C::NS) & 1, abort_flag)) break;
+                if (!wait_or_abort(&a_full[s], (i / C::NS) & 1, abort_flag)) break;
                 tc_fence_after();
                 const uint32_t a_col = tbase + C::DCOLS + s * A_COLS;
                 const uint32_t b_addr = smem_u32(xring + s * C::B_BYTES);
 #pragma unroll
-                for (int j = 0; j < BK / 16; j++)
-                    mma_ts(tbase, a_col + j * 8, sw128_desc(b_addr + j * 32), idesc, (i | j) != 0);
-                mma_commit(&empty_bar[s]);
+                for (int k = 0; k < BK / 16; k++)
+                    mma_ts(tbase, a_col + k * 8, sw128_desc(b_addr + k * 32), idesc, (i | k) != 0);
+                mma_commit(&a_empty[s]);
             }
             mma_commit(&done_bar);
         }
         __syncwarp();
-    } else {
-        // ------------------------------------------------- L2 warm-up + TMA
-        for (int r = lane; r < ROWS; r += 32) {
-            const int64_t n = n0 + r;
-            if (n >= a.N) break;
-            if constexpr (FMT == Q4_NVFP4) {
-                prefetch_l2(a.w + n * (a.K / 2) + kbeg / 2, (uint32_t)(a.k_per_cta / 2));
-                prefetch_l2(a.s + n * (a.K / 16) + kbeg / 16, (uint32_t)(a.k_per_cta / 16));
-            } else {
-                prefetch_l2(a.w + (n * (a.K / 256) + kbeg / 256) * 144, (uint32_t)(a.k_per_cta / 256 * 144));
+    } else if (warp == W_TMA_W) {
+        // ---------------------------------------------------- weight slots
+        if (lane == 0) {
+            for (int j = 0; j < nslots; j++) {
+                const int wi = j % C::NW;
+                if (j >= C::NW && !wait_or_abort(&w_empty[wi], ((j / C::NW) & 1) ^ 1, abort_flag)) break;
+                uint8_t *slot = wring + wi * SLOT_BYTES;
+                mbar_arrive_expect_tx(&w_full[wi], SLOT_BYTES);
+                if constexpr (FMT == Q4_NVFP4) {
+                    tma_2d(slot, &maps.w, kbeg / 2 + j * (SLOT_K / 2), n0, &w_full[wi]);
+                    tma_2d(slot + PAYLOAD_BYTES, &maps.s, kbeg / 16 + j * (SLOT_K / 16), n0, &w_full[wi]);
+                } else {
+                    tma_2d(slot, &maps.w, (kbeg / SLOT_K + j) * 144, n0, &w_full[wi]);
+                }
             }
         }
+        __syncwarp();
+    } else if (warp == W_TMA_X) {
+        // ------------------------------------------------------- X tiles
         if (lane == 0) {
             for (int i = 0; i < nst; i++) {
                 const int s = i % C::NS;
-                if (i >= C::NS && !wait_or_abort(&empty_bar[s], ((i / C::NS) & 1) ^ 1, abort_flag)) break;
-                mbar_arrive_expect_tx(&full_bar[s], C::B_BYTES);
-                tma_2d(xring + s * C::B_BYTES, &tmx, (int)(kbeg + (int64_t)i * BK), 0, &full_bar[s]);
+                if (i >= C::NS && !wait_or_abort(&a_empty[s], ((i / C::NS) & 1) ^ 1, abort_flag)) break;
+                mbar_arrive_expect_tx(&a_full[s], C::B_BYTES);
+                tma_2d(xring + s * C::B_BYTES, &maps.x, kbeg + i * BK, 0, &a_full[s]);
             }
         }
         __syncwarp();
@@ -441,7 +441,7 @@ __global__ void __launch_bounds__(THREADS, 2)
     float *red = reinterpret_cast<float *>(xring);   // [MB][128] partial tile; the X ring is idle now
     if (warp < 4) {
         const int r = threadIdx.x;
-        const int64_t n = n0 + r;
+        const int64_t n = (int64_t)n0 + r;
         bool ok = !aborted && wait_or_abort(&done_bar, 0, abort_flag);
         ok = __all_sync(0xffffffffu, ok);
         if (ok) {
@@ -470,11 +470,16 @@ __global__ void __launch_bounds__(THREADS, 2)
         cluster.sync();   // every partial tile of the cluster is in shared memory
         if (warp < 4 && !*abort_flag) {
             const int r = threadIdx.x;
-            const int64_t n = n0 + r;
+            const int64_t n = (int64_t)n0 + r;
             const int cols = MB / a.splits;
             for (int c = rank * cols; c < (rank + 1) * cols; c++) {
-                float acc = 0.0f;
-                for (int q = 0; q < a.splits; q++) acc += cluster.map_shared_rank(red, q)[c * ROWS + r];
+                float v[8];
+#pragma unroll
+                for (int q = 0; q < 8; q++) v[q] = q < a.splits ? cluster.map_shared_rank(red + c * ROWS + r, q)[0] : 0.0f;
+                float acc = v[0];   // rank order, whatever the arrival order
+#pragma unroll
+                for (int q = 1; q < 8; q++)
+                    if (q < a.splits) acc += v[q];
                 if (c < a.M && n < a.N) a.y[(int64_t)c * a.N + n] = acc * a.mult;
             }
         }
@@ -488,7 +493,7 @@ __global__ void __launch_bounds__(THREADS, 2)
         }
     }
     __syncthreads();
-    if (warp == 4) {
+    if (warp == W_MMA) {
         tc_fence_after();
         tmem_dealloc(tbase);
     }
@@ -513,33 +518,51 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
-// Tensor map of one batch chunk of x (bf16 [rows][K]): 64 k x MB rows per
-// box, 128-byte swizzle; rows past `rows` read as zero.
-bool encode_x(CUtensorMap *map, const void *x, int64_t K, int64_t rows, int MB) {
+// One 2-D tiled tensor map: `inner` elements per row (contiguous), `rows`
+// rows `pitch` bytes apart; boxes of box_inner x box_rows; reads past either
+// edge return zeros.
+bool encode_2d(CUtensorMap *map, CUtensorMapDataType type, const void *base, int64_t inner, int64_t rows,
+               int64_t pitch, int box_inner, int box_rows, CUtensorMapSwizzle swz) {
     EncodeTiledFn enc = encode_fn();
     if (!enc) return false;
-    const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
-    const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
-    const cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)MB};
+    const cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)pitch};
+    const cuuint32_t box[2] = {(cuuint32_t)box_inner, (cuuint32_t)box_rows};
     const cuuint32_t estr[2] = {1, 1};
-    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(x), dims, strides, box, estr,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    return enc(map, type, 2, const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// The weight maps of a tensor (independent of the batch chunk).
+bool encode_weights(Maps *m, const Tensor &t) {
+    if (t.fmt == Q4_NVFP4)
+        return encode_2d(&m->w, CU_TENSOR_MAP_DATA_TYPE_UINT8, t.w, t.K / 2, t.N, t.K / 2, SLOT_K / 2, ROWS,
+                         CU_TENSOR_MAP_SWIZZLE_128B) &&
+               encode_2d(&m->s, CU_TENSOR_MAP_DATA_TYPE_UINT8, t.scales, t.K / 16, t.N, t.K / 16, SLOT_K / 16, ROWS,
+                         CU_TENSOR_MAP_SWIZZLE_NONE);
+    const int64_t row_bytes = t.K / SLOT_K * 144;
+    m->s = m->w;
+    return encode_2d(&m->w, CU_TENSOR_MAP_DATA_TYPE_UINT8, t.w, row_bytes, t.N, row_bytes, 144, ROWS,
+                     CU_TENSOR_MAP_SWIZZLE_NONE);
+}
+
+// X tiles of one batch chunk (bf16 [rows][K]): 64 k x MB rows, 128-byte
+// swizzle; rows past `rows` read as zero.
+bool encode_x(CUtensorMap *map, const void *x, int64_t K, int64_t rows, int MB) {
+    return encode_2d(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, K, rows, K * 2, BK, MB, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 // K slice per CTA: split K over up to 8 cluster ranks until the grid holds
-// about two CTAs per SM, keeping every slice >= 4 stages and (Q4_K) whole
-// super-blocks.
-int pick_splits(int64_t tiles, int64_t K, q4_fmt fmt) {
+// about two CTAs per SM, keeping every slice whole weight slots.
+int pick_splits(int64_t tiles, int64_t K) {
     const int64_t sms = sm_count();
-    const int64_t unit = fmt == Q4_Q4K ? 256 : 4 * BK;
     int S = 1;
-    while (S < 8 && tiles * S < 2 * sms && K % (2 * S) == 0 && (K / (2 * S)) % unit == 0) S *= 2;
+    while (S < 8 && tiles * S < 2 * sms && K % (2 * S) == 0 && (K / (2 * S)) % SLOT_K == 0) S *= 2;
     return S;
 }
 
 template <int FMT, int MB>
-cudaError_t launch_one(const TcArgs &args, const CUtensorMap &map, int64_t tiles, cudaStream_t s) {
+cudaError_t launch_one(const TcArgs &args, const Maps &maps, int64_t tiles, cudaStream_t s) {
     auto kern = gemm_tc_kernel<FMT, MB>;
     static bool attr_set[64] = {};
     int dev = 0;
@@ -562,24 +585,24 @@ cudaError_t launch_one(const TcArgs &args, const CUtensorMap &map, int64_t tiles
     at[0].val.clusterDim.z = 1;
     cfg.attrs = at;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, args, map);
+    return cudaLaunchKernelEx(&cfg, kern, args, maps);
 }
 
 template <int FMT>
-cudaError_t launch_mb(int MB, const TcArgs &args, const CUtensorMap &map, int64_t tiles, cudaStream_t s) {
+cudaError_t launch_mb(int MB, const TcArgs &args, const Maps &maps, int64_t tiles, cudaStream_t s) {
     switch (MB) {
-    case 16: return launch_one<FMT, 16>(args, map, tiles, s);
-    case 32: return launch_one<FMT, 32>(args, map, tiles, s);
-    case 64: return launch_one<FMT, 64>(args, map, tiles, s);
-    default: return launch_one<FMT, 128>(args, map, tiles, s);
+    case 16: return launch_one<FMT, 16>(args, maps, tiles, s);
+    case 32: return launch_one<FMT, 32>(args, maps, tiles, s);
+    case 64: return launch_one<FMT, 64>(args, maps, tiles, s);
+    default: return launch_one<FMT, 128>(args, maps, tiles, s);
     }
 }
 
 }  // namespace
 
 bool gemm_tc_eligible(const Tensor &t, q4_dtype x_dtype, int64_t M) {
-    return M >= 9 && x_dtype == Q4_DT_BF16 && (t.fmt == Q4_NVFP4 || t.fmt == Q4_Q4K) && t.K % (4 * BK) == 0 &&
-           t.K <= (1LL << 30) && (t.N + ROWS - 1) / ROWS * 8 <= (1LL << 31) - 1;
+    return M >= 9 && x_dtype == Q4_DT_BF16 && (t.fmt == Q4_NVFP4 || t.fmt == Q4_Q4K) && t.K % SLOT_K == 0 &&
+           t.K <= (1LL << 30) && t.N <= (1LL << 30);
 }
 
 cudaError_t launch_gemm_tc(const Tensor &t, const void *x, q4_dtype x_dtype, float *y, int64_t M, cudaStream_t s,
@@ -589,15 +612,14 @@ cudaError_t launch_gemm_tc(const Tensor &t, const void *x, q4_dtype x_dtype, flo
     *handled = true;
     note_gemv_path("gemm_tc");
     const int64_t tiles = (t.N + ROWS - 1) / ROWS;
-    const int S = pick_splits(tiles, t.K, t.fmt);
+    const int S = pick_splits(tiles, t.K);
+    Maps maps;
+    if (!encode_weights(&maps, t)) return cudaErrorInvalidValue;
     for (int64_t m0 = 0; m0 < M; m0 += 128) {
         const int64_t rows = M - m0 < 128 ? M - m0 : 128;
         const int MB = rows <= 16 ? 16 : rows <= 32 ? 32 : rows <= 64 ? 64 : 128;
-        CUtensorMap map;
-        if (!encode_x(&map, (const uint8_t *)x + m0 * t.K * 2, t.K, rows, MB)) return cudaErrorInvalidValue;
+        if (!encode_x(&maps.x, (const uint8_t *)x + m0 * t.K * 2, t.K, rows, MB)) return cudaErrorInvalidValue;
         TcArgs args;
-        args.w = t.w;
-        args.s = t.scales;
         args.y = y + m0 * t.N;
         args.N = t.N;
         args.K = t.K;
@@ -605,8 +627,8 @@ cudaError_t launch_gemm_tc(const Tensor &t, const void *x, q4_dtype x_dtype, flo
         args.splits = S;
         args.k_per_cta = (int)(t.K / S);
         args.mult = t.fmt == Q4_NVFP4 ? t.scale2 : 1.0f;
-        const cudaError_t e = t.fmt == Q4_NVFP4 ? launch_mb<Q4_NVFP4>(MB, args, map, tiles, s)
-                                                : launch_mb<Q4_Q4K>(MB, args, map, tiles, s);
+        const cudaError_t e = t.fmt == Q4_NVFP4 ? launch_mb<Q4_NVFP4>(MB, args, maps, tiles, s)
+                                                : launch_mb<Q4_Q4K>(MB, args, maps, tiles, s);
         if (e != cudaSuccess) return e;
     }
     return cudaGetLastError();
