@@ -58,6 +58,8 @@ def parse():
                          "FMT (nvfp4|q4k) at batch M on one 14336x4096 weight copy")
     ap.add_argument("--no-small-m", action="store_true",
                     help="skip the small-batch tensor-core GEMM measurements")
+    ap.add_argument("--no-rows", action="store_true",
+                    help="skip the per-row measurements of the other formats, dequant and repack")
     return ap.parse_args()
 
 
@@ -305,6 +307,8 @@ def run_ours(args, rank, world):
     }
     if not args.no_small_m:
         line["small_m_gemm"] = small_m_gemm(torch, q4, synth, peak)
+    if not args.no_rows:
+        line["other_rows"] = other_rows(torch, q4, synth, peak)
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args.cpu_seconds, host)
     return line
@@ -499,6 +503,114 @@ def small_m_gemm(torch, q4, synth, peak_hbm):
             "l2": "6 rotating weight copies, 198 MB > L2",
             "peaks": {"hbm_GBps": peak_hbm, "bf16_TFLOPs": tflops_peak},
             "entries": out}
+
+
+def _dev_layer(torch, layer):
+    out = {}
+    for k in ("w", "scales", "zeros", "g_idx"):
+        a = layer[k]
+        if a is None:
+            out[k] = None
+            continue
+        a = np.ascontiguousarray(a)
+        out[k] = torch.from_numpy(a.view(np.int16) if a.dtype == np.uint16 else a).cuda()
+    return out
+
+
+def _time_launches(torch, stream, launch, reps=200, warm=10):
+    with torch.cuda.stream(stream):
+        for i in range(warm):
+            launch(i)
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for i in range(reps):
+            launch(i)
+        b.record(stream)
+        torch.cuda.synchronize()
+    return a.elapsed_time(b) * 1e3 / reps
+
+
+def other_rows(torch, q4, synth, peak_hbm):
+    """Each remaining hot-path row on its own configuration's shape: the GEMV
+    of every format at batch 1 (NVFP4 also at batch 4 and 8), dequant and
+    repack.  Every launch reads a different weight copy (working set > L2);
+    CUDA events on the launching stream.  Bytes are the row's algorithmic
+    bytes: packed weights (q4_packed_bytes) + x + y for a GEMV, packed +
+    f32 output for dequant, packed in + packed out for repack."""
+    stream = torch.cuda.Stream()
+    target = 256 * 1024 * 1024
+    rows = []
+
+    def copies_of(d, nbytes):
+        n = max(2, -(-target // nbytes))
+        return [d] + [{k: (None if v is None else v.clone()) for k, v in d.items()} for _ in range(n - 1)]
+
+    def gemv_row(tag, fmt, N, K, M, config, kw, xdtype):
+        layer = synth.make_layer(fmt, N, K, config=config, matrix=0, **kw)
+        packed = q4.q4_packed_bytes(fmt, N, K)
+        cps = copies_of(_dev_layer(torch, layer), packed)
+        xb, _ = synth.draw_x(M, K, config=config, matrix=5, dtype="bf16" if xdtype == q4.Q4_DT_BF16 else "f32")
+        xa = np.ascontiguousarray(xb)
+        x = (torch.from_numpy(xa.view(np.int16)).cuda().view(torch.bfloat16) if xdtype == q4.Q4_DT_BF16
+             else torch.from_numpy(xa.astype(np.float32)).cuda())
+        y = torch.empty((M, N), dtype=torch.float32, device="cuda")
+        auxes = [q4.make_aux(scale2=layer["scale2"], zeros=c["zeros"], g_idx=c["g_idx"], group=layer["group"],
+                             x_dtype=xdtype, fmt=fmt) for c in cps]
+
+        def launch(i):
+            c = cps[i % len(cps)]
+            q4.q4_gemv(fmt, c["w"], c["scales"], auxes[i % len(cps)], x, y, M, N, K, stream=stream)
+        us = _time_launches(torch, stream, launch)
+        moved = packed + x.numel() * x.element_size() + y.numel() * 4
+        rows.append({"row": tag, "shape": f"{N}x{K}", "M": M, "us_per_launch": round(us, 2),
+                     "GBps": round(moved / us / 1e3, 1), "frac_hbm": round(moved / us / 1e3 / peak_hbm, 4),
+                     "path": q4.q4_last_gemv_path()})
+
+    gemv_row("a1 NVFP4 GEMV", "nvfp4", 14336, 4096, 4, 5, dict(row_scale=True), q4.Q4_DT_BF16)
+    gemv_row("a1 NVFP4 GEMV", "nvfp4", 14336, 4096, 8, 5, dict(row_scale=True), q4.Q4_DT_BF16)
+    gemv_row("a2 Q4_K GEMV", "q4k", 4096, 4096, 1, 1, dict(), q4.Q4_DT_F32)
+    gemv_row("a3 MXFP4 GEMV", "mxfp4", 4096, 11008, 1, 2, dict(outliers=True), q4.Q4_DT_BF16)
+    gemv_row("a4 Q4_0 GEMV", "q40", 4096, 11008, 1, 2, dict(outliers=True), q4.Q4_DT_F32)
+    gemv_row("a5 GPTQ GEMV", "gptq", 4096, 11008, 1, 2, dict(outliers=True), q4.Q4_DT_F32)
+    gemv_row("a5 AWQ GEMV", "awq", 4096, 11008, 1, 2, dict(outliers=True), q4.Q4_DT_F32)
+    torch.cuda.empty_cache()
+
+    # a6: dequant NVFP4 14336x4096 to f32 (write-bound)
+    N, K = 14336, 4096
+    layer = synth.make_layer("nvfp4", N, K, config=5, matrix=0, row_scale=True)
+    packed = q4.q4_packed_bytes("nvfp4", N, K)
+    cps = copies_of(_dev_layer(torch, layer), packed)[:6]
+    out = torch.empty((N, K), dtype=torch.float32, device="cuda")
+    aux = q4.make_aux(scale2=layer["scale2"], fmt="nvfp4")
+    us = _time_launches(torch, stream, lambda i: q4.q4_dequant("nvfp4", cps[i % len(cps)]["w"],
+                                                               cps[i % len(cps)]["scales"], aux, out, N, K,
+                                                               stream=stream), reps=60)
+    moved = packed + N * K * 4
+    rows.append({"row": "a6 dequant NVFP4 -> f32", "shape": f"{N}x{K}", "us_per_launch": round(us, 2),
+                 "GBps": round(moved / us / 1e3, 1), "frac_hbm": round(moved / us / 1e3 / peak_hbm, 4)})
+    del cps, out
+    torch.cuda.empty_cache()
+
+    # a7: repack GPTQ -> AWQ 4096x11008 (read once, write once)
+    N, K = 4096, 11008
+    layer = synth.make_layer("gptq", N, K, config=2, matrix=0, outliers=True)
+    packed = q4.q4_packed_bytes("gptq", N, K)
+    cps = copies_of(_dev_layer(torch, layer), packed)
+    w = torch.empty((K, N // 8), dtype=torch.int32, device="cuda")
+    sc = torch.empty((K // 128, N), dtype=torch.int16, device="cuda")
+    z = torch.empty((K // 128, N // 8), dtype=torch.int32, device="cuda")
+    auxes = [q4.make_aux(zeros=c["zeros"], group=128, fmt="gptq") for c in cps]
+    us = _time_launches(torch, stream, lambda i: q4.q4_repack("gptq", cps[i % len(cps)]["w"],
+                                                              cps[i % len(cps)]["scales"], auxes[i % len(cps)],
+                                                              "awq", w, sc, z, None, N, K, stream=stream))
+    moved = 2 * packed
+    rows.append({"row": "a7 repack GPTQ -> AWQ", "shape": f"{N}x{K}", "us_per_launch": round(us, 2),
+                 "GBps": round(moved / us / 1e3, 1), "frac_hbm": round(moved / us / 1e3 / peak_hbm, 4)})
+    del cps
+    torch.cuda.empty_cache()
+    return {"l2": "each launch reads a different weight copy; working set >= 256 MB per row",
+            "peak_hbm_GBps": peak_hbm, "entries": rows}
 
 
 def ncu_gemm_case(spec):

@@ -99,71 +99,67 @@ __device__ __forceinline__ void decode_word(uint32_t w, uint32_t sc2, uint32_t (
     for (int i = 0; i < 4; i++) a[i] = hmul2_u32(a[i], sc2);
 }
 
+// Four bf16 values (two words) times an exact power of two -> two f16x2
+// words; `ok` stays true only if every value survives the f16 rounding.
+__device__ __forceinline__ uint2 bf16x4_to_f16(uint2 v, float scale, bool &ok) {
+    const float f0 = __uint_as_float(v.x << 16) * scale, f1 = __uint_as_float(v.x & 0xffff0000u) * scale;
+    const float f2 = __uint_as_float(v.y << 16) * scale, f3 = __uint_as_float(v.y & 0xffff0000u) * scale;
+    const __half2 h01 = __floats2half2_rn(f0, f1), h23 = __floats2half2_rn(f2, f3);
+    const float2 c01 = __half22float2(h01), c23 = __half22float2(h23);
+    ok = ok && c01.x == f0 && c01.y == f1 && c23.x == f2 && c23.y == f3;
+    return make_uint2(*reinterpret_cast<const uint32_t *>(&h01), *reinterpret_cast<const uint32_t *>(&h23));
+}
+
 // x slice of one warp as exactly-scaled f16 B fragments, staged once per CTA:
 // entry ((i*8 + j)*MT + m)*4 + t = x[m][128(b0+i) + 32t + 4j .. +3] * 2^e_m.
-// One load pass into registers, a warp max per column, then convert.
+// Lane l serves column m = l % MT only.  Pass 1 loads 16-byte runs (8 k) of
+// that row, all independent, keeps the column max and puts the raw bf16 bits
+// straight into their two entries; the max is reduced over the lanes of the
+// column; pass 2 converts the lane's own entries in place.
 template <typename XT, int MT>
 __device__ __forceinline__ bool stage_x(const XT *__restrict__ x, int64_t K, int M, int b0, int nbw, int lane,
                                         uint2 *xs, float (&inv)[MT]) {
-    constexpr int PER = 8;                       // entries per lane per pass (covers nbw <= 2*PER/MT... loop)
-    const int entries = nbw * 8 * MT * 4;
-    float amax[MT];
-#pragma unroll
-    for (int m = 0; m < MT; m++) amax[m] = 0.0f;
-    // pass 1: max per column (register-only for the first PER*32 entries)
-    for (int e0 = 0; e0 < entries; e0 += 32 * PER) {
-#pragma unroll
-        for (int q = 0; q < PER; q++) {
-            const int e = e0 + q * 32 + lane;
-            const int te = e & 3, m = (e >> 2) % MT, j = (e / (4 * MT)) & 7, i = e / (32 * MT);
-            if (e < entries && m < M) {
-                const XT *src = x + (int64_t)m * K + (int64_t)(b0 + i) * 128 + 32 * te + 4 * j;
-                float mx = 0.0f;
-#pragma unroll
-                for (int r = 0; r < 4; r++) mx = fmaxf(mx, fabsf(x_to_f32<XT>(src[r])));
-#pragma unroll
-                for (int mm = 0; mm < MT; mm++)
-                    if (mm == m) amax[mm] = fmaxf(amax[mm], mx);
-            }
-        }
+    static_assert(sizeof(XT) == 2 && 32 % MT == 0, "bf16 activations, MT divides the warp");
+    constexpr int LPC = 32 / MT;                // lanes per column
+    const int m = lane % MT;
+    const bool mv = m < M;
+    const int nch = nbw * 16;                   // 16-byte runs in the warp's k range
+    const uint4 *src = reinterpret_cast<const uint4 *>(x + (int64_t)(mv ? m : 0) * K + (int64_t)b0 * 128);
+    uint32_t mx2 = 0;                           // packed |bf16| maximum (bit patterns order like values)
+#pragma unroll 4
+    for (int r = lane / MT; r < nch; r += LPC) {
+        const uint4 v = mv ? __ldg(src + r) : make_uint4(0u, 0u, 0u, 0u);
+        mx2 = __vmaxu2(mx2, __vmaxu2(__vmaxu2(v.x & 0x7fff7fffu, v.y & 0x7fff7fffu),
+                                     __vmaxu2(v.z & 0x7fff7fffu, v.w & 0x7fff7fffu)));
+        const int i = r >> 4, q = r & 15, t = q >> 2, j0 = (q & 3) * 2;
+        xs[((i * 8 + j0) * MT + m) * 4 + t] = make_uint2(v.x, v.y);
+        xs[((i * 8 + j0 + 1) * MT + m) * 4 + t] = make_uint2(v.z, v.w);
     }
-    float scale[MT];
+    const uint32_t mxb = (mx2 & 0xffffu) > (mx2 >> 16) ? (mx2 & 0xffffu) : (mx2 >> 16);
+    float amax = __uint_as_float(mxb << 16);
+#pragma unroll
+    for (int off = MT; off < 32; off <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+    float scale = 1.0f, iv = 1.0f;
     bool exact = true;
-#pragma unroll
-    for (int m = 0; m < MT; m++) {
-#pragma unroll
-        for (int off = 16; off >= 1; off >>= 1) amax[m] = fmaxf(amax[m], __shfl_xor_sync(0xffffffffu, amax[m], off));
-        const int ex = (int)((__float_as_uint(amax[m]) >> 23) & 255u) - 127;
-        scale[m] = 1.0f;
-        inv[m] = 1.0f;
-        if (amax[m] > 0.0f) {
-            if (ex < -100 || ex > 100) exact = false;
-            else {
-                scale[m] = __uint_as_float((uint32_t)(127 + 12 - ex) << 23);     // max |x * scale| < 2^13
-                inv[m] = __uint_as_float((uint32_t)(127 - 12 + ex) << 23);
-            }
+    if (amax > 0.0f) {
+        const int ex = (int)((__float_as_uint(amax) >> 23) & 255u) - 127;
+        if (ex < -100 || ex > 100)
+            exact = false;
+        else {
+            scale = __uint_as_float((uint32_t)(127 + 12 - ex) << 23);   // max |x * scale| < 2^13
+            iv = __uint_as_float((uint32_t)(127 - 12 + ex) << 23);
         }
     }
-    // pass 2: convert (L1-resident re-read) and check that every value survived
-    for (int e = lane; e < entries; e += 32) {
-        const int te = e & 3, m = (e >> 2) % MT, j = (e / (4 * MT)) & 7, i = e / (32 * MT);
-        uint2 v2 = make_uint2(0u, 0u);
-        if (m < M) {
-            const XT *src = x + (int64_t)m * K + (int64_t)(b0 + i) * 128 + 32 * te + 4 * j;
-            float sc = 1.0f;
-#pragma unroll
-            for (int mm = 0; mm < MT; mm++)
-                if (mm == m) sc = scale[mm];
-            float f[4];
-#pragma unroll
-            for (int r = 0; r < 4; r++) f[r] = x_to_f32<XT>(src[r]) * sc;
-            const __half2 h01 = __floats2half2_rn(f[0], f[1]), h23 = __floats2half2_rn(f[2], f[3]);
-            const float2 c01 = __half22float2(h01), c23 = __half22float2(h23);
-            exact = exact && c01.x == f[0] && c01.y == f[1] && c23.x == f[2] && c23.y == f[3];
-            v2 = make_uint2(*reinterpret_cast<const uint32_t *>(&h01), *reinterpret_cast<const uint32_t *>(&h23));
-        }
-        xs[e] = v2;
+#pragma unroll 4
+    for (int r = lane / MT; r < nch; r += LPC) {
+        const int i = r >> 4, q = r & 15, t = q >> 2, j0 = (q & 3) * 2;
+        uint2 *e0 = xs + ((i * 8 + j0) * MT + m) * 4 + t, *e1 = xs + ((i * 8 + j0 + 1) * MT + m) * 4 + t;
+        const uint2 c0 = bf16x4_to_f16(*e0, scale, exact), c1 = bf16x4_to_f16(*e1, scale, exact);
+        *e0 = c0;
+        *e1 = c1;
     }
+#pragma unroll
+    for (int mm = 0; mm < MT; mm++) inv[mm] = __shfl_sync(0xffffffffu, iv, mm);   // lane mm holds column mm
     exact = __all_sync(0xffffffffu, exact);
     __syncwarp();
     return exact;
