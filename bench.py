@@ -2,8 +2,9 @@
 
 One step = the three projections of one decoder MLP in NVFP4 at batch 1
 (gate 14336x4096, up 14336x4096, down 4096x14336): gate and up read the same
-x, down its own; each is one q4_gemv launch, chained by programmatic
-dependent launch.  The weights come from the seeded synthetic
+x and are independent, so they run as one q4_gemv_grouped launch; down (whose
+input a real MLP computes from gate and up) is its own q4_gemv launch after
+it, chained by programmatic dependent launch.  The weights come from the seeded synthetic
 recipe (W ~ N(0,0.02) with U(0.5,2) row scales, NVFP4 per 16, bf16 x).
 
 L2 policy: inputs larger than L2 -- the step rotates through distinct copies
@@ -37,7 +38,7 @@ SET = [("gate", 14336, 4096), ("up", 14336, 4096), ("down", 4096, 14336)]
 CONFIG_ID = 5          # seed block of this workload's synthetic draws
 NOMINAL_HBM_GBS = 7900.0
 FALLBACK_HBM_GBS = 6800.0
-DOMINANT = "gemv_mma_nvfp4<bf16, MT=1, single> (gate/up, 14336x4096)"
+DOMINANT = "gemv_mma_nvfp4<bf16, MT=1, pair> (gate and up, 2 x 14336x4096 in one launch)"
 
 
 def parse():
@@ -51,8 +52,8 @@ def parse():
                     help="target CPU time of the oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ncu-case", action="store_true",
-                    help="small profiling case: 4 launches of the gate GEMV (14336x4096) on one "
-                         "weight copy (33 MB), no timing, no JSON line")
+                    help="small profiling case: 4 grouped gate+up launches (2 x 14336x4096, 66 MB) on "
+                         "one weight copy, no timing, no JSON line")
     ap.add_argument("--ncu-gemm-case", default=None, metavar="FMT:M",
                     help="small profiling case of the tensor-core small-batch GEMM: 3 launches of "
                          "FMT (nvfp4|q4k) at batch M on one 14336x4096 weight copy")
@@ -83,7 +84,7 @@ def source_sha():
 def profiled_traffic():
     """DRAM bytes per launch of the dominant kernel from the committed ncu
     summary, only if it was taken on the current kernel source."""
-    p = os.path.join(ROOT, "profiles", "gemv_mma_nvfp4_14336x4096.md")
+    p = os.path.join(ROOT, "profiles", "gemv_mma_nvfp4_pair_2x14336x4096.md")
     try:
         text = open(p).read()
     except OSError:
@@ -170,6 +171,7 @@ def build_workload(torch, q4, synth):
             mats.append((name, N, K, w, s, layer["scale2"]))
         dev.append(mats)
     xs = [torch.from_numpy(h[4].view(np.int16)).cuda().view(torch.bfloat16) for h in host]
+    xs[1] = xs[0]                      # gate and up read the same activation vector
     xs[1] = xs[0]                                   # gate and up read the same activations
     ys = [torch.empty((1, N), dtype=torch.float32, device="cuda") for _, N, _ in SET]
     return host, dev, xs, ys, set_bytes, copies, l2
@@ -188,15 +190,18 @@ def run_ours(args, rank, world):
     auxes = [q4.make_aux(scale2=h[3]["scale2"], fmt="nvfp4") for h in host]
     stream = torch.cuda.Stream()
 
-    def one(j):
-        def f(c, s):
-            name, N, K, w, sc, _ = dev[c][j]
-            q4.q4_gemv("nvfp4", w, sc, auxes[j], xs[j], ys[j], 1, N, K, stream=s)
-        return f
+    def gate_up(c, s):
+        (_, N0, K0, w0, s0, _), (_, N1, K1, w1, s1, _) = dev[c][0], dev[c][1]
+        q4.q4_gemv_grouped([("nvfp4", w0, s0, auxes[0], xs[0], ys[0], N0, K0),
+                            ("nvfp4", w1, s1, auxes[1], xs[1], ys[1], N1, K1)], 1, stream=s)
+
+    def down(c, s):
+        _, N, K, w, sc, _ = dev[c][2]
+        q4.q4_gemv("nvfp4", w, sc, auxes[2], xs[2], ys[2], 1, N, K, stream=s)
 
     def step(c, s):
-        for j in range(len(SET)):
-            one(j)(c, s)
+        gate_up(c, s)
+        down(c, s)
 
     # one graph per full rotation, plus single-step graphs for the remainder
     with torch.cuda.stream(stream):
@@ -213,9 +218,9 @@ def run_ours(args, rank, world):
             with torch.cuda.graph(g, stream=stream):
                 step(c, stream)
             g_one.append(g)
-        # per-launch graphs for the roofline of each projection
+        # per-launch graphs for the roofline of each launch
         g_kern = []
-        for fn in (one(0), one(1), one(2)):
+        for fn in (gate_up, down):
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=stream):
                 for c in range(copies):
@@ -272,11 +277,13 @@ def run_ours(args, rank, world):
         return None
     peak, peak_kind = measured_hbm_peak()
     value = world * set_bytes * args.steps / (ms * 1e-3) / 1e9
-    gate_bytes = q4.q4_packed_bytes("nvfp4", 14336, 4096)
-    achieved = gate_bytes / (kern_ms[0] * 1e-3) / 1e9
-    per_kernel = {name: {"us_per_launch": round(kern_ms[j] * 1e3, 3),
-                         "GBps": round(q4.q4_packed_bytes("nvfp4", N, K) / (kern_ms[j] * 1e-3) / 1e9, 1)}
-                  for j, (name, N, K) in enumerate(SET)}
+    gate_up_bytes = 2 * q4.q4_packed_bytes("nvfp4", 14336, 4096)
+    down_bytes = q4.q4_packed_bytes("nvfp4", 4096, 14336)
+    achieved = gate_up_bytes / (kern_ms[0] * 1e-3) / 1e9
+    per_kernel = {"gate+up (one grouped launch)": {"us_per_launch": round(kern_ms[0] * 1e3, 3),
+                                                   "GBps": round(gate_up_bytes / (kern_ms[0] * 1e-3) / 1e9, 1)},
+                  "down": {"us_per_launch": round(kern_ms[1] * 1e3, 3),
+                           "GBps": round(down_bytes / (kern_ms[1] * 1e-3) / 1e9, 1)}}
     x_bytes = 4096 * 2 + 14336 * 2
     y_bytes = sum(N * 4 for _, N, _ in SET)
     line = {
@@ -290,8 +297,8 @@ def run_ours(args, rank, world):
                    "y_bytes_per_step": y_bytes,
                    "l2": f"inputs larger than L2: {copies} rotating copies of the set = "
                          f"{copies * set_bytes / 1e9:.2f} GB (L2 {l2 / 1e6:.0f} MB)",
-                   "launch": "one CUDA graph per rotation; 3 q4_gemv launches per step (gate and up "
-                             "share x), chained by programmatic dependent launch",
+                   "launch": "one CUDA graph per rotation; 2 launches per step: q4_gemv_grouped(gate, up) "
+                             "(shared x) then q4_gemv(down), chained by programmatic dependent launch",
                    "parallelism": f"replicas x{world}"},
         "pct_of_hbm_peak": {"measured": round(value / world / peak, 4),
                             "nominal_7900": round(value / world / NOMINAL_HBM_GBS, 4)},
@@ -300,9 +307,9 @@ def run_ours(args, rank, world):
                      "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
                      else "fallback 6.8 TB/s",
                      "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": profiled_traffic(),
-                     "kernel": DOMINANT, "algorithmic_bytes_per_launch": gate_bytes},
+                     "kernel": DOMINANT, "algorithmic_bytes_per_launch": gate_up_bytes},
         "e2e": e2e,
-        "gpu_launches": 3 * args.steps,
+        "gpu_launches": 2 * args.steps,
         "clocks": clk.summary(),
     }
     if not args.no_small_m:
@@ -316,8 +323,8 @@ def run_ours(args, rank, world):
 
 def run_e2e(args, torch, q4, dev, auxes, host, stream):
     """Same metric through the public API with host buffers: every step copies
-    the two activation vectors from pinned host memory, runs the three
-    q4_gemv calls, and reads the three outputs back."""
+    the two activation vectors from pinned host memory, runs the grouped
+    gate+up call and the down call, and reads the three outputs back."""
     xh_gu = torch.from_numpy(host[0][4].view(np.int16)).view(torch.bfloat16).pin_memory()
     xh_dn = torch.from_numpy(host[2][4].view(np.int16)).view(torch.bfloat16).pin_memory()
     xd_gu, xd_dn = torch.empty_like(xh_gu, device="cuda"), torch.empty_like(xh_dn, device="cuda")
@@ -329,8 +336,10 @@ def run_e2e(args, torch, q4, dev, auxes, host, stream):
     def one(c):
         xd_gu.copy_(xh_gu, non_blocking=True)
         xd_dn.copy_(xh_dn, non_blocking=True)
-        for j, (name, N, K, w, sc, _) in enumerate(dev[c]):
-            q4.q4_gemv("nvfp4", w, sc, auxes[j], xd_dn if j == 2 else xd_gu, ys_d[j], 1, N, K, stream=stream)
+        (_, N0, K0, w0, s0, _), (_, N1, K1, w1, s1, _), (_, N2, K2, w2, s2, _) = dev[c]
+        q4.q4_gemv_grouped([("nvfp4", w0, s0, auxes[0], xd_gu, ys_d[0], N0, K0),
+                            ("nvfp4", w1, s1, auxes[1], xd_gu, ys_d[1], N1, K1)], 1, stream=stream)
+        q4.q4_gemv("nvfp4", w2, s2, auxes[2], xd_dn, ys_d[2], 1, N2, K2, stream=stream)
         for j in range(3):
             ys_h[j].copy_(ys_d[j], non_blocking=True)
         stream.synchronize()
@@ -347,7 +356,8 @@ def run_e2e(args, torch, q4, dev, auxes, host, stream):
             "h2d_bytes_per_step": xh_gu.numel() * 2 + xh_dn.numel() * 2,
             "d2h_bytes_per_step": sum(N * 4 for _, N, _ in SET),
             "steps": n, "ms_per_step": dt * 1e3 / n,
-            "note": "per step: pinned x H2D (2 vectors), 3 q4_gemv, y D2H, host sync (no graph)"}
+            "note": "per step: pinned x H2D (2 vectors), q4_gemv_grouped(gate, up) + q4_gemv(down), "
+                    "y D2H, host sync (no graph)"}
 
 
 # --------------------------------------------------------- oracle on host
@@ -639,24 +649,26 @@ def ncu_gemm_case(spec):
 
 
 def ncu_case():
-    """A few launches of the dominant kernel on one matrix, for ncu captures
-    sized well under a few GB of device memory."""
+    """A few launches of the dominant kernel (gate and up as one grouped
+    launch, 66 MB) on one weight copy, for ncu captures sized well under a
+    few GB of device memory."""
     import torch
 
     import bit_block_quantized_gb300 as q4
     import synth
     from bit_block_quantized_gb300 import build as q4build
     q4build.build()
-    name, N, K = SET[0]
-    layer = synth.make_layer("nvfp4", N, K, config=CONFIG_ID, matrix=0, row_scale=True)
-    xbits, _ = synth.draw_x(1, K, config=CONFIG_ID, matrix=0)
-    w = torch.from_numpy(layer["w"]).cuda()
-    sc = torch.from_numpy(layer["scales"]).cuda()
+    mats = []
+    for i in (0, 1):
+        name, N, K = SET[i]
+        layer = synth.make_layer("nvfp4", N, K, config=CONFIG_ID, matrix=i, row_scale=True)
+        mats.append((N, K, torch.from_numpy(layer["w"]).cuda(), torch.from_numpy(layer["scales"]).cuda(),
+                     q4.make_aux(scale2=layer["scale2"], fmt="nvfp4")))
+    xbits, _ = synth.draw_x(1, SET[0][2], config=CONFIG_ID, matrix=0)
     x = torch.from_numpy(xbits.view(np.int16)).cuda().view(torch.bfloat16)
-    y = torch.empty((1, N), dtype=torch.float32, device="cuda")
-    aux = q4.make_aux(scale2=layer["scale2"], fmt="nvfp4")
+    ys = [torch.empty((1, N), dtype=torch.float32, device="cuda") for N, *_ in mats]
     for _ in range(4):
-        q4.q4_gemv("nvfp4", w, sc, aux, x, y, 1, N, K)
+        q4.q4_gemv_grouped([("nvfp4", w, s, aux, x, y, N, K) for (N, K, w, s, aux), y in zip(mats, ys)], 1)
     torch.cuda.synchronize()
     print("ncu case done, last_error", q4.q4_last_error())
 

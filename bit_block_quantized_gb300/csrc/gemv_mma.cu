@@ -215,8 +215,11 @@ template <typename XT> struct Group {
 // while the current tile finishes; one barrier per tile hands the warp
 // partials (double buffered) to a fixed-order final sum.  A warp restages its
 // x slice only when the member's activation pointer changes.
-template <typename XT, int MT, bool MULTI>
-__global__ void __launch_bounds__(MW * 32, Q4_MMA_MINB) gemv_mma_nvfp4(const __grid_constant__ Group<XT> grp,
+// MODE 0: one matrix; 1: two matrices that read the same x (e.g. gate and
+// up), the member chosen by one compare per tile; 2: any group.
+template <typename XT, int MT, int MODE>
+__global__ void __launch_bounds__(MW * 32, MT >= 8 ? 1 : Q4_MMA_MINB)
+    gemv_mma_nvfp4(const __grid_constant__ Group<XT> grp,
                                                                       int64_t K, int M, int nbw_max) {
     extern __shared__ __align__(16) uint8_t mma_smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -225,7 +228,7 @@ __global__ void __launch_bounds__(MW * 32, Q4_MMA_MINB) gemv_mma_nvfp4(const __g
     const int b0 = min(nb, warp * nbw_max), b1 = min(nb, (warp + 1) * nbw_max), nbw = b1 - b0;
     uint2 *xs = reinterpret_cast<uint2 *>(mma_smem) + (size_t)warp * nbw_max * 8 * MT * 4;
     float *red = reinterpret_cast<float *>(mma_smem + (size_t)MW * nbw_max * 8 * MT * 4 * sizeof(uint2));
-    const int ntiles = MULTI ? grp.tile_start[grp.count] : grp.tile_start[1];
+    const int ntiles = MODE == 2 ? grp.tile_start[grp.count] : grp.tile_start[MODE == 1 ? 2 : 1];
 
     const int my_tiles = blockIdx.x < ntiles ? (ntiles - 1 - blockIdx.x) / gridDim.x + 1 : 0;
     const int items = my_tiles * nbw_max;          // every warp walks the same item count
@@ -236,6 +239,7 @@ __global__ void __launch_bounds__(MW * 32, Q4_MMA_MINB) gemv_mma_nvfp4(const __g
     // offsets are payload offsets / 8 (K/16 = (K/2)/8 bytes per row).
     const uint32_t rowb = (uint32_t)(K >> 1);
     const uint8_t *lw = grp.w[0], *ls = grp.s[0];
+    bool lsec = false;                             // MODE 1: the load cursor is in the second matrix
     uint32_t ow0 = 0, ow_d = 0;
     int lc_i = 0, lc_tile = blockIdx.x, lc_p = 0;
     auto cursor_tile = [&](int tile) {
@@ -243,12 +247,16 @@ __global__ void __launch_bounds__(MW * 32, Q4_MMA_MINB) gemv_mma_nvfp4(const __g
         lc_i = 0;
         if (tile >= ntiles) return;
         int64_t Np, n0;
-        if (MULTI) {
+        if (MODE == 2) {
             while (lc_p + 1 < grp.count && tile >= grp.tile_start[lc_p + 1]) lc_p++;
             Np = grp.N[lc_p];
             lw = grp.w[lc_p];
             ls = grp.s[lc_p];
             n0 = (int64_t)(tile - grp.tile_start[lc_p]) * 16;
+        } else if (MODE == 1) {
+            lsec = tile >= grp.tile_start[1];
+            Np = lsec ? grp.N[1] : grp.N[0];
+            n0 = (int64_t)(tile - (lsec ? grp.tile_start[1] : 0)) * 16;
         } else {
             Np = grp.N[0];
             n0 = (int64_t)tile * 16;
@@ -262,7 +270,8 @@ __global__ void __launch_bounds__(MW * 32, Q4_MMA_MINB) gemv_mma_nvfp4(const __g
     auto load_next = [&](Blk &r) {
         if (lc_tile < ntiles) {
             if (lc_i < nbw) {
-                const uint8_t *bw = MULTI ? lw : grp.w[0], *bs = MULTI ? ls : grp.s[0];
+                const uint8_t *bw = MODE == 2 ? lw : MODE == 1 ? (lsec ? grp.w[1] : grp.w[0]) : grp.w[0];
+                const uint8_t *bs = MODE == 2 ? ls : MODE == 1 ? (lsec ? grp.s[1] : grp.s[0]) : grp.s[0];
                 r.p0 = ldg_stream16(bw + ow0);
                 r.p1 = ldg_stream16(bw + ow0 + ow_d);
                 r.s0 = ldg_stream2(bs + (ow0 >> 3));
@@ -302,7 +311,7 @@ __global__ void __launch_bounds__(MW * 32, Q4_MMA_MINB) gemv_mma_nvfp4(const __g
             if (u < items) {
                 const int i = ci;
                 if (i == 0) {                          // a new tile: its member's x staged?
-                    if (MULTI) {
+                    if (MODE == 2) {
                         while (cp + 1 < grp.count && ctile >= grp.tile_start[cp + 1]) cp++;
                         if (staged < 0 || grp.x[cp] != grp.x[staged]) {
                             staged = cp;
@@ -339,7 +348,7 @@ __global__ void __launch_bounds__(MW * 32, Q4_MMA_MINB) gemv_mma_nvfp4(const __g
                 if (++ci == nbw_max) { ci = 0; ctile += gridDim.x; xb = xbase; }
                 if (i == nbw_max - 1) {
                     // ---- end of tile `ti`: partials -> shared, one barrier, final sum
-                    const int mb = MULTI ? cp : 0;
+                    const int mb = MODE == 2 ? cp : MODE == 1 ? (ti >= grp.tile_start[1] ? 1 : 0) : 0;
                     const int64_t Np = grp.N[mb];
                     const int64_t n0 = (int64_t)(ti - grp.tile_start[mb]) * 16;
                     float *rw = red + (par * MW + warp) * 16 * MT;
@@ -391,9 +400,9 @@ size_t smem_bytes(int64_t K, int mt) {
 
 int mt_for(int64_t M) { return M == 1 ? 1 : (M == 2 ? 2 : (M <= 4 ? 4 : 8)); }
 
-template <typename XT, int MT, bool MULTI>
+template <typename XT, int MT, int MODE>
 cudaError_t run_group(const Group<XT> &grp, int64_t K, int M, cudaStream_t s) {
-    auto kern = gemv_mma_nvfp4<XT, MT, MULTI>;
+    auto kern = gemv_mma_nvfp4<XT, MT, MODE>;
     const size_t smem = smem_bytes(K, MT);
     static bool attr_set[64] = {};
     static int bps_cache[64] = {};
@@ -440,16 +449,22 @@ cudaError_t launch_group_x(const Tensor *ts, const void *const *xs, float *const
     }
     const int64_t K = ts[0].K;
     const int m = (int)M;
-    if (count > 1) {
-        if (m == 1) return run_group<XT, 1, true>(grp, K, m, s);
-        if (m == 2) return run_group<XT, 2, true>(grp, K, m, s);
-        if (m <= 4) return run_group<XT, 4, true>(grp, K, m, s);
-        return run_group<XT, 8, true>(grp, K, m, s);
+    if (count == 2 && xs[0] == xs[1]) {
+        if (m == 1) return run_group<XT, 1, 1>(grp, K, m, s);
+        if (m == 2) return run_group<XT, 2, 1>(grp, K, m, s);
+        if (m <= 4) return run_group<XT, 4, 1>(grp, K, m, s);
+        return run_group<XT, 8, 1>(grp, K, m, s);
     }
-    if (m == 1) return run_group<XT, 1, false>(grp, K, m, s);
-    if (m == 2) return run_group<XT, 2, false>(grp, K, m, s);
-    if (m <= 4) return run_group<XT, 4, false>(grp, K, m, s);
-    return run_group<XT, 8, false>(grp, K, m, s);
+    if (count > 1) {
+        if (m == 1) return run_group<XT, 1, 2>(grp, K, m, s);
+        if (m == 2) return run_group<XT, 2, 2>(grp, K, m, s);
+        if (m <= 4) return run_group<XT, 4, 2>(grp, K, m, s);
+        return run_group<XT, 8, 2>(grp, K, m, s);
+    }
+    if (m == 1) return run_group<XT, 1, 0>(grp, K, m, s);
+    if (m == 2) return run_group<XT, 2, 0>(grp, K, m, s);
+    if (m <= 4) return run_group<XT, 4, 0>(grp, K, m, s);
+    return run_group<XT, 8, 0>(grp, K, m, s);
 }
 
 }  // namespace
