@@ -59,6 +59,8 @@ def parse():
                          "FMT (nvfp4|q4k) at batch M on one 14336x4096 weight copy")
     ap.add_argument("--no-small-m", action="store_true",
                     help="skip the small-batch tensor-core GEMM measurements")
+    ap.add_argument("--kernel-reps", type=int, default=0,
+                    help="replays of each per-launch graph for the roofline timing (0: about 2000 launches)")
     ap.add_argument("--no-rows", action="store_true",
                     help="skip the per-row measurements of the other formats, dequant and repack")
     return ap.parse_args()
@@ -253,7 +255,7 @@ def run_ours(args, rank, world):
         ms = start.elapsed_time(end)
         # per-kernel average launch duration (same stream, inputs > L2)
         kern_ms = []
-        reps = max(3, 2000 // copies)
+        reps = args.kernel_reps if args.kernel_reps > 0 else max(3, 2000 // copies)
         for j in range(len(g_kern)):
             g_kern[j].replay()
             torch.cuda.synchronize()
