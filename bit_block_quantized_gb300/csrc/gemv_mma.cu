@@ -71,28 +71,17 @@ struct Blk {
     uint32_t s0, s1;
 };
 
-__device__ __forceinline__ void load_blk(const Tensor &t, int64_t n0, int b, int g, int tt, bool ok0, bool ok1,
-                                         Blk &r) {
-    const int64_t K = t.K;
-    const int64_t off = (int64_t)b * 64 + 16 * tt;
-    const int64_t soff = (int64_t)b * 8 + 2 * tt;
-    if (ok0) {
-        r.p0 = ldg_stream16(t.w + (n0 + g) * (K >> 1) + off);
-        r.s0 = ldg_stream2(t.scales + (n0 + g) * (K >> 4) + soff);
-    } else {
-        r.p0 = make_uint4(0, 0, 0, 0);
-        r.s0 = 0;
-    }
-    if (ok1) {
-        r.p1 = ldg_stream16(t.w + (n0 + g + 8) * (K >> 1) + off);
-        r.s1 = ldg_stream2(t.scales + (n0 + g + 8) * (K >> 4) + soff);
-    } else {
-        r.p1 = make_uint4(0, 0, 0, 0);
-        r.s1 = 0;
-    }
+// MXFP4 scale byte b -> 2^(b-127) as an f16x2 pair.  Every E2M1 multiple of
+// 2^k is an f16 number exactly when k is in [-23, 13]; outside that range
+// `ok` is cleared (the warp then recomputes its tile in f32).
+__device__ __forceinline__ uint32_t e8m0_f16x2(uint32_t b, bool &ok) {
+    const int k = (int)(b & 255u) - 127;
+    ok = ok && k >= -23 && k <= 13;
+    const uint32_t h = k >= -14 ? ((uint32_t)(k + 15) & 31u) << 10 : (k >= -24 ? 1u << (k + 24) : 0u);
+    return h | (h << 16);
 }
 
-// A-fragment source for one payload word (8 k): four f16x2 of e2m1 * e4m3.
+// A-fragment source for one payload word (8 k): four f16x2 of e2m1 * scale.
 __device__ __forceinline__ void decode_word(uint32_t w, uint32_t sc2, uint32_t (&a)[4]) {
     e2m1x8_h2(w, a[0], a[1], a[2], a[3]);
 #pragma unroll
@@ -166,8 +155,9 @@ __device__ __forceinline__ bool stage_x(const XT *__restrict__ x, int64_t K, int
 }
 
 // f32 CUDA-core path for one warp's k range of a 16-row tile (used only when
-// the activations' dynamic range is too wide for exact f16 staging).
-template <typename XT, int MT>
+// the activations' dynamic range is too wide for exact f16 staging, or, for
+// MXFP4, when a scale of the slice is outside the exact f16 range).
+template <typename XT, int MT, int FMT>
 __device__ __noinline__ void warp_rows_f32(const uint8_t *w, const uint8_t *scales, int64_t N, int64_t K,
                                            const XT *__restrict__ x, int M, int64_t n0, int b0, int b1, int lane,
                                            float *rw) {
@@ -179,7 +169,8 @@ __device__ __noinline__ void warp_rows_f32(const uint8_t *w, const uint8_t *scal
                 for (int64_t k = (int64_t)b0 * 128 + lane; k < (int64_t)b1 * 128; k += 32) {
                     const uint32_t byte = w[n * (K >> 1) + (k >> 1)];
                     const float v = e2m1x2_f32((k & 1) ? (byte >> 4) : (byte & 15u)).x;
-                    const float sc = e4m3_f32(scales[n * (K >> 4) + (k >> 4)]);
+                    const float sc = FMT == Q4_NVFP4 ? e4m3_f32(scales[n * (K >> 4) + (k >> 4)])
+                                                     : e8m0_f32(scales[n * (K >> 5) + (k >> 5)]);
                     acc = fmaf(v * sc, x_to_f32<XT>(x[(int64_t)m * K + k]), acc);
                 }
 #pragma unroll
@@ -217,7 +208,7 @@ template <typename XT> struct Group {
 // x slice only when the member's activation pointer changes.
 // MODE 0: one matrix; 1: two matrices that read the same x (e.g. gate and
 // up), the member chosen by one compare per tile; 2: any group.
-template <typename XT, int MT, int MODE>
+template <typename XT, int MT, int MODE, int FMT>
 __global__ void __launch_bounds__(MW * 32, MT >= 8 ? 1 : Q4_MMA_MINB)
     gemv_mma_nvfp4(const __grid_constant__ Group<XT> grp,
                                                                       int64_t K, int M, int nbw_max) {
@@ -274,8 +265,13 @@ __global__ void __launch_bounds__(MW * 32, MT >= 8 ? 1 : Q4_MMA_MINB)
                 const uint8_t *bs = MODE == 2 ? ls : MODE == 1 ? (lsec ? grp.s[1] : grp.s[0]) : grp.s[0];
                 r.p0 = ldg_stream16(bw + ow0);
                 r.p1 = ldg_stream16(bw + ow0 + ow_d);
-                r.s0 = ldg_stream2(bs + (ow0 >> 3));
-                r.s1 = ldg_stream2(bs + ((ow0 + ow_d) >> 3));
+                if (FMT == Q4_NVFP4) {   // two E4M3 scales per 32 k: payload offset / 8
+                    r.s0 = ldg_stream2(bs + (ow0 >> 3));
+                    r.s1 = ldg_stream2(bs + ((ow0 + ow_d) >> 3));
+                } else {                 // one E8M0 scale per 32 k: payload offset / 16
+                    r.s0 = ldg_stream1(bs + (ow0 >> 4));
+                    r.s1 = ldg_stream1(bs + ((ow0 + ow_d) >> 4));
+                }
             }
             ow0 += 64;
             if (++lc_i == nbw_max) cursor_tile(lc_tile + gridDim.x);
@@ -295,6 +291,7 @@ __global__ void __launch_bounds__(MW * 32, MT >= 8 ? 1 : Q4_MMA_MINB)
 #pragma unroll
     for (int m = 0; m < MT; m++) inv[m] = 1.0f;
     bool exact = true;
+    bool sok = true;                                   // MXFP4: every scale of the tile in the exact range
     int staged = -1;                                   // member whose x is in shared memory
     const int mlane = g < M ? g : 0;
     const uint2 *xbase = xs + mlane * 4 + tt;
@@ -325,11 +322,19 @@ __global__ void __launch_bounds__(MW * 32, MT >= 8 ? 1 : Q4_MMA_MINB)
                 const Blk r = buf[q];
                 load_next(buf[q]);
                 if (i < nbw && exact) {
-                    uint32_t h0, h1;
-                    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h0) : "h"((uint16_t)r.s0));
-                    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h1) : "h"((uint16_t)r.s1));
-                    const uint32_t sc0[2] = {prmt(h0, h0, 0x1010u), prmt(h0, h0, 0x3232u)};
-                    const uint32_t sc1[2] = {prmt(h1, h1, 0x1010u), prmt(h1, h1, 0x3232u)};
+                    uint32_t sc0[2], sc1[2];
+                    if (FMT == Q4_NVFP4) {
+                        uint32_t h0, h1;
+                        asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h0) : "h"((uint16_t)r.s0));
+                        asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h1) : "h"((uint16_t)r.s1));
+                        sc0[0] = prmt(h0, h0, 0x1010u);
+                        sc0[1] = prmt(h0, h0, 0x3232u);
+                        sc1[0] = prmt(h1, h1, 0x1010u);
+                        sc1[1] = prmt(h1, h1, 0x3232u);
+                    } else {
+                        sc0[0] = sc0[1] = e8m0_f16x2(r.s0, sok);
+                        sc1[0] = sc1[1] = e8m0_f16x2(r.s1, sok);
+                    }
                     const uint32_t w0[4] = {r.p0.x, r.p0.y, r.p0.z, r.p0.w};
                     const uint32_t w1[4] = {r.p1.x, r.p1.y, r.p1.z, r.p1.w};
 #pragma unroll
@@ -358,20 +363,25 @@ __global__ void __launch_bounds__(MW * 32, MT >= 8 ? 1 : Q4_MMA_MINB)
                         d[0] += dacc[a][0]; d[1] += dacc[a][1]; d[2] += dacc[a][2]; d[3] += dacc[a][3];
                         dacc[a][0] = dacc[a][1] = dacc[a][2] = dacc[a][3] = 0.0f;
                     }
-                    if (exact) {
+                    bool tile_ok = exact;
+                    if (FMT != Q4_NVFP4) {
+                        tile_ok = __all_sync(0xffffffffu, sok) && exact;
+                        sok = true;
+                    }
+                    if (tile_ok) {
 #pragma unroll
                         for (int mm = 0; mm < MT; mm++) {
                             if (mm == 2 * tt) { rw[g * MT + mm] = d[0] * inv[mm]; rw[(g + 8) * MT + mm] = d[2] * inv[mm]; }
                             if (mm == 2 * tt + 1) { rw[g * MT + mm] = d[1] * inv[mm]; rw[(g + 8) * MT + mm] = d[3] * inv[mm]; }
                         }
                     } else {
-                        warp_rows_f32<XT, MT>(grp.w[mb], grp.s[mb], Np, K, grp.x[mb], M, n0, b0, b1, lane, rw);
+                        warp_rows_f32<XT, MT, FMT>(grp.w[mb], grp.s[mb], Np, K, grp.x[mb], M, n0, b0, b1, lane, rw);
                     }
                     __syncthreads();
                     const float *rt = red + par * MW * 16 * MT;
                     par ^= 1;
                     float *yp = grp.y[mb];
-                    const float s2 = grp.scale2[mb];
+                    const float s2 = FMT == Q4_NVFP4 ? grp.scale2[mb] : 1.0f;
                     for (int e = threadIdx.x; e < 16 * MT; e += blockDim.x) {
                         const int rr = e / MT, m = e % MT;
                         const int64_t n = n0 + rr;
@@ -400,9 +410,9 @@ size_t smem_bytes(int64_t K, int mt) {
 
 int mt_for(int64_t M) { return M == 1 ? 1 : (M == 2 ? 2 : (M <= 4 ? 4 : 8)); }
 
-template <typename XT, int MT, int MODE>
+template <typename XT, int MT, int MODE, int FMT = Q4_NVFP4>
 cudaError_t run_group(const Group<XT> &grp, int64_t K, int M, cudaStream_t s) {
-    auto kern = gemv_mma_nvfp4<XT, MT, MODE>;
+    auto kern = gemv_mma_nvfp4<XT, MT, MODE, FMT>;
     const size_t smem = smem_bytes(K, MT);
     static bool attr_set[64] = {};
     static int bps_cache[64] = {};
@@ -449,6 +459,12 @@ cudaError_t launch_group_x(const Tensor *ts, const void *const *xs, float *const
     }
     const int64_t K = ts[0].K;
     const int m = (int)M;
+    if (ts[0].fmt == Q4_MXFP4) {   // single matrix only (groups are NVFP4)
+        if (m == 1) return run_group<XT, 1, 0, Q4_MXFP4>(grp, K, m, s);
+        if (m == 2) return run_group<XT, 2, 0, Q4_MXFP4>(grp, K, m, s);
+        if (m <= 4) return run_group<XT, 4, 0, Q4_MXFP4>(grp, K, m, s);
+        return run_group<XT, 8, 0, Q4_MXFP4>(grp, K, m, s);
+    }
     if (count == 2 && xs[0] == xs[1]) {
         if (m == 1) return run_group<XT, 1, 1>(grp, K, m, s);
         if (m == 2) return run_group<XT, 2, 1>(grp, K, m, s);
@@ -471,7 +487,8 @@ cudaError_t launch_group_x(const Tensor *ts, const void *const *xs, float *const
 
 // Eligible: NVFP4, K % 128 == 0, x slice fits in shared memory.
 bool gemv_mma_eligible(const Tensor &t, int64_t M) {
-    return t.fmt == Q4_NVFP4 && M >= 1 && M <= 8 && t.K % 128 == 0 && smem_bytes(t.K, mt_for(M)) <= SMEM_MAX &&
+    return (t.fmt == Q4_NVFP4 || t.fmt == Q4_MXFP4) && M >= 1 && M <= 8 && t.K % 128 == 0 &&
+           smem_bytes(t.K, mt_for(M)) <= SMEM_MAX &&
            t.N * (t.K / 2) < (int64_t(1) << 32) &&
            (((uintptr_t)t.w | (uintptr_t)t.scales) & 15) == 0;
 }

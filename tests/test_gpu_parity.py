@@ -162,6 +162,30 @@ def test_gemv_nvfp4_tensor_core_path(M):
         check_gemv(synth.make_layer("nvfp4", N, K, config=30, matrix=M, row_scale=True), M, config=30 + M)
 
 
+@pytest.mark.parametrize("M", [1, 3, 8])
+def test_gemv_mxfp4_tensor_core_path(M):
+    """MXFP4 with K % 128 == 0 and bf16 x also runs the mma.sync decode-dot
+    kernel (E8M0 scale folded into the f16 A fragment)."""
+    for N, K in ((41, 2048), (263, 11008), (16, 128)):
+        check_gemv(synth.make_layer("mxfp4", N, K, config=33, matrix=M, outliers=True), M, config=33 + M)
+        assert q4.q4_last_gemv_path() == "gemv_mma"
+
+
+def test_gemv_mxfp4_scales_outside_the_exact_f16_range():
+    """E8M0 scales whose E2M1 multiples are not all f16 numbers (2^-40, 2^20;
+    2^-23 and 2^13 are the edges that still are) make those warps recompute
+    their tiles in f32; the result stays within tolerance."""
+    layer = synth.make_layer("mxfp4", 40, 4096, config=34, matrix=0)
+    s = layer["scales"].copy()
+    s[3, 5] = 127 - 40
+    s[17, :] = 127 + 20
+    s[30, 100] = 127 - 23
+    s[31, 7] = 127 + 13
+    layer = dict(layer, scales=s)
+    for M in (1, 4):
+        check_gemv(layer, M, config=34)
+
+
 def test_gemv_nvfp4_wide_dynamic_range_x():
     """x whose range defeats the f16 staging (1e30 next to 1e-10): those warps
     fall back to f32 and the result is still within tolerance."""
