@@ -186,6 +186,36 @@ def test_gemv_mxfp4_scales_outside_the_exact_f16_range():
         check_gemv(layer, M, config=34)
 
 
+@pytest.mark.parametrize("xdtype", ["f32", "bf16"])
+@pytest.mark.parametrize("M", [1, 3, 8])
+def test_gemv_q4k_tensor_core_path(M, xdtype):
+    """Q4_K at batch 1..8 runs the mma.sync kernel with one fresh accumulator
+    per 32-k sub-block (step and offset applied on the CUDA cores), x staged
+    as hi + lo f16 parts; ragged 16-row tiles and uneven K splits.  At batch
+    5..8 with K = 11008 the staged x would not fit in shared memory and the
+    general kernel answers instead."""
+    for N, K in ((29, 1536), (263, 4096), (16, 256), (40, 11008)):
+        check_gemv(synth.make_layer("q4k", N, K, config=35, matrix=M, outliers=True), M, config=35 + M,
+                   xdtype=xdtype)
+        want = "gemv_general" if (M > 4 and K > 4096) else "gemv_mma_q4k"
+        assert q4.q4_last_gemv_path() == want
+
+
+def test_gemv_q4k_wide_dynamic_range_x():
+    """f32 x spanning 1e30 to 1e-10: the hi + lo staging keeps the result
+    within tolerance (tiny values fall below the scaled f16 range)."""
+    N, K = 40, 4096
+    layer = synth.make_layer("q4k", N, K, config=36, matrix=0)
+    for M in (1, 3):
+        xf = np.random.default_rng(M).normal(0, 1e-10, (M, K)).astype(np.float32)
+        xf[:, 7] = 1e30
+        xf[:, 1000] = -3e20
+        y = gpu_gemv(layer, x_device(xf), M)
+        ref, bound = oracle.gemv(to_oracle(layer), xf)
+        ok, worst = within_tolerance(y, ref, bound)
+        assert ok, worst
+
+
 def test_gemv_nvfp4_wide_dynamic_range_x():
     """x whose range defeats the f16 staging (1e30 next to 1e-10): those warps
     fall back to f32 and the result is still within tolerance."""
