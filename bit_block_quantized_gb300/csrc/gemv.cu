@@ -874,7 +874,7 @@ int gemv_read_and_clear_error() {
 cudaError_t launch_gemv(const Tensor &t, const void *x, q4_dtype x_dtype, float *y, int64_t M,
                         cudaStream_t s) {
     if (gemv_blk_eligible(t, M)) {
-        note_gemv_path("gemv_mma_q4k");
+        note_gemv_path(t.fmt == Q4_Q4K ? "gemv_mma_q4k" : "gemv_mma_q40");
         return launch_gemv_blk(t, x, x_dtype, y, M, s);
     }
     if (x_dtype == Q4_DT_BF16) return dispatch<__nv_bfloat16>(t, (const __nv_bfloat16 *)x, y, M, s);

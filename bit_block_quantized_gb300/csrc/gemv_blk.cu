@@ -1,6 +1,6 @@
-// gemv_blk.cu -- Q4_K decode-GEMV for batch 1..8 on the tensor cores
-// (mma.sync m16n8k16, f16 x f16 -> f32) with one fresh accumulator per 32-k
-// sub-block, scaled on the CUDA cores.
+// gemv_blk.cu -- Q4_K and Q4_0 decode-GEMV for batch 1..8 on the tensor
+// cores (mma.sync m16n8k16, f16 x f16 -> f32) with one fresh accumulator per
+// 32-k group (Q4_K sub-block, Q4_0 block), scaled on the CUDA cores.
 //
 // Q4_K weights are w = q * (d*sc_j) - dmin*m_j ([FBTC] sections 5-6).  The
 // step d*sc_j has up to 17 significant bits, so it cannot ride in an f16 MMA
@@ -17,6 +17,12 @@
 // 1024 + q construction); x is staged in the same order.  The word's low
 // nibbles feed k16 chunk s, its high nibbles chunk s + 2 of the same 64-k
 // chunk.
+//
+// Q4_0 ([BPA] "Real layouts compared") uses the same 256-k unit: 8 blocks of
+// 18 bytes (fp16 d, then 16 code bytes whose low nibbles are elements 0-15
+// and high nibbles 16-31).  A holds q - 8 (exact), and each lane adds
+// d_b * D_b per block; the code words of even blocks start 2 bytes off a
+// 4-byte boundary and are assembled from two aligned words by a funnel shift.
 //
 // Activations (f32 or bf16) are staged once per CTA as hi + lo f16 pairs
 // after an exact power-of-two column scale, so each value keeps 22 of its
@@ -39,12 +45,14 @@ __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// Two 4-bit codes (bits 0-3 and 16-19 of v) -> f16x2 of the exact integers.
+// Two 4-bit codes (bits 0-3 and 16-19 of v) -> f16x2 of q - BIAS, exact.
+template <int BIAS>
 __device__ __forceinline__ uint32_t codes_f16x2(uint32_t v) {
     const uint32_t mask = 0x000f000fu, magic = 0x64006400u;   // f16x2 (1024, 1024)
+    const uint32_t base = BIAS == 8 ? 0x64086408u : 0x64006400u;  // f16x2 (1024 + BIAS)
     uint32_t h, d;
     asm("lop3.b32 %0, %1, %2, %3, 0xea;" : "=r"(h) : "r"(v), "r"(mask), "r"(magic));   // (v & mask) | magic
-    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(h), "r"(magic));                    // (1024 + q) - 1024
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(h), "r"(base));                     // (1024 + q) - (1024 + BIAS)
     return d;
 }
 
@@ -66,7 +74,7 @@ __device__ __forceinline__ float4 x4(const __nv_bfloat16 *p) {
                        __uint_as_float(v.y & 0xffff0000u));
 }
 
-template <typename XT, int MT>
+template <typename XT, int MT, bool SUMS>
 __device__ void stage_x_blk(const XT *__restrict__ x, int64_t K, int M, int sb0, int nsb, int lane, uint2 *xh,
                             uint2 *xl, float *S, float (&inv)[MT]) {
     // column scale: max |x| over the warp's slice -> 2^(12 - e), exact
@@ -121,6 +129,7 @@ __device__ void stage_x_blk(const XT *__restrict__ x, int64_t K, int M, int sb0,
         xl[e] = lo;
     }
     __syncwarp();
+    if (!SUMS) return;
     // sub-block sums ((u*8 + j)*MT + m) of the staged values (hi + lo): the
     // same numbers the MMA multiplies
     const int nsum = nsb * 8 * MT;
@@ -158,7 +167,7 @@ __device__ __forceinline__ void q4k_sc_m(uint32_t B0, uint32_t B1, uint32_t B2, 
 }
 
 struct BlkArgs {
-    const uint8_t *w;   // Q4_K blocks [N][K/256][144]
+    const uint8_t *w;   // Q4_K blocks [N][K/256][144] or Q4_0 blocks [N][K/32][18]
     const void *x;      // [M][K] f32 or bf16
     float *y;           // [M][N]
     int64_t N, K;
@@ -166,25 +175,48 @@ struct BlkArgs {
     int nsbw;           // super-blocks per warp
 };
 
-// One super-block of rows g and g+8 for lane t: header word t of each row and
-// the eight code words (64-k chunk cc, half h) at bytes 16 + 32cc + 16h + 4t.
+// One 256-k unit of rows g and g+8 for lane t.
+//   Q4_K: header word t of each row (h0, h1) and the eight code words
+//         (64-k chunk cc, half h) at bytes 16 + 32cc + 16h + 4t.
+//   Q4_0: c[b] = code bytes 4t..4t+3 of block b (unit bytes 18b+2+4t ..),
+//         h = the fp16 d of blocks 2t (low half) and 2t+1 (high half).
 struct SB {
     uint32_t h0, h1;
     uint32_t c0[8], c1[8];
 };
 
+template <int FMT>
 __device__ __forceinline__ void load_sb(const uint8_t *r0, const uint8_t *r1, int t, SB &s) {
-    s.h0 = __ldg(reinterpret_cast<const uint32_t *>(r0) + t);
-    s.h1 = __ldg(reinterpret_cast<const uint32_t *>(r1) + t);
+    const uint32_t *w0 = reinterpret_cast<const uint32_t *>(r0), *w1 = reinterpret_cast<const uint32_t *>(r1);
+    if constexpr (FMT == Q4_Q4K) {
+        s.h0 = __ldg(w0 + t);
+        s.h1 = __ldg(w1 + t);
 #pragma unroll
-    for (int q = 0; q < 8; q++) {
-        s.c0[q] = __ldg(reinterpret_cast<const uint32_t *>(r0 + 16 + 16 * q) + t);
-        s.c1[q] = __ldg(reinterpret_cast<const uint32_t *>(r1 + 16 + 16 * q) + t);
+        for (int q = 0; q < 8; q++) {
+            s.c0[q] = __ldg(w0 + 4 + 4 * q + t);
+            s.c1[q] = __ldg(w1 + 4 + 4 * q + t);
+        }
+    } else {
+        // d of block 2t sits in the low half of word 9t, of block 2t+1 in the high half of word 9t+4
+        s.h0 = (__ldg(w0 + 9 * t) & 0xffffu) | (__ldg(w0 + 9 * t + 4) & 0xffff0000u);
+        s.h1 = (__ldg(w1 + 9 * t) & 0xffffu) | (__ldg(w1 + 9 * t + 4) & 0xffff0000u);
+#pragma unroll
+        for (int b = 0; b < 8; b++) {
+            // code bytes 18b + 2 + 4t: word-aligned for odd b, 2 bytes past a word for even b
+            if (b & 1) {
+                s.c0[b] = __ldg(w0 + (18 * b + 2) / 4 + t);
+                s.c1[b] = __ldg(w1 + (18 * b + 2) / 4 + t);
+            } else {
+                const int wi = (18 * b) / 4 + t;
+                s.c0[b] = __funnelshift_r(__ldg(w0 + wi), __ldg(w0 + wi + 1), 16);
+                s.c1[b] = __funnelshift_r(__ldg(w1 + wi), __ldg(w1 + wi + 1), 16);
+            }
+        }
     }
 }
 
-template <typename XT, int MT>
-__global__ void __launch_bounds__(BW * 32, 2) gemv_mma_q4k(const __grid_constant__ BlkArgs a) {
+template <typename XT, int MT, int FMT>
+__global__ void __launch_bounds__(BW * 32, 2) gemv_mma_blk(const __grid_constant__ BlkArgs a) {
     extern __shared__ __align__(16) uint8_t blk_smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, t = lane & 3;
@@ -208,8 +240,8 @@ __global__ void __launch_bounds__(BW * 32, 2) gemv_mma_q4k(const __grid_constant
         if (u >= nsbw) return;
         const int64_t n0 = (int64_t)(blockIdx.x + (i / a.nsbw) * gridDim.x) * 16;
         const int64_t ra = n0 + g < a.N ? n0 + g : a.N - 1, rb = n0 + g + 8 < a.N ? n0 + g + 8 : a.N - 1;
-        load_sb(a.w + ra * row_bytes + (int64_t)(sb0 + u) * 144, a.w + rb * row_bytes + (int64_t)(sb0 + u) * 144, t,
-                s);
+        load_sb<FMT>(a.w + ra * row_bytes + (int64_t)(sb0 + u) * 144, a.w + rb * row_bytes + (int64_t)(sb0 + u) * 144,
+                     t, s);
     };
     SB cur, nxt;
     if (items > 0) load_item(0, cur);        // weight bytes do not depend on the previous kernel
@@ -218,7 +250,7 @@ __global__ void __launch_bounds__(BW * 32, 2) gemv_mma_q4k(const __grid_constant
     asm volatile("griddepcontrol.wait;" ::: "memory");
 
     float inv[MT];
-    if (nsbw > 0) stage_x_blk<XT, MT>((const XT *)a.x, a.K, a.M, sb0, nsbw, lane, xh, xl, S, inv);
+    if (nsbw > 0) stage_x_blk<XT, MT, FMT == Q4_Q4K>((const XT *)a.x, a.K, a.M, sb0, nsbw, lane, xh, xl, S, inv);
     else {
 #pragma unroll
         for (int m = 0; m < MT; m++) inv[m] = 1.0f;
@@ -231,59 +263,85 @@ __global__ void __launch_bounds__(BW * 32, 2) gemv_mma_q4k(const __grid_constant
         if (i + 1 < items) load_item(i + 1, nxt);
         const int u = i % a.nsbw;
         if (u < nsbw) {
-            // the full 16-byte headers of rows g and g+8 (word t' from lane 4g + t')
-            uint32_t H0[4], H1[4];
-#pragma unroll
-            for (int q = 0; q < 4; q++) {
-                H0[q] = __shfl_sync(0xffffffffu, cur.h0, (lane & ~3) | q);
-                H1[q] = __shfl_sync(0xffffffffu, cur.h1, (lane & ~3) | q);
-            }
-            // this lane's sub-blocks 2t and 2t+1 of both rows: step and offset
-            float st[4], of[4];   // [row g: 2t, 2t+1 | row g+8: 2t, 2t+1]
-            {
-                const float d0 = half_bits_f32(H0[0]), m0 = half_bits_f32(H0[0] >> 16);
-                const float d1 = half_bits_f32(H1[0]), m1 = half_bits_f32(H1[0] >> 16);
-#pragma unroll
-                for (int q = 0; q < 2; q++) {
-                    uint32_t sc, mn;
-                    q4k_sc_m(H0[1], H0[2], H0[3], 2 * t + q, sc, mn);
-                    st[q] = d0 * (float)sc;
-                    of[q] = m0 * (float)mn;
-                    q4k_sc_m(H1[1], H1[2], H1[3], 2 * t + q, sc, mn);
-                    st[2 + q] = d1 * (float)sc;
-                    of[2 + q] = m1 * (float)mn;
-                }
-            }
             const uint2 *xhu = xh + (size_t)u * 16 * MT * 4 + mcol * 4 + t;
             const uint2 *xlu = xl + (size_t)u * 16 * MT * 4 + mcol * 4 + t;
-            const float *Su = S + (size_t)u * 8 * MT;
+            if constexpr (FMT == Q4_Q4K) {
+                // the full 16-byte headers of rows g and g+8 (word t' from lane 4g + t')
+                uint32_t H0[4], H1[4];
 #pragma unroll
-            for (int j = 0; j < 8; j++) {
-                // sub-block j = k16 chunks 2j, 2j+1 = 64-k chunk j/2, nibble j%2,
-                // code words (j/2, 0) and (j/2, 1)
-                const int cc = j >> 1, sh = 4 * (j & 1);
-                float dj[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-                for (int h = 0; h < 2; h++) {
-                    const uint32_t w0 = cur.c0[2 * cc + h] >> sh, w1 = cur.c1[2 * cc + h] >> sh;
-                    const uint32_t a0 = codes_f16x2(w0), a2 = codes_f16x2(w0 >> 8);
-                    const uint32_t a1 = codes_f16x2(w1), a3 = codes_f16x2(w1 >> 8);
-                    const int c = 4 * cc + 2 * (j & 1) + h;   // k16 chunk of the super-block
-                    const uint2 bh = xhu[(size_t)c * MT * 4], bl = xlu[(size_t)c * MT * 4];
-                    mma16816(dj, a0, a1, a2, a3, bh.x, bh.y);
-                    mma16816(dj, a0, a1, a2, a3, bl.x, bl.y);
+                for (int q = 0; q < 4; q++) {
+                    H0[q] = __shfl_sync(0xffffffffu, cur.h0, (lane & ~3) | q);
+                    H1[q] = __shfl_sync(0xffffffffu, cur.h1, (lane & ~3) | q);
                 }
-                // step and offset of sub-block j for rows g, g+8: lane 4g + j/2 computed them
-                const int src = (lane & ~3) | (j >> 1);
-                const float sg = __shfl_sync(0xffffffffu, (j & 1) ? st[1] : st[0], src);
-                const float og = __shfl_sync(0xffffffffu, (j & 1) ? of[1] : of[0], src);
-                const float sg8 = __shfl_sync(0xffffffffu, (j & 1) ? st[3] : st[2], src);
-                const float og8 = __shfl_sync(0xffffffffu, (j & 1) ? of[3] : of[2], src);
-                const float sa = Su[j * MT + c2a], sb = Su[j * MT + c2b];
-                acc[0] = fmaf(sg, dj[0], fmaf(-og, sa, acc[0]));
-                acc[1] = fmaf(sg, dj[1], fmaf(-og, sb, acc[1]));
-                acc[2] = fmaf(sg8, dj[2], fmaf(-og8, sa, acc[2]));
-                acc[3] = fmaf(sg8, dj[3], fmaf(-og8, sb, acc[3]));
+                // this lane's sub-blocks 2t and 2t+1 of both rows: step and offset
+                float st[4], of[4];   // [row g: 2t, 2t+1 | row g+8: 2t, 2t+1]
+                {
+                    const float d0 = half_bits_f32(H0[0]), m0 = half_bits_f32(H0[0] >> 16);
+                    const float d1 = half_bits_f32(H1[0]), m1 = half_bits_f32(H1[0] >> 16);
+#pragma unroll
+                    for (int q = 0; q < 2; q++) {
+                        uint32_t sc, mn;
+                        q4k_sc_m(H0[1], H0[2], H0[3], 2 * t + q, sc, mn);
+                        st[q] = d0 * (float)sc;
+                        of[q] = m0 * (float)mn;
+                        q4k_sc_m(H1[1], H1[2], H1[3], 2 * t + q, sc, mn);
+                        st[2 + q] = d1 * (float)sc;
+                        of[2 + q] = m1 * (float)mn;
+                    }
+                }
+                const float *Su = S + (size_t)u * 8 * MT;
+#pragma unroll
+                for (int j = 0; j < 8; j++) {
+                    // sub-block j = k16 chunks 2j, 2j+1 = 64-k chunk j/2, nibble j%2,
+                    // code words (j/2, 0) and (j/2, 1)
+                    const int cc = j >> 1, sh = 4 * (j & 1);
+                    float dj[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                    for (int h = 0; h < 2; h++) {
+                        const uint32_t w0 = cur.c0[2 * cc + h] >> sh, w1 = cur.c1[2 * cc + h] >> sh;
+                        const uint32_t a0 = codes_f16x2<0>(w0), a2 = codes_f16x2<0>(w0 >> 8);
+                        const uint32_t a1 = codes_f16x2<0>(w1), a3 = codes_f16x2<0>(w1 >> 8);
+                        const int c = 4 * cc + 2 * (j & 1) + h;   // k16 chunk of the super-block
+                        const uint2 bh = xhu[(size_t)c * MT * 4], bl = xlu[(size_t)c * MT * 4];
+                        mma16816(dj, a0, a1, a2, a3, bh.x, bh.y);
+                        mma16816(dj, a0, a1, a2, a3, bl.x, bl.y);
+                    }
+                    // step and offset of sub-block j for rows g, g+8: lane 4g + j/2 computed them
+                    const int src = (lane & ~3) | (j >> 1);
+                    const float sg = __shfl_sync(0xffffffffu, (j & 1) ? st[1] : st[0], src);
+                    const float og = __shfl_sync(0xffffffffu, (j & 1) ? of[1] : of[0], src);
+                    const float sg8 = __shfl_sync(0xffffffffu, (j & 1) ? st[3] : st[2], src);
+                    const float og8 = __shfl_sync(0xffffffffu, (j & 1) ? of[3] : of[2], src);
+                    const float sa = Su[j * MT + c2a], sb = Su[j * MT + c2b];
+                    acc[0] = fmaf(sg, dj[0], fmaf(-og, sa, acc[0]));
+                    acc[1] = fmaf(sg, dj[1], fmaf(-og, sb, acc[1]));
+                    acc[2] = fmaf(sg8, dj[2], fmaf(-og8, sa, acc[2]));
+                    acc[3] = fmaf(sg8, dj[3], fmaf(-og8, sb, acc[3]));
+                }
+            } else {
+#pragma unroll
+                for (int b = 0; b < 8; b++) {
+                    // block b = k16 chunks 2b (low nibbles) and 2b+1 (high nibbles)
+                    float dj[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                    for (int h = 0; h < 2; h++) {
+                        const uint32_t w0 = cur.c0[b] >> (4 * h), w1 = cur.c1[b] >> (4 * h);
+                        const uint32_t a0 = codes_f16x2<8>(w0), a2 = codes_f16x2<8>(w0 >> 8);
+                        const uint32_t a1 = codes_f16x2<8>(w1), a3 = codes_f16x2<8>(w1 >> 8);
+                        const uint2 bh = xhu[(size_t)(2 * b + h) * MT * 4], bl = xlu[(size_t)(2 * b + h) * MT * 4];
+                        mma16816(dj, a0, a1, a2, a3, bh.x, bh.y);
+                        mma16816(dj, a0, a1, a2, a3, bl.x, bl.y);
+                    }
+                    // d of block b for rows g, g+8: lane 4g + b/2 loaded it (half b%2)
+                    const int src = (lane & ~3) | (b >> 1);
+                    const uint32_t dg = __shfl_sync(0xffffffffu, cur.h0, src) >> (16 * (b & 1));
+                    const uint32_t dg8 = __shfl_sync(0xffffffffu, cur.h1, src) >> (16 * (b & 1));
+                    const float fg = half_bits_f32(dg), fg8 = half_bits_f32(dg8);
+                    acc[0] = fmaf(fg, dj[0], acc[0]);
+                    acc[1] = fmaf(fg, dj[1], acc[1]);
+                    acc[2] = fmaf(fg8, dj[2], acc[2]);
+                    acc[3] = fmaf(fg8, dj[3], acc[3]);
+                }
             }
         }
         if (i + 1 < items) cur = nxt;
@@ -326,9 +384,9 @@ size_t blk_smem_bytes(int64_t K, int mt) {
 
 int blk_mt(int64_t M) { return M == 1 ? 1 : (M == 2 ? 2 : (M <= 4 ? 4 : 8)); }
 
-template <typename XT, int MT>
+template <typename XT, int MT, int FMT>
 cudaError_t run_blk(const BlkArgs &a, cudaStream_t s) {
-    auto kern = gemv_mma_q4k<XT, MT>;
+    auto kern = gemv_mma_blk<XT, MT, FMT>;
     const size_t smem = blk_smem_bytes(a.K, MT);
     static bool attr_set[64] = {};
     static int bps[64] = {};
@@ -361,8 +419,23 @@ cudaError_t run_blk(const BlkArgs &a, cudaStream_t s) {
 }  // namespace
 
 bool gemv_blk_eligible(const Tensor &t, int64_t M) {
-    return t.fmt == Q4_Q4K && M >= 1 && M <= 8 && t.K % 256 == 0 && t.K <= (1LL << 30) &&
+    return (t.fmt == Q4_Q4K || t.fmt == Q4_Q40) && M >= 1 && M <= 8 && t.K % 256 == 0 && t.K <= (1LL << 30) &&
            blk_smem_bytes(t.K, blk_mt(M)) <= BLK_SMEM_MAX && (((uintptr_t)t.w) & 15) == 0;
+}
+
+template <int FMT>
+cudaError_t launch_blk_fmt(const BlkArgs &a, q4_dtype xd, cudaStream_t s) {
+    const int mt = blk_mt(a.M);
+    if (xd == Q4_DT_BF16) {
+        if (mt == 1) return run_blk<__nv_bfloat16, 1, FMT>(a, s);
+        if (mt == 2) return run_blk<__nv_bfloat16, 2, FMT>(a, s);
+        if (mt == 4) return run_blk<__nv_bfloat16, 4, FMT>(a, s);
+        return run_blk<__nv_bfloat16, 8, FMT>(a, s);
+    }
+    if (mt == 1) return run_blk<float, 1, FMT>(a, s);
+    if (mt == 2) return run_blk<float, 2, FMT>(a, s);
+    if (mt == 4) return run_blk<float, 4, FMT>(a, s);
+    return run_blk<float, 8, FMT>(a, s);
 }
 
 cudaError_t launch_gemv_blk(const Tensor &t, const void *x, q4_dtype xd, float *y, int64_t M, cudaStream_t s) {
@@ -374,17 +447,7 @@ cudaError_t launch_gemv_blk(const Tensor &t, const void *x, q4_dtype xd, float *
     a.K = t.K;
     a.M = (int)M;
     a.nsbw = (int)(((t.K >> 8) + BW - 1) / BW);
-    const int mt = blk_mt(M);
-    if (xd == Q4_DT_BF16) {
-        if (mt == 1) return run_blk<__nv_bfloat16, 1>(a, s);
-        if (mt == 2) return run_blk<__nv_bfloat16, 2>(a, s);
-        if (mt == 4) return run_blk<__nv_bfloat16, 4>(a, s);
-        return run_blk<__nv_bfloat16, 8>(a, s);
-    }
-    if (mt == 1) return run_blk<float, 1>(a, s);
-    if (mt == 2) return run_blk<float, 2>(a, s);
-    if (mt == 4) return run_blk<float, 4>(a, s);
-    return run_blk<float, 8>(a, s);
+    return t.fmt == Q4_Q4K ? launch_blk_fmt<Q4_Q4K>(a, xd, s) : launch_blk_fmt<Q4_Q40>(a, xd, s);
 }
 
 }  // namespace q4

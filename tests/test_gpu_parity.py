@@ -201,6 +201,18 @@ def test_gemv_q4k_tensor_core_path(M, xdtype):
         assert q4.q4_last_gemv_path() == want
 
 
+@pytest.mark.parametrize("xdtype", ["f32", "bf16"])
+@pytest.mark.parametrize("M", [1, 3, 8])
+def test_gemv_q40_tensor_core_path(M, xdtype):
+    """Q4_0 on the same kernel: A = q - 8, d applied per 32-k block; the code
+    words of even blocks are assembled across a 4-byte boundary."""
+    for N, K in ((33, 2048), (263, 11008), (16, 256)):
+        check_gemv(synth.make_layer("q40", N, K, config=37, matrix=M, outliers=True), M, config=37 + M,
+                   xdtype=xdtype)
+        want = "gemv_general" if (M > 4 and K > 4096) else "gemv_mma_q40"
+        assert q4.q4_last_gemv_path() == want
+
+
 def test_gemv_q4k_wide_dynamic_range_x():
     """f32 x spanning 1e30 to 1e-10: the hi + lo staging keeps the result
     within tolerance (tiny values fall below the scaled f16 range)."""
