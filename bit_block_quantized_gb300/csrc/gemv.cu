@@ -873,6 +873,10 @@ int gemv_read_and_clear_error() {
 
 cudaError_t launch_gemv(const Tensor &t, const void *x, q4_dtype x_dtype, float *y, int64_t M,
                         cudaStream_t s) {
+    if (gemv_gptq_eligible(t, M)) {
+        note_gemv_path("gemv_mma_gptq");
+        return launch_gemv_gptq(t, x, x_dtype, y, M, s);
+    }
     if (gemv_blk_eligible(t, M)) {
         note_gemv_path(t.fmt == Q4_Q4K ? "gemv_mma_q4k" : "gemv_mma_q40");
         return launch_gemv_blk(t, x, x_dtype, y, M, s);

@@ -376,6 +376,264 @@ __global__ void __launch_bounds__(BW * 32, 2) gemv_mma_blk(const __grid_constant
     }
 }
 
+// ------------------------------------------------------------------ GPTQ
+// GPTQ ([BPA] "Real layouts compared"): qweight int32 [K/8][N] (word (kb, n)
+// holds k = 8kb .. 8kb+7 of column n, nibble i = k % 8), scales f16 [K/G][N],
+// qzeros int32 [K/G][N/8] holding z - 1; w = s * (q - z).  Here G = 128 and no
+// act-order permutation.  Per 32-k super-chunk s, lane (g, t) loads word
+// kb = 4s + t of rows g and g+8 (8 codes: k = 32s + 8t + i).  Two MMAs take
+// them: X holds codes (0, 4 | 1, 5) and Y codes (2, 6 | 3, 7) of every word,
+// so each nibble pair is one LOP3 away; x is staged in the same order.  Per
+// 128-k group the lane adds s * (D - z * S), S the group's x sum.
+template <typename XT, int MT>
+__device__ void stage_x_gptq(const XT *__restrict__ x, int64_t K, int M, int gr0, int ngr, int lane, uint2 *xh,
+                             uint2 *xl, float *S, float (&inv)[MT]) {
+    float amax[MT];
+#pragma unroll
+    for (int m = 0; m < MT; m++) amax[m] = 0.0f;
+    const int nq = ngr * 32;                       // 4-value groups per column
+#pragma unroll 4
+    for (int i = lane; i < nq; i += 32) {
+#pragma unroll
+        for (int m = 0; m < MT; m++)
+            if (m < M) {
+                const float4 v = x4(x + (int64_t)m * K + (int64_t)gr0 * 128 + 4 * i);
+                amax[m] = fmaxf(amax[m], fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
+            }
+    }
+    float scale[MT];
+#pragma unroll
+    for (int m = 0; m < MT; m++) {
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1) amax[m] = fmaxf(amax[m], __shfl_xor_sync(0xffffffffu, amax[m], off));
+        scale[m] = 1.0f;
+        inv[m] = 1.0f;
+        if (amax[m] > 0.0f && amax[m] < INFINITY) {
+            int ex = (int)((__float_as_uint(amax[m]) >> 23) & 255u) - 127;
+            ex = ex < -100 ? -100 : (ex > 100 ? 100 : ex);
+            scale[m] = __uint_as_float((uint32_t)(127 + 12 - ex) << 23);
+            inv[m] = __uint_as_float((uint32_t)(127 - 12 + ex) << 23);
+        }
+    }
+    // entry e = ((sc*2 + which)*MT + m)*4 + t holds x[32sc + 8t + 2*which + {0, 4 | 1, 5}]
+    const int entries = ngr * 4 * 2 * MT * 4;
+#pragma unroll 2
+    for (int e = lane; e < entries; e += 32) {
+        const int t = e & 3, m = (e >> 2) % MT, which = (e / (4 * MT)) & 1, sc = e / (8 * MT);
+        uint2 hi = make_uint2(0u, 0u), lo = make_uint2(0u, 0u);
+        if (m < M) {
+            float cs = 1.0f;
+#pragma unroll
+            for (int mm = 0; mm < MT; mm++)
+                if (mm == m) cs = scale[mm];
+            const XT *p = x + (int64_t)m * K + (int64_t)gr0 * 128 + 32 * sc + 8 * t;
+            const float4 va = x4(p), vb = x4(p + 4);    // k + 0..3, k + 4..7
+            const float v0 = (which ? va.z : va.x) * cs, v1 = (which ? va.w : va.y) * cs;
+            const float v4 = (which ? vb.z : vb.x) * cs, v5 = (which ? vb.w : vb.y) * cs;
+            const __half2 h04 = __floats2half2_rn(v0, v4), h15 = __floats2half2_rn(v1, v5);
+            const float2 r04 = __half22float2(h04), r15 = __half22float2(h15);
+            const __half2 l04 = __floats2half2_rn(v0 - r04.x, v4 - r04.y);
+            const __half2 l15 = __floats2half2_rn(v1 - r15.x, v5 - r15.y);
+            hi = make_uint2(*reinterpret_cast<const uint32_t *>(&h04), *reinterpret_cast<const uint32_t *>(&h15));
+            lo = make_uint2(*reinterpret_cast<const uint32_t *>(&l04), *reinterpret_cast<const uint32_t *>(&l15));
+        }
+        xh[e] = hi;
+        xl[e] = lo;
+    }
+    __syncwarp();
+    // group sums (gr*MT + m) of the staged values
+    const int nsum = ngr * MT;
+    for (int e = lane; e < nsum; e += 32) {
+        const int m = e % MT, gr = e / MT;
+        float sacc = 0.0f;
+        for (int q = 0; q < 8; q++)       // 4 super-chunks x {X, Y}
+#pragma unroll
+            for (int t = 0; t < 4; t++) {
+                const int idx = ((gr * 8 + q) * MT + m) * 4 + t;
+                const uint2 vh = xh[idx], vl = xl[idx];
+                const float2 a0 = __half22float2(*reinterpret_cast<const __half2 *>(&vh.x));
+                const float2 a1 = __half22float2(*reinterpret_cast<const __half2 *>(&vh.y));
+                const float2 b0 = __half22float2(*reinterpret_cast<const __half2 *>(&vl.x));
+                const float2 b1 = __half22float2(*reinterpret_cast<const __half2 *>(&vl.y));
+                sacc += ((a0.x + b0.x) + (a0.y + b0.y)) + ((a1.x + b1.x) + (a1.y + b1.y));
+            }
+        S[e] = sacc;
+    }
+    __syncwarp();
+}
+
+struct GptqArgs {
+    const uint32_t *w;      // qweight [K/8][N]
+    const uint16_t *s;      // scales [K/128][N] (f16 bits)
+    const uint32_t *z;      // qzeros [K/128][N/8]
+    const void *x;
+    float *y;
+    int64_t N, K;
+    int M;
+    int ngw;                // groups per warp
+};
+
+// One 128-k group of rows g and g+8 for lane t: the four code words of each
+// row (super-chunks 0..3, word kb = 4*sc + t), its scale and zero word.
+struct GG {
+    uint32_t c0[4], c1[4];
+    uint32_t s01;           // scales of rows g (low half) and g+8 (high half)
+    uint32_t z0, z1;        // qzeros words holding rows g and g+8
+};
+
+__device__ __forceinline__ void load_gg(const GptqArgs &a, int64_t ra, int64_t rb, int64_t gr, int t, GG &q) {
+    const int64_t kb0 = gr * 16;                   // 128 k = 16 words along K
+#pragma unroll
+    for (int sc = 0; sc < 4; sc++) {
+        q.c0[sc] = __ldg(a.w + (kb0 + 4 * sc + t) * a.N + ra);
+        q.c1[sc] = __ldg(a.w + (kb0 + 4 * sc + t) * a.N + rb);
+    }
+    q.s01 = (uint32_t)__ldg(a.s + gr * a.N + ra) | ((uint32_t)__ldg(a.s + gr * a.N + rb) << 16);
+    q.z0 = __ldg(a.z + gr * (a.N >> 3) + (ra >> 3));
+    q.z1 = __ldg(a.z + gr * (a.N >> 3) + (rb >> 3));
+}
+
+template <typename XT, int MT>
+__global__ void __launch_bounds__(BW * 32, 2) gemv_mma_gptq(const __grid_constant__ GptqArgs a) {
+    extern __shared__ __align__(16) uint8_t blk_smem[];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = lane >> 2, t = lane & 3;
+    const int ngroups = (int)(a.K >> 7);
+    const int gr0 = min(ngroups, warp * a.ngw), gr1 = min(ngroups, (warp + 1) * a.ngw), ngr = gr1 - gr0;
+    const size_t xw = (size_t)a.ngw * 8 * MT * 4;            // entries per warp
+    uint2 *xh = reinterpret_cast<uint2 *>(blk_smem) + (size_t)warp * 2 * xw;
+    uint2 *xl = xh + xw;
+    float *S = reinterpret_cast<float *>(reinterpret_cast<uint2 *>(blk_smem) + (size_t)BW * 2 * xw) +
+               (size_t)warp * a.ngw * MT;
+    float *red = reinterpret_cast<float *>(reinterpret_cast<uint2 *>(blk_smem) + (size_t)BW * 2 * xw) +
+                 (size_t)BW * a.ngw * MT;
+    const int ntiles = (int)((a.N + 15) / 16);
+    const int my_tiles = blockIdx.x < ntiles ? (ntiles - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+    const int items = my_tiles * a.ngw;
+
+    auto load_item = [&](int i, GG &q) {
+        const int u = i % a.ngw;
+        if (u >= ngr) return;
+        const int64_t n0 = (int64_t)(blockIdx.x + (i / a.ngw) * gridDim.x) * 16;
+        // rows past N read row N - 8 + (g & 7) (N % 8 == 0): valid memory, never stored
+        const int64_t ra = n0 + g < a.N ? n0 + g : a.N - 8 + g, rb = n0 + g + 8 < a.N ? n0 + g + 8 : a.N - 8 + g;
+        load_gg(a, ra, rb, gr0 + u, t, q);
+    };
+    GG cur, nxt;
+    if (items > 0) load_item(0, cur);
+
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+
+    float inv[MT];
+    if (ngr > 0) stage_x_gptq<XT, MT>((const XT *)a.x, a.K, a.M, gr0, ngr, lane, xh, xl, S, inv);
+    else {
+#pragma unroll
+        for (int m = 0; m < MT; m++) inv[m] = 1.0f;
+    }
+    const int mcol = g < MT ? g : 0;
+    const int c2a = 2 * t < MT ? 2 * t : 0, c2b = 2 * t + 1 < MT ? 2 * t + 1 : 0;
+
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int i = 0; i < items; i++) {
+        if (i + 1 < items) load_item(i + 1, nxt);
+        const int u = i % a.ngw;
+        if (u < ngr) {
+            const uint2 *xhu = xh + (size_t)u * 8 * MT * 4 + mcol * 4 + t;
+            const uint2 *xlu = xl + (size_t)u * 8 * MT * 4 + mcol * 4 + t;
+            float dj[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int sc = 0; sc < 4; sc++) {
+                const uint32_t w0 = cur.c0[sc], w1 = cur.c1[sc];
+#pragma unroll
+                for (int which = 0; which < 2; which++) {
+                    const int sh = 8 * which;          // X: nibbles (0,4 | 1,5); Y: (2,6 | 3,7)
+                    const uint32_t a0 = codes_f16x2<0>(w0 >> sh), a2 = codes_f16x2<0>(w0 >> (sh + 4));
+                    const uint32_t a1 = codes_f16x2<0>(w1 >> sh), a3 = codes_f16x2<0>(w1 >> (sh + 4));
+                    const int c = sc * 2 + which;
+                    const uint2 bh = xhu[(size_t)c * MT * 4], bl = xlu[(size_t)c * MT * 4];
+                    mma16816(dj, a0, a1, a2, a3, bh.x, bh.y);
+                    mma16816(dj, a0, a1, a2, a3, bl.x, bl.y);
+                }
+            }
+            const float sg = half_bits_f32(cur.s01), sg8 = half_bits_f32(cur.s01 >> 16);
+            const float zg = (float)(((cur.z0 >> (4 * g)) & 15u) + 1u);
+            const float zg8 = (float)(((cur.z1 >> (4 * g)) & 15u) + 1u);
+            const float Sa = S[u * MT + c2a], Sb = S[u * MT + c2b];
+            acc[0] = fmaf(sg, fmaf(-zg, Sa, dj[0]), acc[0]);
+            acc[1] = fmaf(sg, fmaf(-zg, Sb, dj[1]), acc[1]);
+            acc[2] = fmaf(sg8, fmaf(-zg8, Sa, dj[2]), acc[2]);
+            acc[3] = fmaf(sg8, fmaf(-zg8, Sb, dj[3]), acc[3]);
+        }
+        if (i + 1 < items) cur = nxt;
+        if (u == a.ngw - 1) {
+            const int64_t n0 = (int64_t)(blockIdx.x + (i / a.ngw) * gridDim.x) * 16;
+            float *rw = red + warp * 16 * MT;
+#pragma unroll
+            for (int mm = 0; mm < MT; mm++) {
+                if (mm == 2 * t) {
+                    rw[g * MT + mm] = acc[0] * inv[mm];
+                    rw[(g + 8) * MT + mm] = acc[2] * inv[mm];
+                }
+                if (mm == 2 * t + 1) {
+                    rw[g * MT + mm] = acc[1] * inv[mm];
+                    rw[(g + 8) * MT + mm] = acc[3] * inv[mm];
+                }
+            }
+            acc[0] = acc[1] = acc[2] = acc[3] = 0.0f;
+            __syncthreads();
+            for (int e = threadIdx.x; e < 16 * MT; e += blockDim.x) {
+                const int rr = e / MT, m = e % MT;
+                const int64_t n = n0 + rr;
+                if (n < a.N && m < a.M) {
+                    float sum = 0.0f;
+                    for (int w = 0; w < BW; w++) sum += red[w * 16 * MT + e];
+                    a.y[(int64_t)m * a.N + n] = sum;
+                }
+            }
+            __syncthreads();
+        }
+    }
+}
+
+size_t gptq_smem_bytes(int64_t K, int mt) {
+    const int ng = (int)(K >> 7), ngw = (ng + BW - 1) / BW;
+    return (size_t)BW * 2 * ngw * 8 * mt * 4 * sizeof(uint2) + (size_t)BW * ngw * mt * sizeof(float) +
+           (size_t)BW * 16 * mt * sizeof(float);
+}
+
+template <typename XT, int MT>
+cudaError_t run_gptq(const GptqArgs &a, cudaStream_t s) {
+    auto kern = gemv_mma_gptq<XT, MT>;
+    const size_t smem = gptq_smem_bytes(a.K, MT);
+    static bool attr_set[64] = {};
+    static int bps[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (!attr_set[dev & 63]) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)BLK_SMEM_MAX);
+        if (e != cudaSuccess) return e;
+        int b = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, kern, BW * 32, smem) != cudaSuccess || b < 1) b = 1;
+        bps[dev & 63] = b;
+        attr_set[dev & 63] = true;
+    }
+    const int ntiles = (int)((a.N + 15) / 16);
+    int grid = bps[dev & 63] * sm_count();
+    if (grid > ntiles) grid = ntiles;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid, 1, 1);
+    cfg.blockDim = dim3(BW * 32, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, a);
+}
+
 size_t blk_smem_bytes(int64_t K, int mt) {
     const int nsb = (int)(K >> 8), nsbw = (nsb + BW - 1) / BW;
     return (size_t)BW * 2 * nsbw * 16 * mt * 4 * sizeof(uint2) + (size_t)BW * nsbw * 8 * mt * sizeof(float) +
@@ -423,6 +681,36 @@ bool gemv_blk_eligible(const Tensor &t, int64_t M) {
            blk_smem_bytes(t.K, blk_mt(M)) <= BLK_SMEM_MAX && (((uintptr_t)t.w) & 15) == 0;
 }
 
+bool gemv_gptq_eligible(const Tensor &t, int64_t M) {
+    return t.fmt == Q4_GPTQ && t.g_idx == nullptr && t.group == 128 && M >= 1 && M <= 8 && t.K % 128 == 0 &&
+           t.N % 8 == 0 && t.K <= (1LL << 30) && gptq_smem_bytes(t.K, blk_mt(M)) <= BLK_SMEM_MAX;
+}
+
+cudaError_t launch_gemv_gptq(const Tensor &t, const void *x, q4_dtype xd, float *y, int64_t M, cudaStream_t s) {
+    GptqArgs a;
+    a.w = reinterpret_cast<const uint32_t *>(t.w);
+    a.s = reinterpret_cast<const uint16_t *>(t.scales);
+    a.z = reinterpret_cast<const uint32_t *>(t.zeros);
+    a.x = x;
+    a.y = y;
+    a.N = t.N;
+    a.K = t.K;
+    a.M = (int)M;
+    a.ngw = (int)(((t.K >> 7) + BW - 1) / BW);
+    const int mt = blk_mt(M);
+    if (xd == Q4_DT_BF16) {
+        if (mt == 1) return run_gptq<__nv_bfloat16, 1>(a, s);
+        if (mt == 2) return run_gptq<__nv_bfloat16, 2>(a, s);
+        if (mt == 4) return run_gptq<__nv_bfloat16, 4>(a, s);
+        return run_gptq<__nv_bfloat16, 8>(a, s);
+    }
+    if (mt == 1) return run_gptq<float, 1>(a, s);
+    if (mt == 2) return run_gptq<float, 2>(a, s);
+    if (mt == 4) return run_gptq<float, 4>(a, s);
+    return run_gptq<float, 8>(a, s);
+}
+
+namespace {
 template <int FMT>
 cudaError_t launch_blk_fmt(const BlkArgs &a, q4_dtype xd, cudaStream_t s) {
     const int mt = blk_mt(a.M);
@@ -437,6 +725,7 @@ cudaError_t launch_blk_fmt(const BlkArgs &a, q4_dtype xd, cudaStream_t s) {
     if (mt == 4) return run_blk<float, 4, FMT>(a, s);
     return run_blk<float, 8, FMT>(a, s);
 }
+}  // namespace
 
 cudaError_t launch_gemv_blk(const Tensor &t, const void *x, q4_dtype xd, float *y, int64_t M, cudaStream_t s) {
     BlkArgs a;

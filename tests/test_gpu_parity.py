@@ -213,6 +213,18 @@ def test_gemv_q40_tensor_core_path(M, xdtype):
         assert q4.q4_last_gemv_path() == want
 
 
+@pytest.mark.parametrize("xdtype", ["f32", "bf16"])
+@pytest.mark.parametrize("M", [1, 3, 8])
+def test_gemv_gptq_tensor_core_path(M, xdtype):
+    """GPTQ (group 128, no act-order) on the tensor cores: one word of 8 codes
+    per lane feeds two MMAs; s * (D - z * S) per group."""
+    for N, K in ((264, 1152), (520, 4096), (16, 128), (40, 11008)):
+        check_gemv(synth.make_layer("gptq", N, K, config=38, matrix=M, outliers=True), M, config=38 + M,
+                   xdtype=xdtype)
+        want = "gemv_kmajor" if (M > 4 and K > 4096) else "gemv_mma_gptq"
+        assert q4.q4_last_gemv_path() == want
+
+
 def test_gemv_q4k_wide_dynamic_range_x():
     """f32 x spanning 1e30 to 1e-10: the hi + lo staging keeps the result
     within tolerance (tiny values fall below the scaled f16 range)."""
