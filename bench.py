@@ -38,7 +38,10 @@ SET = [("gate", 14336, 4096), ("up", 14336, 4096), ("down", 4096, 14336)]
 CONFIG_ID = 5          # seed block of this workload's synthetic draws
 NOMINAL_HBM_GBS = 7900.0
 FALLBACK_HBM_GBS = 6800.0
-DOMINANT = "gemv_mma_nvfp4<bf16, MT=1, pair> (gate and up, 2 x 14336x4096 in one launch)"
+DOMINANT = "gemv_tma_nvfp4<MT=1> group of 2 (gate and up, 2 x 14336x4096 in one launch)"
+PROFILE = "gemv_tma_nvfp4_pair_2x14336x4096.md"
+PROFILED_SOURCES = ("bit_block_quantized_gb300/csrc/gemv_tma.cu", "bit_block_quantized_gb300/csrc/q4_internal.cuh",
+                    "bit_block_quantized_gb300/csrc/tma_map.cuh")
 
 
 def parse():
@@ -77,7 +80,7 @@ def measured_hbm_peak():
 
 def source_sha():
     h = hashlib.sha256()
-    for rel in ("bit_block_quantized_gb300/csrc/gemv_mma.cu", "bit_block_quantized_gb300/csrc/q4_internal.cuh"):
+    for rel in PROFILED_SOURCES:
         with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -86,7 +89,7 @@ def source_sha():
 def profiled_traffic():
     """DRAM bytes per launch of the dominant kernel from the committed ncu
     summary, only if it was taken on the current kernel source."""
-    p = os.path.join(ROOT, "profiles", "gemv_mma_nvfp4_pair_2x14336x4096.md")
+    p = os.path.join(ROOT, "profiles", PROFILE)
     try:
         text = open(p).read()
     except OSError:
@@ -209,6 +212,10 @@ def run_ours(args, rank, world):
     with torch.cuda.stream(stream):
         for c in range(copies):
             step(c, stream)
+        gate_up(0, stream)
+        path_gate_up = q4.q4_last_gemv_path()
+        down(0, stream)
+        path_down = q4.q4_last_gemv_path()
         torch.cuda.synchronize()
         g_rot = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g_rot, stream=stream):
@@ -283,9 +290,10 @@ def run_ours(args, rank, world):
     down_bytes = q4.q4_packed_bytes("nvfp4", 4096, 14336)
     achieved = gate_up_bytes / (kern_ms[0] * 1e-3) / 1e9
     per_kernel = {"gate+up (one grouped launch)": {"us_per_launch": round(kern_ms[0] * 1e3, 3),
-                                                   "GBps": round(gate_up_bytes / (kern_ms[0] * 1e-3) / 1e9, 1)},
+                                                   "GBps": round(gate_up_bytes / (kern_ms[0] * 1e-3) / 1e9, 1),
+                                                   "path": path_gate_up},
                   "down": {"us_per_launch": round(kern_ms[1] * 1e3, 3),
-                           "GBps": round(down_bytes / (kern_ms[1] * 1e-3) / 1e9, 1)}}
+                           "GBps": round(down_bytes / (kern_ms[1] * 1e-3) / 1e9, 1), "path": path_down}}
     x_bytes = 4096 * 2 + 14336 * 2
     y_bytes = sum(N * 4 for _, N, _ in SET)
     line = {

@@ -59,6 +59,8 @@ def lib() -> ctypes.CDLL:
         L.q4_gemv.argtypes = [I32, P, P, AUXP, P, P, I64, I64, I64, P]
         L.q4_dequant.argtypes = [I32, P, P, AUXP, P, I64, I64, P]
         L.q4_gemv_grouped.argtypes = [ctypes.POINTER(GemvDesc), I32, I64, P]
+        L.q4_gemv_chain.argtypes = [ctypes.POINTER(GemvDesc), ctypes.POINTER(ctypes.c_int), I32, I64, P, P]
+        L.q4_gemv_chain.restype = ctypes.c_int
         L.q4_repack.argtypes = [I32, P, P, AUXP, I32, P, P, P, P, I64, I64, P]
         L.q4_validate.argtypes = [I32, P, P, AUXP, I64, I64, P, P]
         L.q4_validate_noalloc.argtypes = [I32, P, P, AUXP, I64, I64, ctypes.POINTER(ctypes.c_int64), P]
@@ -141,6 +143,25 @@ def q4_gemv_grouped(descs, M, stream=None, check=True) -> int:
     rc = lib().q4_gemv_grouped(arr, len(descs), int(M), _stream(stream))
     if check:
         _check(rc, "q4_gemv_grouped")
+    return rc
+
+
+def q4_gemv_chain(groups, M, sync=None, stream=None, check=True) -> int:
+    """``groups``: sequence of groups, each a sequence of (fmt, W_packed,
+    scales, aux, x, y, N, K) tuples; group g+1 runs after group g has written
+    its outputs.  ``sync``: a device tensor of at least 2 uint32/int32 words,
+    zero before its first use (required for more than one group)."""
+    flat = [d for grp in groups for d in grp]
+    arr = (GemvDesc * len(flat))()
+    for i, (fmt, w, s, aux, x, y, N, K) in enumerate(flat):
+        arr[i] = GemvDesc(_fmt(fmt), _ptr(w), _ptr(s), None if aux is None else ctypes.pointer(aux),
+                          _ptr(x), _ptr(y), int(N), int(K))
+    first = (ctypes.c_int * (len(groups) + 1))()
+    for g, grp in enumerate(groups):
+        first[g + 1] = first[g] + len(grp)
+    rc = lib().q4_gemv_chain(arr, first, len(groups), int(M), _ptr(sync), _stream(stream))
+    if check:
+        _check(rc, "q4_gemv_chain")
     return rc
 
 

@@ -31,12 +31,11 @@
 //          per-tensor scale2 multiplies the f32 accumulator in the epilogue.
 //   Q4_K   RNE_bf16(fl(q * (d*sc) - dmin*m)) ([FBTC] sections 5-6): the f32
 //          weight of the pinned rule, rounded once to bf16 for the MMA.
-#include <cuda.h>  // CUtensorMap and the encode signature; the function is fetched at run time
-
 #include <cooperative_groups.h>
 #include <mutex>
 
 #include "q4_internal.cuh"
+#include "tma_map.cuh"
 
 namespace cg = cooperative_groups;
 
@@ -500,24 +499,6 @@ __global__ void __launch_bounds__(THREADS, 2)
 }
 
 // ------------------------------------------------------------------ host
-typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
-                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
-                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-    static EncodeTiledFn fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void *p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiledFn>(p);
-    });
-    return fn;
-}
-
 // One 2-D tiled tensor map: `inner` elements per row (contiguous), `rows`
 // rows `pitch` bytes apart; boxes of box_inner x box_rows; reads past either
 // edge return zeros.
@@ -600,6 +581,20 @@ cudaError_t launch_mb(int MB, const TcArgs &args, const Maps &maps, int64_t tile
 
 }  // namespace
 
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
 bool gemm_tc_eligible(const Tensor &t, q4_dtype x_dtype, int64_t M) {
     return M >= 9 && x_dtype == Q4_DT_BF16 && (t.fmt == Q4_NVFP4 || t.fmt == Q4_Q4K) && t.K % SLOT_K == 0 &&
            t.K <= (1LL << 30) && t.N <= (1LL << 30);
@@ -635,6 +630,7 @@ cudaError_t launch_gemm_tc(const Tensor &t, const void *x, q4_dtype x_dtype, flo
 }
 
 int gemv_read_and_clear_error();
+int gemv_tma_read_and_clear_error();
 
 int read_and_clear_device_error() {
     int v = 0;
@@ -643,7 +639,8 @@ int read_and_clear_device_error() {
     if (cudaMemcpyFromSymbol(&v, g_device_error, sizeof(v)) != cudaSuccess) return Q4_ECUDA;
     if (cudaMemcpyToSymbol(g_device_error, &zero, sizeof(zero)) != cudaSuccess) return Q4_ECUDA;
     const int g = gemv_read_and_clear_error();
-    return v ? v : g;
+    const int tm = gemv_tma_read_and_clear_error();
+    return v ? v : g ? g : tm;
 }
 
 }  // namespace q4

@@ -837,6 +837,10 @@ cudaError_t kmajor(const Tensor &t, const XT *x, float *y, int64_t M, cudaStream
 
 template <typename XT>
 cudaError_t dispatch(const Tensor &t, const XT *x, float *y, int64_t M, cudaStream_t s) {
+    if (std::is_same<XT, __nv_bfloat16>::value && gemv_tma_eligible(t, M)) {
+        note_gemv_path("gemv_tma");
+        return launch_gemv_tma(t, x, y, M, s);
+    }
     if (std::is_same<XT, __nv_bfloat16>::value && gemv_mma_eligible(t, M)) {
         note_gemv_path("gemv_mma");
         return launch_gemv_mma(t, x, Q4_DT_BF16, y, M, s);

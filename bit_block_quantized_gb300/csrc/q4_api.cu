@@ -118,6 +118,7 @@ int q4_gemv_grouped(const q4_gemv_desc *descs, int count, int64_t M, void *strea
     const void *xs[8];
     float *ys[8];
     bool one_launch = count <= 8;
+    bool tma = count <= 8;                     // every member NVFP4 on the TMA kernel, one shared x
     for (int i = 0; i < count; i++) {          // check every member before launching any
         const q4_gemv_desc &d = descs[i];
         Tensor t;
@@ -135,6 +136,13 @@ int q4_gemv_grouped(const q4_gemv_desc *descs, int count, int64_t M, void *strea
         }
         one_launch = one_launch && d.fmt == Q4_NVFP4 && xd == Q4_DT_BF16 && d.K == descs[0].K && M <= 8 &&
                      gemv_mma_eligible(t, M);
+        tma = tma && d.fmt == Q4_NVFP4 && xd == Q4_DT_BF16 && d.K == descs[0].K && d.x == descs[0].x &&
+              gemv_tma_eligible(t, M);
+    }
+    if (tma) {
+        note_gemv_path(count == 1 ? "gemv_tma" : "gemv_tma_group");
+        return launch_gemv_tma_group(ts, descs[0].x, ys, count, M, (cudaStream_t)stream) == cudaSuccess ? Q4_OK
+                                                                                                  : Q4_ECUDA;
     }
     if (one_launch) {
         note_gemv_path("gemv_mma_group");
@@ -143,6 +151,52 @@ int q4_gemv_grouped(const q4_gemv_desc *descs, int count, int64_t M, void *strea
     for (int i = 0; i < count; i++) {
         const q4_gemv_desc &d = descs[i];
         const int rc = q4_gemv(d.fmt, d.W_packed, d.scales, d.aux, d.x, d.y, M, d.N, d.K, stream);
+        if (rc) return rc;
+    }
+    return Q4_OK;
+}
+
+int q4_gemv_chain(const q4_gemv_desc *descs, const int *first, int ngroups, int64_t M, uint32_t *sync,
+                  void *stream) {
+    if (!descs || !first || ngroups <= 0) return Q4_EINVAL;
+    if (M <= 0) return Q4_EDIM;
+    if (first[0] != 0) return Q4_EINVAL;
+    for (int g = 0; g < ngroups; g++)
+        if (first[g + 1] <= first[g]) return Q4_EINVAL;
+    const int count = first[ngroups];
+    if (ngroups > 1 && !sync) return Q4_EINVAL;
+    if (sync && (((uintptr_t)sync) & 7u) != 0) return Q4_EALIGN;
+    Tensor ts[8];
+    const void *xs[4];
+    float *ys[8];
+    bool one_launch = count <= 8 && ngroups <= 4;
+    for (int g = 0; g < ngroups; g++) {
+        for (int i = first[g]; i < first[g + 1]; i++) {   // check every member before launching any
+            const q4_gemv_desc &d = descs[i];
+            Tensor t;
+            const int rc = make_tensor(d.fmt, d.W_packed, d.scales, d.aux, d.N, d.K, t);
+            if (rc) return rc;
+            if (d.fmt == Q4_NVFP4_SPLITHALF || d.fmt == Q4_LOGICAL) return Q4_EUNSUPPORTED;
+            if (!d.x || !d.y) return Q4_EINVAL;
+            if (!aligned16(d.x) || !aligned16(d.y)) return Q4_EALIGN;
+            const q4_dtype xd = d.aux ? d.aux->x_dtype : default_x_dtype(d.fmt);
+            if (xd != Q4_DT_F32 && xd != Q4_DT_BF16) return Q4_EINVAL;
+            one_launch = one_launch && xd == Q4_DT_BF16 && d.x == descs[first[g]].x && d.K == descs[first[g]].K;
+            if (one_launch) {
+                ts[i] = t;
+                ys[i] = d.y;
+            }
+        }
+        if (one_launch) xs[g] = descs[first[g]].x;
+    }
+    if (one_launch && gemv_tma_chain_fits(ts, first, ngroups, M)) {
+        note_gemv_path(ngroups == 1 ? (count == 1 ? "gemv_tma" : "gemv_tma_group") : "gemv_tma_chain");
+        return launch_gemv_tma_chain(ts, xs, ys, first, ngroups, M, sync, (cudaStream_t)stream) == cudaSuccess
+                   ? Q4_OK
+                   : Q4_ECUDA;
+    }
+    for (int g = 0; g < ngroups; g++) {
+        const int rc = q4_gemv_grouped(descs + first[g], first[g + 1] - first[g], M, stream);
         if (rc) return rc;
     }
     return Q4_OK;

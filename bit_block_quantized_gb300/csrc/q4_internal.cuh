@@ -205,6 +205,13 @@ cudaError_t launch_gemv(const Tensor &t, const void *x, q4_dtype x_dtype, float 
 cudaError_t launch_gemm_tc(const Tensor &t, const void *x, q4_dtype x_dtype, float *y, int64_t M,
                            cudaStream_t s, bool *handled);
 bool gemv_mma_eligible(const Tensor &t, int64_t M);
+bool gemv_tma_eligible(const Tensor &t, int64_t M);
+cudaError_t launch_gemv_tma(const Tensor &t, const void *x, float *y, int64_t M, cudaStream_t s);
+cudaError_t launch_gemv_tma_group(const Tensor *ts, const void *x, float *const *ys, int count, int64_t M,
+                                  cudaStream_t s);
+bool gemv_tma_chain_fits(const Tensor *ts, const int *first, int ngroups, int64_t M);
+cudaError_t launch_gemv_tma_chain(const Tensor *ts, const void *const *xs, float *const *ys, const int *first,
+                                  int ngroups, int64_t M, unsigned *sync, cudaStream_t s);
 bool gemv_blk_eligible(const Tensor &t, int64_t M);
 cudaError_t launch_gemv_blk(const Tensor &t, const void *x, q4_dtype xd, float *y, int64_t M, cudaStream_t s);
 bool gemv_gptq_eligible(const Tensor &t, int64_t M);

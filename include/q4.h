@@ -141,6 +141,28 @@ typedef struct {
  * rejected nothing is launched. */
 int q4_gemv_grouped(const q4_gemv_desc *descs, int count, int64_t M, void *stream);
 
+/* A chain of GEMV groups with stream-order semantics, in one launch where
+ * possible: group g is descs[first[g] .. first[g+1]-1] (first[0] = 0, ngroups
+ * entries after it), its members read the same x and share K, and group g+1
+ * reads its x and writes its y only after every member of groups 0..g has
+ * written its y -- exactly as if each group were its own q4_gemv_grouped call
+ * on `stream`, so a later group's x may be (a view of) an earlier group's y.
+ * This is the decode sequence of one layer's projections (the pages' decode
+ * path streams every weight of every layer once per token, [W4K] section 7d)
+ * with the per-launch ramp and tail paid once.  When every member is NVFP4
+ * with bf16 x, M <= 4, K % 256 == 0, ngroups <= 4 and count <= 8, the chain
+ * runs as ONE cooperative launch whose CTAs meet at a grid-wide barrier
+ * between groups while the next group's weights are already streaming;
+ * otherwise the groups are issued one after the other as q4_gemv_grouped.
+ * sync: caller-owned device memory of 2 uint32 words, zero before its first
+ * use and not written by the caller afterwards; the launch leaves it ready
+ * for the next call (also across CUDA-graph replays).  Chains that may run
+ * at the same time (other streams) need their own sync words.  May be NULL
+ * when ngroups == 1.  Same checks, accuracy and stream semantics as
+ * q4_gemv_grouped; if any member is rejected nothing is launched. */
+int q4_gemv_chain(const q4_gemv_desc *descs, const int *first, int ngroups, int64_t M, uint32_t *sync,
+                  void *stream);
+
 /* out[N][K] = w_hat, f32 or bf16 per aux->out_dtype, by the pinned per-format
  * rule ([MUS7] 7.2 for NVFP4; the per-format sections cited above).  Bit-exact
  * with the definition.  Asynchronous on `stream`. */
@@ -201,8 +223,10 @@ int q4_validate_noalloc(q4_fmt fmt, const void *W_packed, const void *scales, co
 int q4_last_error(void);
 
 /* Name of the kernel family the calling host thread's latest q4_gemv or
- * q4_gemv_grouped launched ("gemm_tc", "gemv_mma", "gemv_mma_group",
- * "gemv_rows_tma", "gemv_rows_m1", "gemv_general", "gemv_kmajor"; "" before
+ * q4_gemv_grouped or q4_gemv_chain launched ("gemv_tma", "gemv_tma_group",
+ * "gemv_tma_chain", "gemm_tc", "gemv_mma", "gemv_mma_group", "gemv_mma_q4k",
+ * "gemv_mma_q40", "gemv_mma_gptq", "gemv_rows_tma", "gemv_rows_m1",
+ * "gemv_general", "gemv_kmajor"; "" before
  * the first call).  A diagnostic with no counterpart in the pages: it lets a
  * caller (and the tests) confirm which path a shape takes.  Static storage. */
 const char *q4_last_gemv_path(void);

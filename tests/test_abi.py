@@ -110,3 +110,13 @@ def test_host_side_rejections(lib):
                               check=False) == q4.Q4_EALIGN      # nothing launched
     assert q4.q4_gemv_grouped([good], 0, stream=0, check=False) == q4.Q4_EDIM
     assert q4.q4_gemv_grouped([], 1, stream=0, check=False) == q4.Q4_EINVAL
+    # chains: a group barrier needs the caller's sync words; every member is
+    # checked before anything is launched
+    chain = q4.q4_gemv_chain
+    assert chain([[good], [good]], 1, sync=None, stream=0, check=False) == q4.Q4_EINVAL
+    assert chain([[good], [good]], 1, sync=0x50004, stream=0, check=False) == q4.Q4_EALIGN
+    assert chain([[good], [("nvfp4", A, B, nv, C, D + 4, 64, 64)]], 1, sync=0x50000, stream=0,
+                 check=False) == q4.Q4_EALIGN
+    assert chain([[good]], 0, stream=0, check=False) == q4.Q4_EDIM
+    assert chain([], 1, stream=0, check=False) == q4.Q4_EINVAL
+    assert chain([[good], []], 1, sync=0x50000, stream=0, check=False) == q4.Q4_EINVAL
