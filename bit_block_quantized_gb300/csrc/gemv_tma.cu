@@ -125,16 +125,27 @@ __device__ __forceinline__ uint32_t lds8(uint32_t a) {
     return v;
 }
 
-__device__ __forceinline__ void tma_3d(uint32_t dst, const CUtensorMap *map, int c0, int c1, int c2, uint32_t bar) {
+// Weight copies carry an L2 evict-first policy: they are read exactly once,
+// and should not push the activations and outputs out of L2.
+__device__ __forceinline__ uint64_t evict_first_policy() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+__device__ __forceinline__ void tma_3d(uint32_t dst, const CUtensorMap *map, int c0, int c1, int c2, uint32_t bar,
+                                       uint64_t pol) {
     asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];"
-        ::"r"(dst), "l"(map), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3, %4}], [%5], %6;"
+        ::"r"(dst), "l"(map), "r"(c0), "r"(c1), "r"(c2), "r"(bar), "l"(pol)
         : "memory");
 }
-__device__ __forceinline__ void tma_2d(uint32_t dst, const CUtensorMap *map, int c0, int c1, uint32_t bar) {
+__device__ __forceinline__ void tma_2d(uint32_t dst, const CUtensorMap *map, int c0, int c1, uint32_t bar,
+                                       uint64_t pol) {
     asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
-        ::"r"(dst), "l"(map), "r"(c0), "r"(c1), "r"(bar)
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3}], [%4], %5;"
+        ::"r"(dst), "l"(map), "r"(c0), "r"(c1), "r"(bar), "l"(pol)
         : "memory");
 }
 
@@ -189,6 +200,7 @@ __device__ void grid_barrier(unsigned *sync, volatile int *abort_flag) {
     __threadfence();
 }
 
+
 // Four bf16 values (two words) times an exact power of two -> two f16x2
 // words; `ok` stays true only if every value survives the f16 rounding.
 __device__ __forceinline__ uint2 bf16x4_to_f16(uint2 v, float scale, bool &ok) {
@@ -202,9 +214,44 @@ __device__ __forceinline__ uint2 bf16x4_to_f16(uint2 v, float scale, bool &ok) {
 
 // The x slice of consumer warp w (chunk w of every stage) as exactly-scaled
 // f16 B fragments in the layout above.  Lane l serves column m = l % MT.
-// Pass 1 loads 16-byte runs (8 k) of that row, keeps the column maximum and
-// puts the raw bf16 bits into their entries; pass 2 converts in place.
-// Chunks past K are staged as zeros (their weights are never read).
+// Staging sits on the critical path of every launch (the decode warps wait
+// for it once the launch before has finished), so when a lane's share is at
+// most XR runs of 8 k it is one round trip: all loads issued at once into
+// registers, the column maximum reduced over the lanes, then converted and
+// stored.  Larger shares (batch 4 at large K) take two passes through shared
+// memory.  The scale 2^(12-e) (e the largest exponent) keeps |x| < 2^13; a
+// value that does not survive the f16 rounding sends the warp to the f32
+// CUDA-core path.  Chunks past K are zeros (their weights are never read).
+constexpr int XR = 8;
+
+__device__ __forceinline__ uint32_t absmax8(uint4 v) {   // packed |bf16| maximum (bit patterns order like values)
+    return __vmaxu2(__vmaxu2(v.x & 0x7fff7fffu, v.y & 0x7fff7fffu), __vmaxu2(v.z & 0x7fff7fffu, v.w & 0x7fff7fffu));
+}
+
+// Column scale from the packed maximum: x * 2^(12-e) keeps |x| < 2^13 in f16.
+template <int MT>
+__device__ __forceinline__ bool column_scale(uint32_t mx2, float &scale, float (&inv)[MT]) {
+    const uint32_t mxb = (mx2 & 0xffffu) > (mx2 >> 16) ? (mx2 & 0xffffu) : (mx2 >> 16);
+    float amax = __uint_as_float(mxb << 16);
+#pragma unroll
+    for (int off = MT; off < 32; off <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+    float iv = 1.0f;
+    bool exact = true;
+    scale = 1.0f;
+    if (amax > 0.0f) {
+        const int ex = (int)((__float_as_uint(amax) >> 23) & 255u) - 127;
+        if (ex < -100 || ex > 100)
+            exact = false;
+        else {
+            scale = __uint_as_float((uint32_t)(127 + 12 - ex) << 23);
+            iv = __uint_as_float((uint32_t)(127 - 12 + ex) << 23);
+        }
+    }
+#pragma unroll
+    for (int mm = 0; mm < MT; mm++) inv[mm] = __shfl_sync(0xffffffffu, iv, mm);   // lane mm holds column mm
+    return exact;
+}
+
 template <int MT>
 __device__ __forceinline__ bool stage_x(const __nv_bfloat16 *__restrict__ x, int K, int M, int nst, int w, int lane,
                                         uint2 *xs, float (&inv)[MT]) {
@@ -214,44 +261,53 @@ __device__ __forceinline__ bool stage_x(const __nv_bfloat16 *__restrict__ x, int
     const int nrun = nst * 32;                  // 8-k runs of the warp's k set
     const __nv_bfloat16 *row = x + (int64_t)(mv ? m : 0) * K;
     uint32_t mx2 = 0;
-#pragma unroll 4
-    for (int r = lane / MT; r < nrun; r += LPC) {
-        const int s = r >> 5, rr = r & 31;
-        const int k = s * KS + w * 256 + rr * 8;
-        // L2-coherent load: in a chain, x may have been written by an earlier group of this launch
-        const uint4 v = (mv && k < K) ? __ldcg(reinterpret_cast<const uint4 *>(row + k)) : make_uint4(0u, 0u, 0u, 0u);
-        mx2 = __vmaxu2(mx2, __vmaxu2(__vmaxu2(v.x & 0x7fff7fffu, v.y & 0x7fff7fffu),
-                                     __vmaxu2(v.z & 0x7fff7fffu, v.w & 0x7fff7fffu)));
-        const int t = rr >> 3, h = (rr >> 2) & 1, j0 = (rr & 3) * 2, vb = 2 * s + h;
-        xs[((vb * 8 + j0) * MT + m) * 4 + t] = make_uint2(v.x, v.y);
-        xs[((vb * 8 + j0 + 1) * MT + m) * 4 + t] = make_uint2(v.z, v.w);
-    }
-    const uint32_t mxb = (mx2 & 0xffffu) > (mx2 >> 16) ? (mx2 & 0xffffu) : (mx2 >> 16);
-    float amax = __uint_as_float(mxb << 16);
+    float scale;
+    bool exact;
+    if (nrun <= XR * LPC) {
+        uint4 v[XR];
 #pragma unroll
-    for (int off = MT; off < 32; off <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
-    float scale = 1.0f, iv = 1.0f;
-    bool exact = true;
-    if (amax > 0.0f) {
-        const int ex = (int)((__float_as_uint(amax) >> 23) & 255u) - 127;
-        if (ex < -100 || ex > 100)
-            exact = false;
-        else {
-            scale = __uint_as_float((uint32_t)(127 + 12 - ex) << 23);   // max |x * scale| < 2^13
-            iv = __uint_as_float((uint32_t)(127 - 12 + ex) << 23);
+        for (int i = 0; i < XR; i++) {
+            const int r = lane / MT + i * LPC;
+            const int k = (r >> 5) * KS + w * 256 + (r & 31) * 8;
+            // L2-coherent load: in a chain, x may have been written by an earlier group of this launch
+            v[i] = (r < nrun && mv && k < K) ? __ldcg(reinterpret_cast<const uint4 *>(row + k))
+                                             : make_uint4(0u, 0u, 0u, 0u);
+            mx2 = __vmaxu2(mx2, absmax8(v[i]));
+        }
+        exact = column_scale<MT>(mx2, scale, inv);
+#pragma unroll
+        for (int i = 0; i < XR; i++) {
+            const int r = lane / MT + i * LPC;
+            if (r < nrun) {
+                const int s = r >> 5, rr = r & 31;
+                const int t = rr >> 3, h = (rr >> 2) & 1, j0 = (rr & 3) * 2, vb = 2 * s + h;
+                xs[((vb * 8 + j0) * MT + m) * 4 + t] = bf16x4_to_f16(make_uint2(v[i].x, v[i].y), scale, exact);
+                xs[((vb * 8 + j0 + 1) * MT + m) * 4 + t] = bf16x4_to_f16(make_uint2(v[i].z, v[i].w), scale, exact);
+            }
+        }
+    } else {
+#pragma unroll 4
+        for (int r = lane / MT; r < nrun; r += LPC) {
+            const int s = r >> 5, rr = r & 31;
+            const int k = s * KS + w * 256 + rr * 8;
+            const uint4 v = (mv && k < K) ? __ldcg(reinterpret_cast<const uint4 *>(row + k))
+                                          : make_uint4(0u, 0u, 0u, 0u);
+            mx2 = __vmaxu2(mx2, absmax8(v));
+            const int t = rr >> 3, h = (rr >> 2) & 1, j0 = (rr & 3) * 2, vb = 2 * s + h;
+            xs[((vb * 8 + j0) * MT + m) * 4 + t] = make_uint2(v.x, v.y);
+            xs[((vb * 8 + j0 + 1) * MT + m) * 4 + t] = make_uint2(v.z, v.w);
+        }
+        exact = column_scale<MT>(mx2, scale, inv);
+#pragma unroll 4
+        for (int r = lane / MT; r < nrun; r += LPC) {
+            const int s = r >> 5, rr = r & 31;
+            const int t = rr >> 3, h = (rr >> 2) & 1, j0 = (rr & 3) * 2, vb = 2 * s + h;
+            uint2 *e0 = xs + ((vb * 8 + j0) * MT + m) * 4 + t, *e1 = xs + ((vb * 8 + j0 + 1) * MT + m) * 4 + t;
+            const uint2 c0 = bf16x4_to_f16(*e0, scale, exact), c1 = bf16x4_to_f16(*e1, scale, exact);
+            *e0 = c0;
+            *e1 = c1;
         }
     }
-#pragma unroll 4
-    for (int r = lane / MT; r < nrun; r += LPC) {
-        const int s = r >> 5, rr = r & 31;
-        const int t = rr >> 3, h = (rr >> 2) & 1, j0 = (rr & 3) * 2, vb = 2 * s + h;
-        uint2 *e0 = xs + ((vb * 8 + j0) * MT + m) * 4 + t, *e1 = xs + ((vb * 8 + j0 + 1) * MT + m) * 4 + t;
-        const uint2 c0 = bf16x4_to_f16(*e0, scale, exact), c1 = bf16x4_to_f16(*e1, scale, exact);
-        *e0 = c0;
-        *e1 = c1;
-    }
-#pragma unroll
-    for (int mm = 0; mm < MT; mm++) inv[mm] = __shfl_sync(0xffffffffu, iv, mm);
     exact = __all_sync(0xffffffffu, exact);
     __syncwarp();
     return exact;
@@ -320,6 +376,7 @@ __global__ void __launch_bounds__(THREADS, Q4_TMA_CTAS_PER_SM)
         // ------------------------------------------------------ producer
         if (lane == 0) {
             const uint32_t ring = smem_u32(base);
+            const uint64_t pol = evict_first_policy();
             int issued = 0, slot = 0, phase = 0;
             bool stop = false;
             for (int p = 0; p < a.ngroups && !stop; p++) {
@@ -335,8 +392,8 @@ __global__ void __launch_bounds__(THREADS, Q4_TMA_CTAS_PER_SM)
                         }
                         const uint32_t dst = ring + (uint32_t)(slot * STAGE_BYTES), bar = smem_u32(&full[slot]);
                         mbar_arrive_expect_tx(&full[slot], STAGE_BYTES);
-                        tma_3d(dst, &maps.pay[member], 0, row0, st * (KS / 256), bar);
-                        tma_2d(dst + PAY_BYTES, &maps.sc[member], st * (KS / 16), row0, bar);
+                        tma_3d(dst, &maps.pay[member], 0, row0, st * (KS / 256), bar, pol);
+                        tma_2d(dst + PAY_BYTES, &maps.sc[member], st * (KS / 16), row0, bar, pol);
                         issued++;
                         if (++slot == S) { slot = 0; phase ^= 1; }
                     }
@@ -351,6 +408,19 @@ __global__ void __launch_bounds__(THREADS, Q4_TMA_CTAS_PER_SM)
     }
 
     // ---------------------------------------------------------- consumers
+    // Warm L2 with this warp's slice of the first group's x while the launch
+    // before may still be running: a prefetch only fills L2, the coherence
+    // point, so a later write to x by that launch is still what the loads
+    // after the dependency wait see.  Lane l covers 128-byte line l & 3 of
+    // the warp's 512-byte run in stage l >> 2.
+    {
+        const int K0 = a.K[0];
+        for (int m = 0; m < a.M; m++)
+            for (int r = lane; r < a.nst[0] * 4; r += 32) {
+                const int k = (r >> 2) * KS + warp * 256 + (r & 3) * 64;
+                if (k < K0) asm volatile("prefetch.global.L2 [%0];" ::"l"(a.x[0] + (int64_t)m * K0 + k));
+            }
+    }
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const int g = lane >> 2, tt = lane & 3;
     uint2 *xs = xs_all + (size_t)warp * a.max_nst * 2 * 8 * MT * 4;
