@@ -104,7 +104,12 @@ typedef struct {
 /* y[M][N] (f32) = x[M][K] . W^T.  The fused decode + dot of [W4K] section 1:
  * packed weights are streamed once from HBM, decoded on chip and accumulated
  * in f32; no dequantized matrix is written.  M <= 8 runs the bandwidth-bound
- * GEMV kernels.  M >= 9 with bf16 x on NVFP4 or Q4_K (K % 256 == 0) runs the
+ * GEMV kernels: NVFP4 with bf16 x, M <= 4 and K % 256 == 0 streams its
+ * weights into shared memory by tensor TMA (weights are read before the
+ * stream dependency on the previous launch resolves, x and y after it, so W
+ * must not be written by a still-running kernel that released its dependents
+ * early; the library's own kernels that do so only read weights).  M >= 9
+ * with bf16 x on NVFP4 or Q4_K (K % 256 == 0) runs the
  * tcgen05 tensor-core kernel: weights decoded to bf16 straight into tensor
  * memory, x tiles by TMA, f32 accumulation in TMEM, K split over a cluster
  * and reduced in a fixed order (repeated calls agree bit for bit), batch in
