@@ -326,12 +326,12 @@ __global__ void __launch_bounds__(THREADS, 2)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::NS; s++) {
-            mbar_init(&a_full[s], 2 * ROWS + 1);   // the 256 decode threads + the X-tile thread
+            mbar_init(&a_full[s], DEC_WARPS + 1);  // one arrive per decode warp + the X-tile thread
             mbar_init(&a_empty[s], 1);         // one tcgen05.commit
         }
         for (int s = 0; s < C::NW; s++) {
             mbar_init(&w_full[s], 1);          // the weight thread's arrive + its bytes
-            mbar_init(&w_empty[s], 2 * ROWS);      // the 256 decode threads that read the slot
+            mbar_init(&w_empty[s], DEC_WARPS);     // one arrive per decode warp that read the slot
         }
         mbar_init(&done_bar, 1);
         abort_s = 0;
@@ -375,7 +375,10 @@ __global__ void __launch_bounds__(THREADS, 2)
                     const uint32_t blk = slot + r * 144 + 16 + 32 * c;
                     q4k_half(meta, lds128(blk), lds128(blk + 16), c, h, o);
                 }
-                if (c == 3) mbar_arrive(&w_empty[wi]);   // the slot's bytes are all in registers
+                if (c == 3) {                        // the slot's bytes are all in this warp's registers
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&w_empty[wi]);
+                }
                 const int s = i % C::NS;
                 ok = i < C::NS || wait_or_abort(&a_empty[s], ((i / C::NS) & 1) ^ 1, abort_flag);
                 if (!__all_sync(0xffffffffu, ok)) {   // tcgen05.st is warp-collective
@@ -383,9 +386,10 @@ __global__ void __launch_bounds__(THREADS, 2)
                     break;
                 }
                 tc_fence_after();
-                tmem_st16(lane_base + s * A_COLS, o);
+                tmem_st16(lane_base + s * A_COLS, o);   // returns once this thread's stores are done
                 tc_fence_before();
-                mbar_arrive(&a_full[s]);
+                __syncwarp();                           // ... and every lane's: one arrive per warp
+                if (lane == 0) mbar_arrive(&a_full[s]);
             }
         }
     } else if (warp == W_MMA) {
@@ -533,12 +537,17 @@ bool encode_x(CUtensorMap *map, const void *x, int64_t K, int64_t rows, int MB) 
     return encode_2d(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, K, rows, K * 2, BK, MB, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
-// K slice per CTA: split K over up to 8 cluster ranks until the grid holds
-// about two CTAs per SM, keeping every slice whole weight slots.
-int pick_splits(int64_t tiles, int64_t K) {
+// K slice per CTA: split K over up to 8 cluster ranks until the grid covers
+// every SM once (batch tiles up to 32) or half of them (64 and 128, where the
+// cluster's partial-tile exchange costs more than idle SMs), keeping every
+// slice whole weight slots.  Measured on 14336 x 4096 (112 row tiles): split
+// 2 at batch 16 (24.4 us against 27.7 at split 4), no split at batch 128
+// (31.6 us against 40.9).
+int pick_splits(int64_t tiles, int64_t K, int MB) {
     const int64_t sms = sm_count();
+    const int64_t target = MB >= 64 ? sms / 2 : sms;
     int S = 1;
-    while (S < 8 && tiles * S < 2 * sms && K % (2 * S) == 0 && (K / (2 * S)) % SLOT_K == 0) S *= 2;
+    while (S < 8 && tiles * S < target && K % (2 * S) == 0 && (K / (2 * S)) % SLOT_K == 0) S *= 2;
     return S;
 }
 
@@ -607,12 +616,12 @@ cudaError_t launch_gemm_tc(const Tensor &t, const void *x, q4_dtype x_dtype, flo
     *handled = true;
     note_gemv_path("gemm_tc");
     const int64_t tiles = (t.N + ROWS - 1) / ROWS;
-    const int S = pick_splits(tiles, t.K);
     Maps maps;
     if (!encode_weights(&maps, t)) return cudaErrorInvalidValue;
     for (int64_t m0 = 0; m0 < M; m0 += 128) {
         const int64_t rows = M - m0 < 128 ? M - m0 : 128;
         const int MB = rows <= 16 ? 16 : rows <= 32 ? 32 : rows <= 64 ? 64 : 128;
+        const int S = pick_splits(tiles, t.K, MB);
         if (!encode_x(&maps.x, (const uint8_t *)x + m0 * t.K * 2, t.K, rows, MB)) return cudaErrorInvalidValue;
         TcArgs args;
         args.y = y + m0 * t.N;

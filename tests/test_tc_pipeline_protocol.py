@@ -1,7 +1,8 @@
 """The barrier protocol of the tensor-core small-batch GEMM, checked on the CPU.
 
-The kernel's roles (two decode warpgroups, the MMA thread, the weight-slot
-TMA thread and the X-tile TMA thread) hand stages to each other through
+The kernel's roles (eight decode warps in two warpgroups, each warp arriving
+once per stage and per slot, the MMA thread, the weight-slot TMA thread and
+the X-tile TMA thread) hand stages to each other through
 mbarriers whose waits test only the parity of a phase.  A waiter that can
 fall two phases behind a barrier is fooled: the wait for completion #u
 passes as soon as completion #u-2 has happened.  This module replays the
@@ -21,6 +22,7 @@ import random
 import pytest
 
 TMEM_COLS, A_COLS = 256, 32
+DEC_WARPS = 8
 
 
 def rings(MB):
@@ -55,15 +57,16 @@ def simulate(MB, nslots, seed, alternate_slots=False):
     rnd = random.Random(seed)
     ns, nw = rings(MB)
     nst = 4 * nslots
-    groups_per_stage = 1 if alternate_slots else 2
-    a_full = [Bar(f"a_full[{s}]", groups_per_stage + 1) for s in range(ns)]
+    warps_per_stage = DEC_WARPS // 2 if alternate_slots else DEC_WARPS
+    a_full = [Bar(f"a_full[{s}]", warps_per_stage + 1) for s in range(ns)]
     a_empty = [Bar(f"a_empty[{s}]", 1) for s in range(ns)]
     w_full = [Bar(f"w_full[{s}]", 1) for s in range(nw)]
-    w_empty = [Bar(f"w_empty[{s}]", groups_per_stage) for s in range(nw)]
+    w_empty = [Bar(f"w_empty[{s}]", warps_per_stage) for s in range(nw)]
     done = Bar("done", 1)
 
     progs = {}
-    for g in (0, 1):
+    for wp in range(DEC_WARPS):
+        g = wp // 4                    # the warp's warpgroup
         ops = []
         slots = range(g, nslots, 2) if alternate_slots else range(nslots)
         for j in slots:
@@ -75,7 +78,7 @@ def simulate(MB, nslots, seed, alternate_slots=False):
                 if i >= ns:
                     ops.append(("wait", a_empty[i % ns], i // ns - 1))
                 ops.append(("arrive", a_full[i % ns], i // ns))
-        progs[f"decode{g}"] = ops
+        progs[f"decode{wp}"] = ops
     ops = []
     for i in range(nst):
         ops += [("wait", a_full[i % ns], i // ns), ("mma", a_empty[i % ns], i // ns)]
@@ -95,7 +98,7 @@ def simulate(MB, nslots, seed, alternate_slots=False):
 
     pc = {k: 0 for k in progs}
     tensor, landing = [], []       # MMAs complete in order; copies land in any order
-    for _ in range(200000):
+    for _ in range(400000):
         ready = []
         for k, ops in progs.items():
             if pc[k] < len(ops):
@@ -139,7 +142,7 @@ def simulate(MB, nslots, seed, alternate_slots=False):
 @pytest.mark.parametrize("MB", [16, 32, 64, 128])
 def test_kernel_schedule_never_skips_a_phase(MB):
     for nslots in range(1, 9):
-        for seed in range(60):
+        for seed in range(25):
             simulate(MB, nslots, seed)
 
 
@@ -147,5 +150,5 @@ def test_alternate_slot_schedule_is_caught():
     """Alternating warpgroups over a 4-stage ring (batch 128) let one group
     reach a stage two uses ahead of the barrier: the check must fire."""
     with pytest.raises(AssertionError, match="passed in phase"):
-        for seed in range(200):
+        for seed in range(400):
             simulate(128, 4, seed, alternate_slots=True)
