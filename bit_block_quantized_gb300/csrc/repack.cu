@@ -97,6 +97,61 @@ __global__ void repack_codes(Src s, const int32_t *__restrict__ perm, void *__re
     }
 }
 
+// GPTQ <-> AWQ without act-order is a transpose of 8 x 8 nibble blocks: the
+// GPTQ words (r, 8c .. 8c+7) hold codes k = 8r .. 8r+7 of columns 8c .. 8c+7
+// (one column per word), the AWQ words (8r .. 8r+7, c) hold the same codes
+// one row per word, columns in slot order 0,2,4,6,1,3,5,7.  Each thread
+// moves one block: 32 contiguous bytes on the GPTQ side, eight coalesced
+// words on the AWQ side, and three rounds of masked swaps transpose the
+// nibbles in registers.  Feeding the GPTQ words in slot order makes the
+// transposed rows come out in AWQ slot order.
+__device__ __forceinline__ void transpose_nibbles8(uint32_t (&w)[8]) {
+#pragma unroll
+    for (int st = 0; st < 3; st++) {
+        const int sh = 4 << st;                                     // 4, 8, 16
+        const uint32_t mask = st == 0 ? 0x0F0F0F0Fu : st == 1 ? 0x00FF00FFu : 0x0000FFFFu;
+        const int d = 1 << st;                                      // row distance 1, 2, 4
+#pragma unroll
+        for (int a = 0; a < 8; a++) {
+            if (a & d) continue;
+            const int b = a + d;
+            const uint32_t t = ((w[a] >> sh) ^ w[b]) & mask;
+            w[b] ^= t;
+            w[a] ^= t << sh;
+        }
+    }
+}
+
+template <bool TO_AWQ>
+__global__ void repack_gptq_awq(const uint32_t *__restrict__ src, uint32_t *__restrict__ dst, int64_t K,
+                                int64_t N) {
+    const int64_t C = N >> 3, units = (K >> 3) * C;
+    for (int64_t u = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; u < units;
+         u += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t r = u / C, c = u % C;
+        uint32_t w[8];
+        if (TO_AWQ) {
+            const uint4 lo = *reinterpret_cast<const uint4 *>(src + r * N + 8 * c);
+            const uint4 hi = *reinterpret_cast<const uint4 *>(src + r * N + 8 * c + 4);
+            const uint32_t g[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+#pragma unroll
+            for (int p = 0; p < 8; p++) w[p] = g[p < 4 ? 2 * p : 2 * (p - 4) + 1];   // slot p holds column col(p)
+            transpose_nibbles8(w);
+#pragma unroll
+            for (int k = 0; k < 8; k++) dst[(8 * r + k) * C + c] = w[k];
+        } else {
+#pragma unroll
+            for (int k = 0; k < 8; k++) w[k] = src[(8 * r + k) * C + c];
+            transpose_nibbles8(w);                                  // w[p] = GPTQ word of column col(p)
+            uint32_t g[8];
+#pragma unroll
+            for (int n = 0; n < 8; n++) g[n] = w[awq_slot(n)];
+            *reinterpret_cast<uint4 *>(dst + r * N + 8 * c) = make_uint4(g[0], g[1], g[2], g[3]);
+            *reinterpret_cast<uint4 *>(dst + r * N + 8 * c + 4) = make_uint4(g[4], g[5], g[6], g[7]);
+        }
+    }
+}
+
 template <int DST>
 __global__ void repack_meta(Src s, uint16_t *__restrict__ dst_scales, void *__restrict__ dst_zeros) {
     const int64_t N = s.N, G = s.K / s.group;
@@ -247,9 +302,11 @@ int launch_repack(q4_fmt src, const Tensor &t, q4_fmt dst, void *dst_w, void *ds
     if (!src_ok || !dst_ok) return Q4_EUNSUPPORTED;
 
     Src s{src, t.w, t.scales, t.zeros, src == Q4_Q40 ? 32 : t.group, t.N, t.K};
-    const unsigned int zero = 0;
-    if (cudaMemcpyToSymbolAsync(g_repack_flags, &zero, sizeof(zero), 0, cudaMemcpyHostToDevice, st) !=
-        cudaSuccess)
+    // Reset the flags on the device: a copy from (pageable) host memory would
+    // first wait for the stream, a second host round trip per call.
+    void *flags_dev = nullptr;
+    if (cudaGetSymbolAddress(&flags_dev, g_repack_flags) != cudaSuccess ||
+        cudaMemsetAsync(flags_dev, 0, sizeof(unsigned int), st) != cudaSuccess)
         return Q4_ECUDA;
     const int32_t *perm = nullptr;
     if (t.g_idx && (src == Q4_GPTQ || src == Q4_LOGICAL)) {
@@ -264,10 +321,18 @@ int launch_repack(q4_fmt src, const Tensor &t, q4_fmt dst, void *dst_w, void *ds
     const int64_t code_units = (dst == Q4_GPTQ) ? (K / 8) * N : (dst == Q4_AWQ ? K * (N / 8) : K * N);
     const int64_t meta_units = (K / s.group) * (N / 8);
     if (dst == Q4_GPTQ) {
-        repack_codes<Q4_GPTQ><<<grid_for(code_units), 256, 0, st>>>(s, perm, dst_w);
+        if (src == Q4_AWQ && !perm)
+            repack_gptq_awq<false><<<grid_for(code_units / 8), 256, 0, st>>>((const uint32_t *)t.w,
+                                                                               (uint32_t *)dst_w, K, N);
+        else
+            repack_codes<Q4_GPTQ><<<grid_for(code_units), 256, 0, st>>>(s, perm, dst_w);
         repack_meta<Q4_GPTQ><<<grid_for(meta_units), 256, 0, st>>>(s, (uint16_t *)dst_scales, dst_zeros);
     } else if (dst == Q4_AWQ) {
-        repack_codes<Q4_AWQ><<<grid_for(code_units), 256, 0, st>>>(s, perm, dst_w);
+        if (src == Q4_GPTQ && !perm)
+            repack_gptq_awq<true><<<grid_for(code_units / 8), 256, 0, st>>>((const uint32_t *)t.w, (uint32_t *)dst_w,
+                                                                              K, N);
+        else
+            repack_codes<Q4_AWQ><<<grid_for(code_units), 256, 0, st>>>(s, perm, dst_w);
         repack_meta<Q4_AWQ><<<grid_for(meta_units), 256, 0, st>>>(s, (uint16_t *)dst_scales, dst_zeros);
     } else {
         repack_codes<Q4_LOGICAL><<<grid_for(code_units), 256, 0, st>>>(s, perm, dst_w);
