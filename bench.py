@@ -57,6 +57,8 @@ def parse():
     ap.add_argument("--ncu-case", action="store_true",
                     help="small profiling case: 4 grouped gate+up launches (2 x 14336x4096, 66 MB) on "
                          "one weight copy, no timing, no JSON line")
+    ap.add_argument("--ncu-rows-case", action="store_true",
+                    help="small profiling case: one launch of each remaining row's kernel on its own shape")
     ap.add_argument("--ncu-gemm-case", default=None, metavar="FMT:M",
                     help="small profiling case of the tensor-core small-batch GEMM: 3 launches of "
                          "FMT (nvfp4|q4k) at batch M on one 14336x4096 weight copy")
@@ -683,8 +685,64 @@ def ncu_case():
     print("ncu case done, last_error", q4.q4_last_error())
 
 
+def ncu_rows_case():
+    """One launch of each remaining row's kernel on its own shape (one weight
+    copy, a few hundred MB of device memory at most), for a single-pass ncu
+    launch list with DRAM bytes.  Prints each row's algorithmic bytes."""
+    import torch
+
+    import bit_block_quantized_gb300 as q4
+    import synth
+    from bit_block_quantized_gb300 import build as q4build
+    q4build.build()
+    stream = torch.cuda.Stream()
+    for tag, fmt, N, K, M, config, kw, xdt in (
+            ("a1 NVFP4 M=4", "nvfp4", 14336, 4096, 4, 5, dict(row_scale=True), q4.Q4_DT_BF16),
+            ("a1 NVFP4 M=8", "nvfp4", 14336, 4096, 8, 5, dict(row_scale=True), q4.Q4_DT_BF16),
+            ("a2 Q4_K", "q4k", 4096, 4096, 1, 1, dict(), q4.Q4_DT_F32),
+            ("a3 MXFP4", "mxfp4", 4096, 11008, 1, 2, dict(outliers=True), q4.Q4_DT_BF16),
+            ("a4 Q4_0", "q40", 4096, 11008, 1, 2, dict(outliers=True), q4.Q4_DT_F32),
+            ("a5 GPTQ", "gptq", 4096, 11008, 1, 2, dict(outliers=True), q4.Q4_DT_F32),
+            ("a5 AWQ", "awq", 4096, 11008, 1, 2, dict(outliers=True), q4.Q4_DT_F32)):
+        layer = synth.make_layer(fmt, N, K, config=config, matrix=0, **kw)
+        d = _dev_layer(torch, layer)
+        xb, _ = synth.draw_x(M, K, config=config, matrix=5, dtype="bf16" if xdt == q4.Q4_DT_BF16 else "f32")
+        xa = np.ascontiguousarray(xb)
+        x = (torch.from_numpy(xa.view(np.int16)).cuda().view(torch.bfloat16) if xdt == q4.Q4_DT_BF16
+             else torch.from_numpy(xa.astype(np.float32)).cuda())
+        y = torch.empty((M, N), dtype=torch.float32, device="cuda")
+        aux = q4.make_aux(scale2=layer["scale2"], zeros=d["zeros"], g_idx=d["g_idx"], group=layer["group"],
+                          x_dtype=xdt, fmt=fmt)
+        q4.q4_gemv(fmt, d["w"], d["scales"], aux, x, y, M, N, K, stream=stream)
+        torch.cuda.synchronize()
+        moved = q4.q4_packed_bytes(fmt, N, K) + x.numel() * x.element_size() + y.numel() * 4
+        print(f"{tag}: {N}x{K} path {q4.q4_last_gemv_path()} algorithmic bytes {moved}")
+    N, K = 14336, 4096
+    layer = synth.make_layer("nvfp4", N, K, config=5, matrix=0, row_scale=True)
+    d = _dev_layer(torch, layer)
+    out = torch.empty((N, K), dtype=torch.float32, device="cuda")
+    q4.q4_dequant("nvfp4", d["w"], d["scales"], q4.make_aux(scale2=layer["scale2"], fmt="nvfp4"), out, N, K,
+                  stream=stream)
+    torch.cuda.synchronize()
+    print(f"a6 dequant NVFP4 -> f32: {N}x{K} algorithmic bytes {q4.q4_packed_bytes('nvfp4', N, K) + N * K * 4}")
+    del out
+    N, K = 4096, 11008
+    layer = synth.make_layer("gptq", N, K, config=2, matrix=0, outliers=True)
+    d = _dev_layer(torch, layer)
+    w = torch.empty((K, N // 8), dtype=torch.int32, device="cuda")
+    sc = torch.empty((K // 128, N), dtype=torch.int16, device="cuda")
+    z = torch.empty((K // 128, N // 8), dtype=torch.int32, device="cuda")
+    q4.q4_repack("gptq", d["w"], d["scales"], q4.make_aux(zeros=d["zeros"], group=128, fmt="gptq"), "awq", w, sc, z,
+                 None, N, K, stream=stream)
+    print(f"a7 repack GPTQ -> AWQ: {N}x{K} algorithmic bytes {2 * q4.q4_packed_bytes('gptq', N, K)}")
+    print("ncu rows case done, last_error", q4.q4_last_error())
+
+
 def main():
     args = parse()
+    if args.ncu_rows_case:
+        ncu_rows_case()
+        return
     if args.ncu_case:
         ncu_case()
         return
