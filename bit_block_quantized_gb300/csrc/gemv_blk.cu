@@ -519,8 +519,11 @@ __global__ void __launch_bounds__(BW * 32, 2) gemv_mma_gptq(const __grid_constan
         const int64_t ra = n0 + g < a.N ? n0 + g : a.N - 8 + g, rb = n0 + g + 8 < a.N ? n0 + g + 8 : a.N - 8 + g;
         load_gg(a, ra, rb, gr0 + u, t, q);
     };
-    GG cur, nxt;
+    // two groups in flight ahead of the one being computed (register ring,
+    // rotated by copies so no register array is indexed dynamically)
+    GG cur, n1, n2;
     if (items > 0) load_item(0, cur);
+    if (items > 1) load_item(1, n1);
 
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -536,7 +539,7 @@ __global__ void __launch_bounds__(BW * 32, 2) gemv_mma_gptq(const __grid_constan
 
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
     for (int i = 0; i < items; i++) {
-        if (i + 1 < items) load_item(i + 1, nxt);
+        if (i + 2 < items) load_item(i + 2, n2);
         const int u = i % a.ngw;
         if (u < ngr) {
             const uint2 *xhu = xh + (size_t)u * 8 * MT * 4 + mcol * 4 + t;
@@ -565,7 +568,8 @@ __global__ void __launch_bounds__(BW * 32, 2) gemv_mma_gptq(const __grid_constan
             acc[2] = fmaf(sg8, fmaf(-zg8, Sa, dj[2]), acc[2]);
             acc[3] = fmaf(sg8, fmaf(-zg8, Sb, dj[3]), acc[3]);
         }
-        if (i + 1 < items) cur = nxt;
+        cur = n1;
+        n1 = n2;
         if (u == a.ngw - 1) {
             const int64_t n0 = (int64_t)(blockIdx.x + (i / a.ngw) * gridDim.x) * 16;
             float *rw = red + warp * 16 * MT;
