@@ -395,17 +395,30 @@ __global__ void __launch_bounds__(THREADS, 2)
     } else if (warp == W_MMA) {
         // ------------------------------------------------------------ MMA
         if (lane == 0) {
+            // One thread issues every MMA, and its loop is the kernel's critical
+            // path (a tcgen05.mma of 128 x N x 16 costs ~94 issue cycles for
+            // any N <= 128 even back to back): the loop is unrolled over the
+            // ring so every descriptor is a constant offset from one base.
             constexpr uint32_t idesc = idesc_bf16<MB>();
-            for (int i = 0; i < nst; i++) {
-                const int s = i % C::NS;
-                if (!wait_or_abort(&a_full[s], (i / C::NS) & 1, abort_flag)) break;
-                tc_fence_after();
-                const uint32_t a_col = tbase + C::DCOLS + s * A_COLS;
-                const uint32_t b_addr = smem_u32(xring + s * C::B_BYTES);
+            const uint64_t b0 = sw128_desc(smem_u32(xring));
+            const uint32_t a0 = tbase + C::DCOLS;
+            bool stop = false;
+            for (int base = 0; base < nst && !stop; base += C::NS) {
+                const uint32_t par = (uint32_t)(base / C::NS) & 1;
 #pragma unroll
-                for (int k = 0; k < BK / 16; k++)
-                    mma_ts(tbase, a_col + k * 8, sw128_desc(b_addr + k * 32), idesc, (i | k) != 0);
-                mma_commit(&a_empty[s]);
+                for (int s = 0; s < C::NS; s++) {
+                    if (base + s >= nst) break;
+                    if (!wait_or_abort(&a_full[s], par, abort_flag)) {
+                        stop = true;
+                        break;
+                    }
+                    tc_fence_after();
+#pragma unroll
+                    for (int k = 0; k < BK / 16; k++)
+                        mma_ts(tbase, a0 + s * A_COLS + k * 8, b0 + (uint64_t)((s * C::B_BYTES + k * 32) >> 4), idesc,
+                               (base + s + k) != 0);
+                    mma_commit(&a_empty[s]);
+                }
             }
             mma_commit(&done_bar);
         }
