@@ -63,6 +63,7 @@ constexpr int SC_BYTES = 16 * KS / 16;         // 16 rows x 128 scale bytes
 constexpr int STAGE_BYTES = PAY_BYTES + SC_BYTES;
 constexpr int MAX_STAGES = 8;
 constexpr int MIN_STAGES = 3;
+constexpr int PREFETCH_STAGES = 3;             // stages a CTA loads before its decode warps have staged x
 constexpr int MAXM = 8;                        // matrices per launch
 constexpr int MAXP = 4;                        // groups per chain
 constexpr size_t SMEM_CAP = Q4_TMA_SMEM_KB * 1024;   // 112 KB: two CTAs per SM
@@ -357,6 +358,7 @@ __global__ void __launch_bounds__(THREADS, Q4_TMA_CTAS_PER_SM)
     float *red = reinterpret_cast<float *>(abort_s + 4);               // [2][CW][16][MT]
     uint2 *xs_all = reinterpret_cast<uint2 *>(red + 2 * CW * 16 * MT);  // [CW][max_nst*2][8][MT][4]
     volatile int *abort_flag = abort_s;
+    volatile int *x_staged = abort_s + 1;   // decode warps that have staged the first group's x
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
@@ -365,6 +367,7 @@ __global__ void __launch_bounds__(THREADS, Q4_TMA_CTAS_PER_SM)
             mbar_init(&empty[s], CW);    // one arrive per consumer warp
         }
         *abort_s = 0;
+        *x_staged = 0;
         fence_mbar_init();
     }
     __syncthreads();
@@ -396,6 +399,13 @@ __global__ void __launch_bounds__(THREADS, Q4_TMA_CTAS_PER_SM)
                         tma_2d(dst + PAY_BYTES, &maps.sc[member], st * (KS / 16), row0, bar, pol);
                         issued++;
                         if (++slot == S) { slot = 0; phase ^= 1; }
+                        if (issued == PREFETCH_STAGES) {
+                            // Hold further copies until the decode warps have read x (or ~0.5 s,
+                            // or an abort): a deeper prefetch queues their x loads behind this
+                            // launch's weight stream while they cannot start without x.
+                            const long long t0 = clock64();
+                            while (*x_staged < CW && !*abort_flag && clock64() - t0 < (1LL << 30)) __nanosleep(64);
+                        }
                     }
                 }
             }
@@ -448,6 +458,7 @@ __global__ void __launch_bounds__(THREADS, Q4_TMA_CTAS_PER_SM)
         const int K = a.K[p], nst = a.nst[p], ntiles = a.ntiles[p], m_end = a.m0[p + 1];
         float inv[MT];
         const bool exact = stage_x<MT>(x, K, a.M, nst, warp, lane, xs, inv);
+        if (p == 0 && lane == 0) atomicAdd((int *)x_staged, 1);
         const uint2 *xbase = xs + mlane * 4 + tt;
         int mb = a.m0[p];
         for (int tile = (int)blockIdx.x; tile < ntiles; tile += (int)gridDim.x) {
