@@ -82,6 +82,7 @@ struct TcArgs {
     int splits;         // CTAs per cluster, each owning K / splits
     int k_per_cta;
     float mult;         // epilogue multiplier: scale2 for NVFP4, 1 for Q4_K
+    int ystore;         // 1: without a K split, y leaves through shared memory by one TMA store (maps.y)
 };
 
 // ------------------------------------------------------------ PTX helpers
@@ -126,6 +127,15 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
            (2ull << 61);
 }
 
+// One tiled tensor store from shared memory (bulk group of this thread), and
+// the wait until it has completed.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, int c0, int c1, const void *src) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(map), "r"(c0),
+                 "r"(c1), "r"(smem_u32(src))
+                 : "memory");
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
 __device__ __forceinline__ void tma_2d(void *dst, const CUtensorMap *map, int c0, int c1, uint64_t *bar) {
     asm volatile(
         "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
@@ -301,6 +311,7 @@ __device__ __forceinline__ void q4k_half(uint4 h, uint4 q0, uint4 q1, int c, int
 
 // ------------------------------------------------------------ the kernel
 struct Maps {
+    CUtensorMap y;   // f32 [rows][N] of this batch chunk, box 128 n x MB rows (used when ystore)
     CUtensorMap x;   // bf16 [rows][K], box 64 k x MB rows, 128-byte swizzle
     CUtensorMap w;   // NVFP4 payload u8 [N][K/2] (box 128 x 128, 128-byte swizzle) or Q4_K u8 [N][K/256*144] (box 144 x 128)
     CUtensorMap s;   // NVFP4 scales u8 [N][K/16], box 16 x 128 (unused for Q4_K)
@@ -454,7 +465,9 @@ __global__ void __launch_bounds__(THREADS, 2)
     }
 
     // ---------------------------------------------------------- epilogue
-    float *red = reinterpret_cast<float *>(xring);   // [MB][128] partial tile; the X ring is idle now
+    // [MB][128] f32 tile (the partial tile of a K split, or y on its way to the
+    // TMA store); the X ring is idle once the MMAs are done
+    float *red = reinterpret_cast<float *>(xring);
     if (warp < 4) {
         const int r = threadIdx.x;
         const int64_t n = (int64_t)n0 + r;
@@ -467,7 +480,10 @@ __global__ void __launch_bounds__(THREADS, 2)
             for (int c0 = 0; c0 < MB; c0 += 16) {
                 float v[16];
                 tmem_ld16(lane_d + c0, v);
-                if (a.splits == 1) {
+                if (a.splits == 1 && a.ystore) {
+#pragma unroll
+                    for (int j = 0; j < 16; j++) red[(c0 + j) * ROWS + r] = v[j] * a.mult;
+                } else if (a.splits == 1) {
                     if (n < a.N) {
 #pragma unroll
                         for (int j = 0; j < 16; j++)
@@ -480,6 +496,13 @@ __global__ void __launch_bounds__(THREADS, 2)
             }
         }
         tc_fence_before();
+        if (a.splits == 1 && a.ystore) {
+            // the tile's generic-proxy stores, then one TMA store of all of it
+            // (rows past M and columns past N are clipped by the tensor map)
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            asm volatile("bar.sync 1, 128;" ::: "memory");   // the four epilogue warps
+            if (r == 0 && ok) tma_store_2d(&maps.y, n0, 0, red);
+        }
     }
     if (a.splits > 1) {
         cg::cluster_group cluster = cg::this_cluster();
@@ -644,6 +667,13 @@ cudaError_t launch_gemm_tc(const Tensor &t, const void *x, q4_dtype x_dtype, flo
         args.splits = S;
         args.k_per_cta = (int)(t.K / S);
         args.mult = t.fmt == Q4_NVFP4 ? t.scale2 : 1.0f;
+        // without a K split the output tile leaves by one TMA store: rows of y
+        // must be a multiple of 16 bytes apart
+        args.ystore = (S == 1 && t.N % 4 == 0 &&
+                       encode_2d(&maps.y, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, y + m0 * t.N, t.N, rows, t.N * 4, ROWS, MB,
+                                 CU_TENSOR_MAP_SWIZZLE_NONE))
+                          ? 1
+                          : 0;
         const cudaError_t e = t.fmt == Q4_NVFP4 ? launch_mb<Q4_NVFP4>(MB, args, maps, tiles, s)
                                                 : launch_mb<Q4_Q4K>(MB, args, maps, tiles, s);
         if (e != cudaSuccess) return e;
