@@ -33,39 +33,65 @@ template <> __device__ __forceinline__ __nv_bfloat16 to_out<__nv_bfloat16>(float
     return __float2bfloat16_rn(v);
 }
 
-// NVFP4 / split-half NVFP4 / MXFP4: one thread per 16-value group (8 payload
-// bytes).  NVFP4 order (e2m1 * e4m3fn) * scale2 ([MUS7] 7.2): the first
-// product is exact, the second is the single rounding.
+// NVFP4 / split-half NVFP4 / MXFP4: one thread per 16 output bytes (4 f32 or
+// 8 bf16 values, a quarter or half of a 16-value group), so each warp store
+// writes 512 contiguous bytes; the lanes of one group read its 8 payload
+// bytes together.  NVFP4 order (e2m1 * e4m3fn) * scale2 ([MUS7] 7.2): the
+// first product is exact, the second is the single rounding.
+template <typename OT> __device__ __forceinline__ void store_chunk(OT *out, const float *v);
+template <> __device__ __forceinline__ void store_chunk<float>(float *out, const float *v) {
+    *reinterpret_cast<float4 *>(out) = make_float4(v[0], v[1], v[2], v[3]);
+}
+template <> __device__ __forceinline__ void store_chunk<__nv_bfloat16>(__nv_bfloat16 *out, const float *v) {
+    uint32_t p[4];
+#pragma unroll
+    for (int i = 0; i < 4; i++) {
+        __nv_bfloat162 b = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+        p[i] = *reinterpret_cast<uint32_t *>(&b);
+    }
+    *reinterpret_cast<uint4 *>(out) = make_uint4(p[0], p[1], p[2], p[3]);
+}
+
 template <int FMT, typename OT>
 __global__ void dequant_fp4(const uint8_t *__restrict__ w, const uint8_t *__restrict__ scales,
-                            float scale2, OT *__restrict__ out, int64_t ngroups) {
-    for (int64_t g = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; g < ngroups;
-         g += (int64_t)gridDim.x * blockDim.x) {
-        uint2 p = *reinterpret_cast<const uint2 *>(w + 8 * g);
-        float s = (FMT == Q4_MXFP4) ? e8m0_f32(scales[g >> 1]) : e4m3_f32(scales[g]);
-        uint32_t words[2] = {p.x, p.y};
-        float v[16];
+                            float scale2, OT *__restrict__ out, int64_t nchunks) {
+    constexpr int VPL = 16 / (int)sizeof(OT);   // values per thread
+    constexpr int CPG = 16 / VPL;               // threads per 16-value group
+    for (int64_t u = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; u < nchunks;
+         u += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t g = u / CPG;
+        const int part = (int)(u % CPG);
+        const uint2 p = *reinterpret_cast<const uint2 *>(w + 8 * g);
+        const uint64_t bits = (uint64_t)p.x | ((uint64_t)p.y << 32);
+        const float sc = (FMT == Q4_MXFP4) ? e8m0_f32(scales[g >> 1]) : e4m3_f32(scales[g]);
+        float v[VPL];
+        if (FMT == Q4_NVFP4_SPLITHALF) {
+            // value j: low nibble of byte j (j < 8), high nibble of byte j - 8 ([W4K] section 5)
 #pragma unroll
-        for (int b = 0; b < 8; b++) {
-            float2 c = e2m1x2_f32(words[b >> 2] >> (8 * (b & 3)));
-            if (FMT == Q4_NVFP4_SPLITHALF) {
-                v[b] = c.x;          // low nibble of byte b = lane b
-                v[b + 8] = c.y;      // high nibble = lane b + 8 ([W4K] section 5)
-            } else {
-                v[2 * b] = c.x;      // low nibble = even k
+            for (int i = 0; i < VPL; i++) {
+                const int j = part * VPL + i;
+                const uint32_t nib = (uint32_t)(bits >> (j < 8 ? 8 * j : 8 * (j - 8) + 4)) & 15u;
+                v[i] = e2m1x2_f32(nib).x;
+            }
+        } else {
+            // value j: nibble j (low nibble = even k); byte pairs decode together
+#pragma unroll
+            for (int b = 0; b < VPL / 2; b++) {
+                const float2 c = e2m1x2_f32((uint32_t)(bits >> (8 * (part * VPL / 2 + b))) & 0xffu);
+                v[2 * b] = c.x;
                 v[2 * b + 1] = c.y;
             }
         }
 #pragma unroll
-        for (int i = 0; i < 16; i++) {
+        for (int i = 0; i < VPL; i++) {
             if (FMT == Q4_MXFP4) {
-                v[i] = __fmul_rn(v[i], s);
+                v[i] = __fmul_rn(v[i], sc);
             } else {
-                float prod = __fmul_rn(v[i], s);
+                const float prod = __fmul_rn(v[i], sc);
                 v[i] = __fmul_rn(prod, scale2);
             }
         }
-        store16<OT>(out + 16 * g, v);
+        store_chunk<OT>(out + VPL * u, v);
     }
 }
 
@@ -172,17 +198,17 @@ template <typename OT> cudaError_t dispatch(const Tensor &t, OT *out, cudaStream
     const int T = 256;
     switch (t.fmt) {
     case Q4_NVFP4: {
-        int64_t n = t.N * t.K / 16;
+        int64_t n = t.N * t.K * (int64_t)sizeof(OT) / 16;   // 16-byte output chunks
         dequant_fp4<Q4_NVFP4, OT><<<grid_for(n, T), T, 0, s>>>(t.w, t.scales, t.scale2, out, n);
         break;
     }
     case Q4_NVFP4_SPLITHALF: {
-        int64_t n = t.N * t.K / 16;
+        int64_t n = t.N * t.K * (int64_t)sizeof(OT) / 16;
         dequant_fp4<Q4_NVFP4_SPLITHALF, OT><<<grid_for(n, T), T, 0, s>>>(t.w, t.scales, t.scale2, out, n);
         break;
     }
     case Q4_MXFP4: {
-        int64_t n = t.N * t.K / 16;
+        int64_t n = t.N * t.K * (int64_t)sizeof(OT) / 16;
         dequant_fp4<Q4_MXFP4, OT><<<grid_for(n, T), T, 0, s>>>(t.w, t.scales, 1.0f, out, n);
         break;
     }

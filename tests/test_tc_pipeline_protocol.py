@@ -29,7 +29,7 @@ def rings(MB):
     """(stages, weight slots) of the kernel for batch tile MB."""
     dcols = max(32, MB)
     ns = (TMEM_COLS - dcols) // A_COLS
-    nw = 4 if MB <= 32 else 3 if MB == 64 else 2
+    nw = 3 if MB == 64 else 2
     return ns, nw
 
 
