@@ -330,6 +330,8 @@ def run_ours(args, rank, world):
         line["other_rows"] = other_rows(torch, q4, synth, peak)
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args.cpu_seconds, host)
+        if not args.no_rows:
+            line["cpu_baseline"]["rows"] = cpu_baseline_rows()
     return line
 
 
@@ -434,6 +436,53 @@ def cpu_baseline(seconds, host=None, sample_rows=None):
     return {"value": round(bytes_done / t_total / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
             "sample": f"{rows_done} rows ({frac:.3%}) of each of the 3 set matrices, batch 1, "
                       f"{t_total:.1f} s", "cpu": _cpu_name()}
+
+
+# The other rows' shapes and synthetic recipes (see other_rows), for the oracle beside each.
+ORACLE_ROWS = [("a1 NVFP4 GEMV", "nvfp4", 14336, 4096, 4, 5, dict(row_scale=True), "bf16"),
+               ("a2 Q4_K GEMV", "q4k", 4096, 4096, 1, 1, dict(), "f32"),
+               ("a3 MXFP4 GEMV", "mxfp4", 4096, 11008, 1, 2, dict(outliers=True), "bf16"),
+               ("a4 Q4_0 GEMV", "q40", 4096, 11008, 1, 2, dict(outliers=True), "f32"),
+               ("a5 GPTQ GEMV", "gptq", 4096, 11008, 1, 2, dict(outliers=True), "f32"),
+               ("a5 AWQ GEMV", "awq", 4096, 11008, 1, 2, dict(outliers=True), "f32")]
+
+
+def cpu_baseline_rows(rows_per_matrix=1024):
+    """The CPU oracle as it stands (single thread, f64 accumulation) beside
+    each other row: a GEMV over a bounded sample of rows of the row's K,
+    format and synthetic recipe (the oracle's cost per row does not depend
+    on N), and the NVFP4 dequant of the same rows; GB/s over the sampled
+    rows' packed bytes (plus the f32 output for dequant)."""
+    import oracle
+    import synth
+    oracle.build()
+    out = []
+    for tag, fmt, N, K, M, config, kw, xd in ORACLE_ROWS:
+        layer = synth.make_layer(fmt, rows_per_matrix, K, config=config, matrix=0, **kw)
+        T = oracle.Tensor(layer["fmt"], rows_per_matrix, K, layer["w"], layer["scales"], layer["zeros"],
+                          layer["g_idx"], layer["group"], layer["scale2"])
+        xb, xf = synth.draw_x(M, K, config=config, matrix=5, dtype=xd)
+        rows = np.arange(rows_per_matrix)
+        t0 = time.perf_counter()
+        if tag.startswith("a1"):
+            oracle.dequant(T, rows=rows)
+            dq = time.perf_counter() - t0
+            t0 = time.perf_counter()
+        oracle.gemv(T, xf, rows=rows)
+        dt = time.perf_counter() - t0
+        row_bytes = q4_packed_row_bytes(fmt, K)
+        out.append({"row": tag, "shape": f"{N}x{K}", "M": M, "sample": f"{rows.size} rows of K = {K}",
+                    "GBps": round(rows.size * row_bytes / dt / 1e9, 4), "seconds": round(dt, 3)})
+        if tag.startswith("a1"):
+            out.append({"row": "a6 dequant NVFP4 -> f32", "shape": f"{N}x{K}", "sample": f"{rows.size} rows of K = {K}",
+                        "GBps": round(rows.size * (row_bytes + 4 * K) / dq / 1e9, 4), "seconds": round(dq, 3)})
+    return out
+
+
+def q4_packed_row_bytes(fmt, K):
+    """Packed bytes of one weight row, payload + scales (+ zeros), group 128."""
+    return {"nvfp4": K // 2 + K // 16, "mxfp4": K // 2 + K // 32, "q4k": K // 256 * 144, "q40": K // 32 * 18,
+            "gptq": K // 2 + K // 128 * 2 + K // 128 // 2, "awq": K // 2 + K // 128 * 2 + K // 128 // 2}[fmt]
 
 
 def _cpu_name():
