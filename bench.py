@@ -687,6 +687,19 @@ def other_rows(torch, q4, synth, peak_hbm):
     del cps, out
     torch.cuda.empty_cache()
 
+    # a6: dequant Q4_K 14336x4096 to f32 (same output, 144-byte super-blocks in)
+    layer = synth.make_layer("q4k", N, K, config=4, matrix=0)
+    packed = q4.q4_packed_bytes("q4k", N, K)
+    cps = copies_of(_dev_layer(torch, layer), packed)[:6]
+    out = torch.empty((N, K), dtype=torch.float32, device="cuda")
+    us = _time_launches(torch, stream, lambda i: q4.q4_dequant("q4k", cps[i % len(cps)]["w"], None, None, out, N, K,
+                                                               stream=stream), reps=60)
+    moved = packed + N * K * 4
+    rows.append({"row": "a6 dequant Q4_K -> f32", "shape": f"{N}x{K}", "us_per_launch": round(us, 2),
+                 "GBps": round(moved / us / 1e3, 1), "frac_hbm": round(moved / us / 1e3 / peak_hbm, 4)})
+    del cps, out
+    torch.cuda.empty_cache()
+
     # a7: repack GPTQ -> AWQ 4096x11008 (read once, write once)
     N, K = 4096, 11008
     layer = synth.make_layer("gptq", N, K, config=2, matrix=0, outliers=True)

@@ -6,27 +6,6 @@
 namespace q4 {
 namespace {
 
-template <typename OT> __device__ __forceinline__ void store16(OT *out, const float *v);
-
-template <> __device__ __forceinline__ void store16<float>(float *out, const float *v) {
-    float4 *o = reinterpret_cast<float4 *>(out);
-#pragma unroll
-    for (int i = 0; i < 4; i++) o[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
-}
-
-template <>
-__device__ __forceinline__ void store16<__nv_bfloat16>(__nv_bfloat16 *out, const float *v) {
-    uint4 *o = reinterpret_cast<uint4 *>(out);
-    uint32_t p[8];
-#pragma unroll
-    for (int i = 0; i < 8; i++) {
-        __nv_bfloat162 b = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
-        p[i] = *reinterpret_cast<uint32_t *>(&b);
-    }
-    o[0] = make_uint4(p[0], p[1], p[2], p[3]);
-    o[1] = make_uint4(p[4], p[5], p[6], p[7]);
-}
-
 template <typename OT> __device__ __forceinline__ OT to_out(float v);
 template <> __device__ __forceinline__ float to_out<float>(float v) { return v; }
 template <> __device__ __forceinline__ __nv_bfloat16 to_out<__nv_bfloat16>(float v) {
@@ -95,10 +74,10 @@ __global__ void dequant_fp4(const uint8_t *__restrict__ w, const uint8_t *__rest
     }
 }
 
-// Q4_K: one thread per (super-block, 64-chunk c, half h): 16 code bytes -> 32
-// weights at k = 64c+16h+i (low nibbles, sub-block 2c) and 64c+32+16h+i (high
-// nibbles, sub-block 2c+1) ([FBTC] sections 5-6).  w = fma(q, d*s, -dmin*m)
-// equals the pinned (d*s)*q - dmin*m: d*s*q is exact, one rounding.
+// Q4_K: code byte b of 32-byte group c holds k = 64c + b (low nibble,
+// sub-block 2c) and 64c + 32 + b (high nibble, sub-block 2c+1) ([FBTC]
+// sections 5-6).  w = fma(q, d*s, -dmin*m) equals the pinned (d*s)*q - dmin*m:
+// d*s*q is exact, one rounding.
 __device__ __forceinline__ uint32_t byte_of(uint4 hdr, int i) {
     uint32_t word = i < 4 ? hdr.y : (i < 8 ? hdr.z : hdr.w);
     return (word >> (8 * (i & 3))) & 0xffu;
@@ -118,55 +97,58 @@ __device__ __forceinline__ void q4k_scale_min(uint4 hdr, int j, float &sc, float
 }
 
 template <typename OT>
-__global__ void dequant_q4k(const uint8_t *__restrict__ w, OT *__restrict__ out, int64_t nunits) {
-    for (int64_t u = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; u < nunits;
+__global__ void dequant_q4k(const uint8_t *__restrict__ w, OT *__restrict__ out, int64_t nchunks) {
+    // one thread per 16 output bytes: VPL consecutive k of one sub-block
+    constexpr int VPL = 16 / (int)sizeof(OT);
+    constexpr int CPB = 256 / VPL;   // chunks per super-block
+    for (int64_t u = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; u < nchunks;
          u += (int64_t)gridDim.x * blockDim.x) {
-        int64_t blk = u >> 3;
-        int c = (int)((u >> 1) & 3), h = (int)(u & 1);
+        const int64_t blk = u / CPB;
+        const int k0 = (int)(u % CPB) * VPL;            // within the super-block
+        const int c = k0 >> 6, hi = (k0 >> 5) & 1, b0 = k0 & 31;
         const uint8_t *b = w + blk * 144;
-        uint4 hdr = *reinterpret_cast<const uint4 *>(b);
-        uint4 qs = *reinterpret_cast<const uint4 *>(b + 16 + 32 * c + 16 * h);
-        float d = half_bits_f32(hdr.x), dmin = half_bits_f32(hdr.x >> 16);
-        float sc_lo, m_lo, sc_hi, m_hi;
-        q4k_scale_min(hdr, 2 * c, sc_lo, m_lo);
-        q4k_scale_min(hdr, 2 * c + 1, sc_hi, m_hi);
-        float step_lo = __fmul_rn(d, sc_lo), off_lo = __fmul_rn(dmin, m_lo);
-        float step_hi = __fmul_rn(d, sc_hi), off_hi = __fmul_rn(dmin, m_hi);
-        uint32_t words[4] = {qs.x, qs.y, qs.z, qs.w};
-        float lo[16], hi[16];
+        const uint4 hdr = *reinterpret_cast<const uint4 *>(b);
+        float sc, mn;
+        q4k_scale_min(hdr, 2 * c + hi, sc, mn);
+        const float step = __fmul_rn(half_bits_f32(hdr.x), sc), off = __fmul_rn(half_bits_f32(hdr.x >> 16), mn);
+        uint32_t words[VPL / 4];
 #pragma unroll
-        for (int i = 0; i < 16; i++) {
-            uint32_t byte = (words[i >> 2] >> (8 * (i & 3))) & 0xffu;
-            lo[i] = __fmaf_rn((float)(byte & 15u), step_lo, -off_lo);
-            hi[i] = __fmaf_rn((float)(byte >> 4), step_hi, -off_hi);
+        for (int i = 0; i < VPL / 4; i++) words[i] = *reinterpret_cast<const uint32_t *>(b + 16 + 32 * c + b0 + 4 * i);
+        float v[VPL];
+#pragma unroll
+        for (int i = 0; i < VPL; i++) {
+            const uint32_t byte = (words[i >> 2] >> (8 * (i & 3))) & 0xffu;
+            v[i] = __fmaf_rn((float)(hi ? byte >> 4 : byte & 15u), step, -off);
         }
-        OT *o = out + blk * 256 + 64 * c + 16 * h;
-        store16<OT>(o, lo);
-        store16<OT>(o + 32, hi);
+        store_chunk<OT>(out + blk * 256 + k0, v);
     }
 }
 
-// Q4_0: one thread per 18-byte block: fp16 d, byte j = element j (low) and
-// j+16 (high); w = d*(q-8), exact ([BPA] "Real layouts compared").
+// Q4_0: one thread per 16 output bytes of an 18-byte block: fp16 d, byte j =
+// element j (low) and j+16 (high); w = d*(q-8), exact ([BPA] "Real layouts
+// compared").  The block is 2-byte aligned, so the codes are read as u16.
 template <typename OT>
-__global__ void dequant_q40(const uint8_t *__restrict__ w, OT *__restrict__ out, int64_t nblocks) {
-    for (int64_t bi = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; bi < nblocks;
-         bi += (int64_t)gridDim.x * blockDim.x) {
+__global__ void dequant_q40(const uint8_t *__restrict__ w, OT *__restrict__ out, int64_t nchunks) {
+    constexpr int VPL = 16 / (int)sizeof(OT);
+    constexpr int CPB = 32 / VPL;
+    for (int64_t u = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; u < nchunks;
+         u += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t bi = u / CPB;
+        const int k0 = (int)(u % CPB) * VPL;
         const uint16_t *b = reinterpret_cast<const uint16_t *>(w + bi * 18);
-        float d = half_bits_f32(b[0]);
-        float lo[16], hi[16];
+        const float d = half_bits_f32(b[0]);
+        const int hi = k0 >> 4, j0 = k0 & 15;
+        float v[VPL];
 #pragma unroll
-        for (int j = 0; j < 8; j++) {
-            uint32_t two = b[1 + j];
+        for (int i = 0; i < VPL; i += 2) {
+            const uint32_t two = b[1 + (j0 + i) / 2];
 #pragma unroll
             for (int e = 0; e < 2; e++) {
-                uint32_t byte = (two >> (8 * e)) & 0xffu;
-                lo[2 * j + e] = __fmul_rn(d, (float)((int)(byte & 15u) - 8));
-                hi[2 * j + e] = __fmul_rn(d, (float)((int)(byte >> 4) - 8));
+                const uint32_t byte = (two >> (8 * e)) & 0xffu;
+                v[i + e] = __fmul_rn(d, (float)((int)(hi ? byte >> 4 : byte & 15u) - 8));
             }
         }
-        store16<OT>(out + bi * 32, lo);
-        store16<OT>(out + bi * 32 + 16, hi);
+        store_chunk<OT>(out + bi * 32 + k0, v);
     }
 }
 
@@ -213,12 +195,12 @@ template <typename OT> cudaError_t dispatch(const Tensor &t, OT *out, cudaStream
         break;
     }
     case Q4_Q4K: {
-        int64_t n = t.N * (t.K / 256) * 8;
+        int64_t n = t.N * t.K * (int64_t)sizeof(OT) / 16;
         dequant_q4k<OT><<<grid_for(n, T), T, 0, s>>>(t.w, out, n);
         break;
     }
     case Q4_Q40: {
-        int64_t n = t.N * (t.K / 32);
+        int64_t n = t.N * t.K * (int64_t)sizeof(OT) / 16;
         dequant_q40<OT><<<grid_for(n, T), T, 0, s>>>(t.w, out, n);
         break;
     }
