@@ -630,7 +630,9 @@ __global__ void __launch_bounds__(KM_WARPS * 32) gemv_kmajor(Tensor t, const XT 
                 }
             }
         } else {
-#pragma unroll 4
+            // one 4-byte word per lane and k row: unrolled deep so that many rows'
+            // loads are in flight per warp (4 -> 32: 51.5 -> 41.8 us on 4096 x 11008)
+#pragma unroll 32
             for (int kk = 0; kk < kcount; kk++) {
                 const uint32_t word = ldg_stream4(qw + (kg0 + kk) * (N >> 3) + cword);
                 const float *xr = xs + (kg0 - k0) + kk;
