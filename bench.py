@@ -276,10 +276,7 @@ def run_ours(args, rank, world):
             torch.cuda.synchronize()
             kern_ms.append(a.elapsed_time(b) / (reps * copies))
 
-    if world > 1:
-        t = torch.tensor([ms], dtype=torch.float64, device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, world, "cuda")
 
     # end to end through the public API: pinned host x in, y out, every step
     e2e = run_e2e(args, torch, q4, dev, auxes, host, stream)
@@ -287,7 +284,7 @@ def run_ours(args, rank, world):
     if rank != 0:
         return None
     peak, peak_kind = measured_hbm_peak()
-    value = world * set_bytes * args.steps / (ms * 1e-3) / 1e9
+    value = whole_job_gbps(world, set_bytes, args.steps, ms)
     gate_up_bytes = 2 * q4.q4_packed_bytes("nvfp4", 14336, 4096)
     down_bytes = q4.q4_packed_bytes("nvfp4", 4096, 14336)
     achieved = gate_up_bytes / (kern_ms[0] * 1e-3) / 1e9
@@ -333,6 +330,22 @@ def run_ours(args, rank, world):
         if not args.no_rows:
             line["cpu_baseline"]["rows"] = cpu_baseline_rows()
     return line
+
+
+def max_over_ranks(value, world, device):
+    """The largest of every rank's value: the job's time is its slowest rank's."""
+    if world <= 1:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_gbps(world, bytes_per_step, steps, ms):
+    """Whole-job throughput: every rank streams the set `steps` times within
+    the slowest rank's `ms` (replicas: per-rank work fixed as N grows)."""
+    return world * bytes_per_step * steps / (ms * 1e-3) / 1e9
 
 
 def run_e2e(args, torch, q4, dev, auxes, host, stream):
