@@ -33,6 +33,43 @@ def test_header_declares_the_boundary():
         assert required in names
 
 
+_LAYOUT_PROBE = r"""
+#include <stdio.h>
+#include <stddef.h>
+#include "q4.h"
+#define F(T, m) printf(#T " " #m " %zu\n", offsetof(T, m))
+int main(void) {
+    printf("q4_aux size %zu\n", sizeof(q4_aux));
+    F(q4_aux, scale2); F(q4_aux, zeros); F(q4_aux, g_idx); F(q4_aux, group); F(q4_aux, x_dtype);
+    F(q4_aux, out_dtype);
+    printf("q4_gemv_desc size %zu\n", sizeof(q4_gemv_desc));
+    F(q4_gemv_desc, fmt); F(q4_gemv_desc, W_packed); F(q4_gemv_desc, scales); F(q4_gemv_desc, aux);
+    F(q4_gemv_desc, x); F(q4_gemv_desc, y); F(q4_gemv_desc, N); F(q4_gemv_desc, K);
+    return 0;
+}
+"""
+
+
+def test_binding_structs_match_the_header(tmp_path):
+    """The ctypes mirrors of q4_aux and q4_gemv_desc have the C layout (a C
+    probe built against include/q4.h prints sizes and offsets)."""
+    import shutil
+    import subprocess
+    if shutil.which("gcc") is None:
+        pytest.skip("no C compiler")
+    src, exe = tmp_path / "layout.c", tmp_path / "layout"
+    src.write_text(_LAYOUT_PROBE)
+    subprocess.check_call(["gcc", "-std=c99", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)])
+    c = {}
+    for line in subprocess.check_output([str(exe)], text=True).splitlines():
+        t, m, v = line.split()
+        c[(t, m)] = int(v)
+    for T, name in ((q4.Aux, "q4_aux"), (q4.GemvDesc, "q4_gemv_desc")):
+        assert ctypes.sizeof(T) == c[(name, "size")], name
+        for field, _ in T._fields_:
+            assert getattr(T, field).offset == c[(name, field)], (name, field)
+
+
 def test_every_declared_symbol_is_exported(lib):
     for name in declared_functions():
         assert hasattr(lib, name), name
