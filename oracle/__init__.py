@@ -80,6 +80,17 @@ def _load():
             lib.orc_round_bf16_array.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64]
             lib.orc_count_nan_scales.restype = ctypes.c_int64
             lib.orc_count_nan_scales.argtypes = [ctypes.c_int, ctypes.c_void_p, ctypes.c_int64]
+            lib.orc_e2m1_q1.restype = ctypes.c_int
+            lib.orc_e2m1_q1.argtypes = [ctypes.c_uint]
+            lib.orc_e4m3fn_q9.restype = ctypes.c_int
+            lib.orc_e4m3fn_q9.argtypes = [ctypes.c_uint, ctypes.POINTER(ctypes.c_int32)]
+            lib.orc_q8_block.restype = None
+            lib.orc_q8_block.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.POINTER(ctypes.c_float)]
+            lib.orc_f16_round.restype = ctypes.c_float
+            lib.orc_f16_round.argtypes = [ctypes.c_float]
+            lib.orc_gemv_a16q8_rows.restype = ctypes.c_int
+            lib.orc_gemv_a16q8_rows.argtypes = [ctypes.POINTER(_Tensor), ctypes.c_void_p, ctypes.c_int64,
+                                                ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p]
             _lib = lib
     return _lib
 
@@ -217,3 +228,73 @@ def count_nan_scales(fmt, scales: np.ndarray) -> int:
 def gemv_tolerance(bound: np.ndarray) -> np.ndarray:
     """The GEMV acceptance bound: |y_gpu - y_ref| <= 1e-5 * sum|w_hat||x| + 1e-6."""
     return 1e-5 * bound + 1e-6
+
+
+# ------------------------------------------- the integer-exact A16-Q8 lane
+# [MUS7] 7.4.2: NVFP4 weights against activations quantized per 256-value
+# block to signed 8-bit codes; the block contraction is an exact integer sum
+# and only a pinned four-step f32 epilogue rounds.
+
+def e2m1_q1(code: int) -> int:
+    """E2M1 code as an integer number of halves (2 * v(code))."""
+    return int(_load().orc_e2m1_q1(code))
+
+
+def e4m3fn_q9(byte: int) -> int:
+    """E4M3FN byte as an integer number of 2^-9 units."""
+    v = ctypes.c_int32()
+    if _load().orc_e4m3fn_q9(byte, ctypes.byref(v)):
+        raise OracleError(f"E4M3FN byte 0x{byte:02x} is a NaN encoding")
+    return int(v.value)
+
+
+def q8_block(x: np.ndarray):
+    """(codes int8 [256], scale f32) for one 256-value f32 activation block."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    assert x.shape == (256,)
+    q = np.empty(256, dtype=np.int8)
+    sc = ctypes.c_float()
+    _load().orc_q8_block(x.ctypes.data, q.ctypes.data, ctypes.byref(sc))
+    return q, np.float32(sc.value)
+
+
+def q8_quantize(x: np.ndarray):
+    """(codes int8 [M][K], scales f32 [M][K/256]) block by block."""
+    x = np.ascontiguousarray(np.atleast_2d(x), dtype=np.float32)
+    M, K = x.shape
+    assert K % 256 == 0
+    codes = np.empty((M, K), dtype=np.int8)
+    scales = np.empty((M, K // 256), dtype=np.float32)
+    for m in range(M):
+        for b in range(K // 256):
+            codes[m, b * 256:(b + 1) * 256], scales[m, b] = q8_block(x[m, b * 256:(b + 1) * 256])
+    return codes, scales
+
+
+def f16_round(x: np.ndarray) -> np.ndarray:
+    """Each f32 rounded to the nearest binary16 value (ties to even), as f32."""
+    lib = _load()
+    x = np.asarray(x, dtype=np.float32)
+    return np.array([lib.orc_f16_round(float(v)) for v in x.ravel()], dtype=np.float32).reshape(x.shape)
+
+
+def gemv_a16q8(t: Tensor, x: np.ndarray, rows=None) -> np.ndarray:
+    """y f32 [M][len(rows)] of the A16-Q8 contraction (NVFP4 only, K % 256 == 0);
+    each value is the binary16-rounded total, widened to f32.  ``x`` is f32
+    [M][K] (or [K])."""
+    x = np.ascontiguousarray(np.atleast_2d(x), dtype=np.float32)
+    M = x.shape[0]
+    assert x.shape[1] == t.K
+    rows = np.arange(t.N, dtype=np.int64) if rows is None else np.asarray(rows, dtype=np.int64)
+    rows = np.ascontiguousarray(rows)
+    y = np.empty((M, rows.size), dtype=np.float32)
+    ct = _Tensor.from_buffer_copy(t._c())
+    rc = _load().orc_gemv_a16q8_rows(ctypes.byref(ct), x.ctypes.data, M, rows.ctypes.data, rows.size,
+                                     y.ctypes.data)
+    if rc == 1:
+        raise OracleError("a scale byte is a NaN encoding")
+    if rc == 2:
+        raise OracleError("the A16-Q8 contraction takes NVFP4 with K a multiple of 256")
+    if rc:
+        raise OracleError("out of memory")
+    return y

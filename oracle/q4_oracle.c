@@ -22,6 +22,7 @@
  */
 #include <math.h>
 #include <stdint.h>
+#include <stdlib.h>
 #include <string.h>
 
 enum { F_NVFP4 = 1, F_MXFP4 = 2, F_Q4K = 3, F_Q40 = 4, F_GPTQ = 5, F_AWQ = 6,
@@ -365,4 +366,157 @@ int64_t orc_count_nan_scales(int fmt, const uint8_t *scales, int64_t count)
             bad += orc_e4m3fn(scales[i], &v);
     }
     return bad;
+}
+
+/* ------------------------------------------ the integer-exact A16-Q8 lane */
+
+/* E2M1 code as an integer count of halves: the weight encoding of the
+ * weight-only contraction in [MUS7] 7.4.2.  The smallest nonzero E2M1 value
+ * is 1/2, so every value is an integer multiple of it: 2*v(code), which is
+ * f for exponent field 0 and (2+f) << (e-1) otherwise; bit 3 is the sign. */
+int orc_e2m1_q1(unsigned code)
+{
+    unsigned s = (code >> 3) & 1u, e = (code >> 1) & 3u, f = code & 1u;
+    int mag = (e == 0) ? (int)f : (int)((2u + f) << (e - 1u));
+    return s ? -mag : mag;
+}
+
+/* E4M3FN byte as an integer count of 2^-9 (the smallest subnormal), the
+ * scale encoding of [MUS7] 7.4.2: f for exponent field 0, else
+ * (1 + f/8) * 2^(e-7) / 2^-9 = (8+f) << (e-1); bit 7 is the sign.
+ * Returns 1 for a NaN encoding (0x7f / 0xff). */
+int orc_e4m3fn_q9(unsigned byte, int32_t *out)
+{
+    unsigned s = (byte >> 7) & 1u, e = (byte >> 3) & 15u, f = byte & 7u;
+    if (e == 15u && f == 7u) {
+        *out = 0;
+        return 1;
+    }
+    int32_t mag = (e == 0) ? (int32_t)f : (int32_t)((8u + f) << (e - 1u));
+    *out = s ? -mag : mag;
+    return 0;
+}
+
+/* One 256-value activation block onto the signed 8-bit grid, [MUS7] 7.4.2:
+ * first_max is the signed value of the first element of largest magnitude,
+ * iscale = -127 / first_max, each code is x * iscale (rounded to f32) rounded
+ * half-to-even to an integer and capped at 127, and the block's scale is
+ * 1 / iscale.  Reading: a block whose iscale is not finite (first_max zero,
+ * or so small that -127 / first_max overflows) takes all-zero codes and
+ * scale 0. */
+void orc_q8_block(const float *x, int8_t *q, float *scale)
+{
+    float first_max = 0.0f, amax = 0.0f;
+    for (int i = 0; i < 256; i++) {
+        float a = fabsf(x[i]);
+        if (a > amax) {
+            amax = a;
+            first_max = x[i];
+        }
+    }
+    float iscale = -127.0f / first_max;
+    if (!isfinite(iscale)) {
+        for (int i = 0; i < 256; i++)
+            q[i] = 0;
+        *scale = 0.0f;
+        return;
+    }
+    for (int i = 0; i < 256; i++) {
+        float v = x[i] * iscale;
+        long r = lrintf(v);             /* default rounding mode: half to even */
+        q[i] = (int8_t)(r > 127 ? 127 : r);
+    }
+    *scale = 1.0f / iscale;
+}
+
+/* f32 -> nearest IEEE binary16 value (ties to even, gradual underflow,
+ * overflow to infinity), returned widened to f32.  Written from the binary16
+ * definition: values of binade [2^E, 2^(E+1)) sit on a grid of 2^(E-10), and
+ * below 2^-14 on the subnormal grid 2^-24; the largest finite value is 65504.
+ * The scaled quotient is exact in double, so nearbyint makes the one rounding. */
+float orc_f16_round(float f)
+{
+    if (isnan(f))
+        return f;
+    double a = fabs((double)f);
+    if (a == 0.0)
+        return f;
+    int ex;
+    frexp(a, &ex);                      /* a = m * 2^ex, m in [0.5, 1) */
+    int E = ex - 1;
+    if (E > 15)
+        return f > 0 ? INFINITY : -INFINITY;
+    double quantum = ldexp(1.0, (E < -14 ? -14 : E) - 10);
+    double r = nearbyint(a / quantum) * quantum;
+    if (r > 65504.0)
+        return f > 0 ? INFINITY : -INFINITY;
+    return (float)(f > 0 ? r : -r);
+}
+
+/* The weight-only NVFP4 contraction of [MUS7] 7.4.2 for logical rows
+ * rows[0..nrows) and activation rows x[0..M) (f32 [M][K], bf16 passed
+ * widened).  Each activation row is first cut into 256-value blocks and
+ * quantized by orc_q8_block.  For output row n and block b,
+ *   T_b = sum over the block's 16 groups g of
+ *         q9(scale[n][g]) * sum_{k in g} q1(code[n][k]) * q8[m][k]
+ * is an exact 64-bit integer; its value is T_b * 2^-10 (halves times 2^-9)
+ * in units of the block's activation scale.  The floating-point epilogue is
+ * the page's four steps, in block order:
+ *   c = fma(float(T_b), 2^-10, 0); c = fma(c, act_scale_b, 0);
+ *   c = fma(c, scale2, 0);         total = fma(1, c, total)
+ * and the output is total rounded to binary16 (stored widened, f32).
+ * Returns 0; 1 if a scale byte is a NaN encoding; 2 if the tensor is not
+ * NVFP4 or K is not a multiple of 256; 3 if memory runs out. */
+int orc_gemv_a16q8_rows(const orc_tensor *t, const float *x, int64_t M,
+                        const int64_t *rows, int64_t nrows, float *y)
+{
+    if (t->fmt != F_NVFP4 || t->K % 256 != 0)
+        return 2;
+    const int64_t K = t->K, nb = K / 256;
+    int8_t *q8 = (int8_t *)malloc((size_t)(M * K));
+    float *act_scale = (float *)malloc((size_t)(M * nb) * sizeof(float));
+    if (!q8 || !act_scale) {
+        free(q8);
+        free(act_scale);
+        return 3;
+    }
+    for (int64_t m = 0; m < M; m++)
+        for (int64_t b = 0; b < nb; b++)
+            orc_q8_block(x + m * K + b * 256, q8 + m * K + b * 256, act_scale + m * nb + b);
+    int rc = 0;
+    for (int64_t i = 0; i < nrows && !rc; i++) {
+        const int64_t n = rows[i];
+        const uint8_t *row = t->w + n * (K / 2);
+        const uint8_t *srow = t->scales + n * (K / 16);
+        for (int64_t m = 0; m < M && !rc; m++) {
+            float total = 0.0f;
+            for (int64_t b = 0; b < nb; b++) {
+                int64_t T = 0;
+                for (int64_t g = b * 16; g < b * 16 + 16; g++) {
+                    int32_t q9;
+                    if (orc_e4m3fn_q9(srow[g], &q9)) {
+                        rc = 1;
+                        break;
+                    }
+                    int64_t dot = 0;
+                    for (int64_t k = g * 16; k < g * 16 + 16; k++) {
+                        uint8_t byte = row[k / 2];
+                        unsigned code = (k % 2 == 0) ? (byte & 15u) : (byte >> 4);
+                        dot += (int64_t)orc_e2m1_q1(code) * (int64_t)q8[m * K + k];
+                    }
+                    T += dot * (int64_t)q9;
+                }
+                if (rc)
+                    break;
+                float c = fmaf((float)T, 0x1p-10f, 0.0f);
+                c = fmaf(c, act_scale[m * nb + b], 0.0f);
+                c = fmaf(c, t->scale2, 0.0f);
+                total = fmaf(1.0f, c, total);
+            }
+            y[m * nrows + i] = orc_f16_round(total);
+        }
+    }
+    free(q8);
+    free(act_scale);
+    return rc;
 }
