@@ -451,6 +451,8 @@ def cpu_baseline(seconds, host=None, sample_rows=None):
                       f"{t_total:.1f} s", "cpu": _cpu_name()}
 
 
+A16Q8_ROW = "f2 NVFP4 A16-Q8 GEMV (integer-exact)"
+
 # The other rows' shapes and synthetic recipes (see other_rows), for the oracle beside each.
 ORACLE_ROWS = [("a1 NVFP4 GEMV", "nvfp4", 14336, 4096, 4, 5, dict(row_scale=True), "bf16"),
                ("a2 Q4_K GEMV", "q4k", 4096, 4096, 1, 1, dict(), "f32"),
@@ -489,6 +491,15 @@ def cpu_baseline_rows(rows_per_matrix=1024):
         if tag.startswith("a1"):
             out.append({"row": "a6 dequant NVFP4 -> f32", "shape": f"{N}x{K}", "sample": f"{rows.size} rows of K = {K}",
                         "GBps": round(rows.size * (row_bytes + 4 * K) / dq / 1e9, 4), "seconds": round(dq, 3)})
+    layer = synth.make_layer("nvfp4", rows_per_matrix, 4096, config=5, matrix=0, row_scale=True)
+    T = oracle.Tensor("nvfp4", rows_per_matrix, 4096, layer["w"], layer["scales"], scale2=layer["scale2"])
+    _, xf = synth.draw_x(1, 4096, config=5, matrix=5, dtype="bf16")
+    t0 = time.perf_counter()
+    oracle.gemv_a16q8(T, xf)
+    dt = time.perf_counter() - t0
+    out.append({"row": A16Q8_ROW, "shape": "14336x4096", "M": 1, "sample": f"{rows_per_matrix} rows of K = 4096",
+                "GBps": round(rows_per_matrix * q4_packed_row_bytes("nvfp4", 4096) / dt / 1e9, 4),
+                "seconds": round(dt, 3)})
     return out
 
 
@@ -684,6 +695,24 @@ def other_rows(torch, q4, synth, peak_hbm):
     gemv_row("a5 AWQ GEMV", "awq", 4096, 11008, 1, 2, dict(outliers=True), q4.Q4_DT_F32)
     torch.cuda.empty_cache()
 
+    # the integer-exact A16-Q8 lane on the 14336x4096 NVFP4 layer at batch 1
+    N, K, M = 14336, 4096, 1
+    layer = synth.make_layer("nvfp4", N, K, config=5, matrix=0, row_scale=True)
+    packed = q4.q4_packed_bytes("nvfp4", N, K)
+    cps = copies_of(_dev_layer(torch, layer), packed)
+    xb, _ = synth.draw_x(M, K, config=5, matrix=5, dtype="bf16")
+    x = torch.from_numpy(np.ascontiguousarray(xb).view(np.int16)).cuda().view(torch.bfloat16)
+    y = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    aux = q4.make_aux(scale2=layer["scale2"], x_dtype=q4.Q4_DT_BF16, fmt="nvfp4")
+    us = _time_launches(torch, stream, lambda i: q4.q4_gemv_a16q8(cps[i % len(cps)]["w"], cps[i % len(cps)]["scales"],
+                                                                  aux, x, y, M, N, K, stream=stream))
+    moved = packed + x.numel() * 2 + y.numel() * 4
+    rows.append({"row": A16Q8_ROW, "shape": f"{N}x{K}", "M": M, "us_per_launch": round(us, 2),
+                 "GBps": round(moved / us / 1e3, 1), "frac_hbm": round(moved / us / 1e3 / peak_hbm, 4),
+                 "path": q4.q4_last_gemv_path()})
+    del cps
+    torch.cuda.empty_cache()
+
     # a6: dequant NVFP4 14336x4096 to f32 (write-bound)
     N, K = 14336, 4096
     layer = synth.make_layer("nvfp4", N, K, config=5, matrix=0, row_scale=True)
@@ -834,6 +863,16 @@ def ncu_rows_case():
     q4.q4_repack("gptq", d["w"], d["scales"], q4.make_aux(zeros=d["zeros"], group=128, fmt="gptq"), "awq", w, sc, z,
                  None, N, K, stream=stream)
     print(f"a7 repack GPTQ -> AWQ: {N}x{K} algorithmic bytes {2 * q4.q4_packed_bytes('gptq', N, K)}")
+    N, K = 14336, 4096
+    layer = synth.make_layer("nvfp4", N, K, config=5, matrix=0, row_scale=True)
+    d = _dev_layer(torch, layer)
+    xb, _ = synth.draw_x(1, K, config=5, matrix=5, dtype="bf16")
+    x = torch.from_numpy(np.ascontiguousarray(xb).view(np.int16)).cuda().view(torch.bfloat16)
+    y = torch.empty((1, N), dtype=torch.float32, device="cuda")
+    q4.q4_gemv_a16q8(d["w"], d["scales"], q4.make_aux(scale2=layer["scale2"], fmt="nvfp4"), x, y, 1, N, K,
+                     stream=stream)
+    torch.cuda.synchronize()
+    print(f"{A16Q8_ROW}: {N}x{K} algorithmic bytes {q4.q4_packed_bytes('nvfp4', N, K) + K * 2 + N * 4}")
     print("ncu rows case done, last_error", q4.q4_last_error())
 
 

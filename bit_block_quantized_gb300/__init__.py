@@ -58,6 +58,7 @@ def lib() -> ctypes.CDLL:
         AUXP = ctypes.POINTER(Aux)
         L.q4_gemv.argtypes = [I32, P, P, AUXP, P, P, I64, I64, I64, P]
         L.q4_dequant.argtypes = [I32, P, P, AUXP, P, I64, I64, P]
+        L.q4_gemv_a16q8.argtypes = [P, P, AUXP, P, P, I64, I64, I64, P]
         L.q4_gemv_grouped.argtypes = [ctypes.POINTER(GemvDesc), I32, I64, P]
         L.q4_gemv_chain.argtypes = [ctypes.POINTER(GemvDesc), ctypes.POINTER(ctypes.c_int), I32, I64, P, P]
         L.q4_gemv_chain.restype = ctypes.c_int
@@ -65,7 +66,7 @@ def lib() -> ctypes.CDLL:
         L.q4_validate.argtypes = [I32, P, P, AUXP, I64, I64, P, P]
         L.q4_validate_noalloc.argtypes = [I32, P, P, AUXP, I64, I64, ctypes.POINTER(ctypes.c_int64), P]
         L.q4_validate_noalloc.restype = ctypes.c_int
-        for f in ("q4_gemv", "q4_gemv_grouped", "q4_dequant", "q4_repack", "q4_validate", "q4_last_error"):
+        for f in ("q4_gemv", "q4_gemv_a16q8", "q4_gemv_grouped", "q4_dequant", "q4_repack", "q4_validate", "q4_last_error"):
             getattr(L, f).restype = ctypes.c_int
         L.q4_last_error.argtypes = []
         L.q4_strerror.restype = ctypes.c_char_p
@@ -131,6 +132,16 @@ def q4_gemv(fmt, W_packed, scales, aux, x, y, M, N, K, stream=None, check=True) 
                        int(M), int(N), int(K), _stream(stream))
     if check:
         _check(rc, "q4_gemv")
+    return rc
+
+
+def q4_gemv_a16q8(W_packed, scales, aux, x, y, M, N, K, stream=None, check=True) -> int:
+    """The integer-exact NVFP4 contraction with per-256 Q8 activations; y holds
+    binary16-rounded values widened to f32."""
+    rc = lib().q4_gemv_a16q8(_ptr(W_packed), _ptr(scales), _aux_ref(aux), _ptr(x), _ptr(y),
+                             int(M), int(N), int(K), _stream(stream))
+    if check:
+        _check(rc, "q4_gemv_a16q8")
     return rc
 
 

@@ -204,6 +204,20 @@ int q4_gemv_chain(const q4_gemv_desc *descs, const int *first, int ngroups, int6
 
 const char *q4_last_gemv_path(void) { return q4::g_last_path; }
 
+int q4_gemv_a16q8(const void *W_packed, const void *scales, const q4_aux *aux, const void *x, float *y, int64_t M,
+                  int64_t N, int64_t K, void *stream) {
+    Tensor t;
+    const int rc = make_tensor(Q4_NVFP4, W_packed, scales, aux, N, K, t);   // aux is non-null past this
+    if (rc) return rc;
+    if (M <= 0 || K % 256) return Q4_EDIM;
+    if (!x || !y) return Q4_EINVAL;
+    if (!aligned16(x) || !aligned16(y)) return Q4_EALIGN;
+    const q4_dtype xd = aux->x_dtype;
+    if (xd != Q4_DT_F32 && xd != Q4_DT_BF16) return Q4_EINVAL;
+    if (gemv_a16q8_chunk(M, K) == 0) return Q4_EDIM;
+    return launch_gemv_a16q8(t, x, xd, y, M, (cudaStream_t)stream) == cudaSuccess ? Q4_OK : Q4_ECUDA;
+}
+
 int q4_dequant(q4_fmt fmt, const void *W_packed, const void *scales, const q4_aux *aux, void *out, int64_t N,
                int64_t K, void *stream) {
     Tensor t;

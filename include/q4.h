@@ -168,6 +168,30 @@ int q4_gemv_grouped(const q4_gemv_desc *descs, int count, int64_t M, void *strea
 int q4_gemv_chain(const q4_gemv_desc *descs, const int *first, int ngroups, int64_t M, uint32_t *sync,
                   void *stream);
 
+/* The integer-exact weight-only NVFP4 contraction ([MUS7] 7.4.2): y[M][N]
+ * from NVFP4 weights (layout as Q4_NVFP4; aux->scale2 required) and
+ * activations x[M][K] (aux->x_dtype: bf16 or f32), in three pinned stages.
+ *   1. Each activation row is cut into 256-value blocks.  A block's signed
+ *      first maximum m (the first element of largest magnitude) gives
+ *      iscale = -127/m; each code is the f32 product x*iscale rounded half to
+ *      even and capped at 127, and the block scale is 1/iscale.  A block
+ *      whose iscale is not finite (m zero, or so small that -127/m
+ *      overflows) takes zero codes and scale 0.
+ *   2. Per output row and block, T = sum over the block's 16 groups of
+ *      q9(scale) * sum(q1(code) * q8) is an exact 64-bit integer (q1: E2M1 in
+ *      halves; q9: E4M3FN in units of 2^-9), independent of summation order.
+ *   3. In block order, in f32: c = fma(float(T), 2^-10, 0); c = fma(c,
+ *      block scale, 0); c = fma(c, scale2, 0); total = fma(1, c, total).
+ *      y = total rounded to binary16, stored widened to f32.
+ * The result is therefore bit-reproducible: every run, batch size and
+ * device gives the same bits.  K % 256 == 0 (Q4_EDIM otherwise); x must be
+ * finite.  Each launch quantizes up to 8 activation rows into a 200 KiB
+ * shared-memory budget (8 rows up to K = 24,832; fewer rows per launch above
+ * that; K > 200,448 gets Q4_EDIM); larger M runs as several launches.
+ * Allocates nothing; asynchronous on `stream`. */
+int q4_gemv_a16q8(const void *W_packed, const void *scales, const q4_aux *aux, const void *x, float *y,
+                  int64_t M, int64_t N, int64_t K, void *stream);
+
 /* out[N][K] = w_hat, f32 or bf16 per aux->out_dtype, by the pinned per-format
  * rule ([MUS7] 7.2 for NVFP4; the per-format sections cited above).  Bit-exact
  * with the definition.  Asynchronous on `stream`. */
@@ -231,7 +255,7 @@ int q4_last_error(void);
  * q4_gemv_grouped or q4_gemv_chain launched ("gemv_tma", "gemv_tma_group",
  * "gemv_tma_chain", "gemm_tc", "gemv_mma", "gemv_mma_group", "gemv_mma_q4k",
  * "gemv_mma_q40", "gemv_mma_gptq", "gemv_rows_tma", "gemv_rows_m1",
- * "gemv_general", "gemv_kmajor"; "" before
+ * "gemv_general", "gemv_kmajor"; "gemv_a16q8" after q4_gemv_a16q8; "" before
  * the first call).  A diagnostic with no counterpart in the pages: it lets a
  * caller (and the tests) confirm which path a shape takes.  Static storage. */
 const char *q4_last_gemv_path(void);

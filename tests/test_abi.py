@@ -157,3 +157,21 @@ def test_host_side_rejections(lib):
     assert chain([[good]], 0, stream=0, check=False) == q4.Q4_EDIM
     assert chain([], 1, stream=0, check=False) == q4.Q4_EINVAL
     assert chain([[good], []], 1, sync=0x50000, stream=0, check=False) == q4.Q4_EINVAL
+
+
+def test_a16q8_host_side_rejections(lib):
+    nv = q4.make_aux(scale2=0.5, fmt="nvfp4")
+
+    def call(aux=nv, M=1, N=64, K=256, w=A, s=B, x=C, y=D):
+        return q4.q4_gemv_a16q8(w, s, aux, x, y, M, N, K, stream=0, check=False)
+
+    assert call(K=128) == q4.Q4_EDIM                  # K % 256
+    assert call(K=200_704) == q4.Q4_EDIM              # one row of codes exceeds the budget
+    assert call(M=0) == q4.Q4_EDIM
+    assert call(N=0) == q4.Q4_EDIM
+    assert call(aux=None) == q4.Q4_EINVAL             # scale2 lives in aux
+    assert call(aux=q4.make_aux(scale2=0.0, fmt="nvfp4")) == q4.Q4_ESCALE2
+    assert call(aux=q4.make_aux(scale2=1.0, x_dtype=7, fmt="nvfp4")) == q4.Q4_EINVAL
+    assert call(x=0) == q4.Q4_EINVAL
+    assert call(x=C + 2) == q4.Q4_EALIGN
+    assert call(s=B + 8) == q4.Q4_EALIGN
