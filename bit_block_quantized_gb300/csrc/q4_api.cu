@@ -13,6 +13,11 @@ thread_local const char *g_last_path = "";
 
 void note_gemv_path(const char *name) { g_last_path = name; }
 
+// The integer-exact A16-Q8 lane (gemv_a16q8.cu): activation rows per launch
+// (0 if K does not fit the shared-memory budget) and the launcher.
+int gemv_a16q8_chunk(int64_t M, int64_t K);
+cudaError_t launch_gemv_a16q8(const Tensor &t, const void *x, q4_dtype xd, float *y, int64_t M, cudaStream_t s);
+
 int sm_count() {
     int dev = 0, n = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 1;

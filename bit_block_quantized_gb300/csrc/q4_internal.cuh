@@ -222,8 +222,6 @@ cudaError_t launch_gemv_mma_group(const Tensor *ts, const void *const *xs, float
 int launch_repack(q4_fmt src, const Tensor &t, q4_fmt dst, void *dst_w, void *dst_scales,
                   void *dst_zeros, int32_t *perm_out, cudaStream_t s);
 int run_validate(const Tensor &t, int64_t *d_bad, cudaStream_t s);
-int gemv_a16q8_chunk(int64_t M, int64_t K);
-cudaError_t launch_gemv_a16q8(const Tensor &t, const void *x, q4_dtype xd, float *y, int64_t M, cudaStream_t s);
 
 // ------------------------------------------------- per-element decoders
 // w_hat(n, k) for every format, f32, by the pinned rule: one weight at a time
