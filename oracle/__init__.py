@@ -91,6 +91,9 @@ def _load():
             lib.orc_gemv_a16q8_rows.restype = ctypes.c_int
             lib.orc_gemv_a16q8_rows.argtypes = [ctypes.POINTER(_Tensor), ctypes.c_void_p, ctypes.c_int64,
                                                 ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p]
+            lib.orc_gemv_q4k_q8_rows.restype = ctypes.c_int
+            lib.orc_gemv_q4k_q8_rows.argtypes = [ctypes.POINTER(_Tensor), ctypes.c_void_p, ctypes.c_int64,
+                                                 ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p]
             _lib = lib
     return _lib
 
@@ -295,6 +298,26 @@ def gemv_a16q8(t: Tensor, x: np.ndarray, rows=None) -> np.ndarray:
         raise OracleError("a scale byte is a NaN encoding")
     if rc == 2:
         raise OracleError("the A16-Q8 contraction takes NVFP4 with K a multiple of 256")
+    if rc:
+        raise OracleError("out of memory")
+    return y
+
+
+def gemv_q4k_q8(t: Tensor, x: np.ndarray, rows=None) -> np.ndarray:
+    """y f32 [M][len(rows)] of the Q4_K x Q8 contraction ([W4K] section 7):
+    activations on the per-256 Q8 grid of :func:`q8_block`, exact integer
+    sub-block sums, f32 epilogue per super-block.  ``x`` is f32 [M][K]."""
+    x = np.ascontiguousarray(np.atleast_2d(x), dtype=np.float32)
+    M = x.shape[0]
+    assert x.shape[1] == t.K
+    rows = np.arange(t.N, dtype=np.int64) if rows is None else np.asarray(rows, dtype=np.int64)
+    rows = np.ascontiguousarray(rows)
+    y = np.empty((M, rows.size), dtype=np.float32)
+    ct = _Tensor.from_buffer_copy(t._c())
+    rc = _load().orc_gemv_q4k_q8_rows(ctypes.byref(ct), x.ctypes.data, M, rows.ctypes.data, rows.size,
+                                      y.ctypes.data)
+    if rc == 2:
+        raise OracleError("the Q4_K x Q8 contraction takes Q4_K with K a multiple of 256")
     if rc:
         raise OracleError("out of memory")
     return y

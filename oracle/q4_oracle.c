@@ -520,3 +520,70 @@ int orc_gemv_a16q8_rows(const orc_tensor *t, const float *x, int64_t M,
     free(act_scale);
     return rc;
 }
+
+/* The Q4_K x Q8 contraction of [W4K] section 7 ("W4A8" and the CKE
+ * Q4_K x Q8_K route of 7b-7c): activations quantized per 256-value block
+ * (orc_q8_block, the same signed-first-maximum grid), weights kept as the
+ * unsigned 4-bit codes of each 32-value sub-block j.  Per super-block, two
+ * exact integers:
+ *   I1 = sum_j sc_j * sum_{k in j} q[k] * q8[k]     (scaled integer dot)
+ *   I2 = sum_j m_j  * sum_{k in j} q8[k]            (minimum term, activation sums)
+ * then, in f32 and in the order the section names the steps (a reading: the
+ * section does not pin the rounding order):
+ *   v = f32(d) * float(I1) - f32(dmin) * float(I2);  c = v * act_scale;
+ *   total = total + c   (super-blocks in order).
+ * Algebraically sum_k w_hat[k] * (q8[k] * act_scale), the section's
+ * s_x (d s_j) sum q_w q_x - s_x (dmin m_j) sum q_x.  Output f32.
+ * Returns 0; 2 if the tensor is not Q4_K; 3 if memory runs out. */
+int orc_gemv_q4k_q8_rows(const orc_tensor *t, const float *x, int64_t M,
+                         const int64_t *rows, int64_t nrows, float *y)
+{
+    if (t->fmt != F_Q4K || t->K % 256 != 0)
+        return 2;
+    const int64_t K = t->K, nb = K / 256;
+    int8_t *q8 = (int8_t *)malloc((size_t)(M * K));
+    float *act_scale = (float *)malloc((size_t)(M * nb) * sizeof(float));
+    if (!q8 || !act_scale) {
+        free(q8);
+        free(act_scale);
+        return 3;
+    }
+    for (int64_t m = 0; m < M; m++)
+        for (int64_t b = 0; b < nb; b++)
+            orc_q8_block(x + m * K + b * 256, q8 + m * K + b * 256, act_scale + m * nb + b);
+    for (int64_t i = 0; i < nrows; i++) {
+        const int64_t n = rows[i];
+        for (int64_t m = 0; m < M; m++) {
+            float total = 0.0f;
+            for (int64_t b = 0; b < nb; b++) {
+                const uint8_t *blk = t->w + (n * nb + b) * 144;
+                const int8_t *qx = q8 + m * K + b * 256;
+                int64_t I1 = 0, I2 = 0;
+                for (int j = 0; j < 8; j++) {
+                    unsigned sc, mn;
+                    q4k_scale_min(blk + 4, j, &sc, &mn);
+                    int64_t dot = 0, bsum = 0;
+                    for (int l = 0; l < 32; l++) {
+                        /* sub-block j = 2c + hi: code byte 32c + l, k = 32j + l */
+                        uint8_t byte = blk[16 + 32 * (j / 2) + l];
+                        unsigned q = (j % 2) ? (byte >> 4) : (byte & 15u);
+                        dot += (int64_t)q * qx[32 * j + l];
+                        bsum += qx[32 * j + l];
+                    }
+                    I1 += (int64_t)sc * dot;
+                    I2 += (int64_t)mn * bsum;
+                }
+                float d = orc_half(rd16(blk)), dmin = orc_half(rd16(blk + 2));
+                float p1 = d * (float)I1;
+                float p2 = dmin * (float)I2;
+                float v = p1 - p2;
+                float c = v * act_scale[m * nb + b];
+                total = total + c;
+            }
+            y[m * nrows + i] = total;
+        }
+    }
+    free(q8);
+    free(act_scale);
+    return 0;
+}

@@ -86,7 +86,7 @@ def test_q8_block_rounds_half_to_even():
 
 
 def test_q8_block_worked_by_hand():
-    # x = [0.5, -1, 2] (the activation of [FBTC] section 7's W4A8 example,
+    # x = [0.5, -1, 2] (the activation of [W4K] section 7's W4A8 example,
     # here on the per-block grid): first max 2, iscale = -63.5 (exact),
     # codes -31.75 -> -32, 63.5 -> 64 (tie, even), -127; scale 1/-63.5.
     x = np.zeros(256, np.float32)
