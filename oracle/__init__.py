@@ -92,6 +92,13 @@ def _load():
             lib.orc_gemv_a16q8_rows.argtypes = [ctypes.POINTER(_Tensor), ctypes.c_void_p, ctypes.c_int64,
                                                 ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p]
             lib.orc_gemv_q4k_q8_rows.restype = ctypes.c_int
+            lib.orc_e2m1_round.restype = ctypes.c_uint
+            lib.orc_e2m1_round.argtypes = [ctypes.c_float]
+            lib.orc_e4m3fn_round.restype = ctypes.c_uint
+            lib.orc_e4m3fn_round.argtypes = [ctypes.c_float]
+            lib.orc_quantize_nvfp4.restype = None
+            lib.orc_quantize_nvfp4.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p,
+                                               ctypes.c_void_p, ctypes.POINTER(ctypes.c_float)]
             lib.orc_gemv_q4k_q8_rows.argtypes = [ctypes.POINTER(_Tensor), ctypes.c_void_p, ctypes.c_int64,
                                                  ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p]
             _lib = lib
@@ -321,3 +328,27 @@ def gemv_q4k_q8(t: Tensor, x: np.ndarray, rows=None) -> np.ndarray:
     if rc:
         raise OracleError("out of memory")
     return y
+
+
+# ------------------------------------------------------ the NVFP4 quantizer
+
+def e2m1_round(r: float) -> int:
+    """Nearest E2M1 code (ties to the even code, saturating at 6, sign kept)."""
+    return int(_load().orc_e2m1_round(float(r)))
+
+
+def e4m3fn_round(v: float) -> int:
+    """Nearest E4M3FN byte (ties to even, saturating at 448, sign kept)."""
+    return int(_load().orc_e4m3fn_round(float(v)))
+
+
+def quantize_nvfp4(W: np.ndarray):
+    """(payload u8 [N][K/2], scales u8 [N][K/16], scale2 f32) of f32 W [N][K]."""
+    W = np.ascontiguousarray(W, dtype=np.float32)
+    N, K = W.shape
+    assert K % 16 == 0
+    payload = np.empty((N, K // 2), dtype=np.uint8)
+    scales = np.empty((N, K // 16), dtype=np.uint8)
+    s2 = ctypes.c_float()
+    _load().orc_quantize_nvfp4(W.ctypes.data, N, K, payload.ctypes.data, scales.ctypes.data, ctypes.byref(s2))
+    return payload, scales, np.float32(s2.value)

@@ -587,3 +587,90 @@ int orc_gemv_q4k_q8_rows(const orc_tensor *t, const float *x, int64_t M,
     free(act_scale);
     return 0;
 }
+
+/* ------------------------------------------------- the NVFP4 quantizer */
+
+/* Nearest E2M1 code to r ([MUS7] 7.2: ModelOpt's midpoints, ties to the even
+ * code), by search over the eight magnitudes; magnitudes above 6 saturate to
+ * 6.  The sign bit follows r, so a negative value that rounds to zero keeps
+ * it (code 8).  NaN is outside the definition. */
+unsigned orc_e2m1_round(float r)
+{
+    double a = fabs((double)r);
+    unsigned best = 0;
+    double best_err = INFINITY;
+    if (a >= 6.0)                       /* saturate (far values would tie in double) */
+        return 7u | (signbit(r) ? 8u : 0u);
+    for (unsigned c = 0; c < 8; c++) {
+        double err = fabs(a - (double)orc_e2m1(c));
+        if (err < best_err || (err == best_err && (c & 1u) == 0)) {
+            best = c;
+            best_err = err;
+        }
+    }
+    return best | (signbit(r) ? 8u : 0u);
+}
+
+/* Nearest E4M3FN byte to v, ties to the even byte (fraction bit 0 clear), by
+ * search over the 127 non-negative finite encodings; magnitudes beyond 448
+ * saturate to 448 (0x7e), so no NaN encoding is produced.  The sign bit
+ * follows v. */
+unsigned orc_e4m3fn_round(float v)
+{
+    double a = fabs((double)v);
+    unsigned best = 0;
+    double best_err = INFINITY;
+    if (a >= 448.0)
+        return 0x7eu | (signbit(v) ? 0x80u : 0u);
+    for (unsigned b = 0; b <= 0x7eu; b++) {
+        float s;
+        orc_e4m3fn(b, &s);
+        double err = fabs(a - (double)s);
+        if (err < best_err || (err == best_err && (b & 1u) == 0)) {
+            best = b;
+            best_err = err;
+        }
+    }
+    return best | (signbit(v) ? 0x80u : 0u);
+}
+
+/* NVFP4 quantization of W [N][K] (f32, finite, K % 16 == 0) by the recipe the
+ * weights of this build are stated in: scale2 = amax(W) / (448 * 6) in f32 (1
+ * for an all-zero W); per 16-value group, scale byte = E4M3FN nearest-even of
+ * (amax_group / 6) / scale2, saturating at 448; each code = E2M1 nearest-even
+ * of w / (dec(scale byte) * scale2), every step an f32 operation; a group
+ * whose scale decodes to 0 takes code 0 throughout.  Packs the payload with
+ * the even k in the low nibble ([MUS7] 7.1). */
+void orc_quantize_nvfp4(const float *W, int64_t N, int64_t K, uint8_t *payload, uint8_t *scales,
+                        float *scale2_out)
+{
+    float amax = 0.0f;
+    for (int64_t i = 0; i < N * K; i++)
+        if (fabsf(W[i]) > amax)
+            amax = fabsf(W[i]);
+    const float scale2 = amax > 0.0f ? amax / 2688.0f : 1.0f;
+    *scale2_out = scale2;
+    for (int64_t n = 0; n < N; n++)
+        for (int64_t g = 0; g < K / 16; g++) {
+            const float *w = W + n * K + g * 16;
+            float amax_g = 0.0f;
+            for (int i = 0; i < 16; i++)
+                if (fabsf(w[i]) > amax_g)
+                    amax_g = fabsf(w[i]);
+            float sv = amax_g / 6.0f;
+            sv = sv / scale2;
+            unsigned sb = orc_e4m3fn_round(sv);
+            float s;
+            orc_e4m3fn(sb, &s);
+            float denom = s * scale2;
+            scales[n * (K / 16) + g] = (uint8_t)sb;
+            for (int i = 0; i < 16; i += 2) {
+                unsigned c0 = 0, c1 = 0;
+                if (denom > 0.0f) {
+                    c0 = orc_e2m1_round(w[i] / denom);
+                    c1 = orc_e2m1_round(w[i + 1] / denom);
+                }
+                payload[n * (K / 2) + g * 8 + i / 2] = (uint8_t)(c0 | (c1 << 4));
+            }
+        }
+}
