@@ -97,6 +97,12 @@ def _load():
             lib.orc_e4m3fn_round.restype = ctypes.c_uint
             lib.orc_e4m3fn_round.argtypes = [ctypes.c_float]
             lib.orc_quantize_nvfp4.restype = None
+            lib.orc_quantize_nvfp4_groups.restype = None
+            lib.orc_quantize_nvfp4_groups.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_float,
+                                                      ctypes.c_void_p, ctypes.c_void_p]
+            lib.orc_gemv_w4a4_rows.restype = ctypes.c_int
+            lib.orc_gemv_w4a4_rows.argtypes = [ctypes.POINTER(_Tensor), ctypes.c_void_p, ctypes.c_int64, ctypes.c_float,
+                                               ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p]
             lib.orc_quantize_nvfp4.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p,
                                                ctypes.c_void_p, ctypes.POINTER(ctypes.c_float)]
             lib.orc_gemv_q4k_q8_rows.argtypes = [ctypes.POINTER(_Tensor), ctypes.c_void_p, ctypes.c_int64,
@@ -352,3 +358,37 @@ def quantize_nvfp4(W: np.ndarray):
     s2 = ctypes.c_float()
     _load().orc_quantize_nvfp4(W.ctypes.data, N, K, payload.ctypes.data, scales.ctypes.data, ctypes.byref(s2))
     return payload, scales, np.float32(s2.value)
+
+
+def quantize_nvfp4_groups(W: np.ndarray, scale2: float):
+    """(payload, scales) of W [N][K] for a given tensor scale (the group rule of
+    :func:`quantize_nvfp4`)."""
+    W = np.ascontiguousarray(W, dtype=np.float32)
+    N, K = W.shape
+    assert K % 16 == 0
+    payload = np.empty((N, K // 2), dtype=np.uint8)
+    scales = np.empty((N, K // 16), dtype=np.uint8)
+    _load().orc_quantize_nvfp4_groups(W.ctypes.data, N, K, float(scale2), payload.ctypes.data, scales.ctypes.data)
+    return payload, scales
+
+
+def gemv_w4a4(t: Tensor, x: np.ndarray, input_scale_inv: float, rows=None) -> np.ndarray:
+    """y f32 [M][len(rows)] of the W4A4 contraction ([MUS7] 7.4.3): x quantized
+    to NVFP4 per 16 with tensor scale 1/input_scale_inv, exact per-group
+    integer products, the f32 epilogue per group in order, binary16 output."""
+    x = np.ascontiguousarray(np.atleast_2d(x), dtype=np.float32)
+    M = x.shape[0]
+    assert x.shape[1] == t.K
+    rows = np.arange(t.N, dtype=np.int64) if rows is None else np.asarray(rows, dtype=np.int64)
+    rows = np.ascontiguousarray(rows)
+    y = np.empty((M, rows.size), dtype=np.float32)
+    ct = _Tensor.from_buffer_copy(t._c())
+    rc = _load().orc_gemv_w4a4_rows(ctypes.byref(ct), x.ctypes.data, M, float(input_scale_inv), rows.ctypes.data,
+                                    rows.size, y.ctypes.data)
+    if rc == 1:
+        raise OracleError("a scale byte is a NaN encoding")
+    if rc == 2:
+        raise OracleError("W4A4 takes NVFP4 weights and a finite input_scale_inv > 0")
+    if rc:
+        raise OracleError("out of memory")
+    return y

@@ -634,22 +634,15 @@ unsigned orc_e4m3fn_round(float v)
     return best | (signbit(v) ? 0x80u : 0u);
 }
 
-/* NVFP4 quantization of W [N][K] (f32, finite, K % 16 == 0) by the recipe the
- * weights of this build are stated in: scale2 = amax(W) / (448 * 6) in f32 (1
- * for an all-zero W); per 16-value group, scale byte = E4M3FN nearest-even of
+/* NVFP4 groups of W [N][K] (f32, finite, K % 16 == 0) for a given tensor
+ * scale: per 16-value group, scale byte = E4M3FN nearest-even of
  * (amax_group / 6) / scale2, saturating at 448; each code = E2M1 nearest-even
  * of w / (dec(scale byte) * scale2), every step an f32 operation; a group
- * whose scale decodes to 0 takes code 0 throughout.  Packs the payload with
- * the even k in the low nibble ([MUS7] 7.1). */
-void orc_quantize_nvfp4(const float *W, int64_t N, int64_t K, uint8_t *payload, uint8_t *scales,
-                        float *scale2_out)
+ * whose scale decodes to 0 takes code 0 throughout.  Payload with the even k
+ * in the low nibble ([MUS7] 7.1). */
+void orc_quantize_nvfp4_groups(const float *W, int64_t N, int64_t K, float scale2, uint8_t *payload,
+                               uint8_t *scales)
 {
-    float amax = 0.0f;
-    for (int64_t i = 0; i < N * K; i++)
-        if (fabsf(W[i]) > amax)
-            amax = fabsf(W[i]);
-    const float scale2 = amax > 0.0f ? amax / 2688.0f : 1.0f;
-    *scale2_out = scale2;
     for (int64_t n = 0; n < N; n++)
         for (int64_t g = 0; g < K / 16; g++) {
             const float *w = W + n * K + g * 16;
@@ -673,4 +666,81 @@ void orc_quantize_nvfp4(const float *W, int64_t N, int64_t K, uint8_t *payload, 
                 payload[n * (K / 2) + g * 8 + i / 2] = (uint8_t)(c0 | (c1 << 4));
             }
         }
+}
+
+/* NVFP4 quantization of W [N][K] by the recipe the weights of this build are
+ * stated in: scale2 = amax(W) / (448 * 6) in f32 (1 for an all-zero W), then
+ * the groups as above. */
+void orc_quantize_nvfp4(const float *W, int64_t N, int64_t K, uint8_t *payload, uint8_t *scales,
+                        float *scale2_out)
+{
+    float amax = 0.0f;
+    for (int64_t i = 0; i < N * K; i++)
+        if (fabsf(W[i]) > amax)
+            amax = fabsf(W[i]);
+    const float scale2 = amax > 0.0f ? amax / 2688.0f : 1.0f;
+    *scale2_out = scale2;
+    orc_quantize_nvfp4_groups(W, N, K, scale2, payload, scales);
+}
+
+/* The W4A4 contraction of [MUS7] 7.4.3.  Each activation row is quantized to
+ * NVFP4 in groups of 16 with the tensor scale G = 1 / input_scale_inv (f32),
+ * by the same rule as the weights (orc_quantize_nvfp4_groups).  Per group g of
+ * output row n the product of the four integer encodings
+ *   T_g = q9(sw) * q9(sx) * sum_{k in g} q1(w_k) * q1(x_k)
+ * is exact in 64 bits with denominator 2^-20 (halves x halves x 2^-9 x 2^-9).
+ * Epilogue per group, in group order (a reading: the section names the
+ * factors, the per-group i64 sum and the binary16 output):
+ *   c = fma(float(T_g), 2^-20, 0); c = fma(c, scale2, 0); c = fma(c, G, 0);
+ *   total = fma(1, c, total)
+ * and y = total rounded to binary16 (stored widened, f32).
+ * Returns 0; 1 for a NaN weight-scale encoding; 2 for a non-NVFP4 tensor or
+ * an input_scale_inv that is not finite and > 0; 3 if memory runs out. */
+int orc_gemv_w4a4_rows(const orc_tensor *t, const float *x, int64_t M, float input_scale_inv,
+                       const int64_t *rows, int64_t nrows, float *y)
+{
+    if (t->fmt != F_NVFP4 || !(input_scale_inv > 0.0f) || !isfinite(input_scale_inv))
+        return 2;
+    const int64_t K = t->K, ng = K / 16;
+    const float G = 1.0f / input_scale_inv;
+    uint8_t *xp = (uint8_t *)malloc((size_t)(M * K / 2));
+    uint8_t *xs = (uint8_t *)malloc((size_t)(M * ng));
+    if (!xp || !xs) {
+        free(xp);
+        free(xs);
+        return 3;
+    }
+    orc_quantize_nvfp4_groups(x, M, K, G, xp, xs);
+    int rc = 0;
+    for (int64_t i = 0; i < nrows && !rc; i++) {
+        const int64_t n = rows[i];
+        const uint8_t *wrow = t->w + n * (K / 2), *srow = t->scales + n * ng;
+        for (int64_t m = 0; m < M && !rc; m++) {
+            const uint8_t *xrow = xp + m * (K / 2), *xsrow = xs + m * ng;
+            float total = 0.0f;
+            for (int64_t g = 0; g < ng; g++) {
+                int32_t q9w, q9x;
+                if (orc_e4m3fn_q9(srow[g], &q9w)) {
+                    rc = 1;
+                    break;
+                }
+                orc_e4m3fn_q9(xsrow[g], &q9x);       /* produced by the quantizer: never NaN */
+                int64_t dot = 0;
+                for (int64_t k = g * 16; k < g * 16 + 16; k++) {
+                    unsigned cw = (k % 2 == 0) ? (wrow[k / 2] & 15u) : (wrow[k / 2] >> 4);
+                    unsigned cx = (k % 2 == 0) ? (xrow[k / 2] & 15u) : (xrow[k / 2] >> 4);
+                    dot += (int64_t)orc_e2m1_q1(cw) * (int64_t)orc_e2m1_q1(cx);
+                }
+                int64_t T = dot * (int64_t)q9w * (int64_t)q9x;
+                float c = fmaf((float)T, 0x1p-20f, 0.0f);
+                c = fmaf(c, t->scale2, 0.0f);
+                c = fmaf(c, G, 0.0f);
+                total = fmaf(1.0f, c, total);
+            }
+            y[m * nrows + i] = orc_f16_round(total);
+        }
+    }
+    free(xp);
+    free(xs);
+    return rc;
 }
