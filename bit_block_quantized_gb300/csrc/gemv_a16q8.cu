@@ -24,7 +24,7 @@
 //     bit (selector bit 3 = the E2M1 sign bit) turns the negative codes into
 //     0x00, and the same PRMT on code^8 yields the magnitudes of exactly the
 //     negative codes, so dot = dp4a(pos, q8) - dp4a(neg, q8) with no per-byte
-//     negation.  Eleven instructions per eight weights.
+//     negation.  Fourteen instructions per eight weights.
 //   * The per-group 32-bit dots times q9 (a 256-entry shared table) add in
 //     64-bit; the eight lanes of a block reduce by shuffles, and the block
 //     contributions enter the row total in block order.
