@@ -217,16 +217,35 @@ gemv_a16q8_kernel(const uint8_t *__restrict__ W, const uint8_t *__restrict__ S, 
     }
 }
 
+constexpr int A8_SMEM_LIMIT = 200 * 1024;   // the budget gemv_a16q8_chunk keeps every launch within
+
+// Per device: the shared-memory attribute is set once (to the budget) and the
+// blocks per SM of the latest shared-memory size are kept, so a repeated call
+// costs no driver queries.  Any grid >= 1 gives the same result (grid-stride).
 template <int MT, typename XT>
 cudaError_t launch_mt(const Tensor &t, const XT *x, float *y, int mrows, cudaStream_t s) {
     const int64_t smem = a8_smem_bytes(MT, t.K);
     auto kern = gemv_a16q8_kernel<MT, XT>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    static bool attr_set[64] = {};
+    static int64_t cached_smem[64] = {};
+    static int cached_per_sm[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    int per_sm = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, A8_THREADS, (size_t)smem);
-    if (e != cudaSuccess) return e;
-    if (per_sm < 1) return cudaErrorInvalidConfiguration;
+    dev &= 63;
+    if (!attr_set[dev]) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, A8_SMEM_LIMIT);
+        if (e != cudaSuccess) return e;
+        attr_set[dev] = true;
+    }
+    int per_sm = cached_per_sm[dev];
+    if (cached_smem[dev] != smem || per_sm < 1) {
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, A8_THREADS, (size_t)smem);
+        if (e != cudaSuccess) return e;
+        if (per_sm < 1) return cudaErrorInvalidConfiguration;
+        cached_smem[dev] = smem;
+        cached_per_sm[dev] = per_sm;
+    }
     const int64_t want = (t.N + A8_WARPS - 1) / A8_WARPS;
     const int64_t grid = std::min<int64_t>(want, (int64_t)per_sm * sm_count());
     kern<<<(unsigned)grid, A8_THREADS, (size_t)smem, s>>>(t.w, t.scales, t.scale2, x, y, mrows, t.N, t.K);
@@ -247,7 +266,7 @@ cudaError_t launch_chunk(const Tensor &t, const XT *x, float *y, int mrows, cuda
 // serves it (MT = 8, 4, 2 or 1 rows) fits the shared-memory budget; 0 if not
 // even one row of quantized activations fits.
 int gemv_a16q8_chunk(int64_t M, int64_t K) {
-    const int64_t limit = 200 * 1024;
+    const int64_t limit = A8_SMEM_LIMIT;
     for (int rows = (int)std::min<int64_t>(M, 8); rows >= 1; rows--) {
         const int mt = rows > 4 ? 8 : rows > 2 ? 4 : rows;
         if (a8_smem_bytes(mt, K) <= limit) return rows;
