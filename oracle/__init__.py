@@ -9,7 +9,8 @@ the repack-through-the-logical-matrix route in ``packing.py`` (numpy).
 Citations name the source page and its section:
   [FBTC] "Four Bits, Three Contracts"; [W4K] "Why 4-Bit Quantization Is King";
   [BPA] "Bit Packing Architecture, in depth"; [MUS7] "Muser book, Chapter 7".
-Every function is pinned by ``tests/test_oracle_pins.py``.
+Every function is pinned by ``tests/test_oracle_pins.py`` or, for the A16-Q8,
+W4A8, W4A4 and quantizer functions, by ``tests/test_oracle_{a16q8,w4a8,w4a4,quantize}.py``.
 """
 from __future__ import annotations
 

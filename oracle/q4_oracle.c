@@ -17,8 +17,10 @@
  *   [BPA]   "Bit Packing Architecture, in depth" (aicassindra.com quant_bit_packing)
  *   [MUS7]  "Muser book, Chapter 7 - NVFP4: the native lane" (highperformanceailab.com)
  *
- * Parity status: every function below is pinned by tests/test_oracle_pins.py
- * (printed worked examples, library decoders, brute force, invariants).
+ * Parity status: every function below is pinned (printed worked examples,
+ * library decoders, brute force, invariants) by tests/test_oracle_pins.py, and
+ * the A16-Q8, W4A8, W4A4 and quantizer functions by test_oracle_a16q8.py,
+ * test_oracle_w4a8.py, test_oracle_w4a4.py and test_oracle_quantize.py.
  */
 #include <math.h>
 #include <stdint.h>
