@@ -72,3 +72,13 @@ def test_reference_arm_rank0_only():
     assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["value"] == line["value"]
     assert line["e2e"] == {"value": line["value"], "unit": "GB/s", "h2d_bytes_per_step": 0,
                            "d2h_bytes_per_step": 0}
+
+
+def test_cpu_baseline_rows_cover_every_timed_row():
+    """The CPU leg the bench runs beside the other rows: one entry per GEMV row
+    (the A16-Q8 lane included) plus the dequant, each with a positive rate."""
+    rows = bench.cpu_baseline_rows(rows_per_matrix=4)
+    names = [r["row"] for r in rows]
+    assert bench.A16Q8_ROW in names and "a6 dequant NVFP4 -> f32" in names
+    assert len(names) == len(bench.ORACLE_ROWS) + 2
+    assert all(r["GBps"] > 0 and r["seconds"] >= 0 for r in rows)
