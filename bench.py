@@ -317,6 +317,10 @@ def run_ours(args, rank, world):
                      else "fallback 6.8 TB/s",
                      "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": profiled_traffic(),
                      "kernel": DOMINANT, "algorithmic_bytes_per_launch": gate_up_bytes},
+        "tokens_equivalent_per_s": {"value": round(tokens_equivalent(ms / args.steps, world), 1),
+                                    "layers": LAYERS,
+                                    "note": "batch-1 decode of a model whose every layer is this MLP set, "
+                                            "weight streaming only"},
         "e2e": e2e,
         "gpu_launches": 2 * args.steps,
         "clocks": clk.summary(),
@@ -340,6 +344,15 @@ def max_over_ranks(value, world, device):
     t = torch.tensor([value], dtype=torch.float64, device=device)
     torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
     return float(t.item())
+
+
+LAYERS = 32   # decoder layers of the model whose every layer is this MLP set (the tokens-equivalent rate)
+
+
+def tokens_equivalent(ms_per_step, world, layers=LAYERS):
+    """Whole-job batch-1 tokens per second if every one of `layers` layers
+    streamed this set once per token: world / (layers x step time)."""
+    return world * 1000.0 / (layers * ms_per_step)
 
 
 def whole_job_gbps(world, bytes_per_step, steps, ms):

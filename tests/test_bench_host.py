@@ -82,3 +82,9 @@ def test_cpu_baseline_rows_cover_every_timed_row():
     assert bench.A16Q8_ROW in names and "a6 dequant NVFP4 -> f32" in names
     assert len(names) == len(bench.ORACLE_ROWS) + 2
     assert all(r["GBps"] > 0 and r["seconds"] >= 0 for r in rows)
+
+
+def test_tokens_equivalent_rate():
+    # 22.1 us per step, 32 layers: 1 / (32 * 22.1e-6) = 1414.03 tokens/s per replica
+    assert bench.tokens_equivalent(0.0221, 1) == pytest.approx(1414.03, abs=0.01)
+    assert bench.tokens_equivalent(0.0221, 8) == pytest.approx(8 * 1414.03, abs=0.1)
