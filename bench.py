@@ -47,8 +47,8 @@ PROFILED_SOURCES = ("bit_block_quantized_gb300/csrc/gemv_tma.cu", "bit_block_qua
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=100000)
-    ap.add_argument("--warmup", type=int, default=200)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=2000)
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
@@ -159,44 +159,42 @@ class ClockSampler:
 
 # ---------------------------------------------------------------- our arm
 
-def build_workload(torch, q4, synth):
-    """Host NVFP4 tensors of the set + device copies rotating past L2."""
-    host = []
-    for i, (name, N, K) in enumerate(SET):
-        layer = synth.make_layer("nvfp4", N, K, config=CONFIG_ID, matrix=i, row_scale=True)
-        xbits, _ = synth.draw_x(1, K, config=CONFIG_ID, matrix=0 if name in ("gate", "up") else i)
-        host.append((name, N, K, layer, xbits))
+def build_workload(torch, q4, synth, copies=None, distinct=False):
+    """Host NVFP4 tensors of the set + device copies rotating past L2.
+
+    ``copies`` None sizes the rotation to max(1 GiB, 4 x L2); ``distinct``
+    draws every copy from its own seeds (the parity test of the step uses it
+    to tell the copies apart; the bench's copies hold the same weights)."""
+    def draw(copy):
+        out = []
+        for i, (name, N, K) in enumerate(SET):
+            layer = synth.make_layer("nvfp4", N, K, config=CONFIG_ID, matrix=i + 10 * copy, row_scale=True)
+            xbits, _ = synth.draw_x(1, K, config=CONFIG_ID, matrix=0 if name in ("gate", "up") else i)
+            out.append((name, N, K, layer, xbits))
+        return out
+    host = draw(0)
     set_bytes = sum(q4.q4_packed_bytes("nvfp4", N, K) for _, N, K in SET)
     l2 = torch.cuda.get_device_properties(0).L2_cache_size
-    copies = int(np.ceil(max(1 << 30, 4 * l2) / set_bytes))
+    if copies is None:
+        copies = int(np.ceil(max(1 << 30, 4 * l2) / set_bytes))
+    hosts = [host] + [draw(c) if distinct else host for c in range(1, copies)]
     dev = []
     for c in range(copies):
         mats = []
-        for name, N, K, layer, xbits in host:
+        for name, N, K, layer, xbits in hosts[c]:
             w = torch.from_numpy(layer["w"]).cuda()
             s = torch.from_numpy(layer["scales"]).cuda()
             mats.append((name, N, K, w, s, layer["scale2"]))
         dev.append(mats)
     xs = [torch.from_numpy(h[4].view(np.int16)).cuda().view(torch.bfloat16) for h in host]
-    xs[1] = xs[0]                      # gate and up read the same activation vector
     xs[1] = xs[0]                                   # gate and up read the same activations
     ys = [torch.empty((1, N), dtype=torch.float32, device="cuda") for _, N, _ in SET]
-    return host, dev, xs, ys, set_bytes, copies, l2
+    return hosts, dev, xs, ys, set_bytes, copies, l2
 
 
-def run_ours(args, rank, world):
-    import torch
-
-    import bit_block_quantized_gb300 as q4
-    import synth
-    from bit_block_quantized_gb300 import build as q4build
-
-    q4build.build()
-    torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
-    host, dev, xs, ys, set_bytes, copies, l2 = build_workload(torch, q4, synth)
-    auxes = [q4.make_aux(scale2=h[3]["scale2"], fmt="nvfp4") for h in host]
-    stream = torch.cuda.Stream()
-
+def mlp_step_fns(q4, dev, auxes, xs, ys):
+    """The step's two calls on weight copy ``c``: q4_gemv_grouped(gate, up)
+    with the shared x, then q4_gemv(down), both on stream ``s``."""
     def gate_up(c, s):
         (_, N0, K0, w0, s0, _), (_, N1, K1, w1, s1, _) = dev[c][0], dev[c][1]
         q4.q4_gemv_grouped([("nvfp4", w0, s0, auxes[0], xs[0], ys[0], N0, K0),
@@ -209,8 +207,55 @@ def run_ours(args, rank, world):
     def step(c, s):
         gate_up(c, s)
         down(c, s)
+    return gate_up, down, step
 
-    # one graph per full rotation, plus single-step graphs for the remainder
+
+MAX_STEPS_PER_GRAPH = 2048
+
+
+def timed_graphs(torch, step, stream, steps, copies, cap=MAX_STEPS_PER_GRAPH):
+    """CUDA graphs that together run exactly ``steps`` steps, step i on copy
+    i % copies: one graph of all of them when steps <= cap (the usual case:
+    no graph boundary inside the timed region, so programmatic dependent
+    launch chains every launch to the next); otherwise a graph of a whole
+    number of rotations, replayed, plus one graph for the remainder.
+    Returns [(graph, replays)]."""
+    def capture(n):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(n):
+                step(i % copies, stream)
+        return g
+    if steps <= cap:
+        return [(capture(steps), 1)]
+    chunk = copies * max(1, cap // copies)
+    plan = [(capture(chunk), steps // chunk)]
+    if steps % chunk:
+        plan.append((capture(steps % chunk), 1))
+    return plan
+
+
+def replay(plan):
+    for g, n in plan:
+        for _ in range(n):
+            g.replay()
+
+
+def run_ours(args, rank, world):
+    import torch
+
+    import bit_block_quantized_gb300 as q4
+    import synth
+    from bit_block_quantized_gb300 import build as q4build
+
+    q4build.build()
+    torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+    hosts, dev, xs, ys, set_bytes, copies, l2 = build_workload(torch, q4, synth)
+    host = hosts[0]
+    auxes = [q4.make_aux(scale2=h[3]["scale2"], fmt="nvfp4") for h in host]
+    stream = torch.cuda.Stream()
+    gate_up, down, step = mlp_step_fns(q4, dev, auxes, xs, ys)
+
     with torch.cuda.stream(stream):
         for c in range(copies):
             step(c, stream)
@@ -219,16 +264,8 @@ def run_ours(args, rank, world):
         down(0, stream)
         path_down = q4.q4_last_gemv_path()
         torch.cuda.synchronize()
-        g_rot = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g_rot, stream=stream):
-            for c in range(copies):
-                step(c, stream)
-        g_one = []
-        for c in range(copies):
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g, stream=stream):
-                step(c, stream)
-            g_one.append(g)
+        warm = timed_graphs(torch, step, stream, max(args.warmup, 1), copies)
+        timed = timed_graphs(torch, step, stream, args.steps, copies)
         # per-launch graphs for the roofline of each launch
         g_kern = []
         for fn in (gate_up, down):
@@ -238,26 +275,21 @@ def run_ours(args, rank, world):
                     fn(c, stream)
             g_kern.append(g)
 
-    def run_steps(n):
-        full, rem = divmod(n, copies)
-        for _ in range(full):
-            g_rot.replay()
-        for c in range(rem):
-            g_one[c].replay()
-
     def barrier():
         if world > 1:
             torch.distributed.barrier()
 
     with torch.cuda.stream(stream):
-        run_steps(args.warmup)
+        replay(warm)
+        for g, _ in timed:           # uploads the timed graphs (untimed; their steps are extra warm-up)
+            g.replay()
         torch.cuda.synchronize()
         barrier()
         torch.cuda.synchronize()
         start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         with ClockSampler(torch.cuda.current_device()) as clk:
             start.record(stream)
-            run_steps(args.steps)
+            replay(timed)
             end.record(stream)
             torch.cuda.synchronize()
         barrier()
@@ -306,8 +338,11 @@ def run_ours(args, rank, world):
                    "y_bytes_per_step": y_bytes,
                    "l2": f"inputs larger than L2: {copies} rotating copies of the set = "
                          f"{copies * set_bytes / 1e9:.2f} GB (L2 {l2 / 1e6:.0f} MB)",
-                   "launch": "one CUDA graph per rotation; 2 launches per step: q4_gemv_grouped(gate, up) "
-                             "(shared x) then q4_gemv(down), chained by programmatic dependent launch",
+                   "launch": "2 launches per step: q4_gemv_grouped(gate, up) (shared x) then q4_gemv(down), "
+                             "chained by programmatic dependent launch; the timed steps are one CUDA graph "
+                             f"(up to {MAX_STEPS_PER_GRAPH} steps per graph), step i on weight copy i % copies",
+                   "warmup": "the --warmup steps as a graph, then one untimed replay of the timed graph "
+                             "(its upload)",
                    "parallelism": f"replicas x{world}"},
         "pct_of_hbm_peak": {"measured": round(value / world / peak, 4),
                             "nominal_7900": round(value / world / NOMINAL_HBM_GBS, 4)},
@@ -903,7 +938,6 @@ def main():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     if args.impl == "reference":
-        args.warmup = min(args.warmup, 3)
         line = run_reference(args, rank, world)
     else:
         if world > 1:

@@ -25,8 +25,6 @@ int sm_count() {
     return n;
 }
 
-namespace {
-
 bool known(q4_fmt f) { return f >= Q4_NVFP4 && f <= Q4_LOGICAL; }
 bool aligned16(const void *p) { return p && (((uintptr_t)p) & 15u) == 0; }
 bool kmajor_fmt(q4_fmt f) { return f == Q4_GPTQ || f == Q4_AWQ || f == Q4_LOGICAL; }
@@ -53,7 +51,7 @@ int check_dims(q4_fmt f, int64_t N, int64_t K, int group) {
 // Common checks for a packed weight tensor; fills `t`.  The NVFP4 scale2
 // check comes last so a caller that does not read scale2 may ignore it.
 int make_tensor(q4_fmt f, const void *W, const void *scales, const q4_aux *aux, int64_t N, int64_t K,
-                Tensor &t, bool need_scale2 = true) {
+                Tensor &t, bool need_scale2) {
     if (!known(f)) return Q4_EINVAL;
     const int group = group_of(aux);
     int rc = check_dims(f, N, K, group);
@@ -87,6 +85,8 @@ int make_tensor(q4_fmt f, const void *W, const void *scales, const q4_aux *aux, 
     }
     return Q4_OK;
 }
+
+namespace {
 
 q4_dtype default_x_dtype(q4_fmt f) { return (f == Q4_NVFP4 || f == Q4_MXFP4) ? Q4_DT_BF16 : Q4_DT_F32; }
 

@@ -196,6 +196,16 @@ struct Tensor {
 };
 
 int sm_count();
+// Host-side argument rules shared by every entry point (q4_api.cu): format
+// known, 16-byte alignment, and the shape rule of each format.
+bool known(q4_fmt f);
+bool aligned16(const void *p);
+int check_dims(q4_fmt f, int64_t N, int64_t K, int group);
+// Every check on a packed weight tensor, then fills `t`.  The NVFP4 scale2
+// check comes last (Q4_ESCALE2), so a caller that does not read scale2 may
+// ignore that status.
+int make_tensor(q4_fmt f, const void *W, const void *scales, const q4_aux *aux, int64_t N, int64_t K, Tensor &t,
+                bool need_scale2 = true);
 // Records, per host thread, which kernel family the latest q4_gemv /
 // q4_gemv_grouped call launched (read back by q4_last_gemv_path).
 void note_gemv_path(const char *name);

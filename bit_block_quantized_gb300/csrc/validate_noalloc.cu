@@ -102,9 +102,6 @@ cudaError_t scratch_for_current_device(unsigned long long **out) {
     return cudaSuccess;
 }
 
-bool known_fmt(q4_fmt f) { return f >= Q4_NVFP4 && f <= Q4_LOGICAL; }
-bool aligned16(const void *p) { return p && (((uintptr_t)p) & 15u) == 0; }
-
 }  // namespace
 }  // namespace q4
 
@@ -112,50 +109,22 @@ using namespace q4;
 
 extern "C" int q4_validate_noalloc(q4_fmt fmt, const void *W_packed, const void *scales, const q4_aux *aux,
                                    int64_t N, int64_t K, int64_t *bad_count, void *stream) {
-    // the same host-side checks as q4_validate
-    if (!known_fmt(fmt)) return Q4_EINVAL;
-    const int group = (aux && aux->group > 0) ? aux->group : 128;
-    if (N <= 0 || K <= 0) return Q4_EDIM;
+    // every host-side check of q4_validate (the same helper), then the scratch bound
+    Tensor t;
+    const int rc = make_tensor(fmt, W_packed, scales, aux, N, K, t);
+    if (rc && rc != Q4_ESCALE2) return rc;
     int64_t count;
     const uint8_t *p;
     switch (fmt) {
     case Q4_NVFP4:
-    case Q4_NVFP4_SPLITHALF:
-        if (K % 16) return Q4_EDIM;
-        count = N * (K / 16);
-        p = (const uint8_t *)scales;
-        break;
-    case Q4_MXFP4:
-        if (K % 32) return Q4_EDIM;
-        count = N * (K / 32);
-        p = (const uint8_t *)scales;
-        break;
-    case Q4_Q4K:
-        if (K % 256) return Q4_EDIM;
-        count = N * (K / 256) * 2;
-        p = (const uint8_t *)W_packed;
-        break;
-    case Q4_Q40:
-        if (K % 32) return Q4_EDIM;
-        count = N * (K / 32);
-        p = (const uint8_t *)W_packed;
-        break;
-    default:
-        if (K % group || N % 8 || (fmt == Q4_GPTQ && K % 8)) return Q4_EDIM;
-        if (!aux || !aux->zeros) return Q4_EINVAL;
-        count = (K / group) * N;
-        p = (const uint8_t *)scales;
-        break;
+    case Q4_NVFP4_SPLITHALF: count = N * (K / 16); p = t.scales; break;
+    case Q4_MXFP4: count = N * (K / 32); p = t.scales; break;
+    case Q4_Q4K: count = N * (K / 256) * 2; p = t.w; break;      // d and dmin of every super-block
+    case Q4_Q40: count = N * (K / 32); p = t.w; break;            // d of every block
+    default: count = (K / t.group) * N; p = t.scales; break;      // GPTQ / AWQ / logical fp16 scales
     }
-    if (!W_packed || !p) return Q4_EINVAL;
-    if (!aligned16(W_packed) || !aligned16(p)) return Q4_EALIGN;
     // the fixed scratch bounds the problem: at most MAX_CHUNKS chunks of CHUNK entries
     if (count > (int64_t)Q4_VALIDATE_NOALLOC_MAX_CHUNKS * CHUNK) return Q4_EDIM;
-    bool bad_scale2 = false;
-    if (fmt == Q4_NVFP4 || fmt == Q4_NVFP4_SPLITHALF) {
-        if (!aux) return Q4_EINVAL;
-        bad_scale2 = !(aux->scale2 > 0.0f) || !(aux->scale2 < INFINITY);
-    }
 
     unsigned long long *scratch = nullptr;
     if (scratch_for_current_device(&scratch) != cudaSuccess) return Q4_ECUDA;
@@ -170,5 +139,5 @@ extern "C" int q4_validate_noalloc(q4_fmt fmt, const void *W_packed, const void 
         return Q4_ECUDA;
     if (bad_count) *bad_count = (int64_t)total;
     if (total) return Q4_ENAN;
-    return bad_scale2 ? Q4_ESCALE2 : Q4_OK;
+    return rc;                        // Q4_OK, or Q4_ESCALE2 for a bad NVFP4 scale2
 }

@@ -160,9 +160,14 @@ int q4_gemv_grouped(const q4_gemv_desc *descs, int count, int64_t M, void *strea
  * between groups while the next group's weights are already streaming;
  * otherwise the groups are issued one after the other as q4_gemv_grouped.
  * sync: caller-owned device memory of 2 uint32 words, zero before its first
- * use and not written by the caller afterwards; the launch leaves it ready
- * for the next call (also across CUDA-graph replays).  Chains that may run
- * at the same time (other streams) need their own sync words.  May be NULL
+ * use and not written by the caller afterwards; a launch that completes
+ * without error leaves it ready for the next call (also across CUDA-graph
+ * replays).  A launch whose barrier gave up (q4_last_error() returns
+ * Q4_ETIMEOUT) leaves the count holding the CTAs that did arrive: the caller
+ * must then set both words to zero again (e.g. cudaMemsetAsync) before the
+ * next chain that uses them, or that chain may pass a barrier early or time
+ * out.  Chains that may run at the same time (other streams) need their own
+ * sync words.  May be NULL
  * when ngroups == 1.  Same checks, accuracy and stream semantics as
  * q4_gemv_grouped; if any member is rejected nothing is launched. */
 int q4_gemv_chain(const q4_gemv_desc *descs, const int *first, int ngroups, int64_t M, uint32_t *sync,

@@ -41,3 +41,17 @@ def within_tolerance(y_gpu, y_ref, bound):
     tol = oracle.gemv_tolerance(bound)
     err = np.abs(np.asarray(y_gpu, np.float64) - y_ref)
     return bool(np.all(err <= tol)), float(np.max(err / tol))
+
+
+def oracle_gemv_all_rows(t, xf, threads=None):
+    """oracle.gemv over every row, the rows split into chunks that run on
+    host threads (the C oracle releases the GIL); the per-row arithmetic is
+    the oracle's own, so the result is identical to one call."""
+    import os
+    from concurrent.futures import ThreadPoolExecutor
+
+    threads = threads or min(16, os.cpu_count() or 1)
+    chunks = np.array_split(np.arange(t.N), max(1, min(threads * 4, t.N)))
+    with ThreadPoolExecutor(threads) as ex:
+        parts = list(ex.map(lambda r: oracle.gemv(t, xf, rows=r), chunks))
+    return (np.concatenate([p[0] for p in parts], axis=1), np.concatenate([p[1] for p in parts], axis=1))

@@ -3,7 +3,7 @@
 Dequant and repack: bit-exact.  GEMV: |y_gpu - y_ref| <= 1e-5 * sum|w||x| + 1e-6
 against the oracle's f64 accumulation of the pinned weights.  Shapes span
 several tiles with ragged tails; the full-size workloads are checked on
-sampled rows.
+every row.
 """
 import numpy as np
 import pytest
@@ -12,7 +12,7 @@ import oracle
 import synth
 from oracle import packing
 
-from _helpers import aux_for, to_device, to_oracle, within_tolerance, x_device
+from _helpers import aux_for, oracle_gemv_all_rows, to_device, to_oracle, within_tolerance, x_device
 
 torch = pytest.importorskip("torch")
 q4 = pytest.importorskip("bit_block_quantized_gb300")
@@ -132,8 +132,10 @@ def check_gemv(layer, M, config=20, xdtype="bf16", rows=None):
     K = layer["K"]
     xbits, xf = synth.draw_x(M, K, config=config, matrix=5, dtype=xdtype)
     y = gpu_gemv(layer, x_device(xbits), M)
-    ref, bound = oracle.gemv(to_oracle(layer), xf, rows=rows)
-    if rows is not None:
+    if rows is None:
+        ref, bound = oracle_gemv_all_rows(to_oracle(layer), xf)
+    else:
+        ref, bound = oracle.gemv(to_oracle(layer), xf, rows=rows)
         y = y[:, rows]
     ok, worst = within_tolerance(y, ref, bound)
     assert ok, f"worst error / tolerance = {worst}"
@@ -343,7 +345,7 @@ def test_gemv_one_hot_gives_exact_column():
         assert np.array_equal(y, ref[:, k])      # exact; a -0.0 weight sums to +0.0
 
 
-# Full-size workloads (the decode-GEMV study's layer shapes), sampled rows.
+# Full-size workloads (the decode-GEMV study's layer shapes), every row.
 FULL = [
     ("nvfp4", 1024, 4096, dict(), 0),                        # NVFP4 1024 x 4096
     ("q4k", 4096, 4096, dict(), 1),                          # Q4_K 4096 x 4096
@@ -357,11 +359,11 @@ FULL = [
 
 
 @pytest.mark.parametrize("fmt,N,K,kw,config", FULL)
-def test_gemv_full_size_sampled_rows(fmt, N, K, kw, config):
+def test_gemv_full_size_every_row(fmt, N, K, kw, config):
     layer = synth.make_layer(fmt, N, K, config=config, matrix=0, **kw)
-    rows = np.unique(np.concatenate([[0, 1, N - 1], np.random.default_rng(config).integers(0, N, 40)]))
     for M in (1, 4):
-        check_gemv(layer, M, config=config, rows=rows)
+        for xdtype in ("bf16", "f32"):
+            check_gemv(layer, M, config=config, xdtype=xdtype)
 
 
 # ------------------------------------------------------------------ repack

@@ -88,3 +88,59 @@ def test_reading_the_generation_after_the_add_is_caught():
             rnd = random.Random(seed)
             words = {"count": 0, "gen": 0}
             run_launch(words, 4, barriers=3, rnd=rnd, read_after_add=True)
+
+
+def run_launch_with_abort(words, ctas, aborting, rnd):
+    """One launch with one barrier in which CTA `aborting` gives up before it
+    arrives (its own bounded wait ran out, or the abort flag was raised).
+    The others add, spin, and leave when their spin limit runs out: in the
+    model, when nothing else can move.  Returns the CTAs that left through
+    the timeout."""
+    state = {c: "start" for c in range(ctas) if c != aborting}
+    my_gen = {}
+    timed_out = set()
+    while state:
+        movable = [c for c, st in state.items() if not (st == "spin" and words["gen"] == my_gen[c])]
+        if not movable:                                       # every spinner's limit runs out
+            timed_out.update(state)
+            return timed_out
+        c = rnd.choice(movable)
+        st = state[c]
+        if st == "start":
+            my_gen[c] = words["gen"]
+            state[c] = "add"
+        elif st == "add":
+            old = words["count"]
+            words["count"] += 1
+            state[c] = "reset" if old == ctas - 1 else "spin"
+        elif st == "reset":
+            words["count"] = 0
+            state[c] = "bump"
+        elif st == "bump":
+            words["gen"] += 1
+            del state[c]
+        else:
+            del state[c]
+    return timed_out
+
+
+@pytest.mark.parametrize("ctas", [2, 3, 5])
+def test_an_aborted_barrier_leaves_the_words_dirty_until_the_caller_zeroes_them(ctas):
+    """After a Q4_ETIMEOUT the count holds the CTAs that did arrive, so a next
+    launch on the same words can release a barrier early, hang, or leave the
+    count non-zero again: the header therefore requires the caller to zero
+    both words after any Q4_ETIMEOUT.  Once zeroed, the words work again."""
+    wrong = 0
+    for seed in range(40):
+        rnd = random.Random(seed)
+        words = {"count": 0, "gen": 0}
+        run_launch(words, ctas, barriers=2, rnd=rnd)
+        timed_out = run_launch_with_abort(words, ctas, aborting=seed % ctas, rnd=rnd)
+        assert len(timed_out) == ctas - 1 and words["count"] == ctas - 1
+        try:
+            run_launch(dict(words), ctas, barriers=1, rnd=random.Random(seed))
+        except AssertionError:
+            wrong += 1
+        words = {"count": 0, "gen": 0}                        # the caller's re-zeroing
+        run_launch(words, ctas, barriers=2, rnd=rnd)
+    assert wrong > 0

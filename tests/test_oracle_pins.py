@@ -119,6 +119,42 @@ def test_nvfp4_fixture_row_bit_for_bit():
     assert same_f32(row[10:], g["extension"])
 
 
+def test_splithalf_group_bytes_pinned_by_hand():
+    """One 16-group whose lanes all carry distinct codes, written out byte by
+    byte from the split-half sentence: the split-half decoder must put low
+    nibbles in lanes 0-7 and high nibbles in lanes 8-15, and the plain NVFP4
+    decoder must read the same bytes as adjacent pairs."""
+    g = gold("lane_orders.json")["nvfp4_splithalf_group"]
+    payload = np.frombuffer(bytes.fromhex(g["bytes_hex"]), dtype=np.uint8).reshape(1, 8)
+    scales = np.array([[g["scale_byte"]]], np.uint8)
+    half = oracle.dequant(oracle.Tensor("nvfp4_splithalf", 1, 16, payload, scales, scale2=g["scale2"]))[0]
+    assert same_f32(half, g["splithalf_w_hat"])
+    pair = oracle.dequant(oracle.Tensor("nvfp4", 1, 16, payload, scales, scale2=g["scale2"]))[0]
+    assert same_f32(pair, g["adjacent_pair_w_hat"])
+    # the packer's split-half route reproduces the hand-written bytes
+    hw, _, _, _ = packing.repack("nvfp4", "nvfp4_splithalf", 1, 16,
+                                 packing.pack_nvfp4_codes(np.arange(16, dtype=np.uint8).reshape(1, 16)), scales)
+    assert bytes(np.asarray(hw, np.uint8).ravel()) == bytes.fromhex(g["bytes_hex"])
+
+
+def test_q40_block_bytes_pinned_by_hand():
+    """A Q4_0 block whose low and high nibbles differ in every byte, written
+    out from the page's byte rule: element j is the low nibble of byte j and
+    element j + 16 its high nibble."""
+    g = gold("lane_orders.json")["q4_0_block"]
+    blk = np.frombuffer(bytes.fromhex(g["block_hex"]), dtype=np.uint8).reshape(1, 18)
+    assert same_f32(oracle.dequant(oracle.Tensor("q40", 1, 32, blk))[0], g["w_hat"])
+    # the packer writes the same bytes from the codes and d
+    codes = np.array([[j for j in range(16)] + [15 - j for j in range(16)]], np.uint8)
+    packed = packing.pack_q40(codes, np.array([[0x3800]], np.uint16))
+    assert bytes(np.asarray(packed, np.uint8).ravel()) == bytes.fromhex(g["block_hex"])
+    # one-hot x picks single elements: x = e_j gives w_hat[j] exactly
+    for j in (0, 1, 15, 16, 17, 31):
+        x = np.zeros((1, 32), np.float32)
+        x[0, j] = 1.0
+        assert oracle.gemv(oracle.Tensor("q40", 1, 32, blk), x)[0][0, 0] == g["w_hat"][j]
+
+
 def test_fp4_small_examples():
     g = gold("worked_examples.json")["fp4_small"]
     inv = {oracle.e2m1(c): c for c in range(8)}
