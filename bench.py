@@ -192,17 +192,23 @@ def build_workload(torch, q4, synth, copies=None, distinct=False):
     return hosts, dev, xs, ys, set_bytes, copies, l2
 
 
+def mlp_auxes(q4, dev):
+    """One q4_aux per matrix of every copy (each carries its copy's scale2)."""
+    return [[q4.make_aux(scale2=m[5], fmt="nvfp4") for m in mats] for mats in dev]
+
+
 def mlp_step_fns(q4, dev, auxes, xs, ys):
     """The step's two calls on weight copy ``c``: q4_gemv_grouped(gate, up)
-    with the shared x, then q4_gemv(down), both on stream ``s``."""
+    with the shared x, then q4_gemv(down), both on stream ``s``.  ``auxes``
+    is :func:`mlp_auxes` of ``dev``."""
     def gate_up(c, s):
         (_, N0, K0, w0, s0, _), (_, N1, K1, w1, s1, _) = dev[c][0], dev[c][1]
-        q4.q4_gemv_grouped([("nvfp4", w0, s0, auxes[0], xs[0], ys[0], N0, K0),
-                            ("nvfp4", w1, s1, auxes[1], xs[1], ys[1], N1, K1)], 1, stream=s)
+        q4.q4_gemv_grouped([("nvfp4", w0, s0, auxes[c][0], xs[0], ys[0], N0, K0),
+                            ("nvfp4", w1, s1, auxes[c][1], xs[1], ys[1], N1, K1)], 1, stream=s)
 
     def down(c, s):
         _, N, K, w, sc, _ = dev[c][2]
-        q4.q4_gemv("nvfp4", w, sc, auxes[2], xs[2], ys[2], 1, N, K, stream=s)
+        q4.q4_gemv("nvfp4", w, sc, auxes[c][2], xs[2], ys[2], 1, N, K, stream=s)
 
     def step(c, s):
         gate_up(c, s)
@@ -252,7 +258,7 @@ def run_ours(args, rank, world):
     torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
     hosts, dev, xs, ys, set_bytes, copies, l2 = build_workload(torch, q4, synth)
     host = hosts[0]
-    auxes = [q4.make_aux(scale2=h[3]["scale2"], fmt="nvfp4") for h in host]
+    auxes = mlp_auxes(q4, dev)
     stream = torch.cuda.Stream()
     gate_up, down, step = mlp_step_fns(q4, dev, auxes, xs, ys)
 
@@ -420,9 +426,9 @@ def run_e2e(args, torch, q4, dev, auxes, host, stream):
     def one(c):
         x_d.copy_(x_h, non_blocking=True)
         (_, N0, K0, w0, s0, _), (_, N1, K1, w1, s1, _), (_, N2, K2, w2, s2, _) = dev[c]
-        q4.q4_gemv_grouped([("nvfp4", w0, s0, auxes[0], xd_gu, ys_d[0], N0, K0),
-                            ("nvfp4", w1, s1, auxes[1], xd_gu, ys_d[1], N1, K1)], 1, stream=stream)
-        q4.q4_gemv("nvfp4", w2, s2, auxes[2], xd_dn, ys_d[2], 1, N2, K2, stream=stream)
+        q4.q4_gemv_grouped([("nvfp4", w0, s0, auxes[c][0], xd_gu, ys_d[0], N0, K0),
+                            ("nvfp4", w1, s1, auxes[c][1], xd_gu, ys_d[1], N1, K1)], 1, stream=stream)
+        q4.q4_gemv("nvfp4", w2, s2, auxes[c][2], xd_dn, ys_d[2], 1, N2, K2, stream=stream)
         y_h.copy_(y_d, non_blocking=True)
 
     with torch.cuda.stream(stream):

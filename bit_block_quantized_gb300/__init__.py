@@ -59,6 +59,12 @@ def lib() -> ctypes.CDLL:
         L.q4_gemv.argtypes = [I32, P, P, AUXP, P, P, I64, I64, I64, P]
         L.q4_dequant.argtypes = [I32, P, P, AUXP, P, I64, I64, P]
         L.q4_gemv_a16q8.argtypes = [P, P, AUXP, P, P, I64, I64, I64, P]
+        L.q4_gemv_q4k_q8.argtypes = [P, AUXP, P, P, I64, I64, I64, P]
+        L.q4_gemv_w4a4.argtypes = [P, P, AUXP, ctypes.c_float, P, P, I64, I64, I64, P]
+        L.q4_quantize_nvfp4.argtypes = [P, I32, P, P, P, I64, I64, P]
+        L.q4_pack_bits.argtypes = [P, I64, I32, P, P]
+        L.q4_unpack_bits.argtypes = [P, I64, I32, P, P]
+        L.q4_permute_k.argtypes = [P, I32, P, P, I64, I64, P]
         L.q4_gemv_grouped.argtypes = [ctypes.POINTER(GemvDesc), I32, I64, P]
         L.q4_gemv_chain.argtypes = [ctypes.POINTER(GemvDesc), ctypes.POINTER(ctypes.c_int), I32, I64, P, P]
         L.q4_gemv_chain.restype = ctypes.c_int
@@ -66,7 +72,9 @@ def lib() -> ctypes.CDLL:
         L.q4_validate.argtypes = [I32, P, P, AUXP, I64, I64, P, P]
         L.q4_validate_noalloc.argtypes = [I32, P, P, AUXP, I64, I64, ctypes.POINTER(ctypes.c_int64), P]
         L.q4_validate_noalloc.restype = ctypes.c_int
-        for f in ("q4_gemv", "q4_gemv_a16q8", "q4_gemv_grouped", "q4_dequant", "q4_repack", "q4_validate", "q4_last_error"):
+        for f in ("q4_gemv", "q4_gemv_a16q8", "q4_gemv_grouped", "q4_dequant", "q4_repack", "q4_validate",
+                  "q4_last_error", "q4_gemv_q4k_q8", "q4_gemv_w4a4", "q4_quantize_nvfp4", "q4_pack_bits", "q4_unpack_bits",
+                  "q4_permute_k"):
             getattr(L, f).restype = ctypes.c_int
         L.q4_last_error.argtypes = []
         L.q4_strerror.restype = ctypes.c_char_p
@@ -142,6 +150,54 @@ def q4_gemv_a16q8(W_packed, scales, aux, x, y, M, N, K, stream=None, check=True)
                              int(M), int(N), int(K), _stream(stream))
     if check:
         _check(rc, "q4_gemv_a16q8")
+    return rc
+
+
+def q4_gemv_q4k_q8(W_packed, aux, x, y, M, N, K, stream=None, check=True) -> int:
+    """The Q4_K x Q8 (W4A8) contraction: exact integer sub-block sums, f32 y."""
+    rc = lib().q4_gemv_q4k_q8(_ptr(W_packed), _aux_ref(aux), _ptr(x), _ptr(y), int(M), int(N), int(K),
+                              _stream(stream))
+    if check:
+        _check(rc, "q4_gemv_q4k_q8")
+    return rc
+
+
+def q4_gemv_w4a4(W_packed, scales, aux, input_scale_inv, x, y, M, N, K, stream=None, check=True) -> int:
+    """The integer-exact W4A4 contraction; y holds binary16 values widened to f32."""
+    rc = lib().q4_gemv_w4a4(_ptr(W_packed), _ptr(scales), _aux_ref(aux), float(input_scale_inv), _ptr(x), _ptr(y),
+                            int(M), int(N), int(K), _stream(stream))
+    if check:
+        _check(rc, "q4_gemv_w4a4")
+    return rc
+
+
+def q4_quantize_nvfp4(W, w_dtype, payload, scales, scale2, N, K, stream=None, check=True) -> int:
+    """NVFP4 quantization of W [N][K]; scale2 is a device f32 word."""
+    rc = lib().q4_quantize_nvfp4(_ptr(W), int(w_dtype), _ptr(payload), _ptr(scales), _ptr(scale2), int(N), int(K),
+                                 _stream(stream))
+    if check:
+        _check(rc, "q4_quantize_nvfp4")
+    return rc
+
+
+def q4_pack_bits(codes, n, bits, words, stream=None, check=True) -> int:
+    rc = lib().q4_pack_bits(_ptr(codes), int(n), int(bits), _ptr(words), _stream(stream))
+    if check:
+        _check(rc, "q4_pack_bits")
+    return rc
+
+
+def q4_unpack_bits(words, n, bits, codes, stream=None, check=True) -> int:
+    rc = lib().q4_unpack_bits(_ptr(words), int(n), int(bits), _ptr(codes), _stream(stream))
+    if check:
+        _check(rc, "q4_unpack_bits")
+    return rc
+
+
+def q4_permute_k(x, x_dtype, perm, out, M, K, stream=None, check=True) -> int:
+    rc = lib().q4_permute_k(_ptr(x), int(x_dtype), _ptr(perm), _ptr(out), int(M), int(K), _stream(stream))
+    if check:
+        _check(rc, "q4_permute_k")
     return rc
 
 

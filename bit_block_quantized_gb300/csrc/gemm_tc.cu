@@ -685,6 +685,7 @@ cudaError_t launch_gemm_tc(const Tensor &t, const void *x, q4_dtype x_dtype, flo
 
 int gemv_read_and_clear_error();
 int gemv_tma_read_and_clear_error();
+int pack_read_and_clear_error();
 
 int read_and_clear_device_error() {
     int v = 0;
@@ -694,7 +695,8 @@ int read_and_clear_device_error() {
     if (cudaMemcpyToSymbol(g_device_error, &zero, sizeof(zero)) != cudaSuccess) return Q4_ECUDA;
     const int g = gemv_read_and_clear_error();
     const int tm = gemv_tma_read_and_clear_error();
-    return v ? v : g ? g : tm;
+    const int pk = pack_read_and_clear_error();
+    return v ? v : g ? g : tm ? tm : pk;
 }
 
 }  // namespace q4

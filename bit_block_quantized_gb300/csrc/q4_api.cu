@@ -18,6 +18,20 @@ void note_gemv_path(const char *name) { g_last_path = name; }
 int gemv_a16q8_chunk(int64_t M, int64_t K);
 cudaError_t launch_gemv_a16q8(const Tensor &t, const void *x, q4_dtype xd, float *y, int64_t M, cudaStream_t s);
 
+// The Q4_K x Q8 (W4A8) contraction (gemv_q4k_q8.cu), the NVFP4 quantizer
+// (quantize.cu) and the b-bit packers (pack_bits.cu).
+int gemv_q4k_q8_chunk(int64_t M, int64_t K);
+cudaError_t launch_gemv_q4k_q8(const Tensor &t, const void *x, q4_dtype xd, float *y, int64_t M, cudaStream_t s);
+cudaError_t launch_quantize_nvfp4(const void *W, q4_dtype wd, int64_t N, int64_t K, uint8_t *payload, uint8_t *scales,
+                                  float *scale2, cudaStream_t s);
+int gemv_w4a4_chunk(int64_t M, int64_t K);
+cudaError_t launch_gemv_w4a4(const Tensor &t, float input_scale_inv, const void *x, q4_dtype xd, float *y, int64_t M,
+                             cudaStream_t s);
+cudaError_t launch_pack_bits(const uint8_t *codes, int64_t n, int bits, uint32_t *words, cudaStream_t s);
+cudaError_t launch_unpack_bits(const uint32_t *words, int64_t n, int bits, uint8_t *codes, cudaStream_t s);
+cudaError_t launch_permute_k(const void *x, q4_dtype xd, const int32_t *perm, void *out, int64_t M, int64_t K,
+                             cudaStream_t s);
+
 int sm_count() {
     int dev = 0, n = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 1;
@@ -221,6 +235,69 @@ int q4_gemv_a16q8(const void *W_packed, const void *scales, const q4_aux *aux, c
     if (xd != Q4_DT_F32 && xd != Q4_DT_BF16) return Q4_EINVAL;
     if (gemv_a16q8_chunk(M, K) == 0) return Q4_EDIM;
     return launch_gemv_a16q8(t, x, xd, y, M, (cudaStream_t)stream) == cudaSuccess ? Q4_OK : Q4_ECUDA;
+}
+
+int q4_gemv_q4k_q8(const void *W_packed, const q4_aux *aux, const void *x, float *y, int64_t M, int64_t N,
+                   int64_t K, void *stream) {
+    Tensor t;
+    const int rc = make_tensor(Q4_Q4K, W_packed, nullptr, aux, N, K, t);
+    if (rc) return rc;
+    if (M <= 0) return Q4_EDIM;
+    if (!x || !y) return Q4_EINVAL;
+    if (!aligned16(x) || !aligned16(y)) return Q4_EALIGN;
+    const q4_dtype xd = aux ? aux->x_dtype : Q4_DT_F32;
+    if (xd != Q4_DT_F32 && xd != Q4_DT_BF16) return Q4_EINVAL;
+    if (gemv_q4k_q8_chunk(M, K) == 0) return Q4_EDIM;
+    return launch_gemv_q4k_q8(t, x, xd, y, M, (cudaStream_t)stream) == cudaSuccess ? Q4_OK : Q4_ECUDA;
+}
+
+int q4_gemv_w4a4(const void *W_packed, const void *scales, const q4_aux *aux, float input_scale_inv, const void *x,
+                 float *y, int64_t M, int64_t N, int64_t K, void *stream) {
+    Tensor t;
+    const int rc = make_tensor(Q4_NVFP4, W_packed, scales, aux, N, K, t);   // aux is non-null past this
+    if (rc) return rc;
+    if (M <= 0 || K % 64) return Q4_EDIM;
+    if (!std::isfinite(input_scale_inv) || !(input_scale_inv > 0.0f)) return Q4_ESCALE2;
+    if (!x || !y) return Q4_EINVAL;
+    if (!aligned16(x) || !aligned16(y)) return Q4_EALIGN;
+    const q4_dtype xd = aux->x_dtype;
+    if (xd != Q4_DT_F32 && xd != Q4_DT_BF16) return Q4_EINVAL;
+    if (gemv_w4a4_chunk(M, K) == 0) return Q4_EDIM;
+    return launch_gemv_w4a4(t, input_scale_inv, x, xd, y, M, (cudaStream_t)stream) == cudaSuccess ? Q4_OK : Q4_ECUDA;
+}
+
+int q4_quantize_nvfp4(const void *W, q4_dtype w_dtype, void *payload, void *scales, float *scale2, int64_t N,
+                      int64_t K, void *stream) {
+    if (N <= 0 || K <= 0 || K % 16) return Q4_EDIM;
+    if (!W || !payload || !scales || !scale2) return Q4_EINVAL;
+    if (!aligned16(W) || !aligned16(payload) || !aligned16(scales) || (((uintptr_t)scale2) & 3u)) return Q4_EALIGN;
+    if (w_dtype != Q4_DT_F32 && w_dtype != Q4_DT_BF16) return Q4_EINVAL;
+    return launch_quantize_nvfp4(W, w_dtype, N, K, (uint8_t *)payload, (uint8_t *)scales, scale2,
+                                 (cudaStream_t)stream) == cudaSuccess ? Q4_OK : Q4_ECUDA;
+}
+
+int q4_pack_bits(const uint8_t *codes, int64_t n, int bits, uint32_t *words, void *stream) {
+    if (bits < 1 || bits > 8 || n <= 0 || (n * bits) % 32) return Q4_EDIM;
+    if (!codes || !words) return Q4_EINVAL;
+    if (!aligned16(codes) || !aligned16(words)) return Q4_EALIGN;
+    return launch_pack_bits(codes, n, bits, words, (cudaStream_t)stream) == cudaSuccess ? Q4_OK : Q4_ECUDA;
+}
+
+int q4_unpack_bits(const uint32_t *words, int64_t n, int bits, uint8_t *codes, void *stream) {
+    if (bits < 1 || bits > 8 || n <= 0 || (n * bits) % 32) return Q4_EDIM;
+    if (!codes || !words) return Q4_EINVAL;
+    if (!aligned16(codes) || !aligned16(words)) return Q4_EALIGN;
+    return launch_unpack_bits(words, n, bits, codes, (cudaStream_t)stream) == cudaSuccess ? Q4_OK : Q4_ECUDA;
+}
+
+int q4_permute_k(const void *x, q4_dtype x_dtype, const int32_t *perm, void *out, int64_t M, int64_t K,
+                 void *stream) {
+    if (M <= 0 || K <= 0) return Q4_EDIM;
+    if (!x || !perm || !out) return Q4_EINVAL;
+    if (!aligned16(x) || !aligned16(perm) || !aligned16(out)) return Q4_EALIGN;
+    if (x_dtype != Q4_DT_F32 && x_dtype != Q4_DT_BF16) return Q4_EINVAL;
+    if (x == out) return Q4_EINVAL;
+    return launch_permute_k(x, x_dtype, perm, out, M, K, (cudaStream_t)stream) == cudaSuccess ? Q4_OK : Q4_ECUDA;
 }
 
 int q4_dequant(q4_fmt fmt, const void *W_packed, const void *scales, const q4_aux *aux, void *out, int64_t N,

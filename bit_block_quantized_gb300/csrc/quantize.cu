@@ -1,0 +1,139 @@
+// quantize.cu -- NVFP4 quantization on the GPU (the write side of the format):
+// scale2 = amax(W) / (448 * 6) (1 for an all-zero W); per 16-value group the
+// E4M3FN scale byte = nearest-even of (amax_group / 6) / scale2, saturating at
+// 448; each code = nearest-even E2M1 of w / (dec(scale) * scale2), saturating
+// at 6, the sign kept (a negative value that rounds to 0 is code 8); every
+// step an IEEE f32 operation ([MUS7] 7.2 for the E2M1 rounding contract).
+//
+// Four stream-ordered steps, no allocation: the caller's scale2 word is
+// zeroed, holds the running amax (non-negative f32 bit patterns order like
+// unsigned integers, so atomicMax on the bits is a float max), is turned into
+// scale2 by one thread, and is read by the quantize kernel.  The quantize
+// kernel gives each thread one 16-value group: 64 (f32) or 32 (bf16)
+// contiguous input bytes, 8 payload bytes and one scale byte out.
+#include <algorithm>
+
+#include "q4_internal.cuh"
+
+namespace q4 {
+namespace {
+
+template <typename WT> __device__ __forceinline__ float wload(const WT *p, int64_t i);
+template <> __device__ __forceinline__ float wload<float>(const float *p, int64_t i) { return p[i]; }
+template <> __device__ __forceinline__ float wload<__nv_bfloat16>(const __nv_bfloat16 *p, int64_t i) {
+    return __bfloat162float(p[i]);
+}
+
+template <typename WT>
+__global__ void amax_kernel(const WT *__restrict__ W, int64_t n, unsigned *amax_bits) {
+    float m = 0.0f;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
+        m = fmaxf(m, fabsf(wload(W, i)));
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+    if ((threadIdx.x & 31) == 0) atomicMax(amax_bits, __float_as_uint(m));
+}
+
+__global__ void scale2_kernel(float *s2) {
+    const float amax = *s2;
+    *s2 = amax > 0.0f ? __fdiv_rn(amax, 2688.0f) : 1.0f;
+}
+
+// E4M3FN byte -> value (finite bytes), exact in f32.
+__device__ __forceinline__ float e4m3_value(uint32_t b) {
+    const uint32_t e = (b >> 3) & 15u, f = b & 7u;
+    const float mag = e == 0 ? (float)f * 0x1p-9f : __uint_as_float(((e + 120u) << 23) | (f << 20));
+    return (b & 0x80u) ? -mag : mag;
+}
+
+// Nearest-even E4M3FN byte of a >= 0 (finite), saturating at 448 (0x7e).
+// Values of binade [2^e, 2^(e+1)) sit on a grid of 2^(e-3) for e >= -6, and
+// below 2^-6 on the subnormal grid 2^-9; the scaled quotient is exact, so
+// rintf (ties to even) makes the one rounding, and a carry into the next
+// binade lands on its first grid point.
+__device__ __forceinline__ uint32_t e4m3_round(float a) {
+    if (a >= 448.0f) return 0x7eu;
+    if (a < 0x1p-6f) {
+        const uint32_t q = (uint32_t)rintf(a * 512.0f);           // exact scaling; 8 = 2^-6 rolls into 0x08
+        return q;
+    }
+    const int e = (int)((__float_as_uint(a) >> 23) & 255u) - 127;   // a in [2^e, 2^(e+1)), e in -6..8
+    const float m = rintf(__fmul_rn(a, __uint_as_float((uint32_t)(127 - e + 3) << 23)));   // in [8, 16]
+    uint32_t mi = (uint32_t)m, ee = (uint32_t)(e + 7);
+    if (mi == 16u) { mi = 8u; ee += 1u; }
+    const uint32_t b = (ee << 3) | (mi - 8u);
+    return b > 0x7eu ? 0x7eu : b;
+}
+
+// Nearest-even E2M1 code of r (ModelOpt's midpoints), saturating at 6, sign kept.
+__device__ __forceinline__ uint32_t e2m1_round(float r) {
+    const float a = fabsf(r);
+    uint32_t c;
+    if (a <= 0.25f) c = 0;          // 0.25 -> 0 (even)
+    else if (a < 0.75f) c = 1;      // 0.5
+    else if (a <= 1.25f) c = 2;     // 0.75, 1.25 -> 1 (even)
+    else if (a < 1.75f) c = 3;      // 1.5
+    else if (a <= 2.5f) c = 4;      // 1.75, 2.5 -> 2
+    else if (a < 3.5f) c = 5;       // 3
+    else if (a <= 5.0f) c = 6;      // 3.5, 5 -> 4
+    else c = 7;                     // 6 and above
+    return c | (signbit(r) ? 8u : 0u);
+}
+
+template <typename WT>
+__global__ void quantize_nvfp4_kernel(const WT *__restrict__ W, int64_t N, int64_t K, const float *s2p,
+                                      uint8_t *__restrict__ payload, uint8_t *__restrict__ scales) {
+    const float scale2 = *s2p;
+    const int64_t groups = N * (K / 16);
+    for (int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; g < groups; g += (int64_t)gridDim.x * blockDim.x) {
+        float w[16];
+#pragma unroll
+        for (int i = 0; i < 16; i++) w[i] = wload(W, g * 16 + i);
+        float amax_g = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 16; i++) amax_g = fmaxf(amax_g, fabsf(w[i]));
+        const float sv = __fdiv_rn(__fdiv_rn(amax_g, 6.0f), scale2);
+        const uint32_t sb = e4m3_round(sv);
+        const float denom = __fmul_rn(e4m3_value(sb), scale2);
+        uint32_t lo = 0u, hi = 0u;
+        if (denom > 0.0f) {
+#pragma unroll
+            for (int i = 0; i < 16; i++) {
+                const uint32_t c = e2m1_round(__fdiv_rn(w[i], denom));
+                if (i < 8) lo |= c << (4 * i);
+                else hi |= c << (4 * (i - 8));
+            }
+        }
+        *reinterpret_cast<uint2 *>(payload + g * 8) = make_uint2(lo, hi);
+        scales[g] = (uint8_t)sb;
+    }
+}
+
+template <typename WT>
+cudaError_t launch_quantize_t(const WT *W, int64_t N, int64_t K, uint8_t *payload, uint8_t *scales, float *scale2,
+                              cudaStream_t s) {
+    cudaError_t e = cudaMemsetAsync(scale2, 0, sizeof(float), s);
+    if (e != cudaSuccess) return e;
+    const int sms = sm_count();
+    const int64_t n = N * K;
+    const int64_t grid_a = std::min<int64_t>((n + 255) / 256, (int64_t)sms * 8);
+    amax_kernel<WT><<<(unsigned)grid_a, 256, 0, s>>>(W, n, reinterpret_cast<unsigned *>(scale2));
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    scale2_kernel<<<1, 1, 0, s>>>(scale2);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    const int64_t groups = N * (K / 16);
+    const int64_t grid_q = std::min<int64_t>((groups + 255) / 256, (int64_t)sms * 16);
+    quantize_nvfp4_kernel<WT><<<(unsigned)grid_q, 256, 0, s>>>(W, N, K, scale2, payload, scales);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_quantize_nvfp4(const void *W, q4_dtype wd, int64_t N, int64_t K, uint8_t *payload, uint8_t *scales,
+                                  float *scale2, cudaStream_t s) {
+    if (wd == Q4_DT_BF16)
+        return launch_quantize_t(reinterpret_cast<const __nv_bfloat16 *>(W), N, K, payload, scales, scale2, s);
+    return launch_quantize_t(reinterpret_cast<const float *>(W), N, K, payload, scales, scale2, s);
+}
+
+}  // namespace q4

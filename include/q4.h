@@ -197,6 +197,85 @@ int q4_gemv_chain(const q4_gemv_desc *descs, const int *first, int ngroups, int6
 int q4_gemv_a16q8(const void *W_packed, const void *scales, const q4_aux *aux, const void *x, float *y,
                   int64_t M, int64_t N, int64_t K, void *stream);
 
+/* The Q4_K x Q8 (W4A8) contraction ([W4K] section 7: the W4A8 extension of
+ * the section 4 Q4_K sub-block example, and the route of Q4_K weights against
+ * 8-bit activation blocks): y[M][N] f32 from Q4_K weights (layout as Q4_Q4K;
+ * aux may be NULL) and activations x[M][K] (aux->x_dtype, default f32).
+ *   1. Activations go to the per-256 signed 8-bit grid of q4_gemv_a16q8
+ *      (signed first maximum m, iscale = -127/m, codes nearest-even of
+ *      x*iscale capped at 127, block scale 1/iscale); each 32-value
+ *      sub-block's code sum is kept.
+ *   2. Per output row and super-block, I1 = sum_j sc_j * sum q*q8 and
+ *      I2 = sum_j m_j * (code sum of sub-block j) are exact integers.
+ *   3. In f32 and in this order: v = d*float(I1) - dmin*float(I2), then
+ *      c = v * block scale, then total += c over the super-blocks in order.
+ * The page gives the algebra and the order of the steps in words; the
+ * roundings above are this library's reading.  Bit-reproducible across
+ * runs, batch sizes and devices.  K % 256 == 0 (Q4_EDIM otherwise); x must be
+ * finite.  Up to 8 activation rows per launch in a 200 KiB shared-memory
+ * budget; larger M runs as several launches.  Allocates nothing;
+ * asynchronous on `stream`. */
+int q4_gemv_q4k_q8(const void *W_packed, const q4_aux *aux, const void *x, float *y, int64_t M, int64_t N,
+                   int64_t K, void *stream);
+
+/* The W4A4 contraction ([MUS7] 7.4.3): NVFP4 weights (layout as Q4_NVFP4;
+ * aux->scale2 required) against activations x[M][K] (aux->x_dtype bf16 or
+ * f32) that are themselves quantized to NVFP4 in 16-value groups.
+ *   1. Activation tensor scale G = 1 / input_scale_inv (finite, > 0;
+ *      Q4_ESCALE2 otherwise).  Each group takes the weights' own rule: E4M3
+ *      scale = nearest-even of (amax/6)/G saturating at 448, codes =
+ *      nearest-even E2M1 of x/(scale*G) (the midpoints of q4_quantize_nvfp4).
+ *   2. Per output row and group, T_g = q9(weight scale) * q9(activation
+ *      scale) * sum q1(w code) * q1(x code) is an exact 64-bit integer (q1:
+ *      E2M1 in halves, q9: E4M3FN in units of 2^-9; denominator 2^-20).
+ *   3. In group order, in f32: c = fma(float(T_g), 2^-20, 0); c = fma(c,
+ *      scale2, 0); c = fma(c, G, 0); total = fma(1, c, total).  y = total
+ *      rounded to binary16, stored widened to f32.
+ * The section names the encodings, the integer product and the factors; the
+ * per-group order of step 3 is this library's reading.  Bit-reproducible
+ * across runs, batch sizes and devices.  K % 64 == 0; x finite.  Up to 8
+ * activation rows per launch in a 200 KiB shared-memory budget.  Allocates
+ * nothing; asynchronous on `stream`. */
+int q4_gemv_w4a4(const void *W_packed, const void *scales, const q4_aux *aux, float input_scale_inv, const void *x,
+                 float *y, int64_t M, int64_t N, int64_t K, void *stream);
+
+/* NVFP4 quantization on the GPU, the write side of the format ([MUS7] 7.2):
+ * W[N][K] (w_dtype f32 or bf16, finite) -> payload u8 [N][K/2] (even k in the
+ * low nibble), E4M3FN scale bytes u8 [N][K/16] and the tensor scale.
+ *   scale2 = amax(W) / (448 * 6) in f32 (1 if W is all zero), written to the
+ *            DEVICE f32 word *scale2 (4-byte aligned; it holds the running
+ *            maximum during the call, so nothing is allocated);
+ *   per 16-value group: scale byte = nearest-even E4M3FN of
+ *            (amax_group / 6) / scale2, saturating at 448 (never 0x7f);
+ *   codes = nearest-even E2M1 of w / (dec(scale) * scale2), ties to the even
+ *            code at the midpoints 0.25, 0.75, 1.25, 1.75, 2.5, 3.5 and 5,
+ *            saturating at 6, the sign kept (a negative value that rounds to
+ *            zero is code 8); a group whose scale decodes to 0 is all code 0.
+ * Every step is one IEEE f32 operation, so the result is bit-exact with the
+ * definition.  K % 16 == 0.  Four stream-ordered launches; asynchronous on
+ * `stream`. */
+int q4_quantize_nvfp4(const void *W, q4_dtype w_dtype, void *payload, void *scales, float *scale2, int64_t N,
+                      int64_t K, void *stream);
+
+/* b-bit code streams ([BPA] "The packing arithmetic" and "Odd widths: 3-bit,
+ * 2-bit and 6-bit"): code i (the low `bits` bits of codes[i], u8) occupies
+ * bits [i*bits, (i+1)*bits) of one little-endian bit stream cut into 32-bit
+ * words, so 3-, 5-, 6- and 7-bit codes may straddle two words.
+ * q4_pack_bits writes words[n*bits/32]; q4_unpack_bits is its inverse.
+ * 1 <= bits <= 8 and n * bits % 32 == 0 (Q4_EDIM otherwise).  Bit-exact;
+ * asynchronous on `stream`. */
+int q4_pack_bits(const uint8_t *codes, int64_t n, int bits, uint32_t *words, void *stream);
+int q4_unpack_bits(const uint32_t *words, int64_t n, int bits, uint8_t *codes, void *stream);
+
+/* The activation side of an act-order repack ([BPA] "Repacking between
+ * formats": the weights' K permutation must be applied to the activations):
+ * out[m][k] = x[m][perm[k]] for x[M][K] (x_dtype f32 or bf16), with perm the
+ * perm_out of q4_repack (the source row of each target row).  out must not
+ * alias x.  An index outside [0, K) is not read: that element becomes 0 and
+ * q4_last_error() reports Q4_ERANGE.  Asynchronous on `stream`. */
+int q4_permute_k(const void *x, q4_dtype x_dtype, const int32_t *perm, void *out, int64_t M, int64_t K,
+                 void *stream);
+
 /* out[N][K] = w_hat, f32 or bf16 per aux->out_dtype, by the pinned per-format
  * rule ([MUS7] 7.2 for NVFP4; the per-format sections cited above).  Bit-exact
  * with the definition.  Asynchronous on `stream`. */
@@ -252,7 +331,8 @@ int q4_validate_noalloc(q4_fmt fmt, const void *W_packed, const void *scales, co
                         int64_t N, int64_t K, int64_t *bad_count, void *stream);
 
 /* Sticky device-side error of the current device (e.g. Q4_ETIMEOUT from a
- * bounded mbarrier wait in the tensor-core kernel); reading it clears it.
+ * bounded mbarrier wait in the tensor-core kernel, Q4_ERANGE from
+ * q4_permute_k); reading it clears it.
  * Synchronizes the device. */
 int q4_last_error(void);
 
@@ -260,7 +340,8 @@ int q4_last_error(void);
  * q4_gemv_grouped or q4_gemv_chain launched ("gemv_tma", "gemv_tma_group",
  * "gemv_tma_chain", "gemm_tc", "gemv_mma", "gemv_mma_group", "gemv_mma_q4k",
  * "gemv_mma_q40", "gemv_mma_gptq", "gemv_rows_tma", "gemv_rows_m1",
- * "gemv_general", "gemv_kmajor"; "gemv_a16q8" after q4_gemv_a16q8; "" before
+ * "gemv_general", "gemv_kmajor"; "gemv_a16q8" after q4_gemv_a16q8,
+ * "gemv_q4k_q8" after q4_gemv_q4k_q8, "gemv_w4a4" after q4_gemv_w4a4; "" before
  * the first call).  A diagnostic with no counterpart in the pages: it lets a
  * caller (and the tests) confirm which path a shape takes.  Static storage. */
 const char *q4_last_gemv_path(void);

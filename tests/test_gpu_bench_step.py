@@ -26,7 +26,8 @@ def step_setup():
     from bit_block_quantized_gb300 import build
     build.build()
     hosts, dev, xs, ys, set_bytes, copies, _ = bench.build_workload(torch, q4, synth, copies=2, distinct=True)
-    auxes = [q4.make_aux(scale2=h[3]["scale2"], fmt="nvfp4") for h in hosts[0]]
+    auxes = bench.mlp_auxes(q4, dev)
+    assert auxes[0][0].scale2 != auxes[1][0].scale2              # the copies really differ
     refs = []
     for host in hosts:
         per = []
