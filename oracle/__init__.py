@@ -10,7 +10,8 @@ Citations name the source page and its section:
   [FBTC] "Four Bits, Three Contracts"; [W4K] "Why 4-Bit Quantization Is King";
   [BPA] "Bit Packing Architecture, in depth"; [MUS7] "Muser book, Chapter 7".
 Every function is pinned by ``tests/test_oracle_pins.py`` or, for the A16-Q8,
-W4A8, W4A4 and quantizer functions, by ``tests/test_oracle_{a16q8,w4a8,w4a4,quantize}.py``.
+W4A8, W4A4 and quantizer functions, by ``tests/test_oracle_{a16q8,w4a8,w4a4,quantize}.py``
+(the Q4_K fit by ``tests/test_oracle_quantize_q4k.py``).
 """
 from __future__ import annotations
 
@@ -108,6 +109,10 @@ def _load():
                                                ctypes.c_void_p, ctypes.POINTER(ctypes.c_float)]
             lib.orc_gemv_q4k_q8_rows.argtypes = [ctypes.POINTER(_Tensor), ctypes.c_void_p, ctypes.c_int64,
                                                  ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p]
+            lib.orc_f16_bits.restype = ctypes.c_uint16
+            lib.orc_f16_bits.argtypes = [ctypes.c_float]
+            lib.orc_quantize_q4k.restype = None
+            lib.orc_quantize_q4k.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p]
             _lib = lib
     return _lib
 
@@ -393,3 +398,21 @@ def gemv_w4a4(t: Tensor, x: np.ndarray, input_scale_inv: float, rows=None) -> np
     if rc:
         raise OracleError("out of memory")
     return y
+
+
+# ------------------------------------------------------------ the Q4_K fit
+
+def f16_bits(v: float) -> int:
+    """binary16 encoding of f32 v rounded to nearest, ties to even."""
+    return int(_load().orc_f16_bits(float(v)))
+
+
+def quantize_q4k(W: np.ndarray) -> np.ndarray:
+    """Q4_K super-blocks u8 [N][K/256][144] of f32 W [N][K] by the per-sub-block
+    min/max fit of q4_oracle.c (orc_quantize_q4k)."""
+    W = np.ascontiguousarray(W, dtype=np.float32)
+    N, K = W.shape
+    assert K % 256 == 0
+    out = np.empty((N, K // 256, 144), dtype=np.uint8)
+    _load().orc_quantize_q4k(W.ctypes.data, N, K, out.ctypes.data)
+    return out

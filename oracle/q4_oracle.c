@@ -746,3 +746,95 @@ int orc_gemv_w4a4_rows(const orc_tensor *t, const float *x, int64_t M, float inp
     free(xs);
     return rc;
 }
+
+/* ------------------------------------------------ the Q4_K fit (write side) */
+
+/* binary16 bit pattern of f32 f rounded to nearest, ties to even (the value
+ * is orc_f16_round's; this returns its encoding). */
+uint16_t orc_f16_bits(float f)
+{
+    float r = orc_f16_round(f);
+    uint16_t sign = signbit(r) ? 0x8000u : 0u;
+    double a = fabs((double)r);
+    if (isnan(r))
+        return 0x7e00u;
+    if (isinf(r))
+        return sign | 0x7c00u;
+    if (a == 0.0)
+        return sign;
+    int ex;
+    frexp(a, &ex);
+    int E = ex - 1;
+    if (E < -14)                                  /* subnormal: a multiple of 2^-24 */
+        return sign | (uint16_t)nearbyint(a / ldexp(1.0, -24));
+    return sign | (uint16_t)((E + 15) << 10) | (uint16_t)(nearbyint(a / ldexp(1.0, E - 10)) - 1024.0);
+}
+
+/* Q4_K super-blocks of W [N][K] (f32, finite, K % 256 == 0) by a per-sub-block
+ * min/max fit.  The pages give the decode, w = d*s_j*q - dmin*m_j ([FBTC]
+ * sections 5-6, [W4K] section 4), but no fitting recipe; this one is the
+ * plainest that the decode supports, every step one f32 operation:
+ *   per sub-block j of 32:  lo_j = min(0, min w),  scale_j = (max w - lo_j) / 15,
+ *                           min_j = -lo_j;
+ *   d = fp16(max_j scale_j / 63),  dmin = fp16(max_j min_j / 63)  (nearest even);
+ *   s_j = clamp(rint(scale_j / d), 0, 63) and m_j = clamp(rint(min_j / dmin), 0, 63)
+ *         (0 when the divisor is 0);
+ *   q = clamp(rint((w + dmin*m_j) / (d*s_j)), 0, 15)  (0 when d*s_j is 0);
+ * rint rounds half to even.  The 12 metadata bytes are the inverse of the
+ * decode's unpacking: for j < 4, B[j] = s_j | (s_{j+4} >> 4) << 6 and
+ * B[j+4] = m_j | (m_{j+4} >> 4) << 6; B[j+8] = (s_{j+4} & 15) | (m_{j+4} & 15) << 4.
+ * Code byte 32c + l holds k = 64c + l (low nibble) and 64c + 32 + l (high). */
+void orc_quantize_q4k(const float *W, int64_t N, int64_t K, uint8_t *out)
+{
+    const int64_t nb = K / 256;
+    for (int64_t n = 0; n < N; n++)
+        for (int64_t b = 0; b < nb; b++) {
+            const float *w = W + n * K + b * 256;
+            uint8_t *blk = out + (n * nb + b) * 144;
+            float scale[8], mins[8], smax = 0.0f, mmax = 0.0f;
+            for (int j = 0; j < 8; j++) {
+                float lo = 0.0f, hi = w[32 * j];
+                for (int i = 0; i < 32; i++) {
+                    if (w[32 * j + i] < lo)
+                        lo = w[32 * j + i];
+                    if (w[32 * j + i] > hi)
+                        hi = w[32 * j + i];
+                }
+                scale[j] = (hi - lo) / 15.0f;
+                mins[j] = -lo;
+                if (scale[j] > smax)
+                    smax = scale[j];
+                if (mins[j] > mmax)
+                    mmax = mins[j];
+            }
+            const uint16_t dbits = orc_f16_bits(smax / 63.0f), mbits = orc_f16_bits(mmax / 63.0f);
+            const float d = orc_half(dbits), dmin = orc_half(mbits);
+            unsigned s[8], m[8];
+            for (int j = 0; j < 8; j++) {
+                float a = d > 0.0f ? nearbyintf(scale[j] / d) : 0.0f;
+                float c = dmin > 0.0f ? nearbyintf(mins[j] / dmin) : 0.0f;
+                s[j] = a < 0.0f ? 0u : a > 63.0f ? 63u : (unsigned)a;
+                m[j] = c < 0.0f ? 0u : c > 63.0f ? 63u : (unsigned)c;
+            }
+            blk[0] = (uint8_t)(dbits & 0xffu);
+            blk[1] = (uint8_t)(dbits >> 8);
+            blk[2] = (uint8_t)(mbits & 0xffu);
+            blk[3] = (uint8_t)(mbits >> 8);
+            for (int j = 0; j < 4; j++) {
+                blk[4 + j] = (uint8_t)(s[j] | ((s[j + 4] >> 4) << 6));
+                blk[4 + j + 4] = (uint8_t)(m[j] | ((m[j + 4] >> 4) << 6));
+                blk[4 + j + 8] = (uint8_t)((s[j + 4] & 15u) | ((m[j + 4] & 15u) << 4));
+            }
+            uint8_t q[256];
+            for (int j = 0; j < 8; j++) {
+                const float step = d * (float)s[j], off = dmin * (float)m[j];
+                for (int i = 0; i < 32; i++) {
+                    float v = step > 0.0f ? nearbyintf((w[32 * j + i] + off) / step) : 0.0f;
+                    q[32 * j + i] = (uint8_t)(v < 0.0f ? 0 : v > 15.0f ? 15 : (int)v);
+                }
+            }
+            for (int c = 0; c < 4; c++)
+                for (int l = 0; l < 32; l++)
+                    blk[16 + 32 * c + l] = (uint8_t)(q[64 * c + l] | (q[64 * c + 32 + l] << 4));
+        }
+}
