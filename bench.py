@@ -68,6 +68,10 @@ def parse():
                     help="replays of each per-launch graph for the roofline timing (0: about 2000 launches)")
     ap.add_argument("--no-rows", action="store_true",
                     help="skip the per-row measurements of the other formats, dequant and repack")
+    ap.add_argument("--fp4-slices", default="", choices=["", "gate_up", "all"],
+                    help="run those launches of the step on the FP4 tensor-core kernel (Q4_FLAG_FP4_SLICES)")
+    ap.add_argument("--no-sweep", action="store_true",
+                    help="skip the Llama-7B layer-set sweep over every format at batch 1, 4 and 8")
     return ap.parse_args()
 
 
@@ -192,9 +196,14 @@ def build_workload(torch, q4, synth, copies=None, distinct=False):
     return hosts, dev, xs, ys, set_bytes, copies, l2
 
 
-def mlp_auxes(q4, dev):
-    """One q4_aux per matrix of every copy (each carries its copy's scale2)."""
-    return [[q4.make_aux(scale2=m[5], fmt="nvfp4") for m in mats] for mats in dev]
+def mlp_auxes(q4, dev, fp4_slices=""):
+    """One q4_aux per matrix of every copy (each carries its copy's scale2).
+    ``fp4_slices``: "gate_up" or "all" sets Q4_FLAG_FP4_SLICES on those
+    matrices (the FP4 tensor-core kernel instead of the TMA-fed one)."""
+    def flags(i):
+        on = fp4_slices == "all" or (fp4_slices == "gate_up" and i < 2)
+        return q4.Q4_FLAG_FP4_SLICES if on else 0
+    return [[q4.make_aux(scale2=m[5], fmt="nvfp4", flags=flags(i)) for i, m in enumerate(mats)] for mats in dev]
 
 
 def mlp_step_fns(q4, dev, auxes, xs, ys):
@@ -258,7 +267,7 @@ def run_ours(args, rank, world):
     torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
     hosts, dev, xs, ys, set_bytes, copies, l2 = build_workload(torch, q4, synth)
     host = hosts[0]
-    auxes = mlp_auxes(q4, dev)
+    auxes = mlp_auxes(q4, dev, args.fp4_slices)
     stream = torch.cuda.Stream()
     gate_up, down, step = mlp_step_fns(q4, dev, auxes, xs, ys)
 
@@ -338,7 +347,7 @@ def run_ours(args, rank, world):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic (seeded W ~ N(0,0.02) x U(0.5,2) rows, NVFP4 per 16; x ~ N(0,1) bf16)",
-        "config": {"workload": WORKLOAD, "batch": 1,
+        "config": {"workload": WORKLOAD, "batch": 1, "fp4_slices": args.fp4_slices or "off",
                    "matrices": [f"{n} {N}x{K}" for n, N, K in SET],
                    "weight_bytes_per_step": set_bytes, "x_bytes_per_step": x_bytes,
                    "y_bytes_per_step": y_bytes,
@@ -370,6 +379,8 @@ def run_ours(args, rank, world):
         line["small_m_gemm"] = small_m_gemm(torch, q4, synth, peak)
     if not args.no_rows:
         line["other_rows"] = other_rows(torch, q4, synth, peak)
+    if not args.no_sweep:
+        line["layer_set_sweep"] = layer_set_sweep(torch, q4, peak)
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args.cpu_seconds, host)
         if not args.no_rows:
@@ -490,7 +501,8 @@ def cpu_baseline(seconds, host=None, sample_rows=None):
         frac = min(1.0, seconds / (per_row_4096 * (14336 + 14336 + 4096 * 3.5)))
     else:
         frac = sample_rows
-    bytes_done, t_total, rows_done = 0, 0.0, 0
+    bytes_done, t_total, t_all, rows_done = 0, 0.0, 0.0, 0
+    cores = os.cpu_count() or 1
     for name, N, K, layer, xbits in host:
         rows = np.arange(max(1, int(N * frac)))
         T = oracle.Tensor("nvfp4", N, K, layer["w"], layer["scales"], scale2=layer["scale2"])
@@ -498,11 +510,27 @@ def cpu_baseline(seconds, host=None, sample_rows=None):
         t0 = time.perf_counter()
         oracle.gemv(T, xf, rows=rows)
         t_total += time.perf_counter() - t0
+        t0 = time.perf_counter()
+        oracle_rows_all_cores(oracle, T, xf, rows, cores)
+        t_all += time.perf_counter() - t0
         bytes_done += rows.size * (K // 2 + K // 16)
         rows_done += rows.size
     return {"value": round(bytes_done / t_total / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
             "sample": f"{rows_done} rows ({frac:.3%}) of each of the 3 set matrices, batch 1, "
-                      f"{t_total:.1f} s", "cpu": _cpu_name()}
+                      f"{t_total:.1f} s", "cpu": _cpu_name(),
+            "all_cores": {"value": round(bytes_done / t_all / 1e9, 4), "unit": "GB/s", "cores": cores,
+                          "kind": "oracle", "sample": f"the same rows split over {cores} host threads, {t_all:.1f} s",
+                          "nproc": cores}}
+
+
+def oracle_rows_all_cores(oracle, T, xf, rows, cores):
+    """The oracle GEMV over ``rows``, split into chunks that run on ``cores``
+    host threads (the C oracle releases the interpreter lock; each row's
+    arithmetic is the oracle's own)."""
+    from concurrent.futures import ThreadPoolExecutor
+    chunks = np.array_split(np.asarray(rows), max(1, min(len(rows), cores * 4)))
+    with ThreadPoolExecutor(cores) as ex:
+        return list(ex.map(lambda r: oracle.gemv(T, xf, rows=r), chunks))
 
 
 A16Q8_ROW = "f2 NVFP4 A16-Q8 GEMV (integer-exact)"
@@ -815,6 +843,126 @@ def other_rows(torch, q4, synth, peak_hbm):
     torch.cuda.empty_cache()
     return {"l2": "each launch reads a different weight copy; working set >= 256 MB per row",
             "peak_hbm_GBps": peak_hbm, "entries": rows}
+
+
+LLAMA7B_SET = [("q", 4096, 4096), ("k", 4096, 4096), ("v", 4096, 4096), ("o", 4096, 4096),
+               ("gate", 11008, 4096), ("up", 11008, 4096), ("down", 4096, 11008)]
+SWEEP_FORMATS = ("nvfp4", "mxfp4", "q4k", "q40", "gptq", "awq")
+SWEEP_BATCHES = (1, 4, 8)
+
+
+def _device_layer(torch, q4, fmt, N, K, gen):
+    """One seeded synthetic tensor of ``fmt`` built on the device.  NVFP4 and
+    Q4_K: W ~ N(0, 0.02) x U(0.5, 2) per row, quantized by the library's GPU
+    quantizers.  The other formats: seeded random codes with valid scales of
+    the same magnitude (their decode cost does not depend on the values)."""
+    dev = "cuda"
+    d = {"scales": None, "zeros": None, "scale2": 1.0}
+    if fmt in ("nvfp4", "q4k"):
+        W = torch.randn((N, K), generator=gen, device=dev) * 0.02
+        W *= torch.rand((N, 1), generator=gen, device=dev) * 1.5 + 0.5
+        if fmt == "nvfp4":
+            d["w"] = torch.empty((N, K // 2), dtype=torch.uint8, device=dev)
+            d["scales"] = torch.empty((N, K // 16), dtype=torch.uint8, device=dev)
+            s2 = torch.empty(4, dtype=torch.float32, device=dev)
+            q4.q4_quantize_nvfp4(W, q4.Q4_DT_F32, d["w"], d["scales"], s2, N, K)
+            d["scale2"] = float(s2[0].item())
+        else:
+            d["w"] = torch.empty((N, K // 256, 144), dtype=torch.uint8, device=dev)
+            q4.q4_quantize_q4k(W, q4.Q4_DT_F32, d["w"], N, K)
+        del W
+        return d
+    rnd = lambda shape, hi: torch.randint(0, hi, shape, generator=gen, device=dev)  # noqa: E731
+    if fmt == "mxfp4":
+        d["w"] = rnd((N, K // 2), 256).to(torch.uint8)
+        d["scales"] = (rnd((N, K // 32), 3) + 120).to(torch.uint8)            # 2^-7 .. 2^-5
+    elif fmt == "q40":
+        blk = rnd((N, K // 32, 18), 256).to(torch.uint8)
+        blk[:, :, 0:2] = torch.tensor([0x20, 0x1A], dtype=torch.uint8, device=dev)   # fp16 d = 0.0025
+        d["w"] = blk
+    else:
+        G = K // 128
+        words = (N, K // 8) if fmt == "gptq" else (K, N // 8)
+        w = rnd(words, 1 << 16) | (rnd(words, 1 << 16) << 16)
+        d["w"] = (w.t().contiguous() if fmt == "gptq" else w).to(torch.int32)
+        d["scales"] = torch.full((G, N), 0x1A20, dtype=torch.int16, device=dev)
+        z = torch.zeros((G, N // 8), dtype=torch.int64, device=dev)
+        for j in range(8):
+            z |= rnd((G, N // 8), 15) << (4 * j)                             # stored zeros 0..14
+        d["zeros"] = z.to(torch.int32)
+    return d
+
+
+def layer_set_sweep(torch, q4, peak_hbm, batches=SWEEP_BATCHES, formats=SWEEP_FORMATS):
+    """The Llama-7B-shaped decoder layer set (q/k/v/o 4096x4096, gate/up
+    11008x4096, down 4096x11008) in every format at batch 1, 4 and 8: one
+    pass = the seven GEMVs of one layer as four calls (q4_gemv_grouped of
+    q, k, v and of gate, up, which read the same x; o and down alone),
+    captured as one CUDA graph over rotating weight copies (> 4 x L2).  Reported per
+    (format, batch): microseconds per layer, weight bytes per second, the
+    fraction of the measured HBM peak, the tokens-equivalent rate of a
+    32-layer model (weight streaming only) and the kernel paths."""
+    l2 = torch.cuda.get_device_properties(0).L2_cache_size
+    stream = torch.cuda.Stream()
+    gen = torch.Generator(device="cuda")
+    out = []
+    for fi, fmt in enumerate(formats):
+        gen.manual_seed(3000 + fi)
+        base = [_device_layer(torch, q4, fmt, N, K, gen) for _, N, K in LLAMA7B_SET]
+        layer_bytes = sum(q4.q4_packed_bytes(fmt, N, K) for _, N, K in LLAMA7B_SET)
+        ncopies = max(2, -(-4 * l2 // layer_bytes))
+        copies = [base] + [[{k: (v.clone() if torch.is_tensor(v) else v) for k, v in m.items()} for m in base]
+                           for _ in range(ncopies - 1)]
+        for M in batches:
+            xdt = torch.bfloat16 if fmt in ("nvfp4", "mxfp4") else torch.float32
+            xs = {K: torch.randn((M, K), generator=gen, device="cuda").to(xdt) for K in (4096, 11008)}
+            ys = [torch.empty((M, N), device="cuda") for _, N, _ in LLAMA7B_SET]
+            auxes = [[q4.make_aux(scale2=m["scale2"], zeros=m["zeros"], group=128, x_dtype=xdt, fmt=fmt) for m in c]
+                     for c in copies]
+            paths = []
+
+            def layer(c, s, record=False):
+                # q, k, v read one x and gate, up another: one grouped call each; o and down alone
+                for grp in ((0, 1, 2), (3,), (4, 5), (6,)):
+                    q4.q4_gemv_grouped([(fmt, copies[c][i]["w"], copies[c][i]["scales"], auxes[c][i],
+                                         xs[LLAMA7B_SET[i][2]], ys[i], LLAMA7B_SET[i][1], LLAMA7B_SET[i][2])
+                                        for i in grp], M, stream=s)
+                    if record:
+                        paths.append(q4.q4_last_gemv_path())
+            with torch.cuda.stream(stream):
+                layer(0, stream, record=True)
+                torch.cuda.synchronize()
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=stream):
+                    for c in range(ncopies):
+                        layer(c, stream)
+                for _ in range(3):
+                    g.replay()
+                torch.cuda.synchronize()
+                reps = 10
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                for _ in range(reps):
+                    g.replay()
+                b.record(stream)
+                torch.cuda.synchronize()
+            us = a.elapsed_time(b) * 1e3 / (reps * ncopies)
+            gbs = layer_bytes / us / 1e3
+            out.append({"fmt": fmt, "M": M, "us_per_layer": round(us, 2), "GBps": round(gbs, 1),
+                        "frac_hbm": round(gbs / peak_hbm, 4),
+                        "tokens_equivalent_per_s": round(1e6 / (LAYERS * us), 1),
+                        "paths": sorted(set(paths))})
+            del xs, ys
+        del copies, base
+        torch.cuda.empty_cache()
+    return {"workload": "Llama-7B layer set: q, k, v, o 4096x4096; gate, up 11008x4096; down 4096x11008",
+            "formats": list(formats), "batches": list(batches),
+            "data": "seeded on the device: NVFP4 and Q4_K quantized from W ~ N(0,0.02) x U(0.5,2) rows by the "
+                    "library's GPU quantizers; MXFP4, Q4_0, GPTQ, AWQ as seeded random codes with valid scales",
+            "l2": "each layer pass reads a different weight copy (copies > 4 x L2)",
+            "launch": "per layer: q4_gemv_grouped(q, k, v), q4_gemv(o), q4_gemv_grouped(gate, up), q4_gemv(down); "
+                      "one CUDA graph over the copies",
+            "peak_hbm_GBps": peak_hbm, "entries": out}
 
 
 def ncu_gemm_case(spec):

@@ -27,7 +27,10 @@ class Aux(ctypes.Structure):
     """Mirror of ``q4_aux``."""
     _fields_ = [("scale2", ctypes.c_float), ("zeros", ctypes.c_void_p),
                 ("g_idx", ctypes.c_void_p), ("group", ctypes.c_int32),
-                ("x_dtype", ctypes.c_int), ("out_dtype", ctypes.c_int)]
+                ("x_dtype", ctypes.c_int), ("out_dtype", ctypes.c_int), ("flags", ctypes.c_uint32)]
+
+
+Q4_FLAG_FP4_SLICES = 1
 
 
 class GemvDesc(ctypes.Structure):
@@ -61,7 +64,10 @@ def lib() -> ctypes.CDLL:
         L.q4_gemv_a16q8.argtypes = [P, P, AUXP, P, P, I64, I64, I64, P]
         L.q4_gemv_q4k_q8.argtypes = [P, AUXP, P, P, I64, I64, I64, P]
         L.q4_gemv_w4a4.argtypes = [P, P, AUXP, ctypes.c_float, P, P, I64, I64, I64, P]
+        L.q4_gemv_w4a4_tc.argtypes = [P, P, AUXP, P, P, ctypes.c_float, P, I64, I64, I64, P]
+        L.q4_quantize_nvfp4_scaled.argtypes = [P, I32, ctypes.c_float, P, P, I64, I64, P]
         L.q4_quantize_nvfp4.argtypes = [P, I32, P, P, P, I64, I64, P]
+        L.q4_quantize_q4k.argtypes = [P, I32, P, I64, I64, P]
         L.q4_pack_bits.argtypes = [P, I64, I32, P, P]
         L.q4_unpack_bits.argtypes = [P, I64, I32, P, P]
         L.q4_permute_k.argtypes = [P, I32, P, P, I64, I64, P]
@@ -73,10 +79,12 @@ def lib() -> ctypes.CDLL:
         L.q4_validate_noalloc.argtypes = [I32, P, P, AUXP, I64, I64, ctypes.POINTER(ctypes.c_int64), P]
         L.q4_validate_noalloc.restype = ctypes.c_int
         for f in ("q4_gemv", "q4_gemv_a16q8", "q4_gemv_grouped", "q4_dequant", "q4_repack", "q4_validate",
-                  "q4_last_error", "q4_gemv_q4k_q8", "q4_gemv_w4a4", "q4_quantize_nvfp4", "q4_pack_bits", "q4_unpack_bits",
+                  "q4_last_error", "q4_gemv_q4k_q8", "q4_gemv_w4a4", "q4_gemv_w4a4_tc", "q4_quantize_nvfp4_scaled", "q4_quantize_nvfp4", "q4_quantize_q4k", "q4_pack_bits", "q4_unpack_bits",
                   "q4_permute_k"):
             getattr(L, f).restype = ctypes.c_int
         L.q4_last_error.argtypes = []
+        L.q4_set_wait_limit.argtypes = [I64]
+        L.q4_set_wait_limit.restype = ctypes.c_int
         L.q4_strerror.restype = ctypes.c_char_p
         L.q4_last_gemv_path.restype = ctypes.c_char_p
         L.q4_strerror.argtypes = [I32]
@@ -110,7 +118,7 @@ def _fmt(fmt):
 
 
 def make_aux(scale2=0.0, zeros=None, g_idx=None, group=128, x_dtype=None, out_dtype=Q4_DT_F32,
-             fmt=None):
+             fmt=None, flags=0):
     """Build a ``q4_aux``.  x_dtype None picks the format default (bf16 for
     NVFP4/MXFP4, f32 otherwise); it may also be a torch dtype."""
     if x_dtype is None:
@@ -121,7 +129,7 @@ def make_aux(scale2=0.0, zeros=None, g_idx=None, group=128, x_dtype=None, out_dt
     if not isinstance(out_dtype, int):
         import torch
         out_dtype = Q4_DT_BF16 if out_dtype == torch.bfloat16 else Q4_DT_F32
-    return Aux(float(scale2), _ptr(zeros), _ptr(g_idx), int(group), int(x_dtype), int(out_dtype))
+    return Aux(float(scale2), _ptr(zeros), _ptr(g_idx), int(group), int(x_dtype), int(out_dtype), int(flags))
 
 
 def _aux_ref(aux):
@@ -171,12 +179,38 @@ def q4_gemv_w4a4(W_packed, scales, aux, input_scale_inv, x, y, M, N, K, stream=N
     return rc
 
 
+def q4_gemv_w4a4_tc(W_packed, scales, aux, xq, xs, x_scale2, y, M, N, K, stream=None, check=True) -> int:
+    """W4A4 on the native block-scaled FP4 tensor cores; activations already NVFP4."""
+    rc = lib().q4_gemv_w4a4_tc(_ptr(W_packed), _ptr(scales), _aux_ref(aux), _ptr(xq), _ptr(xs), float(x_scale2),
+                               _ptr(y), int(M), int(N), int(K), _stream(stream))
+    if check:
+        _check(rc, "q4_gemv_w4a4_tc")
+    return rc
+
+
+def q4_quantize_nvfp4_scaled(x, x_dtype, scale2, payload, scales, M, K, stream=None, check=True) -> int:
+    """NVFP4 groups of x [M][K] for a given tensor scale."""
+    rc = lib().q4_quantize_nvfp4_scaled(_ptr(x), int(x_dtype), float(scale2), _ptr(payload), _ptr(scales), int(M),
+                                        int(K), _stream(stream))
+    if check:
+        _check(rc, "q4_quantize_nvfp4_scaled")
+    return rc
+
+
 def q4_quantize_nvfp4(W, w_dtype, payload, scales, scale2, N, K, stream=None, check=True) -> int:
     """NVFP4 quantization of W [N][K]; scale2 is a device f32 word."""
     rc = lib().q4_quantize_nvfp4(_ptr(W), int(w_dtype), _ptr(payload), _ptr(scales), _ptr(scale2), int(N), int(K),
                                  _stream(stream))
     if check:
         _check(rc, "q4_quantize_nvfp4")
+    return rc
+
+
+def q4_quantize_q4k(W, w_dtype, out, N, K, stream=None, check=True) -> int:
+    """Q4_K super-blocks [N][K/256][144] of W [N][K] by the min/max fit."""
+    rc = lib().q4_quantize_q4k(_ptr(W), int(w_dtype), _ptr(out), int(N), int(K), _stream(stream))
+    if check:
+        _check(rc, "q4_quantize_q4k")
     return rc
 
 
@@ -267,6 +301,12 @@ def q4_validate_noalloc(fmt, W_packed, scales, aux, N, K, stream=None):
 
 def q4_last_error() -> int:
     return lib().q4_last_error()
+
+
+def q4_set_wait_limit(cycles: int) -> int:
+    """Bounded-wait limit (SM clocks) of the TMA-fed kernels on the current
+    device; cycles <= 0 restores the default (~1 s)."""
+    return lib().q4_set_wait_limit(int(cycles))
 
 
 def q4_last_gemv_path() -> str:

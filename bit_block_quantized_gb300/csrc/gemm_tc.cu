@@ -686,6 +686,7 @@ cudaError_t launch_gemm_tc(const Tensor &t, const void *x, q4_dtype x_dtype, flo
 int gemv_read_and_clear_error();
 int gemv_tma_read_and_clear_error();
 int pack_read_and_clear_error();
+int fp4tc_read_and_clear_error();
 
 int read_and_clear_device_error() {
     int v = 0;
@@ -696,7 +697,8 @@ int read_and_clear_device_error() {
     const int g = gemv_read_and_clear_error();
     const int tm = gemv_tma_read_and_clear_error();
     const int pk = pack_read_and_clear_error();
-    return v ? v : g ? g : tm ? tm : pk;
+    const int f4 = fp4tc_read_and_clear_error();
+    return v ? v : g ? g : tm ? tm : pk ? pk : f4;
 }
 
 }  // namespace q4

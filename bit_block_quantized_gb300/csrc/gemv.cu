@@ -879,6 +879,16 @@ int gemv_read_and_clear_error() {
 
 cudaError_t launch_gemv(const Tensor &t, const void *x, q4_dtype x_dtype, float *y, int64_t M,
                         cudaStream_t s) {
+    // Batch 5..8 whose staged x does not fit the tensor-core kernels' shared
+    // memory (large K) runs as two launches of at most 4 rows: the weights
+    // stream twice, far faster than the general kernel.
+    if (M > 4 && M <= 8 && !gemv_gptq_eligible(t, M) && !gemv_blk_eligible(t, M) &&
+        (gemv_gptq_eligible(t, 4) || gemv_blk_eligible(t, 4))) {
+        const int64_t xe = x_dtype == Q4_DT_BF16 ? 2 : 4;
+        const cudaError_t e = launch_gemv(t, x, x_dtype, y, 4, s);
+        if (e != cudaSuccess) return e;
+        return launch_gemv(t, static_cast<const char *>(x) + 4 * t.K * xe, x_dtype, y + 4 * t.N, M - 4, s);
+    }
     if (gemv_gptq_eligible(t, M)) {
         note_gemv_path("gemv_mma_gptq");
         return launch_gemv_gptq(t, x, x_dtype, y, M, s);

@@ -45,6 +45,9 @@ namespace q4 {
 namespace {
 
 __device__ int g_tma_error;
+// Limit of the role waits and the chain's grid barrier, in SM clocks (the
+// final drain of bulk copies keeps its own full limit).
+__device__ long long g_tma_wait_limit = 1LL << 31;
 
 #ifndef Q4_TMA_SMEM_KB
 #define Q4_TMA_SMEM_KB 112
@@ -150,15 +153,16 @@ __device__ __forceinline__ void tma_2d(uint32_t dst, const CUtensorMap *map, int
         : "memory");
 }
 
-// Bounded mbarrier wait: gives up after ~1 s of SM clocks (records
-// Q4_ETIMEOUT and raises the CTA's abort flag), or at once when another role
-// has raised the flag.
+// Bounded mbarrier wait: gives up after the role-wait limit (~1 s of SM
+// clocks unless q4_set_wait_limit shortened it; records Q4_ETIMEOUT and
+// raises the CTA's abort flag), or at once when another role has raised the
+// flag.
 __device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity, volatile int *abort_flag) {
     if (mbar_try_wait(bar, parity)) return true;
-    const long long t0 = clock64();
+    const long long t0 = clock64(), limit = g_tma_wait_limit;
     while (!mbar_try_wait(bar, parity)) {
         if (*abort_flag) return false;
-        if (clock64() - t0 > (1LL << 31)) {
+        if (clock64() - t0 > limit) {
             atomicExch(&g_tma_error, Q4_ETIMEOUT);
             *abort_flag = 1;
             return false;
@@ -188,10 +192,10 @@ __device__ void grid_barrier(unsigned *sync, volatile int *abort_flag) {
         atomicAdd(gen, 1u);
         return;
     }
-    const long long t0 = clock64();
+    const long long t0 = clock64(), limit = g_tma_wait_limit;
     while (ld_acquire(gen) == my_gen) {
         if (*abort_flag) return;
-        if (clock64() - t0 > (1LL << 31)) {
+        if (clock64() - t0 > limit) {
             atomicExch(&g_tma_error, Q4_ETIMEOUT);
             *abort_flag = 1;
             return;
@@ -712,6 +716,10 @@ int gemv_tma_read_and_clear_error() {
     if (cudaMemcpyFromSymbol(&v, g_tma_error, sizeof(v)) != cudaSuccess) return Q4_ECUDA;
     if (cudaMemcpyToSymbol(g_tma_error, &zero, sizeof(zero)) != cudaSuccess) return Q4_ECUDA;
     return v;
+}
+
+int gemv_tma_set_wait_limit(long long cycles) {
+    return cudaMemcpyToSymbol(g_tma_wait_limit, &cycles, sizeof(cycles)) == cudaSuccess ? Q4_OK : Q4_ECUDA;
 }
 
 }  // namespace q4

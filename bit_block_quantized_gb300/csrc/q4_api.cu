@@ -27,10 +27,17 @@ cudaError_t launch_quantize_nvfp4(const void *W, q4_dtype wd, int64_t N, int64_t
 int gemv_w4a4_chunk(int64_t M, int64_t K);
 cudaError_t launch_gemv_w4a4(const Tensor &t, float input_scale_inv, const void *x, q4_dtype xd, float *y, int64_t M,
                              cudaStream_t s);
+cudaError_t launch_quantize_q4k(const void *W, q4_dtype wd, int64_t N, int64_t K, uint8_t *out, cudaStream_t s);
+cudaError_t launch_quantize_nvfp4_scaled(const void *W, q4_dtype wd, int64_t N, int64_t K, float scale2,
+                                         uint8_t *payload, uint8_t *scales, cudaStream_t s);
 cudaError_t launch_pack_bits(const uint8_t *codes, int64_t n, int bits, uint32_t *words, cudaStream_t s);
 cudaError_t launch_unpack_bits(const uint32_t *words, int64_t n, int bits, uint8_t *codes, cudaStream_t s);
 cudaError_t launch_permute_k(const void *x, q4_dtype xd, const int32_t *perm, void *out, int64_t M, int64_t K,
                              cudaStream_t s);
+
+// Role-wait limits of the bounded-wait kernels (gemv_tma.cu, gemv_fp4tc.cu).
+int gemv_tma_set_wait_limit(long long cycles);
+int fp4tc_set_wait_limit(long long cycles);
 
 int sm_count() {
     int dev = 0, n = 0;
@@ -123,6 +130,11 @@ int q4_gemv(q4_fmt fmt, const void *W_packed, const void *scales, const q4_aux *
     const q4_dtype xd = aux ? aux->x_dtype : default_x_dtype(fmt);
     if (xd != Q4_DT_F32 && xd != Q4_DT_BF16) return Q4_EINVAL;
     cudaStream_t s = (cudaStream_t)stream;
+    if (fmt == Q4_NVFP4 && M == 1 && xd == Q4_DT_BF16 && (aux->flags & Q4_FLAG_FP4_SLICES) &&
+        gemv_fp4tc_eligible(t, M)) {
+        note_gemv_path("gemv_fp4tc");
+        return launch_gemv_fp4tc(t, x, y, s) == cudaSuccess ? Q4_OK : Q4_ECUDA;
+    }
     bool handled = false;
     cudaError_t e = cudaSuccess;
     if (M > 8) e = launch_gemm_tc(t, x, xd, y, M, s, &handled);
@@ -138,6 +150,7 @@ int q4_gemv_grouped(const q4_gemv_desc *descs, int count, int64_t M, void *strea
     float *ys[8];
     bool one_launch = count <= 8;
     bool tma = count <= 8;                     // every member NVFP4 on the TMA kernel, one shared x
+    bool fp4tc = count <= 8 && M == 1;         // every member NVFP4 at batch 1 on the FP4 tensor cores
     for (int i = 0; i < count; i++) {          // check every member before launching any
         const q4_gemv_desc &d = descs[i];
         Tensor t;
@@ -157,6 +170,13 @@ int q4_gemv_grouped(const q4_gemv_desc *descs, int count, int64_t M, void *strea
                      gemv_mma_eligible(t, M);
         tma = tma && d.fmt == Q4_NVFP4 && xd == Q4_DT_BF16 && d.K == descs[0].K && d.x == descs[0].x &&
               gemv_tma_eligible(t, M);
+        fp4tc = fp4tc && d.fmt == Q4_NVFP4 && xd == Q4_DT_BF16 && d.K == descs[0].K && d.x == descs[0].x &&
+                (d.aux->flags & Q4_FLAG_FP4_SLICES) && gemv_fp4tc_eligible(t, M);
+    }
+    if (fp4tc) {
+        note_gemv_path(count == 1 ? "gemv_fp4tc" : "gemv_fp4tc_group");
+        return launch_gemv_fp4tc_group(ts, count, descs[0].x, ys, (cudaStream_t)stream) == cudaSuccess ? Q4_OK
+                                                                                                  : Q4_ECUDA;
     }
     if (tma) {
         note_gemv_path(count == 1 ? "gemv_tma" : "gemv_tma_group");
@@ -223,6 +243,12 @@ int q4_gemv_chain(const q4_gemv_desc *descs, const int *first, int ngroups, int6
 
 const char *q4_last_gemv_path(void) { return q4::g_last_path; }
 
+int q4_set_wait_limit(int64_t cycles) {
+    const long long c = cycles > 0 ? (long long)cycles : (1LL << 31);
+    const int a = gemv_tma_set_wait_limit(c), b = fp4tc_set_wait_limit(c);
+    return a ? a : b;
+}
+
 int q4_gemv_a16q8(const void *W_packed, const void *scales, const q4_aux *aux, const void *x, float *y, int64_t M,
                   int64_t N, int64_t K, void *stream) {
     Tensor t;
@@ -274,6 +300,43 @@ int q4_quantize_nvfp4(const void *W, q4_dtype w_dtype, void *payload, void *scal
     if (w_dtype != Q4_DT_F32 && w_dtype != Q4_DT_BF16) return Q4_EINVAL;
     return launch_quantize_nvfp4(W, w_dtype, N, K, (uint8_t *)payload, (uint8_t *)scales, scale2,
                                  (cudaStream_t)stream) == cudaSuccess ? Q4_OK : Q4_ECUDA;
+}
+
+int q4_quantize_nvfp4_scaled(const void *x, q4_dtype x_dtype, float scale2, void *payload, void *scales, int64_t M,
+                             int64_t K, void *stream) {
+    if (M <= 0 || K <= 0 || K % 16) return Q4_EDIM;
+    if (!x || !payload || !scales) return Q4_EINVAL;
+    if (!aligned16(x) || !aligned16(payload) || !aligned16(scales)) return Q4_EALIGN;
+    if (x_dtype != Q4_DT_F32 && x_dtype != Q4_DT_BF16) return Q4_EINVAL;
+    if (!std::isfinite(scale2) || !(scale2 > 0.0f)) return Q4_ESCALE2;
+    return launch_quantize_nvfp4_scaled(x, x_dtype, M, K, scale2, (uint8_t *)payload, (uint8_t *)scales,
+                                        (cudaStream_t)stream) == cudaSuccess ? Q4_OK : Q4_ECUDA;
+}
+
+int q4_gemv_w4a4_tc(const void *W_packed, const void *scales, const q4_aux *aux, const void *xq, const void *xs,
+                    float x_scale2, float *y, int64_t M, int64_t N, int64_t K, void *stream) {
+    Tensor t;
+    const int rc = make_tensor(Q4_NVFP4, W_packed, scales, aux, N, K, t);
+    if (rc) return rc;
+    if (M <= 0 || K % 256) return Q4_EDIM;
+    if (!std::isfinite(x_scale2) || !(x_scale2 > 0.0f)) return Q4_ESCALE2;
+    if (!xq || !xs || !y) return Q4_EINVAL;
+    if (!aligned16(xq) || !aligned16(xs) || !aligned16(y)) return Q4_EALIGN;
+    if (!gemv_w4a4_tc_eligible(t)) return Q4_EUNSUPPORTED;
+    note_gemv_path("gemv_w4a4_tc");
+    return launch_gemv_w4a4_tc(t, (const uint8_t *)xq, (const uint8_t *)xs, x_scale2, y, M, (cudaStream_t)stream) ==
+                   cudaSuccess
+               ? Q4_OK
+               : Q4_ECUDA;
+}
+
+int q4_quantize_q4k(const void *W, q4_dtype w_dtype, void *out, int64_t N, int64_t K, void *stream) {
+    if (N <= 0 || K <= 0 || K % 256) return Q4_EDIM;
+    if (!W || !out) return Q4_EINVAL;
+    if (!aligned16(W) || !aligned16(out)) return Q4_EALIGN;
+    if (w_dtype != Q4_DT_F32 && w_dtype != Q4_DT_BF16) return Q4_EINVAL;
+    return launch_quantize_q4k(W, w_dtype, N, K, (uint8_t *)out, (cudaStream_t)stream) == cudaSuccess ? Q4_OK
+                                                                                                    : Q4_ECUDA;
 }
 
 int q4_pack_bits(const uint8_t *codes, int64_t n, int bits, uint32_t *words, void *stream) {

@@ -216,6 +216,14 @@ cudaError_t launch_gemm_tc(const Tensor &t, const void *x, q4_dtype x_dtype, flo
                            cudaStream_t s, bool *handled);
 bool gemv_mma_eligible(const Tensor &t, int64_t M);
 bool gemv_tma_eligible(const Tensor &t, int64_t M);
+// Batch-1 NVFP4 on the native block-scaled FP4 tensor cores (gemv_fp4tc.cu).
+bool gemv_fp4tc_eligible(const Tensor &t, int64_t M);
+cudaError_t launch_gemv_fp4tc(const Tensor &t, const void *x, float *y, cudaStream_t s);
+cudaError_t launch_gemv_fp4tc_group(const Tensor *ts, int count, const void *x, float *const *ys, cudaStream_t s);
+// NVFP4 weights x NVFP4 activations on the same tensor-core kernel (W4A4).
+bool gemv_w4a4_tc_eligible(const Tensor &t);
+cudaError_t launch_gemv_w4a4_tc(const Tensor &t, const uint8_t *xq, const uint8_t *xs, float x_scale2, float *y,
+                                int64_t M, cudaStream_t s);
 cudaError_t launch_gemv_tma(const Tensor &t, const void *x, float *y, int64_t M, cudaStream_t s);
 cudaError_t launch_gemv_tma_group(const Tensor *ts, const void *x, float *const *ys, int count, int64_t M,
                                   cudaStream_t s);

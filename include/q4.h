@@ -99,12 +99,25 @@ typedef struct {
     int32_t group;         /* GPTQ/AWQ/LOGICAL group size along K; <= 0 means 128 */
     q4_dtype x_dtype;      /* activation dtype for q4_gemv */
     q4_dtype out_dtype;    /* q4_dequant output dtype (bf16 = nearest-even of the f32 w) */
+    uint32_t flags;        /* Q4_FLAG_* options; 0 = defaults */
 } q4_aux;
+
+/* q4_aux.flags: batch-1 NVFP4 GEMVs with bf16 x (q4_gemv, and
+ * q4_gemv_grouped when every member sets it) run on the native block-scaled
+ * FP4 tensor cores with x entered as its exact 2-bit FP4 slices (see
+ * q4_gemv) instead of the TMA-fed decode kernel. */
+#define Q4_FLAG_FP4_SLICES 1u
 
 /* y[M][N] (f32) = x[M][K] . W^T.  The fused decode + dot of [W4K] section 1:
  * packed weights are streamed once from HBM, decoded on chip and accumulated
  * in f32; no dequantized matrix is written.  M <= 8 runs the bandwidth-bound
- * GEMV kernels: NVFP4 with bf16 x, M <= 4 and K % 256 == 0 streams its
+ * GEMV kernels.  With Q4_FLAG_FP4_SLICES, NVFP4 with bf16 x, M == 1 and
+ * K % 256 == 0 runs on the native block-scaled FP4 tensor cores: TMA lands
+ * the packed weights in shared memory, the MMA applies their E4M3 scales,
+ * and x enters as its exact 2-bit FP4 slices (blocks the slices cannot hold
+ * -- subnormal, non-finite, or more than 2^24 below their block's top -- are
+ * added on the CUDA cores), so the result holds for every x.  Otherwise
+ * NVFP4 with bf16 x, M <= 4 and K % 256 == 0 streams its
  * weights into shared memory by tensor TMA (weights are read before the
  * stream dependency on the previous launch resolves, x and y after it, so W
  * must not be written by a still-running kernel that released its dependents
@@ -239,6 +252,33 @@ int q4_gemv_q4k_q8(const void *W_packed, const q4_aux *aux, const void *x, float
 int q4_gemv_w4a4(const void *W_packed, const void *scales, const q4_aux *aux, float input_scale_inv, const void *x,
                  float *y, int64_t M, int64_t N, int64_t K, void *stream);
 
+/* W4A4 on the native block-scaled FP4 tensor cores ([MUS7] 7.4.3's producer
+ * mode, where activations arrive already in NVFP4; [W4K] section 7: Blackwell
+ * tensor cores consume the block-scaled FP4 layout directly).  Weights as
+ * Q4_NVFP4 (aux->scale2 required); activations xq u8 [M][K/2] (even k in the
+ * low nibble) with E4M3 scales xs u8 [M][K/16] and tensor scale x_scale2
+ * (finite, > 0), e.g. from q4_quantize_nvfp4_scaled.  Both operands go to
+ * tcgen05.mma.kind::mxf4nvf4.block_scale as they are stored: the MMA
+ * multiplies E2M1 codes and applies both E4M3 scales exactly, accumulating
+ * in f32; y[M][N] = accumulator * scale2 * x_scale2.  Accuracy: within
+ * 1e-5 * sum_k |w||x_hat| + 1e-6 of the exact f64 sum over the pinned
+ * weights and activations.  (q4_gemv_w4a4 is the integer-exact contract of
+ * the section; this is the tensor-core lane.)  K % 256 == 0; 16 activation
+ * rows per launch (larger M runs as several launches, each streaming the
+ * weights).  Allocates nothing; asynchronous on `stream`. */
+int q4_gemv_w4a4_tc(const void *W_packed, const void *scales, const q4_aux *aux, const void *xq, const void *xs,
+                    float x_scale2, float *y, int64_t M, int64_t N, int64_t K, void *stream);
+
+/* NVFP4 quantization of activations x[M][K] (f32 or bf16, finite) with a
+ * GIVEN tensor scale (e.g. W4A4's 1 / input_scale_inv, [MUS7] 7.4.3): the
+ * group rule of q4_quantize_nvfp4 (E4M3 scale = nearest-even of
+ * (amax/6)/scale2 saturating at 448, E2M1 codes nearest-even of
+ * x/(scale*scale2)) without the tensor-wide maximum.  payload [M][K/2],
+ * scales [M][K/16].  K % 16 == 0; scale2 finite and > 0 (Q4_ESCALE2).
+ * Bit-exact with the definition; one launch, asynchronous on `stream`. */
+int q4_quantize_nvfp4_scaled(const void *x, q4_dtype x_dtype, float scale2, void *payload, void *scales, int64_t M,
+                             int64_t K, void *stream);
+
 /* NVFP4 quantization on the GPU, the write side of the format ([MUS7] 7.2):
  * W[N][K] (w_dtype f32 or bf16, finite) -> payload u8 [N][K/2] (even k in the
  * low nibble), E4M3FN scale bytes u8 [N][K/16] and the tensor scale.
@@ -256,6 +296,22 @@ int q4_gemv_w4a4(const void *W_packed, const void *scales, const q4_aux *aux, fl
  * `stream`. */
 int q4_quantize_nvfp4(const void *W, q4_dtype w_dtype, void *payload, void *scales, float *scale2, int64_t N,
                       int64_t K, void *stream);
+
+/* Q4_K quantization on the GPU (the write side of Q4_Q4K): W[N][K] (w_dtype
+ * f32 or bf16, finite) -> 144-byte super-blocks out[N][K/256] in the Q4_Q4K
+ * layout.  The pages fix the decode, w = d*s_j*q - dmin*m_j ([FBTC] sections
+ * 5-6) but give no fitting recipe; this is the plainest per-sub-block
+ * min/max fit that decode supports, every step one IEEE f32 operation:
+ *   per 32-value sub-block j: lo = min(0, min w), scale_j = (max w - lo)/15,
+ *                             min_j = -lo;
+ *   d = binary16(max_j scale_j / 63), dmin = binary16(max_j min_j / 63),
+ *       nearest even;
+ *   s_j = clamp(rint(scale_j / d), 0, 63), m_j = clamp(rint(min_j / dmin), 0,
+ *       63), 0 for a zero divisor;
+ *   q = clamp(rint((w + dmin*m_j) / (d*s_j)), 0, 15), 0 for a zero step;
+ * rint rounds half to even.  Bit-exact with that definition.  K % 256 == 0.
+ * One launch; asynchronous on `stream`. */
+int q4_quantize_q4k(const void *W, q4_dtype w_dtype, void *out, int64_t N, int64_t K, void *stream);
 
 /* b-bit code streams ([BPA] "The packing arithmetic" and "Odd widths: 3-bit,
  * 2-bit and 6-bit"): code i (the low `bits` bits of codes[i], u8) occupies
@@ -337,14 +393,28 @@ int q4_validate_noalloc(q4_fmt fmt, const void *W_packed, const void *scales, co
 int q4_last_error(void);
 
 /* Name of the kernel family the calling host thread's latest q4_gemv or
- * q4_gemv_grouped or q4_gemv_chain launched ("gemv_tma", "gemv_tma_group",
+ * q4_gemv_grouped or q4_gemv_chain launched ("gemv_fp4tc",
+ * "gemv_fp4tc_group", "gemv_tma", "gemv_tma_group",
  * "gemv_tma_chain", "gemm_tc", "gemv_mma", "gemv_mma_group", "gemv_mma_q4k",
  * "gemv_mma_q40", "gemv_mma_gptq", "gemv_rows_tma", "gemv_rows_m1",
  * "gemv_general", "gemv_kmajor"; "gemv_a16q8" after q4_gemv_a16q8,
- * "gemv_q4k_q8" after q4_gemv_q4k_q8, "gemv_w4a4" after q4_gemv_w4a4; "" before
+ * "gemv_q4k_q8" after q4_gemv_q4k_q8, "gemv_w4a4" after q4_gemv_w4a4,
+ * "gemv_w4a4_tc" after q4_gemv_w4a4_tc; "" before
  * the first call).  A diagnostic with no counterpart in the pages: it lets a
  * caller (and the tests) confirm which path a shape takes.  Static storage. */
 const char *q4_last_gemv_path(void);
+
+/* Sets, for the current device, how long the bounded waits of the TMA-fed
+ * kernels may spin before they give up: the waits between the roles of the
+ * batch-1 FP4 tensor-core GEMV and of the batch 1-4 TMA GEMV, and the grid
+ * barrier of q4_gemv_chain.  cycles <= 0 restores the default, 2^31 SM clocks
+ * (about one second).  A wait that runs out records Q4_ETIMEOUT (read by
+ * q4_last_error), the kernel's roles stop, the bulk copies and MMAs already
+ * issued are waited for with the full limit, tensor memory is freed, and the
+ * kernel returns: the context stays usable.  A diagnostic with no
+ * counterpart in the pages, for exercising that path; synchronous; affects
+ * every later launch on the device until reset. */
+int q4_set_wait_limit(int64_t cycles);
 
 /* Human-readable text of a status code (static storage). */
 const char *q4_strerror(int status);

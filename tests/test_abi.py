@@ -41,7 +41,7 @@ _LAYOUT_PROBE = r"""
 int main(void) {
     printf("q4_aux size %zu\n", sizeof(q4_aux));
     F(q4_aux, scale2); F(q4_aux, zeros); F(q4_aux, g_idx); F(q4_aux, group); F(q4_aux, x_dtype);
-    F(q4_aux, out_dtype);
+    F(q4_aux, out_dtype); F(q4_aux, flags);
     printf("q4_gemv_desc size %zu\n", sizeof(q4_gemv_desc));
     F(q4_gemv_desc, fmt); F(q4_gemv_desc, W_packed); F(q4_gemv_desc, scales); F(q4_gemv_desc, aux);
     F(q4_gemv_desc, x); F(q4_gemv_desc, y); F(q4_gemv_desc, N); F(q4_gemv_desc, K);

@@ -88,3 +88,19 @@ def test_tokens_equivalent_rate():
     # 22.1 us per step, 32 layers: 1 / (32 * 22.1e-6) = 1414.03 tokens/s per replica
     assert bench.tokens_equivalent(0.0221, 1) == pytest.approx(1414.03, abs=0.01)
     assert bench.tokens_equivalent(0.0221, 8) == pytest.approx(8 * 1414.03, abs=0.1)
+
+
+def test_oracle_all_cores_split_matches_one_call():
+    """The all-cores CPU baseline runs the oracle's own rows on several host
+    threads; the values equal one single-threaded call."""
+    import numpy as np
+    import oracle
+    import synth
+    import bench
+    layer = synth.make_layer("nvfp4", 96, 512, config=5, matrix=0, row_scale=True)
+    T = oracle.Tensor("nvfp4", 96, 512, layer["w"], layer["scales"], scale2=layer["scale2"])
+    _, xf = synth.draw_x(1, 512, config=5, matrix=1)
+    rows = np.arange(96)
+    parts = bench.oracle_rows_all_cores(oracle, T, xf, rows, 4)
+    y = np.concatenate([p[0] for p in parts], axis=1)
+    assert np.array_equal(y, oracle.gemv(T, xf, rows=rows)[0])

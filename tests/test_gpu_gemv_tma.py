@@ -49,13 +49,19 @@ def tma_fits(K, M):
     return (112 * 1024 - fixed) // 18432 >= 3
 
 
+def expected_path(K, M):
+    """Batch 1..4 runs on the TMA-fed kernel when its ring fits, else on the
+    register-fed one (the FP4 tensor-core path is opt-in, tested apart)."""
+    return "gemv_tma" if tma_fits(K, M) else "gemv_mma"
+
+
 def check(layer, M, config, rows=None):
     d = to_device(layer)
     xbits, xf = synth.draw_x(M, layer["K"], config=config, matrix=5)
     y = gemv(layer, d, x_device(xbits), M)
     torch.cuda.synchronize()
     assert q4.q4_last_error() == q4.Q4_OK
-    assert q4.q4_last_gemv_path() == ("gemv_tma" if tma_fits(layer["K"], M) else "gemv_mma")
+    assert q4.q4_last_gemv_path() == expected_path(layer["K"], M)
     yc = y.cpu().numpy()
     if rows is None:
         ref, bound = oracle_gemv_all_rows(to_oracle(layer), xf)
@@ -92,7 +98,7 @@ def test_tma_gemv_wide_dynamic_range_x_falls_back_to_f32():
         xbits = synth.f32_to_bf16_bits(xf)
         xr = oracle.bf16_bits_to_f32(xbits).reshape(M, K)
         y = gemv(layer, d, x_device(xbits), M).cpu().numpy()
-        assert q4.q4_last_gemv_path() == ("gemv_tma" if tma_fits(K, M) else "gemv_mma")
+        assert q4.q4_last_gemv_path() == expected_path(K, M)
         ref, bound = oracle.gemv(to_oracle(layer), xr)
         ok, worst = within_tolerance(y, ref, bound)
         assert ok, worst
@@ -144,7 +150,7 @@ def test_tma_grouped_shared_x(M):
     descs[1] = descs[1][:4] + (x2,) + descs[1][5:]
     ys[1].fill_(float("nan"))
     assert q4.q4_gemv_grouped(descs, M) == q4.Q4_OK
-    assert q4.q4_last_gemv_path() != "gemv_tma_group"
+    assert q4.q4_last_gemv_path() not in ("gemv_tma_group", "gemv_fp4tc_group")
     torch.cuda.synchronize()
     ref, bound = oracle.gemv(to_oracle(layers[1]), xf2)
     ok, worst = within_tolerance(ys[1].cpu().numpy(), ref, bound)
@@ -361,4 +367,7 @@ def test_chain_deterministic_and_falls_back_when_not_eligible():
     ref, bound = oracle.gemv(to_oracle(q), xf)
     ok, worst = within_tolerance(yq.cpu().numpy(), ref, bound)
     assert ok, worst
-    assert torch.equal(y0, a0)
+    # group 0 ran as its own batch-1 launch (another kernel, another rounding order)
+    ref0, bound0 = oracle.gemv(to_oracle(L0), xf)
+    ok, worst = within_tolerance(y0.cpu().numpy(), ref0, bound0)
+    assert ok, worst
