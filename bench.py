@@ -57,6 +57,9 @@ def parse():
     ap.add_argument("--ncu-case", action="store_true",
                     help="small profiling case: 4 grouped gate+up launches (2 x 14336x4096, 66 MB) on "
                          "one weight copy, no timing, no JSON line")
+    ap.add_argument("--ncu-lanes-case", action="store_true",
+                    help="small profiling case: one launch of each kernel of the next rows and of the FP4 "
+                         "tensor-core path")
     ap.add_argument("--ncu-rows-case", action="store_true",
                     help="small profiling case: one launch of each remaining row's kernel on its own shape")
     ap.add_argument("--ncu-gemm-case", default=None, metavar="FMT:M",
@@ -582,6 +585,23 @@ def cpu_baseline_rows(rows_per_matrix=1024):
     out.append({"row": A16Q8_ROW, "shape": "14336x4096", "M": 1, "sample": f"{rows_per_matrix} rows of K = 4096",
                 "GBps": round(rows_per_matrix * q4_packed_row_bytes("nvfp4", 4096) / dt / 1e9, 4),
                 "seconds": round(dt, 3)})
+    isi = float(np.float32(2688.0) / np.float32(np.abs(xf).max()))
+    t0 = time.perf_counter()
+    oracle.gemv_w4a4(T, xf, isi)
+    dt = time.perf_counter() - t0
+    out.append({"row": "f1 W4A4 GEMV, integer-exact contract", "shape": "14336x4096", "M": 1,
+                "sample": f"{rows_per_matrix} rows of K = 4096",
+                "GBps": round(rows_per_matrix * q4_packed_row_bytes("nvfp4", 4096) / dt / 1e9, 4),
+                "seconds": round(dt, 3)})
+    ql = synth.make_layer("q4k", rows_per_matrix, 4096, config=1, matrix=0)
+    _, qxf = synth.draw_x(1, 4096, config=1, matrix=5, dtype="f32")
+    t0 = time.perf_counter()
+    oracle.gemv_q4k_q8(oracle.Tensor("q4k", rows_per_matrix, 4096, ql["w"]), qxf)
+    dt = time.perf_counter() - t0
+    out.append({"row": "f2 Q4_K x Q8 (W4A8) GEMV, integer sub-block sums", "shape": "4096x4096", "M": 1,
+                "sample": f"{rows_per_matrix} rows of K = 4096",
+                "GBps": round(rows_per_matrix * q4_packed_row_bytes("q4k", 4096) / dt / 1e9, 4),
+                "seconds": round(dt, 3)})
     return out
 
 
@@ -793,6 +813,86 @@ def other_rows(torch, q4, synth, peak_hbm):
                  "GBps": round(moved / us / 1e3, 1), "frac_hbm": round(moved / us / 1e3 / peak_hbm, 4),
                  "path": q4.q4_last_gemv_path()})
     del cps
+    torch.cuda.empty_cache()
+
+    # the next rows' lanes on the 14336x4096 layer at batch 1 (and W4A8 on its Q4_K layer)
+    N, K, M = 14336, 4096, 1
+    layer = synth.make_layer("nvfp4", N, K, config=5, matrix=0, row_scale=True)
+    packed = q4.q4_packed_bytes("nvfp4", N, K)
+    cps = copies_of(_dev_layer(torch, layer), packed)
+    xb, xf = synth.draw_x(M, K, config=5, matrix=5, dtype="bf16")
+    x = torch.from_numpy(np.ascontiguousarray(xb).view(np.int16)).cuda().view(torch.bfloat16)
+    y = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    aux = q4.make_aux(scale2=layer["scale2"], x_dtype=q4.Q4_DT_BF16, fmt="nvfp4")
+    isi = float(np.float32(2688.0) / np.float32(np.abs(xf).max()))
+    G = float(np.float32(1.0) / np.float32(isi))
+    moved = packed + x.numel() * 2 + y.numel() * 4
+
+    def lane_row(tag, fn, nbytes=moved, path=True):
+        us = _time_launches(torch, stream, fn)
+        row = {"row": tag, "shape": f"{N}x{K}", "M": M, "us_per_launch": round(us, 2),
+               "GBps": round(nbytes / us / 1e3, 1), "frac_hbm": round(nbytes / us / 1e3 / peak_hbm, 4)}
+        if path:
+            row["path"] = q4.q4_last_gemv_path()
+        rows.append(row)
+    auxf = q4.make_aux(scale2=layer["scale2"], x_dtype=q4.Q4_DT_BF16, fmt="nvfp4", flags=q4.Q4_FLAG_FP4_SLICES)
+    lane_row("a1 NVFP4 GEMV, FP4 tensor cores with exact x slices (opt-in)",
+             lambda i: q4.q4_gemv("nvfp4", cps[i % len(cps)]["w"], cps[i % len(cps)]["scales"], auxf, x, y, M, N, K,
+                                  stream=stream))
+    lane_row("f1 W4A4 GEMV, integer-exact contract", lambda i: q4.q4_gemv_w4a4(
+        cps[i % len(cps)]["w"], cps[i % len(cps)]["scales"], aux, isi, x, y, M, N, K, stream=stream))
+    xq = torch.empty((M, K // 2), dtype=torch.uint8, device="cuda")
+    xsc = torch.empty((M, K // 16), dtype=torch.uint8, device="cuda")
+    q4.q4_quantize_nvfp4_scaled(x, q4.Q4_DT_BF16, G, xq, xsc, M, K, stream=stream)
+    lane_row("f1 W4A4 GEMV on the FP4 tensor cores (activations already NVFP4)", lambda i: q4.q4_gemv_w4a4_tc(
+        cps[i % len(cps)]["w"], cps[i % len(cps)]["scales"], aux, xq, xsc, G, y, M, N, K, stream=stream),
+        nbytes=packed + xq.numel() + xsc.numel() + y.numel() * 4)
+    del cps
+    torch.cuda.empty_cache()
+    qlayer = synth.make_layer("q4k", 4096, 4096, config=1, matrix=0)
+    qpacked = q4.q4_packed_bytes("q4k", 4096, 4096)
+    qcps = copies_of(_dev_layer(torch, qlayer), qpacked)
+    _, qxf = synth.draw_x(1, 4096, config=1, matrix=5, dtype="f32")
+    qx = torch.from_numpy(np.ascontiguousarray(qxf, np.float32)).cuda()
+    qy = torch.empty((1, 4096), dtype=torch.float32, device="cuda")
+    us = _time_launches(torch, stream, lambda i: q4.q4_gemv_q4k_q8(qcps[i % len(qcps)]["w"], None, qx, qy, 1, 4096,
+                                                                    4096, stream=stream))
+    qmoved = qpacked + qx.numel() * 4 + qy.numel() * 4
+    rows.append({"row": "f2 Q4_K x Q8 (W4A8) GEMV, integer sub-block sums", "shape": "4096x4096", "M": 1,
+                 "us_per_launch": round(us, 2), "GBps": round(qmoved / us / 1e3, 1),
+                 "frac_hbm": round(qmoved / us / 1e3 / peak_hbm, 4), "path": q4.q4_last_gemv_path()})
+    del qcps
+    torch.cuda.empty_cache()
+    # f3: the GPU quantizers on the 14336x4096 layer (f32 W in, packed out)
+    Wd = torch.from_numpy(synth.draw_weights(N, K, config=5, matrix=0, row_scale=True)).cuda()
+    pay = torch.empty((N, K // 2), dtype=torch.uint8, device="cuda")
+    scl = torch.empty((N, K // 16), dtype=torch.uint8, device="cuda")
+    s2 = torch.empty(4, dtype=torch.float32, device="cuda")
+    qb = torch.empty((N, K // 256, 144), dtype=torch.uint8, device="cuda")
+    us = _time_launches(torch, stream, lambda i: q4.q4_quantize_nvfp4(Wd, q4.Q4_DT_F32, pay, scl, s2, N, K,
+                                                                      stream=stream), reps=40)
+    qbytes = N * K * 4 + packed
+    rows.append({"row": "f3 NVFP4 quantizer (f32 W -> payload, scales, scale2; four launches)", "shape": f"{N}x{K}",
+                 "us_per_call": round(us, 2), "GBps": round(qbytes / us / 1e3, 1),
+                 "frac_hbm": round(qbytes / us / 1e3 / peak_hbm, 4),
+                 "note": "W is read twice (tensor maximum, then the groups): bytes count it once"})
+    us = _time_launches(torch, stream, lambda i: q4.q4_quantize_q4k(Wd, q4.Q4_DT_F32, qb, N, K, stream=stream), reps=40)
+    qbytes = N * K * 4 + q4.q4_packed_bytes("q4k", N, K)
+    rows.append({"row": "f3 Q4_K fit (f32 W -> 144-byte super-blocks)", "shape": f"{N}x{K}",
+                 "us_per_launch": round(us, 2), "GBps": round(qbytes / us / 1e3, 1),
+                 "frac_hbm": round(qbytes / us / 1e3 / peak_hbm, 4)})
+    del Wd, pay, scl, qb
+    torch.cuda.empty_cache()
+    # f4: 3-bit stream packing of 64 Mi codes (u8 in, words out)
+    n = 64 << 20
+    codes = torch.randint(0, 8, (n,), dtype=torch.uint8, device="cuda")
+    words = torch.empty(n * 3 // 32, dtype=torch.int32, device="cuda")
+    us = _time_launches(torch, stream, lambda i: q4.q4_pack_bits(codes, n, 3, words, stream=stream), reps=40)
+    pbytes = n + words.numel() * 4
+    rows.append({"row": "f4 3-bit stream packer (u8 codes -> words)", "shape": f"{n} codes",
+                 "us_per_launch": round(us, 2), "GBps": round(pbytes / us / 1e3, 1),
+                 "frac_hbm": round(pbytes / us / 1e3 / peak_hbm, 4)})
+    del codes, words
     torch.cuda.empty_cache()
 
     # a6: dequant NVFP4 14336x4096 to f32 (write-bound)
@@ -1078,10 +1178,88 @@ def ncu_rows_case():
     print("ncu rows case done, last_error", q4.q4_last_error())
 
 
+def ncu_lanes_case():
+    """One launch of each kernel added for the next rows and of the FP4
+    tensor-core path, on one weight copy (a few hundred MB of device memory at
+    most), for single-kernel ncu captures.  Prints each launch's algorithmic
+    bytes."""
+    import torch
+
+    import bit_block_quantized_gb300 as q4
+    import synth
+    from bit_block_quantized_gb300 import build as q4build
+    q4build.build()
+    stream = torch.cuda.Stream()
+    mats = []
+    for i in (0, 1):
+        name, N, K = SET[i]
+        layer = synth.make_layer("nvfp4", N, K, config=CONFIG_ID, matrix=i, row_scale=True)
+        d = _dev_layer(torch, layer)
+        mats.append((N, K, d, q4.make_aux(scale2=layer["scale2"], fmt="nvfp4", flags=q4.Q4_FLAG_FP4_SLICES)))
+    xb, xf = synth.draw_x(1, 4096, config=CONFIG_ID, matrix=0)
+    x = torch.from_numpy(xb.view(np.int16)).cuda().view(torch.bfloat16)
+    ys = [torch.empty((1, N), dtype=torch.float32, device="cuda") for N, *_ in mats]
+    q4.q4_gemv_grouped([("nvfp4", d["w"], d["scales"], aux, x, y, N, K) for (N, K, d, aux), y in zip(mats, ys)], 1,
+                       stream=stream)
+    torch.cuda.synchronize()
+    print(f"gemv_fp4tc (slices) gate+up: {q4.q4_last_gemv_path()} algorithmic bytes "
+          f"{2 * q4.q4_packed_bytes('nvfp4', 14336, 4096) + 4096 * 2 + 2 * 14336 * 4}")
+    N, K, d, aux = mats[0]
+    isi = float(np.float32(2688.0) / np.float32(np.abs(xf).max()))
+    G = float(np.float32(1.0) / np.float32(isi))
+    xq = torch.empty((1, K // 2), dtype=torch.uint8, device="cuda")
+    xs = torch.empty((1, K // 16), dtype=torch.uint8, device="cuda")
+    q4.q4_quantize_nvfp4_scaled(x, q4.Q4_DT_BF16, G, xq, xs, 1, K, stream=stream)
+    q4.q4_gemv_w4a4_tc(d["w"], d["scales"], aux, xq, xs, G, ys[0], 1, N, K, stream=stream)
+    torch.cuda.synchronize()
+    print(f"gemv_fp4tc (W4A4) {N}x{K}: algorithmic bytes {q4.q4_packed_bytes('nvfp4', N, K) + K // 2 + K // 16 + N * 4}")
+    q4.q4_gemv_w4a4(d["w"], d["scales"], aux, isi, x, ys[0], 1, N, K, stream=stream)
+    torch.cuda.synchronize()
+    print(f"gemv_w4a4 {N}x{K}: algorithmic bytes {q4.q4_packed_bytes('nvfp4', N, K) + K * 2 + N * 4}")
+    ql = synth.make_layer("q4k", 4096, 4096, config=1, matrix=0)
+    dq = _dev_layer(torch, ql)
+    _, qxf = synth.draw_x(1, 4096, config=1, matrix=5, dtype="f32")
+    qx = torch.from_numpy(np.ascontiguousarray(qxf, np.float32)).cuda()
+    qy = torch.empty((1, 4096), dtype=torch.float32, device="cuda")
+    q4.q4_gemv_q4k_q8(dq["w"], None, qx, qy, 1, 4096, 4096, stream=stream)
+    torch.cuda.synchronize()
+    print(f"gemv_q4k_q8 4096x4096: algorithmic bytes {q4.q4_packed_bytes('q4k', 4096, 4096) + 4096 * 8}")
+    W = torch.from_numpy(synth.draw_weights(N, K, config=5, matrix=0, row_scale=True)).cuda()
+    pay = torch.empty((N, K // 2), dtype=torch.uint8, device="cuda")
+    scl = torch.empty((N, K // 16), dtype=torch.uint8, device="cuda")
+    s2 = torch.empty(4, dtype=torch.float32, device="cuda")
+    qb = torch.empty((N, K // 256, 144), dtype=torch.uint8, device="cuda")
+    q4.q4_quantize_nvfp4(W, q4.Q4_DT_F32, pay, scl, s2, N, K, stream=stream)
+    q4.q4_quantize_q4k(W, q4.Q4_DT_F32, qb, N, K, stream=stream)
+    torch.cuda.synchronize()
+    print(f"quantize {N}x{K}: f32 in {N * K * 4}, NVFP4 out {q4.q4_packed_bytes('nvfp4', N, K)}, "
+          f"Q4_K out {q4.q4_packed_bytes('q4k', N, K)}")
+    n = 64 << 20
+    codes = torch.randint(0, 8, (n,), dtype=torch.uint8, device="cuda")
+    words = torch.empty(n * 3 // 32, dtype=torch.int32, device="cuda")
+    q4.q4_pack_bits(codes, n, 3, words, stream=stream)
+    torch.cuda.synchronize()
+    print(f"pack_bits 3-bit: {n} codes, bytes {n + words.numel() * 4}")
+    al = synth.make_layer("awq", 4096, 11008, config=2, matrix=0, outliers=True)
+    da = _dev_layer(torch, al)
+    axb, _ = synth.draw_x(1, 11008, config=2, matrix=5)
+    ax = torch.from_numpy(axb.view(np.int16)).cuda().view(torch.bfloat16)
+    ay = torch.empty((1, 4096), dtype=torch.float32, device="cuda")
+    aaux = q4.make_aux(zeros=da["zeros"], group=128, x_dtype=torch.bfloat16, fmt="awq")
+    q4.q4_gemv("awq", da["w"], da["scales"], aaux, ax, ay, 1, 4096, 11008, stream=stream)
+    torch.cuda.synchronize()
+    print(f"{q4.q4_last_gemv_path()} AWQ 4096x11008: algorithmic bytes "
+          f"{q4.q4_packed_bytes('awq', 4096, 11008) + 11008 * 2 + 4096 * 4}")
+    print("ncu lanes case done, last_error", q4.q4_last_error())
+
+
 def main():
     args = parse()
     if args.ncu_rows_case:
         ncu_rows_case()
+        return
+    if args.ncu_lanes_case:
+        ncu_lanes_case()
         return
     if args.ncu_case:
         ncu_case()

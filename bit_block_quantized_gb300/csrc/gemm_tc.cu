@@ -687,6 +687,7 @@ int gemv_read_and_clear_error();
 int gemv_tma_read_and_clear_error();
 int pack_read_and_clear_error();
 int fp4tc_read_and_clear_error();
+int awq_read_and_clear_error();
 
 int read_and_clear_device_error() {
     int v = 0;
@@ -698,7 +699,8 @@ int read_and_clear_device_error() {
     const int tm = gemv_tma_read_and_clear_error();
     const int pk = pack_read_and_clear_error();
     const int f4 = fp4tc_read_and_clear_error();
-    return v ? v : g ? g : tm ? tm : pk ? pk : f4;
+    const int aw = awq_read_and_clear_error();
+    return v ? v : g ? g : tm ? tm : pk ? pk : f4 ? f4 : aw;
 }
 
 }  // namespace q4

@@ -889,6 +889,10 @@ cudaError_t launch_gemv(const Tensor &t, const void *x, q4_dtype x_dtype, float 
         if (e != cudaSuccess) return e;
         return launch_gemv(t, static_cast<const char *>(x) + 4 * t.K * xe, x_dtype, y + 4 * t.N, M - 4, s);
     }
+    if (gemv_awq_tc_eligible(t, M) && ((uintptr_t)x & 15) == 0) {     // x read in 16-byte vectors
+        note_gemv_path("gemv_awq_tc");
+        return launch_gemv_awq_tc(t, x, x_dtype, y, M, s);
+    }
     if (gemv_gptq_eligible(t, M)) {
         note_gemv_path("gemv_mma_gptq");
         return launch_gemv_gptq(t, x, x_dtype, y, M, s);

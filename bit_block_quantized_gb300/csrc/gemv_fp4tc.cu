@@ -189,26 +189,43 @@ __device__ __forceinline__ int block_top(const uint32_t u[16]) {
 // the file header) into the B planes; the thread with p0 == 0 also writes the
 // block's B scale byte: 2^(t_b - T + 8) in UE4M3, or 0 for a residual block
 // (a value the slices never use: their smallest scale is 2^-9 = byte 1).
+// Branch-free: each element's 8-bit significand m24 (top bit set) is shifted
+// right by its distance below the block's top (shifts of 32 or more give 0);
+// shifting back and comparing tells whether bits fell off the end.
 __device__ void slice_block(const __nv_bfloat16 *xr, int b, int T, int p0, int p1, uint8_t *bplanes, uint8_t *sfb) {
-    uint32_t u[16];
-    load16_bf16(xr + b * 16, u);
-    const int tb_ = block_top(u);
-    bool resid = tb_ != -1000 && tb_ - T + 8 < -9;                      // scale below UE4M3's 2^-9
-    uint32_t A[16], slo = 0u, shi = 0u;
+    const uint4 qa = *reinterpret_cast<const uint4 *>(xr + b * 16), qb = *reinterpret_cast<const uint4 *>(xr + b * 16 + 8);
+    const uint32_t w[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
+    uint32_t E[16], u[16];
+#pragma unroll
+    for (int i = 0; i < 8; i++) {
+        u[2 * i] = w[i] & 0xffffu;
+        u[2 * i + 1] = w[i] >> 16;
+    }
+    int tb_ = -1000;
+    uint32_t special = 0u;                                               // a subnormal or non-finite element
 #pragma unroll
     for (int i = 0; i < 16; i++) {
-        const int E = (int)((u[i] >> 7) & 0xffu);
-        const uint32_t frac = u[i] & 0x7fu;
-        if (E == 255 || (E == 0 && frac)) resid = true;                  // non-finite or subnormal
-        const uint32_t m = 128u | frac;                                  // 8-bit significand
-        const int sh = tb_ - 1 - (E - 127);                              // value bit j at word bit j + 32 - tb_
-        A[i] = (E != 0 && E != 255 && sh < 32) ? (m << 24) >> sh : 0u;
-        if (E != 0 && E != 255 && sh > 24 && (m & ((1u << min(sh - 24, 8)) - 1u))) resid = true;
-        if (u[i] & 0x8000u) {
-            if (i < 8) slo |= 8u << (4 * i);
-            else shi |= 8u << (4 * (i - 8));
-        }
+        E[i] = (u[i] >> 7) & 0xffu;
+        const bool normal = E[i] - 1u < 254u;                             // biased exponent 1 .. 254
+        tb_ = normal ? max(tb_, (int)E[i] - 126) : tb_;
+        special |= (E[i] == 255u) | ((E[i] == 0u) & ((u[i] & 0x7fu) != 0u));
     }
+    const int C = tb_ + 126;                                              // shift = C - E
+    uint32_t A[16], lost = 0u, slo = 0u, shi = 0u;
+#pragma unroll
+    for (int i = 0; i < 16; i++) {
+        const uint32_t m24 = (u[i] << 24) | 0x80000000u;                  // value bit j at word bit j + 32 - tb_
+        const uint32_t sh = (uint32_t)(C - (int)E[i]);
+        uint32_t a, back;
+        asm("shr.b32 %0, %1, %2;" : "=r"(a) : "r"(m24), "r"(sh));
+        asm("shl.b32 %0, %1, %2;" : "=r"(back) : "r"(a), "r"(sh));
+        const bool normal = E[i] - 1u < 254u;
+        A[i] = normal ? a : 0u;
+        lost |= normal & (back != m24);
+        if (i < 8) slo |= (u[i] >> 15) << (4 * i + 3);                    // the sign bit of each nibble
+        else shi |= (u[i] >> 15) << (4 * (i - 8) + 3);
+    }
+    const bool resid = special | lost | (tb_ != -1000 && tb_ - T + 8 < -9);   // scale below UE4M3's 2^-9
     // transpose the 16 x 16 matrix of 2-bit cells: word q <- cell q of every element
 #pragma unroll
     for (int stage = 0; stage < 4; stage++) {
@@ -436,19 +453,18 @@ gemv_fp4tc_kernel(const __grid_constant__ Fp4Args a, const __grid_constant__ Fp4
             if (share == 1) {
                 for (int b = t; b < nblk; b += 128) slice_block(xs, b, T, 0, P, bplanes, sfb);
             } else {
-                // this rank's 1/share of the planes, four threads per block (four slices each),
-                // then one bulk copy of the planes and one of the scale bytes to every peer
+                // this rank's 1/share of the planes: lane = block, warp w = slices 4w .. 4w+3
+                // (warp-uniform, so no lane idles through another's slices); then one thread
+                // per peer sends the planes and the scale bytes by two bulk copies
                 const int per = nslots / share, me = (int)(blockIdx.x % (unsigned)share);
-                const int b0 = me * per * 16, nb = per * 16;
-                for (int q = t; q < nb * 4; q += 128) slice_block(xs, b0 + (q >> 2), T, 4 * (q & 3), 4 * (q & 3) + 4, bplanes, sfb);
+                const int b0 = me * per * 16, nb = per * 16, sw = t >> 5;
+                for (int bi = lane; bi < nb; bi += 32) slice_block(xs, b0 + bi, T, 4 * sw, 4 * sw + 4, bplanes, sfb);
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                 asm volatile("bar.sync 1, 128;" ::: "memory");
-                if (t == 0) {
-                    for (int pr = 1; pr < share; pr++) {
-                        const uint32_t peer = (uint32_t)((me + pr) % share);
-                        push_to_peer(bplanes + me * per * BPLANE, (uint32_t)(per * BPLANE), &slices_in, peer);
-                        push_to_peer(sfb + b0, (uint32_t)(per * 16), &slices_in, peer);
-                    }
+                if (t >= 1 && t < share) {
+                    const uint32_t peer = (uint32_t)((me + t) % share);
+                    push_to_peer(bplanes + me * per * BPLANE, (uint32_t)(per * BPLANE), &slices_in, peer);
+                    push_to_peer(sfb + b0, (uint32_t)(per * 16), &slices_in, peer);
                 }
                 if (!wait_or_abort(&slices_in, 0, abort_flag)) {
                     // a peer's slices did not arrive: nothing of this range is multiplied

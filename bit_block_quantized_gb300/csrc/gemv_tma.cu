@@ -58,6 +58,12 @@ __device__ long long g_tma_wait_limit = 1LL << 31;
 #ifndef Q4_TMA_NACC
 #define Q4_TMA_NACC 4
 #endif
+#ifndef Q4_TMA_PREFETCH
+#define Q4_TMA_PREFETCH 3
+#endif
+#ifndef Q4_TMA_L2_AHEAD
+#define Q4_TMA_L2_AHEAD 0
+#endif
 constexpr int CW = 8;                          // consumer warps
 constexpr int THREADS = (CW + 1) * 32;         // + the producer warp
 constexpr int KS = 2048;                       // k per ring stage = CW chunks of 256 k
@@ -66,7 +72,8 @@ constexpr int SC_BYTES = 16 * KS / 16;         // 16 rows x 128 scale bytes
 constexpr int STAGE_BYTES = PAY_BYTES + SC_BYTES;
 constexpr int MAX_STAGES = 8;
 constexpr int MIN_STAGES = 3;
-constexpr int PREFETCH_STAGES = 3;             // stages a CTA loads before its decode warps have staged x
+constexpr int PREFETCH_STAGES = Q4_TMA_PREFETCH;   // stages a CTA loads before its decode warps have staged x
+constexpr int L2_AHEAD = Q4_TMA_L2_AHEAD;          // further stages it then only prefetches into L2
 constexpr int MAXM = 8;                        // matrices per launch
 constexpr int MAXP = 4;                        // groups per chain
 constexpr size_t SMEM_CAP = Q4_TMA_SMEM_KB * 1024;   // 112 KB: two CTAs per SM
@@ -143,6 +150,16 @@ __device__ __forceinline__ void tma_3d(uint32_t dst, const CUtensorMap *map, int
         " [%0], [%1, {%2, %3, %4}], [%5], %6;"
         ::"r"(dst), "l"(map), "r"(c0), "r"(c1), "r"(c2), "r"(bar), "l"(pol)
         : "memory");
+}
+// L2-only prefetch of a tile: no shared memory, no completion to wait for.
+__device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap *map, int c0, int c1, int c2) {
+    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(map), "r"(c0), "r"(c1),
+                 "r"(c2)
+                 : "memory");
+}
+__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap *map, int c0, int c1) {
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(map), "r"(c0), "r"(c1)
+                 : "memory");
 }
 __device__ __forceinline__ void tma_2d(uint32_t dst, const CUtensorMap *map, int c0, int c1, uint32_t bar,
                                        uint64_t pol) {
@@ -404,6 +421,20 @@ __global__ void __launch_bounds__(THREADS, Q4_TMA_CTAS_PER_SM)
                         issued++;
                         if (++slot == S) { slot = 0; phase ^= 1; }
                         if (issued == PREFETCH_STAGES) {
+                            // The next stages of this CTA's list into L2 only: their bytes move
+                            // while the launch before finishes, without queueing in front of x.
+                            int pt = tile, pst = st + 1, pm = member;
+                            for (int q = 0; q < L2_AHEAD; q++, pst++) {
+                                if (pst == nst) {
+                                    pst = 0;
+                                    pt += (int)gridDim.x;
+                                    if (pt >= ntiles) break;
+                                    while (pm + 1 < m_end && pt >= a.tile_start[pm + 1]) pm++;
+                                }
+                                const int prow0 = (pt - a.tile_start[pm]) * 16;
+                                tma_prefetch_3d(&maps.pay[pm], 0, prow0, pst * (KS / 256));
+                                tma_prefetch_2d(&maps.sc[pm], pst * (KS / 16), prow0);
+                            }
                             // Hold further copies until the decode warps have read x (or ~0.5 s,
                             // or an abort): a deeper prefetch queues their x loads behind this
                             // launch's weight stream while they cannot start without x.

@@ -76,11 +76,14 @@ def test_reference_arm_rank0_only():
 
 def test_cpu_baseline_rows_cover_every_timed_row():
     """The CPU leg the bench runs beside the other rows: one entry per GEMV row
-    (the A16-Q8 lane included) plus the dequant, each with a positive rate."""
+    (the A16-Q8, W4A4 and W4A8 lanes included) plus the dequant, each with a
+    positive rate."""
     rows = bench.cpu_baseline_rows(rows_per_matrix=4)
     names = [r["row"] for r in rows]
     assert bench.A16Q8_ROW in names and "a6 dequant NVFP4 -> f32" in names
-    assert len(names) == len(bench.ORACLE_ROWS) + 2
+    assert "f1 W4A4 GEMV, integer-exact contract" in names
+    assert "f2 Q4_K x Q8 (W4A8) GEMV, integer sub-block sums" in names
+    assert len(names) == len(bench.ORACLE_ROWS) + 4
     assert all(r["GBps"] > 0 and r["seconds"] >= 0 for r in rows)
 
 

@@ -224,6 +224,45 @@ def test_gemv_gptq_tensor_core_path(M, xdtype):
         assert q4.q4_last_gemv_path() == "gemv_mma_gptq"
 
 
+@pytest.mark.parametrize("xdtype", ["f32", "bf16"])
+@pytest.mark.parametrize("M", [1, 3, 4, 8, 11])
+def test_gemv_awq_tensor_core_path(M, xdtype):
+    """AWQ (group 128, N % 128 == 0) on the TMA-fed tensor-core kernel: the
+    weights are the MMA's B operand, (q - z) * 2^b formed exactly in f16, the
+    K range split over up to 8 cluster ranks (uneven: 9 and 86 groups), batch
+    1..8 per launch and 11 as two launches."""
+    for N, K in ((128, 1152), (384, 4096), (11008, 128), (768, 11008)):
+        check_gemv(synth.make_layer("awq", N, K, config=39, matrix=M, outliers=True), M, config=39 + M,
+                   xdtype=xdtype)
+        assert q4.q4_last_gemv_path() == "gemv_awq_tc"
+    # N % 128 != 0 stays on the CUDA-core kernel
+    check_gemv(synth.make_layer("awq", 264, 1152, config=39, matrix=M), M, config=39, xdtype=xdtype)
+    assert q4.q4_last_gemv_path() != "gemv_awq_tc"
+
+
+def test_gemv_awq_tensor_core_edge_values():
+    """x over 1e30 .. 1e-10 (one power-of-two scale per batch row and rank),
+    an all-zero x (exactly 0), and every code and zero point in use."""
+    N, K = 512, 2048
+    layer = synth.make_layer("awq", N, K, config=41, matrix=0)
+    for M in (1, 3):
+        xf = np.random.default_rng(M).normal(0, 1e-10, (M, K)).astype(np.float32)
+        xf[:, 7] = 1e30
+        xf[:, 1500] = -3e20
+        y = gpu_gemv(layer, x_device(xf), M)
+        assert q4.q4_last_gemv_path() == "gemv_awq_tc"
+        ref, bound = oracle.gemv(to_oracle(layer), xf)
+        ok, worst = within_tolerance(y, ref, bound)
+        assert ok, worst
+    y = gpu_gemv(layer, torch.zeros((2, K), dtype=torch.bfloat16, device="cuda"), 2)
+    assert np.all(y == 0)
+    rng = np.random.default_rng(5)
+    rand = dict(layer, w=rng.integers(-2**31, 2**31, layer["w"].shape, dtype=np.int64).astype(np.int32),
+                zeros=rng.integers(-2**31, 2**31, layer["zeros"].shape, dtype=np.int64).astype(np.int32))
+    check_gemv(rand, 2, config=41)
+    assert q4.q4_last_error() == 0
+
+
 def test_gemv_q4k_wide_dynamic_range_x():
     """f32 x spanning 1e30 to 1e-10: the hi + lo staging keeps the result
     within tolerance (tiny values fall below the scaled f16 range)."""
