@@ -108,12 +108,29 @@ __device__ __forceinline__ uint32_t hsub2_bits(uint32_t a, uint32_t b) {
     asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
     return d;
 }
-__device__ __forceinline__ uint32_t f16x2_bits(float lo, float hi) {
-    const __half2 h = __floats2half2_rn(lo, hi);
-    return *reinterpret_cast<const uint32_t *>(&h);
+__device__ __forceinline__ uint32_t h2bits(__half lo, __half hi) {
+    return (uint32_t)__half_as_ushort(lo) | ((uint32_t)__half_as_ushort(hi) << 16);
 }
-template <typename XT> __device__ __forceinline__ float xval(const void *x, int64_t i) {
-    return x_to_f32<XT>(reinterpret_cast<const XT *>(x)[i]);
+// 16 consecutive x values as f32 (two or four 16-byte loads).
+template <typename XT> __device__ __forceinline__ void load16(const XT *p, float (&v)[16]) {
+    if constexpr (sizeof(XT) == 2) {
+        const uint4 a = __ldg(reinterpret_cast<const uint4 *>(p)), b = __ldg(reinterpret_cast<const uint4 *>(p) + 1);
+        const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+        for (int i = 0; i < 8; i++) {
+            v[2 * i] = __uint_as_float(w[i] << 16);
+            v[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < 4; i++) {
+            const float4 f = __ldg(reinterpret_cast<const float4 *>(p) + i);
+            v[4 * i] = f.x;
+            v[4 * i + 1] = f.y;
+            v[4 * i + 2] = f.z;
+            v[4 * i + 3] = f.w;
+        }
+    }
 }
 // Largest magnitude in 16 bytes of x (NaN-free inputs; a NaN compares false and is skipped).
 template <typename XT> __device__ __forceinline__ float absmax16(uint4 v) {
@@ -211,19 +228,26 @@ gemv_awq_tc(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ Aw
             xinv[t256] = __uint_as_float((uint32_t)(127 - 14 + e) << 23);
         }
         asm volatile("bar.sync 1, 256;" ::: "memory");
-        // fragments: lane (m, t) of chunk c holds k rows t, t+4 (a0 hi, a1 lo) and t+8, t+12 (a2 hi, a3 lo)
-        for (int e = t256; e < nch * M * 4; e += AT_WARPS * 32) {
-            const int t = e & 3, m = (e >> 2) % M, c = (e >> 2) / M;
-            const int64_t kb = m * a.K + k0 + (int64_t)c * 16;
-            float v[4], h[4], l[4];
+        // fragments: lane (m, t) of chunk c holds k rows t, t+4 (a0 hi, a1 lo) and t+8, t+12 (a2 hi, a3 lo);
+        // one thread per (chunk, row m) reads the chunk's 16 values with 16-byte loads
+        for (int e = t256; e < nch * M; e += AT_WARPS * 32) {
+            const int c = e / M, m = e - c * M;
+            const XT *src = reinterpret_cast<const XT *>(a.x) + (int64_t)m * a.K + k0 + (int64_t)c * 16;
+            float v[16];
+            load16<XT>(src, v);
+            const float sc = xscale[m];
+            __half hh[16], hl[16];
 #pragma unroll
-            for (int r = 0; r < 4; r++) {
-                v[r] = xval<XT>(a.x, kb + t + 4 * r) * xscale[m];
-                h[r] = __half2float(__float2half_rn(v[r]));
-                l[r] = __half2float(__float2half_rn(v[r] - h[r]));
+            for (int i = 0; i < 16; i++) {
+                const float f = v[i] * sc;                                 // exact: a power of two
+                hh[i] = __float2half_rn(f);
+                hl[i] = __float2half_rn(f - __half2float(hh[i]));
             }
-            afrag[((size_t)c * MB + m) * 4 + t] =
-                make_uint4(f16x2_bits(h[0], h[1]), f16x2_bits(l[0], l[1]), f16x2_bits(h[2], h[3]), f16x2_bits(l[2], l[3]));
+            uint4 *dst = afrag + ((size_t)c * MB + m) * 4;
+#pragma unroll
+            for (int t = 0; t < 4; t++)
+                dst[t] = make_uint4(h2bits(hh[t], hh[t + 4]), h2bits(hl[t], hl[t + 4]), h2bits(hh[t + 8], hh[t + 12]),
+                                    h2bits(hl[t + 8], hl[t + 12]));
         }
         asm volatile("bar.sync 1, 256;" ::: "memory");
 
@@ -268,7 +292,7 @@ gemv_awq_tc(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ Aw
                 uint4 w4[4];
 #pragma unroll
                 for (int r = 0; r < 4; r++) w4[r] = lds128(st + roff[r] + (uint32_t)(ch * 1024));
-                const uint4 af = arow ? apj[ch * MB * 4] : make_uint4(0u, 0u, 0u, 0u);
+                const uint4 af = apj[ch * MB * 4];     // lanes g >= M read row 0: their MMA rows are never stored
                 const uint32_t wr[4][4] = {{w4[0].x, w4[0].y, w4[0].z, w4[0].w}, {w4[1].x, w4[1].y, w4[1].z, w4[1].w},
                                            {w4[2].x, w4[2].y, w4[2].z, w4[2].w}, {w4[3].x, w4[3].y, w4[3].z, w4[3].w}};
 #pragma unroll

@@ -58,17 +58,20 @@ __device__ long long g_tma_wait_limit = 1LL << 31;
 #ifndef Q4_TMA_NACC
 #define Q4_TMA_NACC 4
 #endif
+#ifndef Q4_TMA_CW
+#define Q4_TMA_CW 8
+#endif
 #ifndef Q4_TMA_PREFETCH
 #define Q4_TMA_PREFETCH 3
 #endif
 #ifndef Q4_TMA_L2_AHEAD
 #define Q4_TMA_L2_AHEAD 0
 #endif
-constexpr int CW = 8;                          // consumer warps
+constexpr int CW = Q4_TMA_CW;                  // consumer warps (a multiple of 8)
 constexpr int THREADS = (CW + 1) * 32;         // + the producer warp
-constexpr int KS = 2048;                       // k per ring stage = CW chunks of 256 k
+constexpr int KS = CW * 256;                   // k per ring stage = CW chunks of 256 k
 constexpr int PAY_BYTES = 16 * KS / 2;         // 16 rows x 1024 payload bytes
-constexpr int SC_BYTES = 16 * KS / 16;         // 16 rows x 128 scale bytes
+constexpr int SC_BYTES = 16 * KS / 16;         // CW / 8 blocks of 16 rows x 128 scale bytes
 constexpr int STAGE_BYTES = PAY_BYTES + SC_BYTES;
 constexpr int MAX_STAGES = 8;
 constexpr int MIN_STAGES = 3;
@@ -79,6 +82,7 @@ constexpr int MAXP = 4;                        // groups per chain
 constexpr size_t SMEM_CAP = Q4_TMA_SMEM_KB * 1024;   // 112 KB: two CTAs per SM
 constexpr int NACC = Q4_TMA_NACC;
 static_assert(STAGE_BYTES % 1024 == 0, "stages keep the 1024-byte swizzle alignment");
+static_assert(CW % 8 == 0, "scale blocks of 128 bytes (2048 k) per row");
 
 struct Maps {
     CUtensorMap pay[MAXM];   // u8 {128, N, K/256}, strides {K/2, 128}: box {128, 16, 8}
@@ -344,7 +348,7 @@ __device__ __noinline__ void chunk_f32(uint32_t stg, const __nv_bfloat16 *__rest
     for (int rr = 0; rr < 16; rr++) {
         const uint32_t word = lds32(stg + (uint32_t)((w * 16 + rr) * 128) +
                                     ((uint32_t)((lane >> 2) ^ (rr & 7)) << 4) + ((uint32_t)(lane & 3) << 2));
-        const uint32_t sb = lds8(stg + PAY_BYTES + (uint32_t)(rr * 128) + ((uint32_t)(w ^ (rr & 7)) << 4) +
+        const uint32_t sb = lds8(stg + PAY_BYTES + (uint32_t)((w >> 3) * 2048 + rr * 128) + ((uint32_t)((w & 7) ^ (rr & 7)) << 4) +
                                  (uint32_t)(lane >> 1));
         const float sc = e4m3_f32(sb);
         for (int m = 0; m < MT; m++) {
@@ -417,7 +421,9 @@ __global__ void __launch_bounds__(THREADS, Q4_TMA_CTAS_PER_SM)
                         const uint32_t dst = ring + (uint32_t)(slot * STAGE_BYTES), bar = smem_u32(&full[slot]);
                         mbar_arrive_expect_tx(&full[slot], STAGE_BYTES);
                         tma_3d(dst, &maps.pay[member], 0, row0, st * (KS / 256), bar, pol);
-                        tma_2d(dst + PAY_BYTES, &maps.sc[member], st * (KS / 16), row0, bar, pol);
+#pragma unroll
+                        for (int sb = 0; sb < CW / 8; sb++)   // 128-byte scale boxes: the swizzle span
+                            tma_2d(dst + PAY_BYTES + sb * 2048, &maps.sc[member], st * (KS / 16) + sb * 128, row0, bar, pol);
                         issued++;
                         if (++slot == S) { slot = 0; phase ^= 1; }
                         if (issued == PREFETCH_STAGES) {
@@ -433,7 +439,8 @@ __global__ void __launch_bounds__(THREADS, Q4_TMA_CTAS_PER_SM)
                                 }
                                 const int prow0 = (pt - a.tile_start[pm]) * 16;
                                 tma_prefetch_3d(&maps.pay[pm], 0, prow0, pst * (KS / 256));
-                                tma_prefetch_2d(&maps.sc[pm], pst * (KS / 16), prow0);
+                                for (int sb = 0; sb < CW / 8; sb++)
+                                    tma_prefetch_2d(&maps.sc[pm], pst * (KS / 16) + sb * 128, prow0);
                             }
                             // Hold further copies until the decode warps have read x (or ~0.5 s,
                             // or an abort): a deeper prefetch queues their x loads behind this
@@ -473,7 +480,8 @@ __global__ void __launch_bounds__(THREADS, Q4_TMA_CTAS_PER_SM)
     // payload byte offsets of this lane's two units in rows g and g+8 of chunk `warp`
     const uint32_t offA0 = (uint32_t)((warp * 16 + g) * 128) + ((uint32_t)((2 * tt) ^ g) << 4);
     const uint32_t offA1 = (uint32_t)((warp * 16 + g) * 128) + ((uint32_t)((2 * tt + 1) ^ g) << 4);
-    const uint32_t offS = (uint32_t)PAY_BYTES + (uint32_t)(g * 128) + ((uint32_t)(warp ^ g) << 4) + 4 * tt;
+    const uint32_t offS = (uint32_t)PAY_BYTES + (uint32_t)((warp >> 3) * 2048 + g * 128) +
+                          ((uint32_t)((warp & 7) ^ g) << 4) + 4 * tt;
     constexpr uint32_t ROW8 = 8 * 128;   // rows g+8: same swizzle phase, 8 lines further
     const int mlane = g < a.M ? g : 0;
 
@@ -617,7 +625,7 @@ bool encode_scales(CUtensorMap *map, const Tensor &t) {
     if (!enc) return false;
     const cuuint64_t dims[2] = {(cuuint64_t)(t.K / 16), (cuuint64_t)t.N};
     const cuuint64_t strides[1] = {(cuuint64_t)(t.K / 16)};
-    const cuuint32_t box[2] = {KS / 16, 16};
+    const cuuint32_t box[2] = {128, 16};
     const cuuint32_t estr[2] = {1, 1};
     return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t *>(t.scales), dims, strides, box, estr,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
