@@ -38,7 +38,7 @@ SET = [("gate", 14336, 4096), ("up", 14336, 4096), ("down", 4096, 14336)]
 CONFIG_ID = 5          # seed block of this workload's synthetic draws
 NOMINAL_HBM_GBS = 7900.0
 FALLBACK_HBM_GBS = 6800.0
-DOMINANT = "gemv_tma_nvfp4<MT=1> group of 2 (gate and up, 2 x 14336x4096 in one launch)"
+DOMINANT = "gemv_tma_fp4<MT=1, NVFP4> group of 2 (gate and up, 2 x 14336x4096 in one launch)"
 PROFILE = "gemv_tma_nvfp4_pair_2x14336x4096.md"
 PROFILED_SOURCES = ("bit_block_quantized_gb300/csrc/gemv_tma.cu", "bit_block_quantized_gb300/csrc/q4_internal.cuh",
                     "bit_block_quantized_gb300/csrc/tma_map.cuh")

@@ -882,7 +882,7 @@ cudaError_t launch_gemv(const Tensor &t, const void *x, q4_dtype x_dtype, float 
     // Batch 5..8 whose staged x does not fit the tensor-core kernels' shared
     // memory (large K) runs as two launches of at most 4 rows: the weights
     // stream twice, far faster than the general kernel.
-    if (M > 4 && M <= 8 && !gemv_gptq_eligible(t, M) && !gemv_blk_eligible(t, M) &&
+    if (M > 4 && M <= 8 && !gemv_gptq_tc_eligible(t, M) && !gemv_gptq_eligible(t, M) && !gemv_blk_eligible(t, M) &&
         (gemv_gptq_eligible(t, 4) || gemv_blk_eligible(t, 4))) {
         const int64_t xe = x_dtype == Q4_DT_BF16 ? 2 : 4;
         const cudaError_t e = launch_gemv(t, x, x_dtype, y, 4, s);
@@ -892,6 +892,10 @@ cudaError_t launch_gemv(const Tensor &t, const void *x, q4_dtype x_dtype, float 
     if (gemv_awq_tc_eligible(t, M) && ((uintptr_t)x & 15) == 0) {     // x read in 16-byte vectors
         note_gemv_path("gemv_awq_tc");
         return launch_gemv_awq_tc(t, x, x_dtype, y, M, s);
+    }
+    if (gemv_gptq_tc_eligible(t, M) && ((uintptr_t)x & 15) == 0) {    // x read in 16-byte vectors
+        note_gemv_path("gemv_gptq_tc");
+        return launch_gemv_gptq_tc(t, x, x_dtype, y, M, s);
     }
     if (gemv_gptq_eligible(t, M)) {
         note_gemv_path("gemv_mma_gptq");

@@ -34,6 +34,7 @@
 #include <mutex>
 
 #include "q4_internal.cuh"
+#include "tc_gemv_common.cuh"
 #include "tma_map.cuh"
 
 namespace q4 {
@@ -43,6 +44,7 @@ __device__ int g_awq_error;
 namespace {
 
 namespace cg = cooperative_groups;
+using namespace tc;
 
 constexpr int AT_COLS = 128;                   // columns per CTA
 constexpr int AT_CG = AT_COLS / 8;             // column groups (AWQ words) per CTA row
@@ -68,85 +70,6 @@ struct AwqArgs {
     int per;                  // groups per rank (the last rank's range may be shorter)
     int groups;               // K / G
 };
-
-__device__ __forceinline__ void mma16816(float (&d)[4], uint4 a, uint32_t b0, uint32_t b1) {
-    asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
-                 : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-                 : "r"(a.x), "r"(a.y), "r"(a.z), "r"(a.w), "r"(b0), "r"(b1));
-}
-__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
-    uint32_t d;
-    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
-    return d;
-}
-__device__ __forceinline__ uint4 lds128(uint32_t addr) {
-    uint4 v;
-    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
-    return v;
-}
-__device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity, volatile int *abort_flag) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const long long t0 = clock64();
-    while (!mbar_try_wait(bar, parity)) {
-        if (*abort_flag) return false;
-        if (clock64() - t0 > AT_WAIT) {
-            atomicExch(&g_awq_error, Q4_ETIMEOUT);
-            *abort_flag = 1;
-            return false;
-        }
-    }
-    return true;
-}
-__device__ __forceinline__ void tma2(uint32_t dst, const CUtensorMap *map, int c0, int c1, uint64_t *bar, uint64_t pol) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
-        " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst), "l"(map), "r"(c0), "r"(c1), "r"(smem_u32(bar)), "l"(pol)
-        : "memory");
-}
-__device__ __forceinline__ uint32_t hsub2_bits(uint32_t a, uint32_t b) {
-    uint32_t d;
-    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
-    return d;
-}
-__device__ __forceinline__ uint32_t h2bits(__half lo, __half hi) {
-    return (uint32_t)__half_as_ushort(lo) | ((uint32_t)__half_as_ushort(hi) << 16);
-}
-// 16 consecutive x values as f32 (two or four 16-byte loads).
-template <typename XT> __device__ __forceinline__ void load16(const XT *p, float (&v)[16]) {
-    if constexpr (sizeof(XT) == 2) {
-        const uint4 a = __ldg(reinterpret_cast<const uint4 *>(p)), b = __ldg(reinterpret_cast<const uint4 *>(p) + 1);
-        const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-#pragma unroll
-        for (int i = 0; i < 8; i++) {
-            v[2 * i] = __uint_as_float(w[i] << 16);
-            v[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
-        }
-    } else {
-#pragma unroll
-        for (int i = 0; i < 4; i++) {
-            const float4 f = __ldg(reinterpret_cast<const float4 *>(p) + i);
-            v[4 * i] = f.x;
-            v[4 * i + 1] = f.y;
-            v[4 * i + 2] = f.z;
-            v[4 * i + 3] = f.w;
-        }
-    }
-}
-// Largest magnitude in 16 bytes of x (NaN-free inputs; a NaN compares false and is skipped).
-template <typename XT> __device__ __forceinline__ float absmax16(uint4 v) {
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-    float m = 0.0f;
-#pragma unroll
-    for (int i = 0; i < 4; i++) {
-        if constexpr (sizeof(XT) == 2) {
-            m = fmaxf(m, fabsf(__uint_as_float(w[i] << 16)));
-            m = fmaxf(m, fabsf(__uint_as_float(w[i] & 0xffff0000u)));
-        } else {
-            m = fmaxf(m, fabsf(__uint_as_float(w[i])));
-        }
-    }
-    return m;
-}
 
 // Dynamic shared memory: ring | A fragments [chunks][M][4 lanes t] uint4 | partial rows [2 k halves][M][128].
 template <typename XT, int MB>
@@ -189,7 +112,7 @@ gemv_awq_tc(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ Aw
             int issued = 0;
             for (int j = 0; j < ng; j++) {
                 const int s = j % AT_NS;
-                if (j >= AT_NS && !wait_or_abort(&empty[s], ((j / AT_NS) & 1) ^ 1, abort_flag)) break;
+                if (j >= AT_NS && !wait_or_abort(&empty[s], ((j / AT_NS) & 1) ^ 1, abort_flag, &g_awq_error, AT_WAIT)) break;
                 uint8_t *st = ring + s * STAGE;
                 const int64_t grp = g0 + j;
                 mbar_arrive_expect_tx(&full[s], W_BYTES + S_BYTES + Z_BYTES);
@@ -273,7 +196,7 @@ gemv_awq_tc(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ Aw
         const uint32_t ring_u = smem_u32(ring);
         for (int j = 0; j < ng; j++) {
             const int s = j % AT_NS;
-            if (!wait_or_abort(&full[s], (uint32_t)((j / AT_NS) & 1), abort_flag)) break;
+            if (!wait_or_abort(&full[s], (uint32_t)((j / AT_NS) & 1), abort_flag, &g_awq_error, AT_WAIT)) break;
             const uint8_t *sp = ring + s * STAGE;
             const uint32_t st = ring_u + (uint32_t)(s * STAGE);
             uint32_t zz[4];                                              // 1024 + z * 2^b in both halves
@@ -382,24 +305,8 @@ int awq_capacity(const void *fn, int mb_index, int S, int64_t smem) {
     std::lock_guard<std::mutex> lock(g_cap_lock);
     CapEntry &c = g_cap[dev & 63][mb_index][S - 1];
     if (c.fn == fn && c.smem == smem) return c.cap;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)S, 1, 1);
-    cfg.blockDim = dim3(AT_THREADS, 1, 1);
-    cfg.dynamicSmemBytes = (size_t)smem;
-    cudaLaunchAttribute at[1];
-    at[0].id = cudaLaunchAttributeClusterDimension;
-    at[0].val.clusterDim.x = (unsigned)S;
-    at[0].val.clusterDim.y = 1;
-    at[0].val.clusterDim.z = 1;
-    cfg.attrs = at;
-    cfg.numAttrs = 1;
-    int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, fn, &cfg) != cudaSuccess) {
-        (void)cudaGetLastError();
-        n = 0;
-    }
-    c = CapEntry{fn, smem, n};
-    return n;
+    c = CapEntry{fn, smem, cluster_capacity(fn, AT_THREADS, S, smem)};
+    return c.cap;
 }
 
 template <typename XT, int MB>

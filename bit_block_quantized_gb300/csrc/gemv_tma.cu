@@ -1,4 +1,4 @@
-// gemv_tma.cu -- NVFP4 decode-GEMV for batch 1..4, weights streamed into
+// gemv_tma.cu -- NVFP4 (and single-matrix MXFP4) decode-GEMV for batch 1..4, weights streamed into
 // shared memory by the tensor-memory accelerator (TMA), dot products on the
 // tensor cores (mma.sync m16n8k16, f16 x f16 -> f32).  One launch runs a
 // chain of GEMV groups: the members of a group read the same x, and group
@@ -33,6 +33,12 @@
 //            of rows g and g+8: a quarter-warp touches every bank once.
 //   scales:  a 2-D box {128 bytes, 16 rows}; row r is line r (same swizzle),
 //            lane (g, t) reads the 4 scale bytes of its 64 k.
+// MXFP4 (one E8M0 scale per 32 k, [MUS7] 7.1's MX block) shares the payload
+// layout; its scale rows (K/32 bytes) need not be 16-byte multiples, so no
+// tensor map reads them: each lane loads the two scale bytes of its rows g
+// and g+8 one stage ahead into registers.  A scale outside the range where
+// every E2M1 multiple is an f16 number sends that warp's stage to the f32
+// CUDA-core dot, which adds into the same partials.
 // The staged x of warp w follows the same k order: entry
 //   ((v*8 + j)*MT + m)*4 + t,  v = 2s + h,
 //   = x[m][2048 s + 256 w + 64 t + 32 h + 4 j .. +3] * 2^e_m   (as f16).
@@ -91,6 +97,7 @@ struct Maps {
 
 struct Args {
     float *y[MAXM];                 // [M][N_i]
+    const uint8_t *mx_scales;       // MXFP4 (a single member): E8M0 [N][K/32]
     int64_t N[MAXM];
     float scale2[MAXM];
     int tile_start[MAXM];           // first 16-row tile of each member within its group
@@ -106,6 +113,24 @@ struct Args {
     int max_nst;
 };
 
+// MXFP4 scale byte b -> 2^(b-127) as an f16x2 pair, built from the exponent
+// field alone: exact (and every E2M1 multiple an f16 number) for b - 127 in
+// [-14, 13], the normal f16 powers; outside, `ok` clears and the stage takes
+// the f32 path.
+__device__ __forceinline__ uint32_t e8m0_h2(uint32_t b, bool &ok) {
+    const uint32_t e = b & 255u;
+    ok = ok && e - 113u <= 27u;
+    const uint32_t h = (e - 112u) << 10;
+    return h | (h << 16);
+}
+__device__ __forceinline__ void sts32(uint32_t addr, uint32_t v) {
+    asm volatile("st.shared.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+__device__ __forceinline__ uint32_t lds16(uint32_t addr) {
+    unsigned short v;
+    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr) : "memory");
+    return v;
+}
 __device__ __forceinline__ uint32_t hmul2_u32(uint32_t a, uint32_t b) {
     uint32_t d;
     asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
@@ -342,15 +367,20 @@ __device__ __forceinline__ bool stage_x(const __nv_bfloat16 *__restrict__ x, int
 // f32 CUDA-core dot of one warp's chunk (16 rows x 256 k) of a stage, used
 // only when the activations' dynamic range is too wide for exact f16
 // staging.  Adds the 16 x MT partial sums into `rw` (lane 0).
-template <int MT>
+template <int MT, int FMT>
 __device__ __noinline__ void chunk_f32(uint32_t stg, const __nv_bfloat16 *__restrict__ x, int K, int M, int k0, int w,
-                                       int lane, float *rw) {
+                                       int lane, float *rw, const uint8_t *__restrict__ mxs, int64_t n0, int64_t N) {
     for (int rr = 0; rr < 16; rr++) {
         const uint32_t word = lds32(stg + (uint32_t)((w * 16 + rr) * 128) +
                                     ((uint32_t)((lane >> 2) ^ (rr & 7)) << 4) + ((uint32_t)(lane & 3) << 2));
-        const uint32_t sb = lds8(stg + PAY_BYTES + (uint32_t)((w >> 3) * 2048 + rr * 128) + ((uint32_t)((w & 7) ^ (rr & 7)) << 4) +
-                                 (uint32_t)(lane >> 1));
-        const float sc = e4m3_f32(sb);
+        float sc;
+        if (FMT == Q4_NVFP4) {
+            const uint32_t sb = lds8(stg + PAY_BYTES + (uint32_t)((w >> 3) * 2048 + rr * 128) +
+                                     ((uint32_t)((w & 7) ^ (rr & 7)) << 4) + (uint32_t)(lane >> 1));
+            sc = e4m3_f32(sb);
+        } else {                 // rows past N carry zero payload: any scale
+            sc = n0 + rr < N ? e8m0_f32(__ldg(mxs + (n0 + rr) * (K >> 5) + ((k0 + lane * 8) >> 5))) : 0.0f;
+        }
         for (int m = 0; m < MT; m++) {
             float acc = 0.0f;
             if (m < M) {
@@ -371,9 +401,9 @@ __device__ __noinline__ void chunk_f32(uint32_t stg, const __nv_bfloat16 *__rest
 
 __device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, %0;" ::"r"(CW * 32) : "memory"); }
 
-template <int MT>
+template <int MT, int FMT>
 __global__ void __launch_bounds__(THREADS, Q4_TMA_CTAS_PER_SM)
-    gemv_tma_nvfp4(const __grid_constant__ Maps maps, const __grid_constant__ Args a) {
+    gemv_tma_fp4(const __grid_constant__ Maps maps, const __grid_constant__ Args a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *base = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     const int S = a.S;
@@ -419,11 +449,14 @@ __global__ void __launch_bounds__(THREADS, Q4_TMA_CTAS_PER_SM)
                             break;
                         }
                         const uint32_t dst = ring + (uint32_t)(slot * STAGE_BYTES), bar = smem_u32(&full[slot]);
-                        mbar_arrive_expect_tx(&full[slot], STAGE_BYTES);
+                        mbar_arrive_expect_tx(&full[slot], FMT == Q4_NVFP4 ? STAGE_BYTES : PAY_BYTES);
                         tma_3d(dst, &maps.pay[member], 0, row0, st * (KS / 256), bar, pol);
+                        if (FMT == Q4_NVFP4) {
 #pragma unroll
-                        for (int sb = 0; sb < CW / 8; sb++)   // 128-byte scale boxes: the swizzle span
-                            tma_2d(dst + PAY_BYTES + sb * 2048, &maps.sc[member], st * (KS / 16) + sb * 128, row0, bar, pol);
+                            for (int sb = 0; sb < CW / 8; sb++)   // 128-byte scale boxes: the swizzle span
+                                tma_2d(dst + PAY_BYTES + sb * 2048, &maps.sc[member], st * (KS / 16) + sb * 128, row0,
+                                       bar, pol);
+                        }
                         issued++;
                         if (++slot == S) { slot = 0; phase ^= 1; }
                         if (issued == PREFETCH_STAGES) {
@@ -439,8 +472,9 @@ __global__ void __launch_bounds__(THREADS, Q4_TMA_CTAS_PER_SM)
                                 }
                                 const int prow0 = (pt - a.tile_start[pm]) * 16;
                                 tma_prefetch_3d(&maps.pay[pm], 0, prow0, pst * (KS / 256));
-                                for (int sb = 0; sb < CW / 8; sb++)
-                                    tma_prefetch_2d(&maps.sc[pm], pst * (KS / 16) + sb * 128, prow0);
+                                if (FMT == Q4_NVFP4)
+                                    for (int sb = 0; sb < CW / 8; sb++)
+                                        tma_prefetch_2d(&maps.sc[pm], pst * (KS / 16) + sb * 128, prow0);
                             }
                             // Hold further copies until the decode warps have read x (or ~0.5 s,
                             // or an abort): a deeper prefetch queues their x loads behind this
@@ -473,8 +507,20 @@ __global__ void __launch_bounds__(THREADS, Q4_TMA_CTAS_PER_SM)
                 if (k < K0) asm volatile("prefetch.global.L2 [%0];" ::"l"(a.x[0] + (int64_t)m * K0 + k));
             }
     }
-    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int g = lane >> 2, tt = lane & 3;
+    // MXFP4: lane l's 4 scale bytes of the warp's chunk in stage `st_` of tile
+    // `tile_`: row l / 2, bytes 4 (l & 1) .. +3 of the chunk's 8 (scale byte j
+    // of row n at n * K/32 + j; aligned since K % 256 == 0).  Weights: read
+    // before the dependency wait like the payload.
+    const int64_t mx_rs = a.K[0] >> 5;
+    auto mx_word = [&](int tile_, int st_) -> uint32_t {
+        const int64_t row = (int64_t)tile_ * 16 + (lane >> 1);
+        const int col = st_ * 64 + warp * 8 + (lane & 1) * 4;
+        if (FMT != Q4_MXFP4 || tile_ >= a.ntiles[0] || col >= (int)mx_rs || row >= a.N[0]) return 0x7f7f7f7fu;
+        return __ldg(reinterpret_cast<const unsigned *>(a.mx_scales + row * mx_rs + col));   // 2^0 above
+    };
+    uint32_t mxv = mx_word((int)blockIdx.x, 0);
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     uint2 *xs = xs_all + (size_t)warp * a.max_nst * 2 * 8 * MT * 4;
     const uint32_t ring = smem_u32(base);
     // payload byte offsets of this lane's two units in rows g and g+8 of chunk `warp`
@@ -506,25 +552,51 @@ __global__ void __launch_bounds__(THREADS, Q4_TMA_CTAS_PER_SM)
         int mb = a.m0[p];
         for (int tile = (int)blockIdx.x; tile < ntiles; tile += (int)gridDim.x) {
             float *rw = red + (par * CW + warp) * 16 * MT;
-            if (!exact) {
+            if (!exact || FMT == Q4_MXFP4) {     // MXFP4 stages may add f32 partials
                 for (int e = lane; e < 16 * MT; e += 32) rw[e] = 0.0f;
                 __syncwarp();
             }
             const uint2 *xb = xbase;
             for (int st = 0, k0 = warp * 256; st < nst; st++, k0 += KS) {
+                const uint32_t mxcur = mxv;
+                if (FMT == Q4_MXFP4)             // the next stage's scale word, one stage ahead
+                    mxv = st + 1 < nst ? mx_word(tile, st + 1) : mx_word(tile + (int)gridDim.x, 0);
                 const bool ok = wait_or_abort(&full[slot], (uint32_t)phase, abort_flag);
                 if (ok && k0 < K) {
-                    if (exact) {
-                        const uint4 pa[2] = {lds128(stg + offA0), lds128(stg + offA1)};
-                        const uint4 pb[2] = {lds128(stg + offA0 + ROW8), lds128(stg + offA1 + ROW8)};
-                        const uint32_t sa = lds32(stg + offS), sb = lds32(stg + offS + ROW8);
+                    bool sok = true;
+                    uint32_t mxs2[2][2];         // MXFP4: [h][row g / g+8] scale as f16x2
+                    if (FMT == Q4_MXFP4) {
+                        // the warp's 16 x 8 scale bytes through the slot's unused scale area
+                        // (rows 68 bytes apart: the lanes' 2-byte reads hit distinct banks)
+                        sts32(stg + PAY_BYTES + (uint32_t)((lane >> 1) * 68 + warp * 8 + (lane & 1) * 4), mxcur);
+                        __syncwarp();
+                        const uint32_t ra = lds16(stg + PAY_BYTES + (uint32_t)(g * 68 + warp * 8 + 2 * tt));
+                        const uint32_t rb = lds16(stg + PAY_BYTES + (uint32_t)((g + 8) * 68 + warp * 8 + 2 * tt));
 #pragma unroll
                         for (int h = 0; h < 2; h++) {
-                            uint32_t ha, hb;
-                            asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(ha) : "h"((uint16_t)(sa >> (16 * h))));
-                            asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(hb) : "h"((uint16_t)(sb >> (16 * h))));
-                            const uint32_t sca[2] = {prmt(ha, ha, 0x1010u), prmt(ha, ha, 0x3232u)};
-                            const uint32_t scb[2] = {prmt(hb, hb, 0x1010u), prmt(hb, hb, 0x3232u)};
+                            mxs2[h][0] = e8m0_h2(ra >> (8 * h), sok);
+                            mxs2[h][1] = e8m0_h2(rb >> (8 * h), sok);
+                        }
+                        sok = __all_sync(0xffffffffu, sok);
+                    }
+                    if (exact && sok) {
+                        const uint4 pa[2] = {lds128(stg + offA0), lds128(stg + offA1)};
+                        const uint4 pb[2] = {lds128(stg + offA0 + ROW8), lds128(stg + offA1 + ROW8)};
+                        uint32_t sa = 0, sb = 0;
+                        if (FMT == Q4_NVFP4) sa = lds32(stg + offS), sb = lds32(stg + offS + ROW8);
+#pragma unroll
+                        for (int h = 0; h < 2; h++) {
+                            uint32_t sca[2], scb[2];
+                            if (FMT == Q4_NVFP4) {
+                                uint32_t ha, hb;
+                                asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(ha) : "h"((uint16_t)(sa >> (16 * h))));
+                                asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(hb) : "h"((uint16_t)(sb >> (16 * h))));
+                                sca[0] = prmt(ha, ha, 0x1010u), sca[1] = prmt(ha, ha, 0x3232u);
+                                scb[0] = prmt(hb, hb, 0x1010u), scb[1] = prmt(hb, hb, 0x3232u);
+                            } else {                 // one scale per 32 k: the whole unit
+                                sca[0] = sca[1] = mxs2[h][0];
+                                scb[0] = scb[1] = mxs2[h][1];
+                            }
                             const uint32_t wa[4] = {pa[h].x, pa[h].y, pa[h].z, pa[h].w};
                             const uint32_t wb[4] = {pb[h].x, pb[h].y, pb[h].z, pb[h].w};
                             const uint2 *xh = xb + h * 8 * MT * 4;
@@ -545,7 +617,7 @@ __global__ void __launch_bounds__(THREADS, Q4_TMA_CTAS_PER_SM)
                             }
                         }
                     } else {
-                        chunk_f32<MT>(stg, x, K, a.M, k0, warp, lane, rw);
+                        chunk_f32<MT, FMT>(stg, x, K, a.M, k0, warp, lane, rw, a.mx_scales, (int64_t)tile * 16, a.N[0]);
                     }
                 }
                 __syncwarp();
@@ -562,11 +634,18 @@ __global__ void __launch_bounds__(THREADS, Q4_TMA_CTAS_PER_SM)
                 d[0] += dacc[i][0]; d[1] += dacc[i][1]; d[2] += dacc[i][2]; d[3] += dacc[i][3];
                 dacc[i][0] = dacc[i][1] = dacc[i][2] = dacc[i][3] = 0.0f;
             }
-            if (exact) {
+            if (exact && FMT == Q4_NVFP4) {
 #pragma unroll
                 for (int mm = 0; mm < MT; mm++) {
                     if (mm == 2 * tt) { rw[g * MT + mm] = d[0] * inv[mm]; rw[(g + 8) * MT + mm] = d[2] * inv[mm]; }
                     if (mm == 2 * tt + 1) { rw[g * MT + mm] = d[1] * inv[mm]; rw[(g + 8) * MT + mm] = d[3] * inv[mm]; }
+                }
+            } else if (exact) {                  // MXFP4: add to the f32 stages' partials
+                __syncwarp();
+#pragma unroll
+                for (int mm = 0; mm < MT; mm++) {
+                    if (mm == 2 * tt) { rw[g * MT + mm] += d[0] * inv[mm]; rw[(g + 8) * MT + mm] += d[2] * inv[mm]; }
+                    if (mm == 2 * tt + 1) { rw[g * MT + mm] += d[1] * inv[mm]; rw[(g + 8) * MT + mm] += d[3] * inv[mm]; }
                 }
             }
             consumer_sync();
@@ -640,9 +719,9 @@ template <typename Kern> int resident_ctas(Kern kern, size_t smem) {
     return b * sm_count();
 }
 
-template <int MT>
+template <int MT, int FMT>
 cudaError_t run(const Maps &maps, const Args &args, int max_tiles, size_t smem, cudaStream_t s) {
-    auto kern = gemv_tma_nvfp4<MT>;
+    auto kern = gemv_tma_fp4<MT, FMT>;
     static bool attr_set[64] = {};
     static int grid_cache[64] = {};
     int dev = 0;
@@ -676,7 +755,8 @@ cudaError_t run(const Maps &maps, const Args &args, int max_tiles, size_t smem, 
 // Eligible: NVFP4 with bf16 x, K % 256 == 0, batch 1..4, and at least
 // MIN_STAGES ring stages beside the staged x in 112 KB of shared memory.
 bool gemv_tma_eligible(const Tensor &t, int64_t M) {
-    if (t.fmt != Q4_NVFP4 || M < 1 || M > 4 || t.K % 256 != 0 || t.K > (1LL << 30) || t.N > (1LL << 31))
+    if ((t.fmt != Q4_NVFP4 && t.fmt != Q4_MXFP4) || M < 1 || M > 4 || t.K % 256 != 0 || t.K > (1LL << 30) ||
+        t.N > (1LL << 31))
         return false;
     if ((((uintptr_t)t.w | (uintptr_t)t.scales) & 15) != 0) return false;
     return stages_for(t.K, mt_for(M)) >= MIN_STAGES && encode_fn() != nullptr;
@@ -691,6 +771,8 @@ bool gemv_tma_chain_fits(const Tensor *ts, const int *first, int ngroups, int64_
         if (first[p + 1] <= first[p]) return false;
         for (int i = first[p]; i < first[p + 1]; i++)
             if (!gemv_tma_eligible(ts[i], M) || ts[i].K != ts[first[p]].K) return false;
+        // MXFP4 runs as a single matrix only (its scales come through one pointer)
+        if (ts[first[p]].fmt == Q4_MXFP4 && (ngroups > 1 || first[p + 1] - first[p] > 1)) return false;
         max_K = ts[first[p]].K > max_K ? ts[first[p]].K : max_K;
     }
     return stages_for(max_K, mt_for(M)) >= MIN_STAGES;
@@ -715,8 +797,13 @@ cudaError_t launch_gemv_tma_chain(const Tensor *ts, const void *const *xs, float
         max_K = ts[first[p]].K > max_K ? ts[first[p]].K : max_K;
         int tiles = 0;
         for (int i = first[p]; i < first[p + 1]; i++) {
-            if (!encode_payload(&maps.pay[i], ts[i]) || !encode_scales(&maps.sc[i], ts[i]))
-                return cudaErrorInvalidValue;
+            if (!encode_payload(&maps.pay[i], ts[i])) return cudaErrorInvalidValue;
+            if (ts[i].fmt == Q4_NVFP4) {
+                if (!encode_scales(&maps.sc[i], ts[i])) return cudaErrorInvalidValue;
+            } else {
+                maps.sc[i] = maps.pay[i];                 // never read: MXFP4 scales come through mx_scales
+                args.mx_scales = ts[i].scales;
+            }
             args.y[i] = ys[i];
             args.N[i] = ts[i].N;
             args.scale2[i] = ts[i].scale2;
@@ -732,9 +819,14 @@ cudaError_t launch_gemv_tma_chain(const Tensor *ts, const void *const *xs, float
     args.S = stages_for(max_K, mt);
     if (args.S < MIN_STAGES) return cudaErrorInvalidValue;
     const size_t smem = fixed_smem(max_K, mt) + (size_t)args.S * STAGE_BYTES;
-    if (mt == 1) return run<1>(maps, args, max_tiles, smem, s);
-    if (mt == 2) return run<2>(maps, args, max_tiles, smem, s);
-    return run<4>(maps, args, max_tiles, smem, s);
+    if (ts[0].fmt == Q4_MXFP4) {
+        if (mt == 1) return run<1, Q4_MXFP4>(maps, args, max_tiles, smem, s);
+        if (mt == 2) return run<2, Q4_MXFP4>(maps, args, max_tiles, smem, s);
+        return run<4, Q4_MXFP4>(maps, args, max_tiles, smem, s);
+    }
+    if (mt == 1) return run<1, Q4_NVFP4>(maps, args, max_tiles, smem, s);
+    if (mt == 2) return run<2, Q4_NVFP4>(maps, args, max_tiles, smem, s);
+    return run<4, Q4_NVFP4>(maps, args, max_tiles, smem, s);
 }
 
 // Several NVFP4 GEMVs that read the same x and share K and M, in one launch

@@ -121,12 +121,13 @@ typedef struct {
  * weights into shared memory by tensor TMA (weights are read before the
  * stream dependency on the previous launch resolves, x and y after it, so W
  * must not be written by a still-running kernel that released its dependents
- * early; the library's own kernels that do so only read weights).  AWQ with
- * group 128, no g_idx, N % 128 == 0 and K % 128 == 0 (any M, in launches of
- * up to 8 rows) runs a TMA-fed tensor-core kernel with the same rule for W,
- * its scales and zeros: codes minus zero points formed exactly in f16 as the
- * MMA's B operand, x as f16 hi + lo terms, K split over a thread-block
- * cluster and reduced in rank order (repeated calls agree bit for bit).  M >= 9
+ * early; the library's own kernels that do so only read weights).  GPTQ
+ * and AWQ with group 128, no g_idx, N % 128 == 0 and K % 128 == 0 (any M, in
+ * launches of up to 8 rows) run TMA-fed tensor-core kernels with the same
+ * rule for W, its scales and zeros: codes minus zero points formed exactly
+ * in f16 as an MMA operand, x as f16 hi + lo terms, K split over a
+ * thread-block cluster and reduced in rank order (repeated calls agree bit
+ * for bit).  M >= 9
  * with bf16 x on NVFP4 or Q4_K (K % 256 == 0) runs the
  * tcgen05 tensor-core kernel: weights decoded to bf16 straight into tensor
  * memory, x tiles by TMA, f32 accumulation in TMEM, K split over a cluster
@@ -402,7 +403,7 @@ int q4_last_error(void);
  * "gemv_fp4tc_group", "gemv_tma", "gemv_tma_group",
  * "gemv_tma_chain", "gemm_tc", "gemv_mma", "gemv_mma_group", "gemv_mma_q4k",
  * "gemv_mma_q40", "gemv_mma_gptq", "gemv_rows_tma", "gemv_rows_m1",
- * "gemv_general", "gemv_kmajor", "gemv_awq_tc"; "gemv_a16q8" after q4_gemv_a16q8,
+ * "gemv_general", "gemv_kmajor", "gemv_awq_tc", "gemv_gptq_tc"; "gemv_a16q8" after q4_gemv_a16q8,
  * "gemv_q4k_q8" after q4_gemv_q4k_q8, "gemv_w4a4" after q4_gemv_w4a4,
  * "gemv_w4a4_tc" after q4_gemv_w4a4_tc; "" before
  * the first call).  A diagnostic with no counterpart in the pages: it lets a

@@ -30,6 +30,16 @@ def built():
     q4.lib()
 
 
+def tma_fits(K, M):
+    """The TMA-fed kernel's shared-memory rule: the staged x (2 bytes per k
+    and batch column, K rounded up to 2048-k stages) and the fixed areas
+    leave room for at least 3 ring stages of 18 KB in 112 KB."""
+    mt = 1 if M == 1 else 2 if M == 2 else 4
+    nst = -(-K // 2048)
+    fixed = 1024 + 144 + 2 * 8 * 16 * mt * 4 + 8 * nst * 2 * 8 * mt * 4 * 8
+    return (112 * 1024 - fixed) // 18432 >= 3
+
+
 def shape_for(fmt, small=True):
     """(N, K) spanning several CTA tiles with ragged tails."""
     return {"nvfp4": (37, 4128), "mxfp4": (41, 2080), "q4k": (29, 1536), "q40": (33, 2080),
@@ -164,19 +174,22 @@ def test_gemv_nvfp4_tensor_core_path(M):
         check_gemv(synth.make_layer("nvfp4", N, K, config=30, matrix=M, row_scale=True), M, config=30 + M)
 
 
-@pytest.mark.parametrize("M", [1, 3, 8])
+@pytest.mark.parametrize("M", [1, 2, 3, 4, 8])
 def test_gemv_mxfp4_tensor_core_path(M):
-    """MXFP4 with K % 128 == 0 and bf16 x also runs the mma.sync decode-dot
-    kernel (E8M0 scale folded into the f16 A fragment)."""
-    for N, K in ((41, 2048), (263, 11008), (16, 128)):
+    """MXFP4 with bf16 x on the tensor cores (E8M0 scale folded into the f16
+    A fragment): batch 1..4 with K % 256 == 0 on the TMA-fed kernel (scales
+    read by the lanes one stage ahead; 4096 x 11008 has 344-byte scale rows
+    that no tensor map could read), otherwise the register-fed kernel."""
+    for N, K in ((41, 2048), (263, 11008), (16, 128), (1, 256)):
         check_gemv(synth.make_layer("mxfp4", N, K, config=33, matrix=M, outliers=True), M, config=33 + M)
-        assert q4.q4_last_gemv_path() == "gemv_mma"
+        assert q4.q4_last_gemv_path() == ("gemv_tma" if M <= 4 and K % 256 == 0 and tma_fits(K, M) else "gemv_mma")
 
 
 def test_gemv_mxfp4_scales_outside_the_exact_f16_range():
     """E8M0 scales whose E2M1 multiples are not all f16 numbers (2^-40, 2^20;
-    2^-23 and 2^13 are the edges that still are) make those warps recompute
-    their tiles in f32; the result stays within tolerance."""
+    2^-23 and 2^13 are the edges that still are) send those warps' tiles
+    (register-fed kernel) or stages (TMA-fed kernel, batch 1 and 4) to f32;
+    the result stays within tolerance."""
     layer = synth.make_layer("mxfp4", 40, 4096, config=34, matrix=0)
     s = layer["scales"].copy()
     s[3, 5] = 127 - 40
@@ -184,8 +197,9 @@ def test_gemv_mxfp4_scales_outside_the_exact_f16_range():
     s[30, 100] = 127 - 23
     s[31, 7] = 127 + 13
     layer = dict(layer, scales=s)
-    for M in (1, 4):
+    for M in (1, 4, 8):
         check_gemv(layer, M, config=34)
+        assert q4.q4_last_gemv_path() == ("gemv_tma" if M <= 4 else "gemv_mma")
 
 
 @pytest.mark.parametrize("xdtype", ["f32", "bf16"])
@@ -238,6 +252,50 @@ def test_gemv_awq_tensor_core_path(M, xdtype):
     # N % 128 != 0 stays on the CUDA-core kernel
     check_gemv(synth.make_layer("awq", 264, 1152, config=39, matrix=M), M, config=39, xdtype=xdtype)
     assert q4.q4_last_gemv_path() != "gemv_awq_tc"
+
+
+@pytest.mark.parametrize("xdtype", ["f32", "bf16"])
+@pytest.mark.parametrize("M", [1, 3, 4, 5, 8, 11])
+def test_gemv_gptq_tma_tensor_core_path(M, xdtype):
+    """GPTQ (group 128, N % 128 == 0) on the TMA-fed tensor-core kernel: the
+    weights are the MMA's A operand (byte t of a word holds k = 2t, 2t+1;
+    q - z and 16 (q - z) formed exactly in f16, odd-k x staged divided by
+    16), x hi and lo terms share the n8 columns (two B tiles at batch 5..8),
+    the K range split over up to 8 cluster ranks, batch 11 as two launches."""
+    for N, K in ((128, 1152), (384, 4096), (11008, 128), (768, 11008)):
+        check_gemv(synth.make_layer("gptq", N, K, config=42, matrix=M, outliers=True), M, config=42 + M,
+                   xdtype=xdtype)
+        assert q4.q4_last_gemv_path() == "gemv_gptq_tc"
+    # N % 128 != 0 stays on the register-fed kernel
+    check_gemv(synth.make_layer("gptq", 264, 1152, config=42, matrix=M), M, config=42, xdtype=xdtype)
+    assert q4.q4_last_gemv_path() != "gemv_gptq_tc"
+
+
+def test_gemv_gptq_tma_tensor_core_edge_values():
+    """x over 1e30 .. 1e-10, an all-zero x (exactly 0), every code and every
+    stored zero (0..15, i.e. zero points 1..16) in use, and act-order (g_idx)
+    tensors staying on the general kernel."""
+    N, K = 256, 2048
+    layer = synth.make_layer("gptq", N, K, config=43, matrix=0)
+    for M in (1, 3):
+        xf = np.random.default_rng(M).normal(0, 1e-10, (M, K)).astype(np.float32)
+        xf[:, 7] = 1e30
+        xf[:, 1501] = -3e20
+        y = gpu_gemv(layer, x_device(xf), M)
+        assert q4.q4_last_gemv_path() == "gemv_gptq_tc"
+        ref, bound = oracle.gemv(to_oracle(layer), xf)
+        ok, worst = within_tolerance(y, ref, bound)
+        assert ok, worst
+    y = gpu_gemv(layer, torch.zeros((2, K), dtype=torch.bfloat16, device="cuda"), 2)
+    assert np.all(y == 0)
+    rng = np.random.default_rng(6)
+    rand = dict(layer, w=rng.integers(-2**31, 2**31, layer["w"].shape, dtype=np.int64).astype(np.int32),
+                zeros=rng.integers(-2**31, 2**31, layer["zeros"].shape, dtype=np.int64).astype(np.int32))
+    check_gemv(rand, 2, config=43)
+    act = synth.make_layer("gptq", 256, 512, config=43, matrix=1, act_order=True)
+    check_gemv(act, 1, config=43)
+    assert q4.q4_last_gemv_path() != "gemv_gptq_tc"
+    assert q4.q4_last_error() == 0
 
 
 def test_gemv_awq_tensor_core_edge_values():
