@@ -27,10 +27,45 @@ template <> __device__ __forceinline__ float wload<__nv_bfloat16>(const __nv_bfl
     return __bfloat162float(p[i]);
 }
 
+// 8 consecutive weights as f32 (one or two 16-byte loads; p 16-byte aligned).
+template <typename WT> __device__ __forceinline__ void load8w(const WT *p, float v[8]);
+template <> __device__ __forceinline__ void load8w<float>(const float *p, float v[8]) {
+    const float4 a = __ldg(reinterpret_cast<const float4 *>(p)), b = __ldg(reinterpret_cast<const float4 *>(p) + 1);
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+}
+template <> __device__ __forceinline__ void load8w<__nv_bfloat16>(const __nv_bfloat16 *p, float v[8]) {
+    const uint4 u = __ldg(reinterpret_cast<const uint4 *>(p));
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; i++) {
+        v[2 * i] = __uint_as_float(w[i] << 16);
+        v[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+    }
+}
+
+// Largest |w| over the tensor: runs of 8 weights (16-byte loads), four runs
+// in flight per thread, then the scalar tail.
 template <typename WT>
 __global__ void amax_kernel(const WT *__restrict__ W, int64_t n, unsigned *amax_bits) {
     float m = 0.0f;
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
+    const int64_t runs = n / 8, stride = (int64_t)gridDim.x * blockDim.x;
+    int64_t r = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    for (; r + 3 * stride < runs; r += 4 * stride) {
+        float v[4][8];
+#pragma unroll
+        for (int u = 0; u < 4; u++) load8w<WT>(W + (r + u * stride) * 8, v[u]);
+#pragma unroll
+        for (int u = 0; u < 4; u++)
+#pragma unroll
+            for (int i = 0; i < 8; i++) m = fmaxf(m, fabsf(v[u][i]));
+    }
+    for (; r < runs; r += stride) {
+        float v[8];
+        load8w<WT>(W + r * 8, v);
+#pragma unroll
+        for (int i = 0; i < 8; i++) m = fmaxf(m, fabsf(v[i]));
+    }
+    for (int64_t i = runs * 8 + (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride)
         m = fmaxf(m, fabsf(wload(W, i)));
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
@@ -90,8 +125,8 @@ __global__ void quantize_nvfp4_kernel(const WT *__restrict__ W, int64_t N, int64
     const int64_t groups = N * (K / 16);
     for (int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; g < groups; g += (int64_t)gridDim.x * blockDim.x) {
         float w[16];
-#pragma unroll
-        for (int i = 0; i < 16; i++) w[i] = wload(W, g * 16 + i);
+        load8w<WT>(W + g * 16, w);
+        load8w<WT>(W + g * 16 + 8, w + 8);
         float amax_g = 0.0f;
 #pragma unroll
         for (int i = 0; i < 16; i++) amax_g = fmaxf(amax_g, fabsf(w[i]));
@@ -175,9 +210,9 @@ __global__ void __launch_bounds__(256) quantize_q4k_kernel(const WT *__restrict_
     const int lane = threadIdx.x & 31;
     const int64_t blk = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
     if (blk >= nblocks) return;                                        // warp-uniform
-    const int64_t nb = K / 256, n = blk / nb, b = blk % nb;
+    (void)K;
     float w[8];
-    load8<WT>(W + n * K + b * 256 + lane * 8, w);
+    load8<WT>(W + blk * 256 + lane * 8, w);                            // row n, block b: (n * K/256 + b) * 256
     float lo = 0.0f, hi = w[0];
 #pragma unroll
     for (int i = 0; i < 8; i++) {
