@@ -298,14 +298,17 @@ def run_ours(args, rank, world):
             torch.distributed.barrier()
 
     with torch.cuda.stream(stream):
-        replay(warm)
-        for g, _ in timed:           # uploads the timed graphs (untimed; their steps are extra warm-up)
-            g.replay()
-        torch.cuda.synchronize()
-        barrier()
-        torch.cuda.synchronize()
         start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        # The clock sampler starts before the warm-up: its start-up (a process and a short sleep) left the
+        # GPU idle just before the timed steps when it started after the barrier, and a 20-step region
+        # (~0.5 ms) then began at lowered clocks (+1.5-2 us per step, measured).
         with ClockSampler(torch.cuda.current_device()) as clk:
+            replay(warm)
+            for g, _ in timed:           # uploads the timed graphs (untimed; their steps are extra warm-up)
+                g.replay()
+            torch.cuda.synchronize()
+            barrier()
+            torch.cuda.synchronize()
             start.record(stream)
             replay(timed)
             end.record(stream)
@@ -359,7 +362,7 @@ def run_ours(args, rank, world):
                    "launch": "2 launches per step: q4_gemv_grouped(gate, up) (shared x) then q4_gemv(down), "
                              "chained by programmatic dependent launch; the timed steps are one CUDA graph "
                              f"(up to {MAX_STEPS_PER_GRAPH} steps per graph), step i on weight copy i % copies",
-                   "warmup": "the --warmup steps as a graph, then one untimed replay of the timed graph "
+                   "warmup": "clock sampling starts, then the --warmup steps as a graph and one untimed replay of the timed graph "
                              "(its upload)",
                    "parallelism": f"replicas x{world}"},
         "pct_of_hbm_peak": {"measured": round(value / world / peak, 4),
