@@ -689,6 +689,7 @@ int pack_read_and_clear_error();
 int fp4tc_read_and_clear_error();
 int awq_read_and_clear_error();
 int gptq_tc_read_and_clear_error();
+int blk_tc_read_and_clear_error();
 
 int read_and_clear_device_error() {
     int v = 0;
@@ -702,7 +703,8 @@ int read_and_clear_device_error() {
     const int f4 = fp4tc_read_and_clear_error();
     const int aw = awq_read_and_clear_error();
     const int gq = gptq_tc_read_and_clear_error();
-    return v ? v : g ? g : tm ? tm : pk ? pk : f4 ? f4 : aw ? aw : gq;
+    const int bt = blk_tc_read_and_clear_error();
+    return v ? v : g ? g : tm ? tm : pk ? pk : f4 ? f4 : aw ? aw : gq ? gq : bt;
 }
 
 }  // namespace q4

@@ -901,6 +901,10 @@ cudaError_t launch_gemv(const Tensor &t, const void *x, q4_dtype x_dtype, float 
         note_gemv_path("gemv_mma_gptq");
         return launch_gemv_gptq(t, x, x_dtype, y, M, s);
     }
+    if (gemv_blk_tc_eligible(t, M) && ((uintptr_t)x & 15) == 0) {     // x read in 16-byte vectors
+        note_gemv_path(t.fmt == Q4_Q4K ? "gemv_blk_tc_q4k" : "gemv_blk_tc_q40");
+        return launch_gemv_blk_tc(t, x, x_dtype, y, s);
+    }
     if (gemv_blk_eligible(t, M)) {
         note_gemv_path(t.fmt == Q4_Q4K ? "gemv_mma_q4k" : "gemv_mma_q40");
         return launch_gemv_blk(t, x, x_dtype, y, M, s);

@@ -35,9 +35,10 @@ cudaError_t launch_unpack_bits(const uint32_t *words, int64_t n, int bits, uint8
 cudaError_t launch_permute_k(const void *x, q4_dtype xd, const int32_t *perm, void *out, int64_t M, int64_t K,
                              cudaStream_t s);
 
-// Role-wait limits of the bounded-wait kernels (gemv_tma.cu, gemv_fp4tc.cu).
+// Role-wait limits of the bounded-wait kernels (gemv_tma.cu, gemv_fp4tc.cu, gemv_blk_tc.cu).
 int gemv_tma_set_wait_limit(long long cycles);
 int fp4tc_set_wait_limit(long long cycles);
+int blk_tc_set_wait_limit(long long cycles);
 
 int sm_count() {
     int dev = 0, n = 0;
@@ -245,8 +246,8 @@ const char *q4_last_gemv_path(void) { return q4::g_last_path; }
 
 int q4_set_wait_limit(int64_t cycles) {
     const long long c = cycles > 0 ? (long long)cycles : (1LL << 31);
-    const int a = gemv_tma_set_wait_limit(c), b = fp4tc_set_wait_limit(c);
-    return a ? a : b;
+    const int a = gemv_tma_set_wait_limit(c), b = fp4tc_set_wait_limit(c), d = blk_tc_set_wait_limit(c);
+    return a ? a : b ? b : d;
 }
 
 int q4_gemv_a16q8(const void *W_packed, const void *scales, const q4_aux *aux, const void *x, float *y, int64_t M,

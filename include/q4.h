@@ -127,7 +127,12 @@ typedef struct {
  * rule for W, its scales and zeros: codes minus zero points formed exactly
  * in f16 as an MMA operand, x as f16 hi + lo terms, K split over a
  * thread-block cluster and reduced in rank order (repeated calls agree bit
- * for bit).  M >= 9
+ * for bit).  Q4_K and Q4_0 with M == 1, K % 256 == 0 and K <= 12288 (the
+ * staged x and three 18 KB ring stages within 112 KB of shared memory) run a
+ * TMA-fed tensor-core kernel with the same rule for W: 16 rows x 2048 k per
+ * stage, the codes as exact f16 MMA operands (Q4_K: q, its sub-block scale
+ * and min applied per lane in f32; Q4_0: q - 8), repeated calls agreeing bit
+ * for bit.  M >= 9
  * with bf16 x on NVFP4 or Q4_K (K % 256 == 0) runs the
  * tcgen05 tensor-core kernel: weights decoded to bf16 straight into tensor
  * memory, x tiles by TMA, f32 accumulation in TMEM, K split over a cluster
@@ -403,7 +408,8 @@ int q4_last_error(void);
  * "gemv_fp4tc_group", "gemv_tma", "gemv_tma_group",
  * "gemv_tma_chain", "gemm_tc", "gemv_mma", "gemv_mma_group", "gemv_mma_q4k",
  * "gemv_mma_q40", "gemv_mma_gptq", "gemv_rows_tma", "gemv_rows_m1",
- * "gemv_general", "gemv_kmajor", "gemv_awq_tc", "gemv_gptq_tc"; "gemv_a16q8" after q4_gemv_a16q8,
+ * "gemv_general", "gemv_kmajor", "gemv_awq_tc", "gemv_gptq_tc", "gemv_blk_tc_q4k",
+ * "gemv_blk_tc_q40"; "gemv_a16q8" after q4_gemv_a16q8,
  * "gemv_q4k_q8" after q4_gemv_q4k_q8, "gemv_w4a4" after q4_gemv_w4a4,
  * "gemv_w4a4_tc" after q4_gemv_w4a4_tc; "" before
  * the first call).  A diagnostic with no counterpart in the pages: it lets a
@@ -412,8 +418,8 @@ const char *q4_last_gemv_path(void);
 
 /* Sets, for the current device, how long the bounded waits of the TMA-fed
  * kernels may spin before they give up: the waits between the roles of the
- * batch-1 FP4 tensor-core GEMV and of the batch 1-4 TMA GEMV, and the grid
- * barrier of q4_gemv_chain.  cycles <= 0 restores the default, 2^31 SM clocks
+ * batch-1 FP4 tensor-core GEMV, of the batch 1-4 TMA GEMV and of the batch-1
+ * Q4_K / Q4_0 TMA GEMV, and the grid barrier of q4_gemv_chain.  cycles <= 0 restores the default, 2^31 SM clocks
  * (about one second).  A wait that runs out records Q4_ETIMEOUT (read by
  * q4_last_error), the kernel's roles stop, the bulk copies and MMAs already
  * issued are waited for with the full limit, tensor memory is freed, and the

@@ -5,6 +5,7 @@ its own copies and MMAs in flight, free tensor memory and return; the
 context stays usable and the next call with the default limit is correct.
 
   * the batch-1 NVFP4 GEMV on the FP4 tensor cores (role waits);
+  * the batch-1 Q4_0 GEMV on the TMA-fed block-format kernel (role waits);
   * the GEMV chain's grid barrier, whose sync words the caller re-zeroes
     after a timeout, as its header requires."""
 import numpy as np
@@ -56,6 +57,32 @@ def test_fp4tc_role_wait_times_out_then_recovers():
     assert q4.q4_set_wait_limit(0) == q4.Q4_OK
     y.fill_(float("nan"))
     q4.q4_gemv("nvfp4", d["w"], d["scales"], aux, x, y, 1, N, K)
+    torch.cuda.synchronize()
+    assert q4.q4_last_error() == q4.Q4_OK
+    ref, bound = oracle_gemv_all_rows(to_oracle(layer), xf)
+    ok, worst = within_tolerance(y.cpu().numpy(), ref, bound)
+    assert ok, worst
+
+
+def test_blk_tc_role_wait_times_out_then_recovers():
+    # 4096 x 11008: six 2048-k stages per CTA through a three-stage ring, so
+    # the producer waits for freed slots and the decode warps for full ones
+    N, K = 4096, 11008
+    layer = synth.make_layer("q40", N, K, config=132, matrix=0)
+    d = to_device(layer)
+    xb, xf = synth.draw_x(1, K, config=132, matrix=1, dtype="f32")
+    x = x_device(xb)
+    y = torch.zeros((1, N), dtype=torch.float32, device="cuda")
+    aux = aux_for(layer, d, x_dtype=torch.float32)
+    assert q4.q4_last_error() == q4.Q4_OK
+    assert q4.q4_set_wait_limit(1) == q4.Q4_OK
+    q4.q4_gemv("q40", d["w"], d["scales"], aux, x, y, 1, N, K)
+    assert q4.q4_last_gemv_path() == "gemv_blk_tc_q40"
+    torch.cuda.synchronize()
+    assert q4.q4_last_error() == q4.Q4_ETIMEOUT
+    assert q4.q4_set_wait_limit(0) == q4.Q4_OK
+    y.fill_(float("nan"))
+    q4.q4_gemv("q40", d["w"], d["scales"], aux, x, y, 1, N, K)
     torch.cuda.synchronize()
     assert q4.q4_last_error() == q4.Q4_OK
     ref, bound = oracle_gemv_all_rows(to_oracle(layer), xf)
