@@ -135,13 +135,9 @@ __device__ __forceinline__ void load8(const __nv_bfloat16 *p, float (&v)[8]) {
 __device__ __forceinline__ void q4k_pair(uint32_t B0, uint32_t B1, uint32_t B2, int t, uint32_t &sc, uint32_t &mn) {
     const uint32_t p = 16u * (uint32_t)(t & 1);
     const uint32_t b0 = B0 >> p, b1 = B1 >> p, b2 = B2 >> p;
-    if (t < 2) {
-        sc = b0 & 0x3F3Fu;
-        mn = b1 & 0x3F3Fu;
-    } else {
-        sc = (b2 & 0x0F0Fu) | ((b0 >> 2) & 0x3030u);
-        mn = ((b2 >> 4) & 0x0F0Fu) | ((b1 >> 2) & 0x3030u);
-    }
+    const bool low = t < 2;                     // both forms, then a select: no divergent branch
+    sc = low ? (b0 & 0x3F3Fu) : ((b2 & 0x0F0Fu) | ((b0 >> 2) & 0x3030u));
+    mn = low ? (b1 & 0x3F3Fu) : (((b2 >> 4) & 0x0F0Fu) | ((b1 >> 2) & 0x3030u));
 }
 
 // step * (D_hi + D_lo) - off * S of one sub-block, where D_hi and D_lo are the
@@ -154,14 +150,21 @@ __device__ __forceinline__ float q4k_sub(float step, float dh, float dl, float o
     const float p = off * S, e = fmaf(off, S, -p);
     return fmaf(step, dl, fmaf(step, dh, -p)) - e;
 }
-// Lane t's two sub-blocks of one row (header H = d | dmin, scale words), each
-// in its own x scale: sv = {S_2t, 1/scale_2t, S_2t+1, 1/scale_2t+1}.
-__device__ __forceinline__ float q4k_rows_term(uint4 H, int t, float l0, float l1, float h0, float h1, float4 sv) {
+// Steps and offsets of lane t's two sub-blocks of one row (header H = d | dmin,
+// scale words): {step_2t, off_2t, step_2t+1, off_2t+1}, the steps carrying the
+// 2^24 of the subnormal codes.  Formed before the row's MMAs, off their path.
+__device__ __forceinline__ float4 q4k_terms(uint4 H, int t) {
     uint32_t sc, mn;
     q4k_pair(H.y, H.z, H.w, t, sc, mn);
-    const float d24 = half_bits_f32(H.x) * 16777216.0f, dmin = half_bits_f32(H.x >> 16);   // 2^24: codes are q * 2^-24
-    const float lo = q4k_sub(d24 * (float)(sc & 255u), l0, l1, dmin * (float)(mn & 255u), sv.x);
-    const float hi = q4k_sub(d24 * (float)(sc >> 8), h0, h1, dmin * (float)(mn >> 8), sv.z);
+    const float d24 = half_bits_f32(H.x) * 16777216.0f, dmin = half_bits_f32(H.x >> 16);
+    return make_float4(d24 * (float)(sc & 255u), dmin * (float)(mn & 255u), d24 * (float)(sc >> 8),
+                       dmin * (float)(mn >> 8));
+}
+// Lane t's two sub-blocks of one row, each in its own x scale:
+// sv = {S_2t, 1/scale_2t, S_2t+1, 1/scale_2t+1}.
+__device__ __forceinline__ float q4k_rows_term(float4 so, float l0, float l1, float h0, float h1, float4 sv) {
+    const float lo = q4k_sub(so.x, l0, l1, so.y, sv.x);
+    const float hi = q4k_sub(so.z, h0, h1, so.w, sv.z);
     return fmaf(hi, sv.w, lo * sv.y);
 }
 
@@ -256,23 +259,27 @@ gemv_blk_tc(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ Bt
             float ssum = 0.0f;
 #pragma unroll
             for (int q = 0; q < 2; q++) {
-                __half hh[4], hl[4];
-#pragma unroll
-                for (int r = 0; r < 4; r++) {
-                    const float f = v[4 * q + r] * sc;
-                    hh[r] = __float2half_rn(f);
-                    hl[r] = __float2half_rn(f - __half2float(hh[r]));
-                    ssum += __half2float(hh[r]) + __half2float(hl[r]);
-                }
+                const float f0 = v[4 * q] * sc, f1 = v[4 * q + 1] * sc, f2 = v[4 * q + 2] * sc, f3 = v[4 * q + 3] * sc;
+                // B pairs (k, k+2) and (k+1, k+3): f16 hi parts, then the f16 lo remainders
+                const __half2 h02 = __floats2half2_rn(f0, f2), h13 = __floats2half2_rn(f1, f3);
+                const float2 r02 = __half22float2(h02), r13 = __half22float2(h13);
+                const __half2 l02 = __floats2half2_rn(f0 - r02.x, f2 - r02.y);
+                const __half2 l13 = __floats2half2_rn(f1 - r13.x, f3 - r13.y);
                 // entry (tq, word i0 + q): [hi part: low-nibble half, high-nibble half][lo part: ...], 8 bytes each
                 const uint32_t e = xs_w + (uint32_t)(s * XU + (tq * 8 + i0 + q) * 32 + half * 8);
-                sts64(e, h2bits(hh[0], hh[2]), h2bits(hh[1], hh[3]));
-                sts64(e + 16, h2bits(hl[0], hl[2]), h2bits(hl[1], hl[3]));
+                sts64(e, *reinterpret_cast<const uint32_t *>(&h02), *reinterpret_cast<const uint32_t *>(&h13));
+                sts64(e + 16, *reinterpret_cast<const uint32_t *>(&l02), *reinterpret_cast<const uint32_t *>(&l13));
+                if (Q4K) {                      // the staged values themselves: the numbers the MMA multiplies
+                    const float2 s02 = __half22float2(l02), s13 = __half22float2(l13);
+                    ssum += ((r02.x + s02.x) + (r02.y + s02.y)) + ((r13.x + s13.x) + (r13.y + s13.y));
+                }
             }
             // the block's x sum in the units the MMA sees x in (Q4_K's min term) and its scale
-            if (half) ssum *= 16.0f;
-            ssum += __shfl_xor_sync(0xffffffffu, ssum, 1);
-            ssum += __shfl_xor_sync(0xffffffffu, ssum, 2);
+            if (Q4K) {
+                if (half) ssum *= 16.0f;
+                ssum += __shfl_xor_sync(0xffffffffu, ssum, 1);
+                ssum += __shfl_xor_sync(0xffffffffu, ssum, 2);
+            }
             if ((lane & 3) == 0) {
                 sx_w[s * 16 + 2 * (lane >> 2)] = ssum;
                 sx_w[s * 16 + 2 * (lane >> 2) + 1] = xinv;
@@ -300,6 +307,8 @@ gemv_blk_tc(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ Bt
             const uint32_t rg = R + (uint32_t)(g * UNIT), rg8 = rg + 8 * UNIT;
             if constexpr (Q4K) {
                 const uint4 H0 = lds128(rg), H1 = lds128(rg8);
+                const float4 sv = *reinterpret_cast<const float4 *>(sx_w + st * 16 + 4 * t);
+                const float4 so0 = q4k_terms(H0, t), so1 = q4k_terms(H1, t);
                 const uint4 c0a = lds128(rg + 16 + 32 * t), c0b = lds128(rg + 32 + 32 * t);
                 const uint4 c1a = lds128(rg8 + 16 + 32 * t), c1b = lds128(rg8 + 32 + 32 * t);
                 const uint32_t w0[8] = {c0a.x, c0a.y, c0a.z, c0a.w, c0b.x, c0b.y, c0b.z, c0b.w};
@@ -315,9 +324,8 @@ gemv_blk_tc(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ Bt
                              bx.z, bx.w);
                 }
                 // sub-blocks 2t (low nibbles) and 2t + 1 (high nibbles) of rows g and g + 8
-                const float4 sv = *reinterpret_cast<const float4 *>(sx_w + st * 16 + 4 * t);
-                acc0 += q4k_rows_term(H0, t, Dl[0], Dl[1], Dh[0], Dh[1], sv);
-                acc1 += q4k_rows_term(H1, t, Dl[2], Dl[3], Dh[2], Dh[3], sv);
+                acc0 += q4k_rows_term(so0, Dl[0], Dl[1], Dh[0], Dh[1], sv);
+                acc1 += q4k_rows_term(so1, Dl[2], Dl[3], Dh[2], Dh[3], sv);
             } else {
                 // blocks 2t (bytes 36t .. 36t+17) and 2t + 1 (36t+18 .. 36t+35) of rows g and g + 8
                 uint32_t W0[9], W1[9];
@@ -326,6 +334,10 @@ gemv_blk_tc(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ Bt
                     W0[c] = lds32(rg + (uint32_t)(36 * t + 4 * c));
                     W1[c] = lds32(rg8 + (uint32_t)(36 * t + 4 * c));
                 }
+                // d of blocks 2t and 2t + 1 of both rows times the blocks' x scales (powers of two: exact)
+                const float4 sv = *reinterpret_cast<const float4 *>(sx_w + st * 16 + 4 * t);
+                const float de0 = half_bits_f32(W0[0]) * sv.y, do0 = half_bits_f32(W0[4] >> 16) * sv.w;
+                const float de1 = half_bits_f32(W1[0]) * sv.y, do1 = half_bits_f32(W1[4] >> 16) * sv.w;
                 uint32_t w0[8], w1[8];
 #pragma unroll
                 for (int c = 0; c < 4; c++) {
@@ -355,10 +367,8 @@ gemv_blk_tc(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ Bt
                         mma16816(DB, ah, bx.z, bx.w);
                     }
                 }
-                // d of each block times its x scale (a power of two: exact)
-                const float4 sv = *reinterpret_cast<const float4 *>(sx_w + st * 16 + 4 * t);
-                acc0 = fmaf(half_bits_f32(W0[0]) * sv.y, DA[0] + DA[1], fmaf(half_bits_f32(W0[4] >> 16) * sv.w, DB[0] + DB[1], acc0));
-                acc1 = fmaf(half_bits_f32(W1[0]) * sv.y, DA[2] + DA[3], fmaf(half_bits_f32(W1[4] >> 16) * sv.w, DB[2] + DB[3], acc1));
+                acc0 = fmaf(de0, DA[0] + DA[1], fmaf(do0, DB[0] + DB[1], acc0));
+                acc1 = fmaf(de1, DA[2] + DA[3], fmaf(do1, DB[2] + DB[3], acc1));
             }
         }
         __syncwarp();
