@@ -37,7 +37,9 @@
 // fragments read it; lanes outside the diagonal read a zero block.  Each 16-row tile's warp partials are summed in a fixed
 // order.  Roles: warp 8 streams stages, warps 0-7 stage x and decode.  Two
 // CTAs fit on an SM; tiles are dealt round-robin to a grid of at most two
-// CTAs per SM.  Weights are requested before the programmatic dependency
+// CTAs per SM.  One launch may serve a group of up to eight matrices of one
+// format and one K that read the same x (a layer's q/k/v, gate/up): their
+// tiles form one list, each stage taken through its member's tensor map.  Weights are requested before the programmatic dependency
 // wait, x read and y written after it.  Every wait is bounded (~1 s): a
 // timeout records Q4_ETIMEOUT, stops the roles, waits for issued copies and
 // returns.
@@ -69,15 +71,30 @@ constexpr int SMEM_CAP = 112 * 1024;               // two CTAs per SM
 constexpr long long BT_WAIT = 1LL << 31;
 static_assert(STAGE % 1024 == 0, "stages stay 1024-byte aligned");
 
-struct BtArgs {
-    const void *x;   // [K] f32 or bf16
-    float *y;        // [N]
-    int64_t N;
-    int nsb;         // units (256 k) per row
-    int nst;         // stages per tile
-    int ntiles;
-    int NS;          // ring stages
+constexpr int BT_MAXM = 8;                         // matrices per launch (a group sharing x and K)
+
+struct BtMaps {
+    CUtensorMap w[BT_MAXM];                        // u8 {144, N_i, K/256}, box {144, 16, 8}
 };
+
+struct BtArgs {
+    const void *x;                 // [K] f32 or bf16, shared by every member
+    float *y[BT_MAXM];             // [N_i]
+    int64_t N[BT_MAXM];
+    int tile_start[BT_MAXM + 1];   // first 16-row tile of each member in the launch's tile list
+    int nsb;                       // units (256 k) per row
+    int nst;                       // stages per tile
+    int ntiles;                    // tiles of all members
+    int NS;                        // ring stages
+};
+
+// Member owning tile `tile` of the launch's tile list.
+__device__ __forceinline__ int member_of(const BtArgs &a, int tile) {
+    int m = 0;
+#pragma unroll
+    for (int i = 1; i < BT_MAXM; i++) m += tile >= a.tile_start[i] ? 1 : 0;
+    return m;
+}
 
 // Shared-memory layout after the 1024-byte aligned ring: staged x [8 warps][nst][1024],
 // a 256-byte zero block at an offset of 64 mod 128 (so its reads never share banks
@@ -170,7 +187,7 @@ __device__ __forceinline__ float q4k_rows_term(float4 so, float l0, float l1, fl
 
 template <typename XT, bool Q4K>
 __global__ void __launch_bounds__(BT_THREADS, 2)
-gemv_blk_tc(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ BtArgs a) {
+gemv_blk_tc(const __grid_constant__ BtMaps maps, const __grid_constant__ BtArgs a) {
     extern __shared__ uint8_t smem_raw[];
     __shared__ uint64_t full[MAX_NS], empty[MAX_NS];
     __shared__ int abort_s;
@@ -205,8 +222,10 @@ gemv_blk_tc(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ Bt
                 const int s = j % NS;
                 if (j >= NS && !wait_or_abort(&empty[s], ((j / NS) & 1) ^ 1, abort_flag, &g_blkt_error, wait_limit)) break;
                 const int tile = (int)blockIdx.x + (j / nst) * (int)gridDim.x, st = j % nst;
+                const int mem = member_of(a, tile);
                 mbar_arrive_expect_tx(&full[s], STAGE);
-                tma3(smem_u32(ring + s * STAGE), &wmap, 0, tile * BT_ROWS, st * BT_WARPS, &full[s], pol);
+                tma3(smem_u32(ring + s * STAGE), &maps.w[mem], 0, (tile - a.tile_start[mem]) * BT_ROWS,
+                     st * BT_WARPS, &full[s], pol);
                 issued++;
             }
             for (int q = issued > NS ? issued - NS : 0; q < issued; q++)
@@ -387,12 +406,13 @@ gemv_blk_tc(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ Bt
             acc0 = acc1 = 0.0f;
             asm volatile("bar.sync 1, 256;" ::: "memory");
             if (threadIdx.x < BT_ROWS) {
-                const int64_t n = (int64_t)((int)blockIdx.x + (j / nst) * (int)gridDim.x) * BT_ROWS + threadIdx.x;
-                if (n < a.N) {
+                const int tile = (int)blockIdx.x + (j / nst) * (int)gridDim.x, mem = member_of(a, tile);
+                const int64_t n = (int64_t)(tile - a.tile_start[mem]) * BT_ROWS + threadIdx.x;
+                if (n < a.N[mem]) {
                     float v = 0.0f;
 #pragma unroll
                     for (int w = 0; w < BT_WARPS; w++) v += rb[w * BT_ROWS + threadIdx.x];
-                    a.y[n] = v;
+                    a.y[mem][n] = v;
                 }
             }
             buf ^= 1;
@@ -417,7 +437,7 @@ bool plan_for(int64_t K, Plan &p) {
 }
 
 template <typename XT, bool Q4K>
-cudaError_t blk_tc_run(const CUtensorMap &map, const BtArgs &a, int smem, cudaStream_t s) {
+cudaError_t blk_tc_run(const BtMaps &maps, const BtArgs &a, int smem, cudaStream_t s) {
     auto kern = gemv_blk_tc<XT, Q4K>;
     static bool attr_set[64] = {};
     static int per_sm[64] = {};
@@ -446,7 +466,19 @@ cudaError_t blk_tc_run(const CUtensorMap &map, const BtArgs &a, int smem, cudaSt
     at[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = at;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, map, a);
+    return cudaLaunchKernelEx(&cfg, kern, maps, a);
+}
+
+bool encode_units(CUtensorMap *map, const Tensor &t, int nsb) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return false;
+    const cuuint64_t dims[3] = {(cuuint64_t)UNIT, (cuuint64_t)t.N, (cuuint64_t)nsb};
+    const cuuint64_t strides[2] = {(cuuint64_t)nsb * UNIT, (cuuint64_t)UNIT};
+    const cuuint32_t box[3] = {(cuuint32_t)UNIT, (cuuint32_t)BT_ROWS, (cuuint32_t)BT_WARPS};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<uint8_t *>(t.w), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 }  // namespace
@@ -459,30 +491,45 @@ bool gemv_blk_tc_eligible(const Tensor &t, int64_t M) {
     return plan_for(t.K, p);
 }
 
-cudaError_t launch_gemv_blk_tc(const Tensor &t, const void *x, q4_dtype xd, float *y, cudaStream_t s) {
-    EncodeTiledFn enc = encode_fn();
+// Up to BT_MAXM members of one format and one K (each eligible) that read the
+// same x: one launch whose tile list runs through the members in order.
+cudaError_t launch_gemv_blk_tc_group(const Tensor *ts, int count, const void *x, q4_dtype xd, float *const *ys,
+                                     cudaStream_t s) {
     Plan p;
-    if (!enc || !plan_for(t.K, p)) return cudaErrorInvalidValue;
-    CUtensorMap map;
-    const cuuint64_t dims[3] = {(cuuint64_t)UNIT, (cuuint64_t)t.N, (cuuint64_t)p.nsb};
-    const cuuint64_t strides[2] = {(cuuint64_t)p.nsb * UNIT, (cuuint64_t)UNIT};
-    const cuuint32_t box[3] = {(cuuint32_t)UNIT, (cuuint32_t)BT_ROWS, (cuuint32_t)BT_WARPS};
-    const cuuint32_t estr[3] = {1, 1, 1};
-    if (enc(&map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<uint8_t *>(t.w), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-        return cudaErrorInvalidValue;
+    if (count < 1 || count > BT_MAXM || !plan_for(ts[0].K, p)) return cudaErrorInvalidValue;
+    BtMaps maps;
     BtArgs a;
     a.x = x;
-    a.y = y;
-    a.N = t.N;
     a.nsb = p.nsb;
     a.nst = p.nst;
-    a.ntiles = (int)((t.N + BT_ROWS - 1) / BT_ROWS);
     a.NS = p.NS;
-    if (t.fmt == Q4_Q4K)
-        return xd == Q4_DT_BF16 ? blk_tc_run<__nv_bfloat16, true>(map, a, p.smem, s) : blk_tc_run<float, true>(map, a, p.smem, s);
-    return xd == Q4_DT_BF16 ? blk_tc_run<__nv_bfloat16, false>(map, a, p.smem, s) : blk_tc_run<float, false>(map, a, p.smem, s);
+    int tiles = 0;
+    for (int i = 0; i < BT_MAXM; i++) {
+        const int m = i < count ? i : count - 1;     // unused slots repeat the last member (never reached)
+        if (i < count) {
+            if (ts[i].fmt != ts[0].fmt || ts[i].K != ts[0].K || !encode_units(&maps.w[i], ts[i], p.nsb))
+                return cudaErrorInvalidValue;
+        } else {
+            maps.w[i] = maps.w[m];
+        }
+        a.y[i] = ys[m];
+        a.N[i] = ts[m].N;
+        a.tile_start[i] = tiles;
+        if (i < count) tiles += (int)((ts[i].N + BT_ROWS - 1) / BT_ROWS);
+    }
+    a.tile_start[BT_MAXM] = tiles;
+    for (int i = count; i < BT_MAXM; i++) a.tile_start[i] = tiles;   // empty: member_of never picks them
+    a.ntiles = tiles;
+    if (ts[0].fmt == Q4_Q4K)
+        return xd == Q4_DT_BF16 ? blk_tc_run<__nv_bfloat16, true>(maps, a, p.smem, s)
+                                : blk_tc_run<float, true>(maps, a, p.smem, s);
+    return xd == Q4_DT_BF16 ? blk_tc_run<__nv_bfloat16, false>(maps, a, p.smem, s)
+                            : blk_tc_run<float, false>(maps, a, p.smem, s);
+}
+
+cudaError_t launch_gemv_blk_tc(const Tensor &t, const void *x, q4_dtype xd, float *y, cudaStream_t s) {
+    float *const ys[1] = {y};
+    return launch_gemv_blk_tc_group(&t, 1, x, xd, ys, s);
 }
 
 int blk_tc_set_wait_limit(long long cycles) {

@@ -164,7 +164,9 @@ typedef struct {
  * token streams every weight once).  When every member is NVFP4 with bf16 x,
  * all share K, count <= 8 and each takes the tensor-core path, the group runs
  * as ONE persistent launch whose tile list spans all members (no launch gap
- * or ramp between them); otherwise each member is issued as its own q4_gemv.
+ * or ramp between them); so does a batch-1 group whose members are all Q4_K
+ * (or all Q4_0) with one K and one x, each taking q4_gemv's TMA-fed block
+ * kernel; otherwise each member is issued as its own q4_gemv.
  * Members must be independent: no y may alias another member's x or weights.
  * Same checks, accuracy and stream semantics as q4_gemv; if any member is
  * rejected nothing is launched. */
@@ -409,7 +411,7 @@ int q4_last_error(void);
  * "gemv_tma_chain", "gemm_tc", "gemv_mma", "gemv_mma_group", "gemv_mma_q4k",
  * "gemv_mma_q40", "gemv_mma_gptq", "gemv_rows_tma", "gemv_rows_m1",
  * "gemv_general", "gemv_kmajor", "gemv_awq_tc", "gemv_gptq_tc", "gemv_blk_tc_q4k",
- * "gemv_blk_tc_q40"; "gemv_a16q8" after q4_gemv_a16q8,
+ * "gemv_blk_tc_q40", "gemv_blk_tc_q4k_group", "gemv_blk_tc_q40_group"; "gemv_a16q8" after q4_gemv_a16q8,
  * "gemv_q4k_q8" after q4_gemv_q4k_q8, "gemv_w4a4" after q4_gemv_w4a4,
  * "gemv_w4a4_tc" after q4_gemv_w4a4_tc; "" before
  * the first call).  A diagnostic with no counterpart in the pages: it lets a

@@ -8,7 +8,7 @@ than CTAs (the ring runs across tile boundaries), and K = 14336, whose staged
 x leaves too little shared memory for the ring (the register-fed kernel takes
 it).  Edge cases: x spanning 1e-10 .. 1e30, all-zero x, random code and scale
 bytes, one-hot x (exact columns), all-zero weights, repeated calls bit for
-bit."""
+bit.  Groups of one format and one K sharing x run as one launch."""
 import numpy as np
 import pytest
 
@@ -127,3 +127,69 @@ def test_blk_tc_repeated_calls_bit_identical(fmt):
     first = run(layer, x)
     for _ in range(3):
         assert np.array_equal(run(layer, x).view(np.uint32), first.view(np.uint32))
+
+
+@pytest.mark.parametrize("xdtype", ["f32", "bf16"])
+@pytest.mark.parametrize("fmt", FMTS)
+def test_blk_tc_grouped_shared_x(fmt, xdtype):
+    """q4_gemv_grouped over members of one format and one K that read the same
+    x: one launch whose tile list runs through the members (ragged last
+    tiles, a 17-row member), every row against the oracle and bit for bit
+    equal to the members' own q4_gemv calls."""
+    K = 2304
+    Ns = (4096, 1024, 1000, 17, 520)
+    layers = [synth.make_layer(fmt, N, K, config=144, matrix=i, outliers=True) for i, N in enumerate(Ns)]
+    devs = [to_device(L) for L in layers]
+    xb, xf = synth.draw_x(1, K, config=144, matrix=9, dtype=xdtype)
+    x = x_device(xb)
+    ys = [torch.full((1, N), float("nan"), dtype=torch.float32, device="cuda") for N in Ns]
+    descs = [(fmt, d["w"], d["scales"], aux_for(L, d, x_dtype=x.dtype), x, y, L["N"], K)
+             for L, d, y in zip(layers, devs, ys)]
+    q4.q4_gemv_grouped(descs, 1)
+    assert q4.q4_last_gemv_path() == f"gemv_blk_tc_{fmt}_group"
+    torch.cuda.synchronize()
+    for L, d, y in zip(layers, devs, ys):
+        got = y.cpu().numpy()
+        ref, bound = oracle_gemv_all_rows(to_oracle(L), xf)
+        ok, worst = within_tolerance(got, ref, bound)
+        assert ok, worst
+        single = run(L, x)
+        assert np.array_equal(single.view(np.uint32), got.view(np.uint32))
+    assert q4.q4_last_error() == q4.Q4_OK
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_blk_tc_groups_it_does_not_take(fmt):
+    """Members with different x, or of different formats, run as their own
+    q4_gemv calls (same results)."""
+    K = 1024
+    other = "q40" if fmt == "q4k" else "q4k"
+    layers = [synth.make_layer(fmt, 64, K, config=145, matrix=0), synth.make_layer(other, 48, K, config=145, matrix=1)]
+    devs = [to_device(L) for L in layers]
+    xb, xf = synth.draw_x(1, K, config=145, matrix=2, dtype="f32")
+    x = x_device(xb)
+    x2 = x.clone()
+    for xs in ((x, x), (x, x2)):
+        ys = [torch.full((1, L["N"]), float("nan"), device="cuda") for L in layers]
+        descs = [(L["fmt"], d["w"], d["scales"], aux_for(L, d, x_dtype=x.dtype), xx, y, L["N"], K)
+                 for L, d, xx, y in zip(layers, devs, xs, ys)]
+        q4.q4_gemv_grouped(descs, 1)
+        assert not q4.q4_last_gemv_path().endswith("_group")
+        torch.cuda.synchronize()
+        for L, y in zip(layers, ys):
+            ref, bound = oracle_gemv_all_rows(to_oracle(L), xf)
+            ok, worst = within_tolerance(y.cpu().numpy(), ref, bound)
+            assert ok, worst
+    # same format, different x: also per member
+    same = [synth.make_layer(fmt, 40, K, config=145, matrix=3 + i) for i in range(2)]
+    dsame = [to_device(L) for L in same]
+    ys = [torch.full((1, 40), float("nan"), device="cuda") for _ in same]
+    descs = [(fmt, d["w"], d["scales"], aux_for(L, d, x_dtype=x.dtype), xx, y, 40, K)
+             for L, d, xx, y in zip(same, dsame, (x, x2), ys)]
+    q4.q4_gemv_grouped(descs, 1)
+    assert q4.q4_last_gemv_path() == f"gemv_blk_tc_{fmt}"
+    torch.cuda.synchronize()
+    for L, y in zip(same, ys):
+        ref, bound = oracle_gemv_all_rows(to_oracle(L), xf)
+        ok, worst = within_tolerance(y.cpu().numpy(), ref, bound)
+        assert ok, worst
