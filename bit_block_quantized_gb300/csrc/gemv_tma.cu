@@ -1,4 +1,4 @@
-// gemv_tma.cu -- NVFP4 (and single-matrix MXFP4) decode-GEMV for batch 1..4, weights streamed into
+// gemv_tma.cu -- NVFP4 (and one-group MXFP4) decode-GEMV for batch 1..4, weights streamed into
 // shared memory by the tensor-memory accelerator (TMA), dot products on the
 // tensor cores (mma.sync m16n8k16, f16 x f16 -> f32).  One launch runs a
 // chain of GEMV groups: the members of a group read the same x, and group
@@ -97,7 +97,7 @@ struct Maps {
 
 struct Args {
     float *y[MAXM];                 // [M][N_i]
-    const uint8_t *mx_scales;       // MXFP4 (a single member): E8M0 [N][K/32]
+    const uint8_t *mx_scales[MAXM]; // MXFP4 (a single group): E8M0 [N_i][K/32] of each member
     int64_t N[MAXM];
     float scale2[MAXM];
     int tile_start[MAXM];           // first 16-row tile of each member within its group
@@ -514,10 +514,14 @@ __global__ void __launch_bounds__(THREADS, Q4_TMA_CTAS_PER_SM)
     // before the dependency wait like the payload.
     const int64_t mx_rs = a.K[0] >> 5;
     auto mx_word = [&](int tile_, int st_) -> uint32_t {
-        const int64_t row = (int64_t)tile_ * 16 + (lane >> 1);
+        if (FMT != Q4_MXFP4 || tile_ >= a.ntiles[0]) return 0x7f7f7f7fu;
+        int m = 0;                       // the member holding tile_ (an MXFP4 launch is one group)
+#pragma unroll
+        for (int i = 1; i < MAXM; i++) m += (i < a.m0[1] && tile_ >= a.tile_start[i]) ? 1 : 0;
+        const int64_t row = (int64_t)(tile_ - a.tile_start[m]) * 16 + (lane >> 1);
         const int col = st_ * 64 + warp * 8 + (lane & 1) * 4;
-        if (FMT != Q4_MXFP4 || tile_ >= a.ntiles[0] || col >= (int)mx_rs || row >= a.N[0]) return 0x7f7f7f7fu;
-        return __ldg(reinterpret_cast<const unsigned *>(a.mx_scales + row * mx_rs + col));   // 2^0 above
+        if (col >= (int)mx_rs || row >= a.N[m]) return 0x7f7f7f7fu;
+        return __ldg(reinterpret_cast<const unsigned *>(a.mx_scales[m] + row * mx_rs + col));   // 2^0 above
     };
     uint32_t mxv = mx_word((int)blockIdx.x, 0);
     asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -551,6 +555,7 @@ __global__ void __launch_bounds__(THREADS, Q4_TMA_CTAS_PER_SM)
         const uint2 *xbase = xs + mlane * 4 + tt;
         int mb = a.m0[p];
         for (int tile = (int)blockIdx.x; tile < ntiles; tile += (int)gridDim.x) {
+            while (mb + 1 < m_end && tile >= a.tile_start[mb + 1]) mb++;   // this tile's member
             float *rw = red + (par * CW + warp) * 16 * MT;
             if (!exact || FMT == Q4_MXFP4) {     // MXFP4 stages may add f32 partials
                 for (int e = lane; e < 16 * MT; e += 32) rw[e] = 0.0f;
@@ -617,7 +622,8 @@ __global__ void __launch_bounds__(THREADS, Q4_TMA_CTAS_PER_SM)
                             }
                         }
                     } else {
-                        chunk_f32<MT, FMT>(stg, x, K, a.M, k0, warp, lane, rw, a.mx_scales, (int64_t)tile * 16, a.N[0]);
+                        chunk_f32<MT, FMT>(stg, x, K, a.M, k0, warp, lane, rw, a.mx_scales[mb],
+                                           (int64_t)(tile - a.tile_start[mb]) * 16, a.N[mb]);
                     }
                 }
                 __syncwarp();
@@ -627,7 +633,6 @@ __global__ void __launch_bounds__(THREADS, Q4_TMA_CTAS_PER_SM)
             }
 
             // ---- end of tile: warp partials -> shared, one consumer barrier, fixed-order sum
-            while (mb + 1 < m_end && tile >= a.tile_start[mb + 1]) mb++;
             float d[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int i = 0; i < NACC; i++) {
@@ -771,8 +776,10 @@ bool gemv_tma_chain_fits(const Tensor *ts, const int *first, int ngroups, int64_
         if (first[p + 1] <= first[p]) return false;
         for (int i = first[p]; i < first[p + 1]; i++)
             if (!gemv_tma_eligible(ts[i], M) || ts[i].K != ts[first[p]].K) return false;
-        // MXFP4 runs as a single matrix only (its scales come through one pointer)
-        if (ts[first[p]].fmt == Q4_MXFP4 && (ngroups > 1 || first[p + 1] - first[p] > 1)) return false;
+        // one format per launch (the kernel is instantiated per format); MXFP4 as a single group only
+        for (int i = first[p]; i < first[p + 1]; i++)
+            if (ts[i].fmt != ts[0].fmt) return false;
+        if (ts[0].fmt == Q4_MXFP4 && ngroups > 1) return false;
         max_K = ts[first[p]].K > max_K ? ts[first[p]].K : max_K;
     }
     return stages_for(max_K, mt_for(M)) >= MIN_STAGES;
@@ -802,7 +809,7 @@ cudaError_t launch_gemv_tma_chain(const Tensor *ts, const void *const *xs, float
                 if (!encode_scales(&maps.sc[i], ts[i])) return cudaErrorInvalidValue;
             } else {
                 maps.sc[i] = maps.pay[i];                 // never read: MXFP4 scales come through mx_scales
-                args.mx_scales = ts[i].scales;
+                args.mx_scales[i] = ts[i].scales;
             }
             args.y[i] = ys[i];
             args.N[i] = ts[i].N;

@@ -172,8 +172,8 @@ int q4_gemv_grouped(const q4_gemv_desc *descs, int count, int64_t M, void *strea
         }
         one_launch = one_launch && d.fmt == Q4_NVFP4 && xd == Q4_DT_BF16 && d.K == descs[0].K && M <= 8 &&
                      gemv_mma_eligible(t, M);
-        tma = tma && d.fmt == Q4_NVFP4 && xd == Q4_DT_BF16 && d.K == descs[0].K && d.x == descs[0].x &&
-              gemv_tma_eligible(t, M);
+        tma = tma && (d.fmt == Q4_NVFP4 || d.fmt == Q4_MXFP4) && d.fmt == descs[0].fmt && xd == Q4_DT_BF16 &&
+              d.K == descs[0].K && d.x == descs[0].x && gemv_tma_eligible(t, M);
         fp4tc = fp4tc && d.fmt == Q4_NVFP4 && xd == Q4_DT_BF16 && d.K == descs[0].K && d.x == descs[0].x &&
                 (d.aux->flags & Q4_FLAG_FP4_SLICES) && gemv_fp4tc_eligible(t, M);
         blk = blk && (d.fmt == Q4_Q4K || d.fmt == Q4_Q40) && d.fmt == descs[0].fmt && xd == xd0 &&

@@ -161,8 +161,9 @@ typedef struct {
 /* Several independent GEMVs with the same batch M, e.g. the projections of
  * one decoder layer that read the same activations (q/k/v, gate/up) -- the
  * grouping the pages' decode path applies per layer ([W4K] section 7d: one
- * token streams every weight once).  When every member is NVFP4 with bf16 x,
- * all share K, count <= 8 and each takes the tensor-core path, the group runs
+ * token streams every weight once).  When every member is NVFP4 (or every
+ * one MXFP4) with bf16 x and one x, all share K, count <= 8 and each takes
+ * the TMA-fed tensor-core path, the group runs
  * as ONE persistent launch whose tile list spans all members (no launch gap
  * or ramp between them); so does a batch-1 group whose members are all Q4_K
  * (or all Q4_0) with one K and one x, each taking q4_gemv's TMA-fed block

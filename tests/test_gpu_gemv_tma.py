@@ -35,7 +35,7 @@ def gemv(layer, d, x, M, y=None):
     if y is None:
         y = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
     aux = aux_for(layer, d, x_dtype=torch.bfloat16)
-    assert q4.q4_gemv("nvfp4", d["w"], d["scales"], aux, x, y, M, N, K) == q4.Q4_OK
+    assert q4.q4_gemv(layer["fmt"], d["w"], d["scales"], aux, x, y, M, N, K) == q4.Q4_OK
     return y
 
 
@@ -155,6 +155,49 @@ def test_tma_grouped_shared_x(M):
     ref, bound = oracle.gemv(to_oracle(layers[1]), xf2)
     ok, worst = within_tolerance(ys[1].cpu().numpy(), ref, bound)
     assert ok, worst
+
+
+@pytest.mark.parametrize("M", [1, 4])
+def test_tma_grouped_mxfp4_shared_x(M):
+    """MXFP4 members sharing x run as one TMA launch as well: each lane's scale
+    word (loaded one stage ahead) comes from its tile's member, and a member
+    whose scales leave the exact f16 range takes those stages in f32 with its
+    own rows and scales.  Every row against the oracle, bit for bit equal to
+    the members' own calls; a group mixing NVFP4 and MXFP4 runs per member."""
+    K = 4096
+    layers = [synth.make_layer("mxfp4", N, K, config=57, matrix=i, outliers=True)
+              for i, N in enumerate((1000, 17, 2048, 300))]
+    s = layers[2]["scales"].copy()
+    s[5, 3] = 127 - 40                                  # 2^-40: that stage goes to the f32 path
+    s[1500, :] = 127 + 20
+    layers[2] = dict(layers[2], scales=s)
+    xb, xf = synth.draw_x(M, K, config=57, matrix=9)
+    x = x_device(xb)
+    devs = [to_device(L) for L in layers]
+    ys = [torch.full((M, L["N"]), float("nan"), device="cuda") for L in layers]
+    descs = [("mxfp4", d["w"], d["scales"], aux_for(L, d, x_dtype=torch.bfloat16), x, y, L["N"], K)
+             for L, d, y in zip(layers, devs, ys)]
+    assert q4.q4_gemv_grouped(descs, M) == q4.Q4_OK
+    assert q4.q4_last_gemv_path() == "gemv_tma_group"
+    torch.cuda.synchronize()
+    for L, d, y in zip(layers, devs, ys):
+        got = y.cpu().numpy()
+        ref, bound = oracle.gemv(to_oracle(L), xf)
+        ok, worst = within_tolerance(got, ref, bound)
+        assert ok, worst
+        single = gemv(L, d, x, M).cpu().numpy()
+        assert np.array_equal(single.view(np.uint32), got.view(np.uint32))
+    nv = synth.make_layer("nvfp4", 64, K, config=57, matrix=8)
+    dn = to_device(nv)
+    yn = torch.full((M, 64), float("nan"), device="cuda")
+    mixed = [descs[0], ("nvfp4", dn["w"], dn["scales"], aux_for(nv, dn, x_dtype=torch.bfloat16), x, yn, 64, K)]
+    assert q4.q4_gemv_grouped(mixed, M) == q4.Q4_OK
+    assert q4.q4_last_gemv_path() != "gemv_tma_group"
+    torch.cuda.synchronize()
+    ref, bound = oracle.gemv(to_oracle(nv), xf)
+    ok, worst = within_tolerance(yn.cpu().numpy(), ref, bound)
+    assert ok, worst
+    assert q4.q4_last_error() == q4.Q4_OK
 
 
 def test_tma_chain_same_output_buffer():
