@@ -1027,7 +1027,7 @@ def layer_set_sweep(torch, q4, peak_hbm, batches=SWEEP_BATCHES, formats=SWEEP_FO
         copies = [base] + [[{k: (v.clone() if torch.is_tensor(v) else v) for k, v in m.items()} for m in base]
                            for _ in range(ncopies - 1)]
         for M in batches:
-            xdt = torch.bfloat16 if fmt in ("nvfp4", "mxfp4") else torch.float32
+            xdt = torch.bfloat16                     # the layer-set configuration's activations, every format
             xs = {K: torch.randn((M, K), generator=gen, device="cuda").to(xdt) for K in (4096, 11008)}
             ys = [torch.empty((M, N), device="cuda") for _, N, _ in LLAMA7B_SET]
             auxes = [[q4.make_aux(scale2=m["scale2"], zeros=m["zeros"], group=128, x_dtype=xdt, fmt=fmt) for m in c]
@@ -1071,7 +1071,8 @@ def layer_set_sweep(torch, q4, peak_hbm, batches=SWEEP_BATCHES, formats=SWEEP_FO
     return {"workload": "Llama-7B layer set: q, k, v, o 4096x4096; gate, up 11008x4096; down 4096x11008",
             "formats": list(formats), "batches": list(batches),
             "data": "seeded on the device: NVFP4 and Q4_K quantized from W ~ N(0,0.02) x U(0.5,2) rows by the "
-                    "library's GPU quantizers; MXFP4, Q4_0, GPTQ, AWQ as seeded random codes with valid scales",
+                    "library's GPU quantizers; MXFP4, Q4_0, GPTQ, AWQ as seeded random codes with valid scales; "
+                    "x ~ N(0,1) bf16 for every format",
             "l2": "each layer pass reads a different weight copy (copies > 4 x L2)",
             "launch": "per layer: q4_gemv_grouped(q, k, v), q4_gemv(o), q4_gemv_grouped(gate, up), q4_gemv(down); "
                       "one CUDA graph over the copies",

@@ -883,7 +883,7 @@ cudaError_t launch_gemv(const Tensor &t, const void *x, q4_dtype x_dtype, float 
     // memory (large K) runs as two launches of at most 4 rows: the weights
     // stream twice, far faster than the general kernel.
     if (M > 4 && M <= 8 && !gemv_gptq_tc_eligible(t, M) && !gemv_gptq_eligible(t, M) && !gemv_blk_eligible(t, M) &&
-        (gemv_gptq_eligible(t, 4) || gemv_blk_eligible(t, 4))) {
+        !gemv_blk_tc_eligible(t, M, x_dtype) && (gemv_gptq_eligible(t, 4) || gemv_blk_eligible(t, 4))) {
         const int64_t xe = x_dtype == Q4_DT_BF16 ? 2 : 4;
         const cudaError_t e = launch_gemv(t, x, x_dtype, y, 4, s);
         if (e != cudaSuccess) return e;
@@ -901,9 +901,9 @@ cudaError_t launch_gemv(const Tensor &t, const void *x, q4_dtype x_dtype, float 
         note_gemv_path("gemv_mma_gptq");
         return launch_gemv_gptq(t, x, x_dtype, y, M, s);
     }
-    if (gemv_blk_tc_eligible(t, M) && ((uintptr_t)x & 15) == 0) {     // x read in 16-byte vectors
+    if (gemv_blk_tc_eligible(t, M, x_dtype) && ((uintptr_t)x & 15) == 0) {     // x read in 16-byte vectors
         note_gemv_path(t.fmt == Q4_Q4K ? "gemv_blk_tc_q4k" : "gemv_blk_tc_q40");
-        return launch_gemv_blk_tc(t, x, x_dtype, y, s);
+        return launch_gemv_blk_tc(t, x, x_dtype, y, M, s);
     }
     if (gemv_blk_eligible(t, M)) {
         note_gemv_path(t.fmt == Q4_Q4K ? "gemv_mma_q4k" : "gemv_mma_q40");

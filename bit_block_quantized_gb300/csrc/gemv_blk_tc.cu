@@ -98,18 +98,18 @@ __device__ __forceinline__ int member_of(const BtArgs &a, int tile) {
 
 // Shared-memory layout after the 1024-byte aligned ring: staged x [8 warps][nst][1024],
 // a 256-byte zero block at an offset of 64 mod 128 (so its reads never share banks
-// with a diagonal lane's), per 32-k block {x sum, x scale} pairs [8][nst][8] x 2 f32,
-// tile partials [2][8][16] f32.
+// with a diagonal lane's), per 32-k block and batch row {x sum, x scale} pairs
+// [8][nst][8][MB] x 2 f32, tile partials [2][MB][8][16] f32.
 struct Layout {
     int xs, zero, sx, red, total;
 };
-__host__ __device__ inline Layout layout(int NS, int nst) {
+__host__ __device__ inline Layout layout(int NS, int nst, int mb) {
     Layout L;
     L.xs = NS * STAGE;
     L.zero = L.xs + BT_WARPS * nst * XU + 64;
     L.sx = L.zero + 256 + 64;
-    L.red = L.sx + BT_WARPS * nst * 64;
-    L.total = L.red + 2 * BT_WARPS * BT_ROWS * 4;
+    L.red = L.sx + BT_WARPS * nst * 64 * mb;
+    L.total = L.red + 2 * mb * BT_WARPS * BT_ROWS * 4;
     return L;
 }
 
@@ -185,15 +185,20 @@ __device__ __forceinline__ float q4k_rows_term(float4 so, float l0, float l1, fl
     return fmaf(hi, sv.w, lo * sv.y);
 }
 
-template <typename XT, bool Q4K>
+// MB = 1: one batch row, B columns 2t and 2t + 1 carrying its f16 hi and lo
+// parts.  MB = 2 (bf16 x, whose 8 significant bits need no lo part): two batch
+// rows, columns 2t and 2t + 1 carrying one row each, for the MMAs and the
+// decode of one.
+template <typename XT, bool Q4K, int MB>
 __global__ void __launch_bounds__(BT_THREADS, 2)
 gemv_blk_tc(const __grid_constant__ BtMaps maps, const __grid_constant__ BtArgs a) {
+    static_assert(MB == 1 || (MB == 2 && sizeof(XT) == 2), "two rows per launch need bf16 x");
     extern __shared__ uint8_t smem_raw[];
     __shared__ uint64_t full[MAX_NS], empty[MAX_NS];
     __shared__ int abort_s;
     uint8_t *ring = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     const int NS = a.NS, nst = a.nst;
-    const Layout L = layout(NS, nst);
+    const Layout L = layout(NS, nst, MB);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int my_tiles = (int)blockIdx.x < a.ntiles ? (a.ntiles - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
     const int J = my_tiles * nst;
@@ -243,7 +248,7 @@ gemv_blk_tc(const __grid_constant__ BtMaps maps, const __grid_constant__ BtArgs 
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const XT *xp = reinterpret_cast<const XT *>(a.x);
     const uint32_t xs_w = smem_u32(ring + L.xs) + (uint32_t)(warp * nst * XU);
-    float *sx_w = reinterpret_cast<float *>(ring + L.sx) + warp * nst * 16;
+    float *sx_w = reinterpret_cast<float *>(ring + L.sx) + warp * nst * 16 * MB;
     {
         // lane l converts k = 8l .. 8l+7 of each unit: two code words' worth of B values
         int tq, half, i0;
@@ -260,48 +265,58 @@ gemv_blk_tc(const __grid_constant__ BtMaps maps, const __grid_constant__ BtArgs 
         for (int s = 0; s < nst; s++) {
             const int u = warp + BT_WARPS * s;
             if (u >= a.nsb) break;
-            float v[8];
-            load8(xp + (int64_t)u * 256 + 8 * lane, v);
-            float amax = 0.0f;
 #pragma unroll
-            for (int r = 0; r < 8; r++) amax = fmaxf(amax, fabsf(v[r]));
-            amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-            amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
-            float xscale = 1.0f, xinv = 1.0f;
-            if (amax > 0.0f && amax < INFINITY) {
-                int ex = (int)((__float_as_uint(amax) >> 23) & 255u) - 127;
-                ex = ex < -100 ? -100 : (ex > 100 ? 100 : ex);
-                xscale = __uint_as_float((uint32_t)(127 + 12 - ex) << 23);    // |x| * xscale < 2^13
-                xinv = __uint_as_float((uint32_t)(127 - 12 + ex) << 23);
-            }
-            const float sc = half ? xscale * 0.0625f : xscale;                // exact: powers of two
-            float ssum = 0.0f;
+            for (int m = 0; m < MB; m++) {
+                float v[8];
+                load8(xp + (int64_t)m * a.nsb * 256 + (int64_t)u * 256 + 8 * lane, v);
+                float amax = 0.0f;
 #pragma unroll
-            for (int q = 0; q < 2; q++) {
-                const float f0 = v[4 * q] * sc, f1 = v[4 * q + 1] * sc, f2 = v[4 * q + 2] * sc, f3 = v[4 * q + 3] * sc;
-                // B pairs (k, k+2) and (k+1, k+3): f16 hi parts, then the f16 lo remainders
-                const __half2 h02 = __floats2half2_rn(f0, f2), h13 = __floats2half2_rn(f1, f3);
-                const float2 r02 = __half22float2(h02), r13 = __half22float2(h13);
-                const __half2 l02 = __floats2half2_rn(f0 - r02.x, f2 - r02.y);
-                const __half2 l13 = __floats2half2_rn(f1 - r13.x, f3 - r13.y);
-                // entry (tq, word i0 + q): [hi part: low-nibble half, high-nibble half][lo part: ...], 8 bytes each
-                const uint32_t e = xs_w + (uint32_t)(s * XU + (tq * 8 + i0 + q) * 32 + half * 8);
-                sts64(e, *reinterpret_cast<const uint32_t *>(&h02), *reinterpret_cast<const uint32_t *>(&h13));
-                sts64(e + 16, *reinterpret_cast<const uint32_t *>(&l02), *reinterpret_cast<const uint32_t *>(&l13));
-                if (Q4K) {                      // the staged values themselves: the numbers the MMA multiplies
-                    const float2 s02 = __half22float2(l02), s13 = __half22float2(l13);
-                    ssum += ((r02.x + s02.x) + (r02.y + s02.y)) + ((r13.x + s13.x) + (r13.y + s13.y));
+                for (int r = 0; r < 8; r++) amax = fmaxf(amax, fabsf(v[r]));
+                amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+                amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+                float xscale = 1.0f, xinv = 1.0f;
+                if (amax > 0.0f && amax < INFINITY) {
+                    int ex = (int)((__float_as_uint(amax) >> 23) & 255u) - 127;
+                    ex = ex < -100 ? -100 : (ex > 100 ? 100 : ex);
+                    xscale = __uint_as_float((uint32_t)(127 + 12 - ex) << 23);    // |x| * xscale < 2^13
+                    xinv = __uint_as_float((uint32_t)(127 - 12 + ex) << 23);
                 }
-            }
-            // the block's x sum in the units the MMA sees x in (Q4_K's min term) and its scale
-            if (Q4K) {
-                if (half) ssum *= 16.0f;
-                ssum += __shfl_xor_sync(0xffffffffu, ssum, 1);
-                ssum += __shfl_xor_sync(0xffffffffu, ssum, 2);
-            }
-            if ((lane & 3) == 0) {
-                sx_w[s * 16 + 2 * (lane >> 2)] = ssum;
-                sx_w[s * 16 + 2 * (lane >> 2) + 1] = xinv;
+                const float sc = half ? xscale * 0.0625f : xscale;                // exact: powers of two
+                float ssum = 0.0f;
+#pragma unroll
+                for (int q = 0; q < 2; q++) {
+                    const float f0 = v[4 * q] * sc, f1 = v[4 * q + 1] * sc, f2 = v[4 * q + 2] * sc,
+                                f3 = v[4 * q + 3] * sc;
+                    // B pairs (k, k+2) and (k+1, k+3) as f16
+                    const __half2 h02 = __floats2half2_rn(f0, f2), h13 = __floats2half2_rn(f1, f3);
+                    const float2 r02 = __half22float2(h02), r13 = __half22float2(h13);
+                    // entry (tq, word i0 + q): [part 0: low-nibble half, high-nibble half][part 1: ...], 8 bytes
+                    // each; part 0 holds x's hi terms (MB = 1) or row 0 (MB = 2), part 1 its lo terms or row 1
+                    const uint32_t e = xs_w + (uint32_t)(s * XU + (tq * 8 + i0 + q) * 32 + half * 8 + m * 16);
+                    sts64(e, *reinterpret_cast<const uint32_t *>(&h02), *reinterpret_cast<const uint32_t *>(&h13));
+                    if (MB == 1) {
+                        const __half2 l02 = __floats2half2_rn(f0 - r02.x, f2 - r02.y);
+                        const __half2 l13 = __floats2half2_rn(f1 - r13.x, f3 - r13.y);
+                        sts64(e + 16, *reinterpret_cast<const uint32_t *>(&l02), *reinterpret_cast<const uint32_t *>(&l13));
+                        if (Q4K) {              // the staged values themselves: the numbers the MMA multiplies
+                            const float2 s02 = __half22float2(l02), s13 = __half22float2(l13);
+                            ssum += ((r02.x + s02.x) + (r02.y + s02.y)) + ((r13.x + s13.x) + (r13.y + s13.y));
+                        }
+                    } else if (Q4K) {
+                        ssum += (r02.x + r02.y) + (r13.x + r13.y);
+                    }
+                }
+                // the block's x sum in the units the MMA sees x in (Q4_K's min term) and its scale
+                if (Q4K) {
+                    if (half) ssum *= 16.0f;
+                    ssum += __shfl_xor_sync(0xffffffffu, ssum, 1);
+                    ssum += __shfl_xor_sync(0xffffffffu, ssum, 2);
+                }
+                if ((lane & 3) == 0) {
+                    float *o = sx_w + ((s * 8 + (lane >> 2)) * MB + m) * 2;
+                    o[0] = ssum;
+                    o[1] = xinv;
+                }
             }
         }
     }
@@ -314,7 +329,7 @@ gemv_blk_tc(const __grid_constant__ BtMaps maps, const __grid_constant__ BtArgs 
     const uint32_t xstep = diag ? XU : 0u;
     const uint32_t ring_u = smem_u32(ring);
     float *red = reinterpret_cast<float *>(ring + L.red);
-    float acc0 = 0.0f, acc1 = 0.0f;                                      // rows g, g + 8
+    float acc[MB][2] = {};                                               // [batch row][rows g, g + 8]
     bool ok = true;
     int buf = 0;
     for (int j = 0; j < J; j++) {
@@ -326,8 +341,10 @@ gemv_blk_tc(const __grid_constant__ BtMaps maps, const __grid_constant__ BtArgs 
             const uint32_t rg = R + (uint32_t)(g * UNIT), rg8 = rg + 8 * UNIT;
             if constexpr (Q4K) {
                 const uint4 H0 = lds128(rg), H1 = lds128(rg8);
-                const float4 sv = *reinterpret_cast<const float4 *>(sx_w + st * 16 + 4 * t);
                 const float4 so0 = q4k_terms(H0, t), so1 = q4k_terms(H1, t);
+                // x sums and scales of sub-blocks 2t, 2t + 1: {S, 1/scale} x 2 (MB = 1), or per block both rows
+                const float4 sa = *reinterpret_cast<const float4 *>(sx_w + (st * 8 + 2 * t) * 2 * MB);
+                const float4 sb = MB == 2 ? *reinterpret_cast<const float4 *>(sx_w + (st * 8 + 2 * t + 1) * 4) : sa;
                 const uint4 c0a = lds128(rg + 16 + 32 * t), c0b = lds128(rg + 32 + 32 * t);
                 const uint4 c1a = lds128(rg8 + 16 + 32 * t), c1b = lds128(rg8 + 32 + 32 * t);
                 const uint32_t w0[8] = {c0a.x, c0a.y, c0a.z, c0a.w, c0b.x, c0b.y, c0b.z, c0b.w};
@@ -343,8 +360,16 @@ gemv_blk_tc(const __grid_constant__ BtMaps maps, const __grid_constant__ BtArgs 
                              bx.z, bx.w);
                 }
                 // sub-blocks 2t (low nibbles) and 2t + 1 (high nibbles) of rows g and g + 8
-                acc0 += q4k_rows_term(so0, Dl[0], Dl[1], Dh[0], Dh[1], sv);
-                acc1 += q4k_rows_term(so1, Dl[2], Dl[3], Dh[2], Dh[3], sv);
+                if constexpr (MB == 1) {
+                    acc[0][0] += q4k_rows_term(so0, Dl[0], Dl[1], Dh[0], Dh[1], sa);
+                    acc[0][1] += q4k_rows_term(so1, Dl[2], Dl[3], Dh[2], Dh[3], sa);
+                } else {
+                    const float4 sv0 = make_float4(sa.x, sa.y, sb.x, sb.y), sv1 = make_float4(sa.z, sa.w, sb.z, sb.w);
+                    acc[0][0] += q4k_rows_term(so0, Dl[0], 0.0f, Dh[0], 0.0f, sv0);
+                    acc[1][0] += q4k_rows_term(so0, Dl[1], 0.0f, Dh[1], 0.0f, sv1);
+                    acc[0][1] += q4k_rows_term(so1, Dl[2], 0.0f, Dh[2], 0.0f, sv0);
+                    acc[1][1] += q4k_rows_term(so1, Dl[3], 0.0f, Dh[3], 0.0f, sv1);
+                }
             } else {
                 // blocks 2t (bytes 36t .. 36t+17) and 2t + 1 (36t+18 .. 36t+35) of rows g and g + 8
                 uint32_t W0[9], W1[9];
@@ -353,10 +378,13 @@ gemv_blk_tc(const __grid_constant__ BtMaps maps, const __grid_constant__ BtArgs 
                     W0[c] = lds32(rg + (uint32_t)(36 * t + 4 * c));
                     W1[c] = lds32(rg8 + (uint32_t)(36 * t + 4 * c));
                 }
-                // d of blocks 2t and 2t + 1 of both rows times the blocks' x scales (powers of two: exact)
-                const float4 sv = *reinterpret_cast<const float4 *>(sx_w + st * 16 + 4 * t);
-                const float de0 = half_bits_f32(W0[0]) * sv.y, do0 = half_bits_f32(W0[4] >> 16) * sv.w;
-                const float de1 = half_bits_f32(W1[0]) * sv.y, do1 = half_bits_f32(W1[4] >> 16) * sv.w;
+                // d of blocks 2t and 2t + 1 of both rows, and the blocks' x scales (powers of two: exact)
+                const float de0 = half_bits_f32(W0[0]), do0 = half_bits_f32(W0[4] >> 16);
+                const float de1 = half_bits_f32(W1[0]), do1 = half_bits_f32(W1[4] >> 16);
+                const float4 sa = *reinterpret_cast<const float4 *>(sx_w + (st * 8 + 2 * t) * 2 * MB);
+                const float4 sb = MB == 2 ? *reinterpret_cast<const float4 *>(sx_w + (st * 8 + 2 * t + 1) * 4) : sa;
+                const float e0s = de0 * sa.y, o0s = do0 * (MB == 1 ? sa.w : sb.y);
+                const float e1s = de1 * sa.y, o1s = do1 * (MB == 1 ? sa.w : sb.y);
                 uint32_t w0[8], w1[8];
 #pragma unroll
                 for (int c = 0; c < 4; c++) {
@@ -386,33 +414,45 @@ gemv_blk_tc(const __grid_constant__ BtMaps maps, const __grid_constant__ BtArgs 
                         mma16816(DB, ah, bx.z, bx.w);
                     }
                 }
-                acc0 = fmaf(de0, DA[0] + DA[1], fmaf(do0, DB[0] + DB[1], acc0));
-                acc1 = fmaf(de1, DA[2] + DA[3], fmaf(do1, DB[2] + DB[3], acc1));
+                if constexpr (MB == 1) {
+                    acc[0][0] = fmaf(e0s, DA[0] + DA[1], fmaf(o0s, DB[0] + DB[1], acc[0][0]));
+                    acc[0][1] = fmaf(e1s, DA[2] + DA[3], fmaf(o1s, DB[2] + DB[3], acc[0][1]));
+                } else {                      // column 2t + m is batch row m; row 1's scales sit at sa.w, sb.w
+                    acc[0][0] = fmaf(e0s, DA[0], fmaf(o0s, DB[0], acc[0][0]));
+                    acc[1][0] = fmaf(de0 * sa.w, DA[1], fmaf(do0 * sb.w, DB[1], acc[1][0]));
+                    acc[0][1] = fmaf(e1s, DA[2], fmaf(o1s, DB[2], acc[0][1]));
+                    acc[1][1] = fmaf(de1 * sa.w, DA[3], fmaf(do1 * sb.w, DB[3], acc[1][1]));
+                }
             }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[s]);
         if (st == nst - 1) {
             // end of a tile: the four lanes of a row, then the eight warps in a fixed order
-            acc0 += __shfl_xor_sync(0xffffffffu, acc0, 1);
-            acc0 += __shfl_xor_sync(0xffffffffu, acc0, 2);
-            acc1 += __shfl_xor_sync(0xffffffffu, acc1, 1);
-            acc1 += __shfl_xor_sync(0xffffffffu, acc1, 2);
-            float *rb = red + buf * BT_WARPS * BT_ROWS;
-            if (t == 0) {
-                rb[warp * BT_ROWS + g] = acc0;
-                rb[warp * BT_ROWS + g + 8] = acc1;
+            float *rb = red + buf * MB * BT_WARPS * BT_ROWS;
+#pragma unroll
+            for (int m = 0; m < MB; m++) {
+#pragma unroll
+                for (int r = 0; r < 2; r++) {
+                    acc[m][r] += __shfl_xor_sync(0xffffffffu, acc[m][r], 1);
+                    acc[m][r] += __shfl_xor_sync(0xffffffffu, acc[m][r], 2);
+                }
+                if (t == 0) {
+                    rb[(m * BT_WARPS + warp) * BT_ROWS + g] = acc[m][0];
+                    rb[(m * BT_WARPS + warp) * BT_ROWS + g + 8] = acc[m][1];
+                }
+                acc[m][0] = acc[m][1] = 0.0f;
             }
-            acc0 = acc1 = 0.0f;
             asm volatile("bar.sync 1, 256;" ::: "memory");
-            if (threadIdx.x < BT_ROWS) {
+            if (threadIdx.x < MB * BT_ROWS) {
+                const int m = threadIdx.x / BT_ROWS, rr = threadIdx.x % BT_ROWS;
                 const int tile = (int)blockIdx.x + (j / nst) * (int)gridDim.x, mem = member_of(a, tile);
-                const int64_t n = (int64_t)(tile - a.tile_start[mem]) * BT_ROWS + threadIdx.x;
+                const int64_t n = (int64_t)(tile - a.tile_start[mem]) * BT_ROWS + rr;
                 if (n < a.N[mem]) {
                     float v = 0.0f;
 #pragma unroll
-                    for (int w = 0; w < BT_WARPS; w++) v += rb[w * BT_ROWS + threadIdx.x];
-                    a.y[mem][n] = v;
+                    for (int w = 0; w < BT_WARPS; w++) v += rb[(m * BT_WARPS + w) * BT_ROWS + rr];
+                    a.y[mem][(int64_t)m * a.N[mem] + n] = v;
                 }
             }
             buf ^= 1;
@@ -424,21 +464,21 @@ struct Plan {
     int nsb, nst, NS, smem;
 };
 
-bool plan_for(int64_t K, Plan &p) {
+bool plan_for(int64_t K, int mb, Plan &p) {
     if (K % 256 != 0 || K <= 0 || K > (1LL << 24)) return false;
     p.nsb = (int)(K / 256);
     p.nst = (p.nsb + BT_WARPS - 1) / BT_WARPS;
-    const Layout L0 = layout(0, p.nst);
+    const Layout L0 = layout(0, p.nst, mb);
     const int ns = (SMEM_CAP - 1024 - L0.total) / STAGE;
     if (ns < 3) return false;
     p.NS = ns < MAX_NS ? ns : MAX_NS;
-    p.smem = 1024 + layout(p.NS, p.nst).total;
+    p.smem = 1024 + layout(p.NS, p.nst, mb).total;
     return true;
 }
 
-template <typename XT, bool Q4K>
+template <typename XT, bool Q4K, int MB>
 cudaError_t blk_tc_run(const BtMaps &maps, const BtArgs &a, int smem, cudaStream_t s) {
-    auto kern = gemv_blk_tc<XT, Q4K>;
+    auto kern = gemv_blk_tc<XT, Q4K, MB>;
     static bool attr_set[64] = {};
     static int per_sm[64] = {};
     int dev = 0;
@@ -483,53 +523,73 @@ bool encode_units(CUtensorMap *map, const Tensor &t, int nsb) {
 
 }  // namespace
 
-// Q4_K or Q4_0 at batch 1, K % 256 == 0, weights 16-byte aligned, staged x and three ring stages within 112 KB.
-bool gemv_blk_tc_eligible(const Tensor &t, int64_t M) {
-    if ((t.fmt != Q4_Q4K && t.fmt != Q4_Q40) || M != 1 || t.N < 1 || t.N > (1LL << 30)) return false;
+// Q4_K or Q4_0, K % 256 == 0, weights 16-byte aligned, the staged x and three
+// ring stages within 112 KB; batch 1 with f32 or bf16 x, batch 2..8 with bf16
+// x (launches of two rows).
+bool gemv_blk_tc_eligible(const Tensor &t, int64_t M, q4_dtype xd) {
+    if ((t.fmt != Q4_Q4K && t.fmt != Q4_Q40) || M < 1 || M > 8 || t.N < 1 || t.N > (1LL << 30)) return false;
+    if (M > 1 && xd != Q4_DT_BF16) return false;
     if ((((uintptr_t)t.w) & 15) != 0 || encode_fn() == nullptr) return false;
     Plan p;
-    return plan_for(t.K, p);
+    return plan_for(t.K, M > 1 ? 2 : 1, p);
 }
 
 // Up to BT_MAXM members of one format and one K (each eligible) that read the
-// same x: one launch whose tile list runs through the members in order.
+// same x, batch rows M (f32 x: 1; bf16 x: up to 8): one launch per pair of
+// rows (and one for an odd last row) whose tile list runs through the members
+// in order.  Row m of x is at x + m K; row m of member i's output at ys[i] + m N_i.
 cudaError_t launch_gemv_blk_tc_group(const Tensor *ts, int count, const void *x, q4_dtype xd, float *const *ys,
-                                     cudaStream_t s) {
-    Plan p;
-    if (count < 1 || count > BT_MAXM || !plan_for(ts[0].K, p)) return cudaErrorInvalidValue;
+                                     int64_t M, cudaStream_t s) {
+    Plan p1, p2;
+    if (count < 1 || count > BT_MAXM || M < 1 || M > 8 || (M > 1 && xd != Q4_DT_BF16) || !plan_for(ts[0].K, 1, p1) ||
+        (M > 1 && !plan_for(ts[0].K, 2, p2)))
+        return cudaErrorInvalidValue;
     BtMaps maps;
-    BtArgs a;
-    a.x = x;
-    a.nsb = p.nsb;
-    a.nst = p.nst;
-    a.NS = p.NS;
+    BtArgs base;
     int tiles = 0;
     for (int i = 0; i < BT_MAXM; i++) {
         const int m = i < count ? i : count - 1;     // unused slots repeat the last member (never reached)
         if (i < count) {
-            if (ts[i].fmt != ts[0].fmt || ts[i].K != ts[0].K || !encode_units(&maps.w[i], ts[i], p.nsb))
+            if (ts[i].fmt != ts[0].fmt || ts[i].K != ts[0].K || !encode_units(&maps.w[i], ts[i], p1.nsb))
                 return cudaErrorInvalidValue;
         } else {
             maps.w[i] = maps.w[m];
         }
-        a.y[i] = ys[m];
-        a.N[i] = ts[m].N;
-        a.tile_start[i] = tiles;
+        base.N[i] = ts[m].N;
+        base.tile_start[i] = tiles;
         if (i < count) tiles += (int)((ts[i].N + BT_ROWS - 1) / BT_ROWS);
     }
-    a.tile_start[BT_MAXM] = tiles;
-    for (int i = count; i < BT_MAXM; i++) a.tile_start[i] = tiles;   // empty: member_of never picks them
-    a.ntiles = tiles;
-    if (ts[0].fmt == Q4_Q4K)
-        return xd == Q4_DT_BF16 ? blk_tc_run<__nv_bfloat16, true>(maps, a, p.smem, s)
-                                : blk_tc_run<float, true>(maps, a, p.smem, s);
-    return xd == Q4_DT_BF16 ? blk_tc_run<__nv_bfloat16, false>(maps, a, p.smem, s)
-                            : blk_tc_run<float, false>(maps, a, p.smem, s);
+    base.tile_start[BT_MAXM] = tiles;
+    for (int i = count; i < BT_MAXM; i++) base.tile_start[i] = tiles;   // empty: member_of never picks them
+    base.ntiles = tiles;
+    const bool q4k = ts[0].fmt == Q4_Q4K;
+    const int64_t xe = xd == Q4_DT_BF16 ? 2 : 4;
+    for (int64_t m0 = 0; m0 < M; m0 += 2) {
+        const int mb = M - m0 >= 2 ? 2 : 1;
+        const Plan &p = mb == 2 ? p2 : p1;
+        BtArgs a = base;
+        a.x = static_cast<const char *>(x) + m0 * ts[0].K * xe;
+        for (int i = 0; i < BT_MAXM; i++) a.y[i] = ys[i < count ? i : count - 1] + m0 * a.N[i];
+        a.nsb = p.nsb;
+        a.nst = p.nst;
+        a.NS = p.NS;
+        cudaError_t e;
+        if (mb == 2)
+            e = q4k ? blk_tc_run<__nv_bfloat16, true, 2>(maps, a, p.smem, s)
+                    : blk_tc_run<__nv_bfloat16, false, 2>(maps, a, p.smem, s);
+        else if (xd == Q4_DT_BF16)
+            e = q4k ? blk_tc_run<__nv_bfloat16, true, 1>(maps, a, p.smem, s)
+                    : blk_tc_run<__nv_bfloat16, false, 1>(maps, a, p.smem, s);
+        else
+            e = q4k ? blk_tc_run<float, true, 1>(maps, a, p.smem, s) : blk_tc_run<float, false, 1>(maps, a, p.smem, s);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
 }
 
-cudaError_t launch_gemv_blk_tc(const Tensor &t, const void *x, q4_dtype xd, float *y, cudaStream_t s) {
+cudaError_t launch_gemv_blk_tc(const Tensor &t, const void *x, q4_dtype xd, float *y, int64_t M, cudaStream_t s) {
     float *const ys[1] = {y};
-    return launch_gemv_blk_tc_group(&t, 1, x, xd, ys, s);
+    return launch_gemv_blk_tc_group(&t, 1, x, xd, ys, M, s);
 }
 
 int blk_tc_set_wait_limit(long long cycles) {

@@ -152,7 +152,7 @@ int q4_gemv_grouped(const q4_gemv_desc *descs, int count, int64_t M, void *strea
     bool one_launch = count <= 8;
     bool tma = count <= 8;                     // every member NVFP4 on the TMA kernel, one shared x
     bool fp4tc = count <= 8 && M == 1;         // every member NVFP4 at batch 1 on the FP4 tensor cores
-    bool blk = count <= 8 && M == 1;           // every member Q4_K (or every one Q4_0) at batch 1, one shared x
+    bool blk = count <= 8 && M <= 8;           // every member Q4_K (or every one Q4_0) on the block kernel, one x
     q4_dtype xd0 = Q4_DT_F32;
     for (int i = 0; i < count; i++) {          // check every member before launching any
         const q4_gemv_desc &d = descs[i];
@@ -177,11 +177,11 @@ int q4_gemv_grouped(const q4_gemv_desc *descs, int count, int64_t M, void *strea
         fp4tc = fp4tc && d.fmt == Q4_NVFP4 && xd == Q4_DT_BF16 && d.K == descs[0].K && d.x == descs[0].x &&
                 (d.aux->flags & Q4_FLAG_FP4_SLICES) && gemv_fp4tc_eligible(t, M);
         blk = blk && (d.fmt == Q4_Q4K || d.fmt == Q4_Q40) && d.fmt == descs[0].fmt && xd == xd0 &&
-              d.K == descs[0].K && d.x == descs[0].x && gemv_blk_tc_eligible(t, M);
+              d.K == descs[0].K && d.x == descs[0].x && gemv_blk_tc_eligible(t, M, xd);
     }
     if (blk && count > 1) {
         note_gemv_path(descs[0].fmt == Q4_Q4K ? "gemv_blk_tc_q4k_group" : "gemv_blk_tc_q40_group");
-        return launch_gemv_blk_tc_group(ts, count, descs[0].x, xd0, ys, (cudaStream_t)stream) == cudaSuccess
+        return launch_gemv_blk_tc_group(ts, count, descs[0].x, xd0, ys, M, (cudaStream_t)stream) == cudaSuccess
                    ? Q4_OK
                    : Q4_ECUDA;
     }

@@ -231,10 +231,10 @@ bool gemv_tma_chain_fits(const Tensor *ts, const int *first, int ngroups, int64_
 cudaError_t launch_gemv_tma_chain(const Tensor *ts, const void *const *xs, float *const *ys, const int *first,
                                   int ngroups, int64_t M, unsigned *sync, cudaStream_t s);
 bool gemv_blk_eligible(const Tensor &t, int64_t M);
-bool gemv_blk_tc_eligible(const Tensor &t, int64_t M);
-cudaError_t launch_gemv_blk_tc(const Tensor &t, const void *x, q4_dtype xd, float *y, cudaStream_t s);
+bool gemv_blk_tc_eligible(const Tensor &t, int64_t M, q4_dtype xd);
+cudaError_t launch_gemv_blk_tc(const Tensor &t, const void *x, q4_dtype xd, float *y, int64_t M, cudaStream_t s);
 cudaError_t launch_gemv_blk_tc_group(const Tensor *ts, int count, const void *x, q4_dtype xd, float *const *ys,
-                                     cudaStream_t s);
+                                     int64_t M, cudaStream_t s);
 cudaError_t launch_gemv_blk(const Tensor &t, const void *x, q4_dtype xd, float *y, int64_t M, cudaStream_t s);
 bool gemv_gptq_eligible(const Tensor &t, int64_t M);
 // GPTQ group 128 (no g_idx) on the tensor cores, weights by tensor TMA (gemv_gptq_tc.cu).

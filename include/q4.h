@@ -127,12 +127,12 @@ typedef struct {
  * rule for W, its scales and zeros: codes minus zero points formed exactly
  * in f16 as an MMA operand, x as f16 hi + lo terms, K split over a
  * thread-block cluster and reduced in rank order (repeated calls agree bit
- * for bit).  Q4_K and Q4_0 with M == 1, K % 256 == 0 and K <= 12288 (the
- * staged x and three 18 KB ring stages within 112 KB of shared memory) run a
- * TMA-fed tensor-core kernel with the same rule for W: 16 rows x 2048 k per
- * stage, the codes as exact f16 MMA operands (Q4_K: q, its sub-block scale
- * and min applied per lane in f32; Q4_0: q - 8), repeated calls agreeing bit
- * for bit.  M >= 9
+ * for bit).  Q4_K and Q4_0 with K % 256 == 0 and K <= 12288 (the staged x
+ * and three 18 KB ring stages within 112 KB of shared memory), at M == 1 or,
+ * with bf16 x, M <= 8 (launches of two rows), run a TMA-fed tensor-core kernel
+ * with the same rule for W: 16 rows x 2048 k per stage, the codes as exact f16
+ * MMA operands (Q4_K: q, its sub-block scale and min applied per lane in f32;
+ * Q4_0: q - 8), repeated calls agreeing bit for bit.  M >= 9
  * with bf16 x on NVFP4 or Q4_K (K % 256 == 0) runs the
  * tcgen05 tensor-core kernel: weights decoded to bf16 straight into tensor
  * memory, x tiles by TMA, f32 accumulation in TMEM, K split over a cluster
@@ -165,9 +165,10 @@ typedef struct {
  * one MXFP4) with bf16 x and one x, all share K, count <= 8 and each takes
  * the TMA-fed tensor-core path, the group runs
  * as ONE persistent launch whose tile list spans all members (no launch gap
- * or ramp between them); so does a batch-1 group whose members are all Q4_K
- * (or all Q4_0) with one K and one x, each taking q4_gemv's TMA-fed block
- * kernel; otherwise each member is issued as its own q4_gemv.
+ * or ramp between them); so does a group whose members are all Q4_K (or all
+ * Q4_0) with one K and one x, each taking q4_gemv's TMA-fed block kernel (one
+ * launch per two batch rows); otherwise each member is issued as its own
+ * q4_gemv.
  * Members must be independent: no y may alias another member's x or weights.
  * Same checks, accuracy and stream semantics as q4_gemv; if any member is
  * rejected nothing is launched. */

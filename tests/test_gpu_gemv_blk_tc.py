@@ -8,7 +8,9 @@ than CTAs (the ring runs across tile boundaries), and K = 14336, whose staged
 x leaves too little shared memory for the ring (the register-fed kernel takes
 it).  Edge cases: x spanning 1e-10 .. 1e30, all-zero x, random code and scale
 bytes, one-hot x (exact columns), all-zero weights, repeated calls bit for
-bit.  Groups of one format and one K sharing x run as one launch."""
+bit.  Groups of one format and one K sharing x run as one launch.  With bf16
+x the kernel takes two batch rows per launch (B columns 2t and 2t + 1 carry
+a row each), up to 8 rows in launches of two."""
 import numpy as np
 import pytest
 
@@ -70,7 +72,7 @@ def test_blk_tc_other_shapes_keep_the_register_fed_kernel(fmt):
     check(layer, xf, x_device(xb))
     assert q4.q4_last_gemv_path() == f"gemv_mma_{fmt}"
     small = synth.make_layer(fmt, 40, 2048, config=141, matrix=2)
-    xb, xf = synth.draw_x(2, 2048, config=141, matrix=3, dtype="bf16")
+    xb, xf = synth.draw_x(2, 2048, config=141, matrix=3, dtype="f32")     # batch 2 with f32 x
     check(small, xf, x_device(xb))
     assert q4.q4_last_gemv_path() == f"gemv_mma_{fmt}"
 
@@ -190,6 +192,70 @@ def test_blk_tc_groups_it_does_not_take(fmt):
     assert q4.q4_last_gemv_path() == f"gemv_blk_tc_{fmt}"
     torch.cuda.synchronize()
     for L, y in zip(same, ys):
+        ref, bound = oracle_gemv_all_rows(to_oracle(L), xf)
+        ok, worst = within_tolerance(y.cpu().numpy(), ref, bound)
+        assert ok, worst
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("M", [2, 3, 4, 5, 8])
+def test_blk_tc_bf16_batches(fmt, M):
+    """bf16 x at batch 2..8: launches of two rows (and one for an odd last
+    row), each row with its own per-block scales; ragged tiles and stages,
+    K = 11008 included (the two-row stage fits as the one-row stage does)."""
+    for i, (N, K) in enumerate(((263, 4096), (40, 11008), (1029, 2304), (16, 256))):
+        layer = synth.make_layer(fmt, N, K, config=146, matrix=i, outliers=True)
+        xb, xf = synth.draw_x(M, K, config=146, matrix=20 + M, dtype="bf16")
+        check(layer, xf, x_device(xb))
+        assert q4.q4_last_gemv_path() == f"gemv_blk_tc_{fmt}"
+    assert q4.q4_last_error() == q4.Q4_OK
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_blk_tc_bf16_batch_rows_are_independent(fmt):
+    """Each batch row of a two-row launch equals that row computed alone (same
+    per-block scaling, same sums), bit for bit; edge rows: all zero, one-hot,
+    and 1e30 next to 1e-10 noise in the other row."""
+    N, K = 300, 2304
+    layer = synth.make_layer(fmt, N, K, config=147, matrix=0)
+    rng = np.random.default_rng(5)
+    x = rng.normal(0, 1, (4, K)).astype(np.float32)
+    x[1] = 0.0
+    x[2] = 0.0
+    x[2, 700] = 1.0
+    x[3] = rng.normal(0, 1e-10, K)
+    x[3, 9] = 1e30
+    xb = x.astype(np.float32).view(np.uint32)
+    bits = ((xb + 0x7FFF + ((xb >> 16) & 1)) >> 16).astype(np.uint16)    # round to bf16
+    xf = (bits.astype(np.uint32) << 16).view(np.float32)
+    xd = x_device(bits)
+    together = run(layer, xd, 4)
+    for m in range(4):
+        alone = run(layer, x_device(bits[m:m + 1]), 1)
+        assert np.array_equal(alone[0].view(np.uint32), together[m].view(np.uint32)), m
+    ref, bound = oracle_gemv_all_rows(to_oracle(layer), xf)
+    ok, worst = within_tolerance(together, ref, bound)
+    assert ok, worst
+    assert np.all(together[1] == 0)
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_blk_tc_grouped_bf16_batch4(fmt):
+    """A grouped call at batch 4 with bf16 x: two launches of two rows over the
+    members' joint tile list, every row of every member against the oracle."""
+    K = 4096
+    Ns = (4096, 1000, 17)
+    layers = [synth.make_layer(fmt, N, K, config=148, matrix=i) for i, N in enumerate(Ns)]
+    devs = [to_device(L) for L in layers]
+    xb, xf = synth.draw_x(4, K, config=148, matrix=9, dtype="bf16")
+    x = x_device(xb)
+    ys = [torch.full((4, N), float("nan"), dtype=torch.float32, device="cuda") for N in Ns]
+    descs = [(fmt, d["w"], d["scales"], aux_for(L, d, x_dtype=x.dtype), x, y, L["N"], K)
+             for L, d, y in zip(layers, devs, ys)]
+    q4.q4_gemv_grouped(descs, 4)
+    assert q4.q4_last_gemv_path() == f"gemv_blk_tc_{fmt}_group"
+    torch.cuda.synchronize()
+    for L, y in zip(layers, ys):
         ref, bound = oracle_gemv_all_rows(to_oracle(L), xf)
         ok, worst = within_tolerance(y.cpu().numpy(), ref, bound)
         assert ok, worst

@@ -205,16 +205,17 @@ def test_gemv_mxfp4_scales_outside_the_exact_f16_range():
 @pytest.mark.parametrize("xdtype", ["f32", "bf16"])
 @pytest.mark.parametrize("M", [1, 3, 8])
 def test_gemv_q4k_tensor_core_path(M, xdtype):
-    """Q4_K at batch 2..8 runs the register-fed mma.sync kernel with one
-    fresh accumulator per 32-k sub-block (step and offset applied on the CUDA
-    cores), x staged as hi + lo f16 parts; ragged 16-row tiles and uneven K
-    splits.  At batch 5..8 with K = 11008 the staged x would not fit in
-    shared memory, so the batch runs as two launches of at most 4 rows.
-    Batch 1 takes the TMA-fed kernel (gemv_blk_tc)."""
+    """Q4_K with f32 x at batch 2..8 runs the register-fed mma.sync kernel
+    with one fresh accumulator per 32-k sub-block (step and offset applied on
+    the CUDA cores), x staged as hi + lo f16 parts; ragged 16-row tiles and
+    uneven K splits.  At batch 5..8 with K = 11008 the staged x would not fit
+    in shared memory, so the batch runs as two launches of at most 4 rows.
+    Batch 1, and bf16 x at any batch up to 8 (two rows per launch), take the
+    TMA-fed kernel (gemv_blk_tc)."""
     for N, K in ((29, 1536), (263, 4096), (16, 256), (40, 11008)):
         check_gemv(synth.make_layer("q4k", N, K, config=35, matrix=M, outliers=True), M, config=35 + M,
                    xdtype=xdtype)
-        assert q4.q4_last_gemv_path() == ("gemv_blk_tc_q4k" if M == 1 else "gemv_mma_q4k")
+        assert q4.q4_last_gemv_path() == ("gemv_blk_tc_q4k" if M == 1 or xdtype == "bf16" else "gemv_mma_q4k")
 
 
 @pytest.mark.parametrize("xdtype", ["f32", "bf16"])
@@ -225,7 +226,7 @@ def test_gemv_q40_tensor_core_path(M, xdtype):
     for N, K in ((33, 2048), (263, 11008), (16, 256)):
         check_gemv(synth.make_layer("q40", N, K, config=37, matrix=M, outliers=True), M, config=37 + M,
                    xdtype=xdtype)
-        assert q4.q4_last_gemv_path() == ("gemv_blk_tc_q40" if M == 1 else "gemv_mma_q40")
+        assert q4.q4_last_gemv_path() == ("gemv_blk_tc_q40" if M == 1 or xdtype == "bf16" else "gemv_mma_q40")
 
 
 @pytest.mark.parametrize("xdtype", ["f32", "bf16"])
