@@ -690,6 +690,7 @@ int fp4tc_read_and_clear_error();
 int awq_read_and_clear_error();
 int gptq_tc_read_and_clear_error();
 int blk_tc_read_and_clear_error();
+int a16tc_read_and_clear_error();
 
 int read_and_clear_device_error() {
     int v = 0;
@@ -704,7 +705,8 @@ int read_and_clear_device_error() {
     const int aw = awq_read_and_clear_error();
     const int gq = gptq_tc_read_and_clear_error();
     const int bt = blk_tc_read_and_clear_error();
-    return v ? v : g ? g : tm ? tm : pk ? pk : f4 ? f4 : aw ? aw : gq ? gq : bt;
+    const int aq = a16tc_read_and_clear_error();
+    return v ? v : g ? g : tm ? tm : pk ? pk : f4 ? f4 : aw ? aw : gq ? gq : bt ? bt : aq;
 }
 
 }  // namespace q4

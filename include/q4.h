@@ -221,6 +221,10 @@ int q4_gemv_chain(const q4_gemv_desc *descs, const int *first, int ngroups, int6
  * finite.  Each launch quantizes up to 8 activation rows into a 200 KiB
  * shared-memory budget (8 rows up to K = 24,832; fewer rows per launch above
  * that; K > 200,448 gets Q4_EDIM); larger M runs as several launches.
+ * M = 1 (K up to 18,432) and M = 2 (K up to 8,192) run a TMA-fed kernel whose
+ * f16 tensor-core MMA forms each group's q1 * q8 dot exactly (E2M1 halves
+ * times 8-bit codes, partial sums below 2^15: no f32 rounding), the rest on
+ * the CUDA cores; both give the same bits.
  * Allocates nothing; asynchronous on `stream`. */
 int q4_gemv_a16q8(const void *W_packed, const void *scales, const q4_aux *aux, const void *x, float *y,
                   int64_t M, int64_t N, int64_t K, void *stream);
@@ -413,7 +417,8 @@ int q4_last_error(void);
  * "gemv_tma_chain", "gemm_tc", "gemv_mma", "gemv_mma_group", "gemv_mma_q4k",
  * "gemv_mma_q40", "gemv_mma_gptq", "gemv_rows_tma", "gemv_rows_m1",
  * "gemv_general", "gemv_kmajor", "gemv_awq_tc", "gemv_gptq_tc", "gemv_blk_tc_q4k",
- * "gemv_blk_tc_q40", "gemv_blk_tc_q4k_group", "gemv_blk_tc_q40_group"; "gemv_a16q8" after q4_gemv_a16q8,
+ * "gemv_blk_tc_q40", "gemv_blk_tc_q4k_group", "gemv_blk_tc_q40_group"; "gemv_a16q8" or
+ * "gemv_a16q8_tc" after q4_gemv_a16q8,
  * "gemv_q4k_q8" after q4_gemv_q4k_q8, "gemv_w4a4" after q4_gemv_w4a4,
  * "gemv_w4a4_tc" after q4_gemv_w4a4_tc; "" before
  * the first call).  A diagnostic with no counterpart in the pages: it lets a

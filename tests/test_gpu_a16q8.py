@@ -6,7 +6,9 @@ a pinned f32 epilogue), so the bar is bit-exact equality with the oracle on
 every output, at small ragged shapes, at the full 14336 x 4096 layer, and on
 the edge cases: zero activation blocks, negative scale bytes, partial
 1024-k chunks, N not a multiple of the warps per CTA, batches that span
-several launches.
+several launches.  Batch 1 and 2 run the tensor-core kernel (exact f16 group
+dots), larger batches the CUDA-core one: the batch-independence test checks
+the two against each other bit for bit.
 """
 import numpy as np
 import pytest
@@ -40,7 +42,11 @@ def gpu_a16q8(layer, xdev, M):
     aux = q4.make_aux(scale2=layer["scale2"], x_dtype=xdev.dtype, fmt="nvfp4")
     q4.q4_gemv_a16q8(d["w"], d["scales"], aux, xdev, y, M, N, K)
     torch.cuda.synchronize()
-    assert q4.q4_last_gemv_path() == "gemv_a16q8"
+    # batch 1 and 2 (staged codes and three ring stages within shared memory) take the
+    # tensor-core kernel; larger batches the CUDA-core one; both hold the same contract
+    assert q4.q4_last_gemv_path() == ("gemv_a16q8_tc" if M <= 2 and K <= (14336 if M == 1 else 6144)
+                                      else "gemv_a16q8")
+    assert q4.q4_last_error() == q4.Q4_OK
     return y.cpu().numpy()
 
 
@@ -120,3 +126,26 @@ def test_a16q8_full_layer_14336x4096():
     y64, bound = oracle_gemv_all_rows(to_oracle(layer), xf[:, :K])
     err = np.abs(got.astype(np.float64) - y64)
     assert np.all(err <= 0.02 * bound + 1e-3)
+
+
+@pytest.mark.parametrize("M", [1, 2])
+@pytest.mark.parametrize("xdtype", ["bf16", "f32"])
+def test_a16q8_tensor_core_shapes(M, xdtype):
+    """The tensor-core kernel on ragged shapes: a partial last 2048-k stage
+    (K = 2304, 4352), one 256-k block, a 17-row last tile, more tiles than
+    CTAs, K = 14336 at batch 1, extreme activation ranges; bit-exact."""
+    shapes = [(4099, 2304), (17, 256), (5000, 4352), (300, 4096)]
+    if M == 1:
+        shapes.append((131, 14336))
+    for i, (N, K) in enumerate(shapes):
+        layer, xh, xf = draw(N, K, M, xdtype, config=32, matrix=i)
+        ref = oracle.gemv_a16q8(to_oracle(layer), xf)
+        assert bits_equal(gpu_a16q8(layer, x_device(xh), M), ref), (N, K)
+    N, K = 64, 2048
+    layer, _, _ = draw(N, K, M, xdtype, config=33)
+    xf = np.random.default_rng(3).normal(0, 1e-10, (M, K)).astype(np.float32)
+    xf[:, 5] = 1e30
+    xf[:, 300] = -3e20
+    xf[M - 1, 512:768] = 0.0
+    ref = oracle.gemv_a16q8(to_oracle(layer), xf)
+    assert bits_equal(gpu_a16q8(layer, x_device(xf), M), ref)
