@@ -691,6 +691,7 @@ int awq_read_and_clear_error();
 int gptq_tc_read_and_clear_error();
 int blk_tc_read_and_clear_error();
 int a16tc_read_and_clear_error();
+int k8tc_read_and_clear_error();
 
 int read_and_clear_device_error() {
     int v = 0;
@@ -706,7 +707,8 @@ int read_and_clear_device_error() {
     const int gq = gptq_tc_read_and_clear_error();
     const int bt = blk_tc_read_and_clear_error();
     const int aq = a16tc_read_and_clear_error();
-    return v ? v : g ? g : tm ? tm : pk ? pk : f4 ? f4 : aw ? aw : gq ? gq : bt ? bt : aq;
+    const int kt = k8tc_read_and_clear_error();
+    return v ? v : g ? g : tm ? tm : pk ? pk : f4 ? f4 : aw ? aw : gq ? gq : bt ? bt : aq ? aq : kt;
 }
 
 }  // namespace q4

@@ -11,11 +11,13 @@
 // c = fma(c, scale2, 0), total = fma(1, c, total) in block order, and the
 // output is total rounded to binary16.
 //
-// Why the tensor cores give the same integers: a 16-k group's
-// sum e2m1 * q8 has E2M1 values (multiples of 1/2, |v| <= 6, exact in f16)
-// times 8-bit codes (exact in f16), products of at most 11 significant bits
-// and partial sums below 2^15 in steps of 1/2, so the f16 MMA's f32
-// accumulation is exact and 2 * D is the group's q1 * q8 dot.
+// Why the tensor cores give the same integers: the activation codes are
+// staged doubled (2 q8, |2 q8| <= 254, exact in f16), so a 16-k group's sum
+// e2m1 * 2 q8 has E2M1 values (multiples of 1/2, |v| <= 6, exact in f16)
+// times even integers: integer products of at most 11 significant bits and
+// partial sums below 2^15, which the f16 MMA's f32 accumulation holds
+// exactly.  D is the group's q1 * q8 dot; adding 1.5 * 2^23 (exact) leaves it
+// in the low mantissa bits, read as an integer with no conversion.
 //
 // Layout and roles are the NVFP4 TMA-fed GEMV's (gemv_tma.cu): a stage is 16
 // rows x 2048 k (the payload as a chunk-major 3-D box with the 128-byte
@@ -49,7 +51,7 @@ constexpr int AQ_PAY = AQ_ROWS * AQ_KS / 2;           // 16 KB of payload
 constexpr int AQ_SC = AQ_ROWS * AQ_KS / 16;           // 2 KB of E4M3 scales
 constexpr int AQ_STAGE = AQ_PAY + AQ_SC;
 constexpr int AQ_MAX_NS = 6;
-constexpr int AQ_XQ = 640;                            // staged codes per block and row: 4 x 144 B, padded to 128
+constexpr int AQ_XQ = 656;                            // staged codes per block and row: 4 x 144 B, padded to 16 mod 128
 constexpr int AQ_SMEM_CAP = 112 * 1024;
 constexpr long long AQ_WAIT = 1LL << 31;
 static_assert(AQ_STAGE % 1024 == 0, "stages stay 1024-byte aligned");
@@ -67,21 +69,23 @@ struct AqArgs {
     float scale2;
 };
 
-// After the ring: staged codes [8 warps][nst][MB][640] (lane quarter t at 144 t:
-// 16 bytes apart modulo 128, so the diagonal lanes' loads never share banks), a
-// 128-byte zero block at 64 mod 128, activation scales [8][nst][MB] f32, the
-// q9 table [256] i32, block results [2][MB][16][nb] f32.
+// After the ring: staged codes [8 warps][nst][MB][656] (lane quarter t at 144 t
+// and batch row m at 656 m: 16 t + 16 m modulo 128), a 128-byte zero block at
+// 80 mod 128, so the diagonal lanes' 16-byte loads and the zero block's never
+// share banks; activation scales [8][nst][MB] f32, the q9 table [256] i32,
+// block results [2][MB][16][nb | 1] f32 (an odd row stride: the lanes' stores
+// and the row sums hit distinct banks).
 struct AqLayout {
     int xs, zero, as, lut, cb, total;
 };
 __host__ __device__ inline AqLayout aq_layout(int NS, int nst, int nb, int mb) {
     AqLayout L;
     L.xs = NS * AQ_STAGE;
-    L.zero = L.xs + AQ_WARPS * nst * mb * AQ_XQ + 64;
-    L.as = L.zero + 128 + 64;
+    L.zero = L.xs + AQ_WARPS * nst * mb * AQ_XQ + 80;
+    L.as = L.zero + 128 + 48;
     L.lut = (L.as + AQ_WARPS * nst * mb * 4 + 15) / 16 * 16;
     L.cb = L.lut + 1024;
-    L.total = L.cb + 2 * mb * AQ_ROWS * nb * 4;
+    L.total = L.cb + 2 * mb * AQ_ROWS * (nb | 1) * 4;
     return L;
 }
 
@@ -212,7 +216,7 @@ gemv_a16q8_tc(const __grid_constant__ AqMaps maps, const __grid_constant__ AqArg
                 int c1 = live ? __float2int_rn(__fmul_rn(v[2 * i + 1], iscale)) : 0;
                 c0 = (int)(int8_t)(uint8_t)((c0 > 127 ? 127 : c0) & 0xff);     // the 8-bit code the contract keeps
                 c1 = (int)(int8_t)(uint8_t)((c1 > 127 ? 127 : c1) & 0xff);
-                h[i] = h2bits(__int2half_rn(c0), __int2half_rn(c1));
+                h[i] = h2bits(__int2half_rn(2 * c0), __int2half_rn(2 * c1));   // 2 q8: the MMA sums q1 q8
             }
             // k = 256 b + 8 lane ..: quarter lane >> 3 of the block, 16 bytes at 16 (lane & 7)
             sts128(xs_w + (uint32_t)((s * MB + m) * AQ_XQ + (lane >> 3) * 144 + (lane & 7) * 16),
@@ -234,6 +238,7 @@ gemv_a16q8_tc(const __grid_constant__ AqMaps maps, const __grid_constant__ AqArg
     const uint32_t offS = (uint32_t)AQ_PAY + (uint32_t)(g * 128) + ((uint32_t)(warp ^ g) << 4) + 4 * t;
     constexpr uint32_t ROW8 = 8 * 128;
     float *cb = reinterpret_cast<float *>(ring + L.cb);
+    const int nbp = nb | 1;                                                  // odd row stride: no bank conflicts
     bool ok = true;
     int buf = 0;
     for (int j = 0; j < J; j++) {
@@ -263,23 +268,25 @@ gemv_a16q8_tc(const __grid_constant__ AqMaps maps, const __grid_constant__ AqArg
                     uint32_t av[4], cv[4];
                     e2m1x8_h2(wa[wd], av[0], av[1], av[2], av[3]);
                     e2m1x8_h2(wb[wd], cv[0], cv[1], cv[2], cv[3]);
-                    const uint2 bA = lds64(xa + (uint32_t)(64 * h + 16 * wd)), bB = lds64(xa + (uint32_t)(64 * h + 16 * wd + 8));
-                    mma16816(D[gq], make_uint4(av[0], cv[0], av[1], cv[1]), bA.x, bA.y);
-                    mma16816(D[gq], make_uint4(av[2], cv[2], av[3], cv[3]), bB.x, bB.y);
+                    const uint4 bx = lds128(xa + (uint32_t)(64 * h + 16 * wd));
+                    mma16816(D[gq], make_uint4(av[0], cv[0], av[1], cv[1]), bx.x, bx.y);
+                    mma16816(D[gq], make_uint4(av[2], cv[2], av[3], cv[3]), bx.z, bx.w);
                 }
 #pragma unroll
                 for (int gq = 0; gq < 2; gq++) {
                     const int q = 2 * h + gq;
 #pragma unroll
                     for (int m = 0; m < MB; m++) {
-                        // 2 D is the group's exact q1 * q8 dot (D a multiple of 1/2 below 2^15)
-                        T[m][0] += (int64_t)__float2int_rn(2.0f * D[gq][m]) * qa[q];
-                        T[m][1] += (int64_t)__float2int_rn(2.0f * D[gq][2 + m]) * qb[q];
+                        // D is the group's exact q1 * q8 dot (an integer below 2^15), read from the bits
+                        // of 1.5 * 2^23 + D
+                        const float da = __fadd_rn(D[gq][m], 0x1.8p23f), db = __fadd_rn(D[gq][2 + m], 0x1.8p23f);
+                        T[m][0] += (int64_t)((int)__float_as_uint(da) - 0x4B400000) * qa[q];
+                        T[m][1] += (int64_t)((int)__float_as_uint(db) - 0x4B400000) * qb[q];
                     }
                 }
             }
             // the block: the four lanes of a row, then the pinned f32 steps
-            float *cbb = cb + buf * MB * AQ_ROWS * nb;
+            float *cbb = cb + buf * MB * AQ_ROWS * nbp;
 #pragma unroll
             for (int m = 0; m < MB; m++) {
                 const float ascale = as_w[st * MB + m];
@@ -291,7 +298,7 @@ gemv_a16q8_tc(const __grid_constant__ AqMaps maps, const __grid_constant__ AqArg
                     float c = __fmaf_rn(__ll2float_rn((long long)v), 0x1p-10f, 0.0f);
                     c = __fmaf_rn(c, ascale, 0.0f);
                     c = __fmaf_rn(c, a.scale2, 0.0f);
-                    if (t == 0) cbb[(m * AQ_ROWS + g + 8 * r) * nb + b] = c;
+                    if (t == 0) cbb[(m * AQ_ROWS + g + 8 * r) * nbp + b] = c;
                 }
             }
         }
@@ -304,8 +311,9 @@ gemv_a16q8_tc(const __grid_constant__ AqMaps maps, const __grid_constant__ AqArg
                 const int m = threadIdx.x / AQ_ROWS, rr = threadIdx.x % AQ_ROWS;
                 const int64_t n = (int64_t)((int)blockIdx.x + (j / nst) * (int)gridDim.x) * AQ_ROWS + rr;
                 if (n < a.N && ok) {
-                    const float *row = cb + buf * MB * AQ_ROWS * nb + (m * AQ_ROWS + rr) * nb;
+                    const float *row = cb + buf * MB * AQ_ROWS * nbp + (m * AQ_ROWS + rr) * nbp;
                     float total = 0.0f;
+#pragma unroll 8
                     for (int bb = 0; bb < nb; bb++) total = __fmaf_rn(1.0f, row[bb], total);
                     a.y[(int64_t)m * a.N + n] = __half2float(__float2half_rn(total));
                 }

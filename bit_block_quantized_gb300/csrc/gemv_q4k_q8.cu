@@ -244,7 +244,16 @@ int gemv_q4k_q8_chunk(int64_t M, int64_t K) {
     return 0;
 }
 
+bool gemv_q4k_q8_tc_eligible(const Tensor &t, int64_t M);
+cudaError_t launch_gemv_q4k_q8_tc(const Tensor &t, const void *x, q4_dtype xd, float *y, int64_t M, cudaStream_t s);
+
 cudaError_t launch_gemv_q4k_q8(const Tensor &t, const void *x, q4_dtype xd, float *y, int64_t M, cudaStream_t s) {
+    // batch 1 and 2: the same contract with the sub-block sums on the tensor cores (gemv_q4k_q8_tc.cu)
+    if (gemv_q4k_q8_tc_eligible(t, M)) {
+        const cudaError_t e = launch_gemv_q4k_q8_tc(t, x, xd, y, M, s);
+        if (e == cudaSuccess) note_gemv_path("gemv_q4k_q8_tc");
+        return e;
+    }
     const int chunk = gemv_q4k_q8_chunk(M, t.K);
     if (chunk == 0) return cudaErrorInvalidValue;
     for (int64_t m0 = 0; m0 < M; m0 += chunk) {

@@ -245,7 +245,11 @@ int q4_gemv_a16q8(const void *W_packed, const void *scales, const q4_aux *aux, c
  * roundings above are this library's reading.  Bit-reproducible across
  * runs, batch sizes and devices.  K % 256 == 0 (Q4_EDIM otherwise); x must be
  * finite.  Up to 8 activation rows per launch in a 200 KiB shared-memory
- * budget; larger M runs as several launches.  Allocates nothing;
+ * budget; larger M runs as several launches.  M = 1 (K up to 12,288) and
+ * M = 2 (K up to 10,240) run a TMA-fed kernel whose f16 tensor-core MMAs form
+ * each 32-value sub-block's sum of q * q8 exactly (codes as f16 subnormals
+ * times 8-bit activation codes, sums below 2^16 * 2^-24: no f32 rounding);
+ * other shapes the CUDA cores; both give the same bits.  Allocates nothing;
  * asynchronous on `stream`. */
 int q4_gemv_q4k_q8(const void *W_packed, const q4_aux *aux, const void *x, float *y, int64_t M, int64_t N,
                    int64_t K, void *stream);
@@ -419,7 +423,7 @@ int q4_last_error(void);
  * "gemv_general", "gemv_kmajor", "gemv_awq_tc", "gemv_gptq_tc", "gemv_blk_tc_q4k",
  * "gemv_blk_tc_q40", "gemv_blk_tc_q4k_group", "gemv_blk_tc_q40_group"; "gemv_a16q8" or
  * "gemv_a16q8_tc" after q4_gemv_a16q8,
- * "gemv_q4k_q8" after q4_gemv_q4k_q8, "gemv_w4a4" after q4_gemv_w4a4,
+ * "gemv_q4k_q8" or "gemv_q4k_q8_tc" after q4_gemv_q4k_q8, "gemv_w4a4" after q4_gemv_w4a4,
  * "gemv_w4a4_tc" after q4_gemv_w4a4_tc; "" before
  * the first call).  A diagnostic with no counterpart in the pages: it lets a
  * caller (and the tests) confirm which path a shape takes.  Static storage. */
