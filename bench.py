@@ -763,11 +763,41 @@ def _time_launches(torch, stream, launch, reps=200, warm=10):
     return a.elapsed_time(b) * 1e3 / reps
 
 
+def _time_graph(torch, stream, launch, reps=200, warm=10):
+    """Average device time per launch with the `reps` launches captured into
+    one CUDA graph and replayed between the two events (on `stream`), so no
+    host launch gap enters the time: how the headline step is timed.  For the
+    GEMV rows, whose calls allocate nothing and never synchronize.  If the
+    capture fails the launches are issued one by one instead.  Returns
+    (us per launch, "graph" or "eager")."""
+    with torch.cuda.stream(stream):
+        for i in range(warm):
+            launch(i)
+        torch.cuda.synchronize()
+        try:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for i in range(reps):
+                    launch(i)
+        except Exception:
+            torch.cuda.synchronize()
+            return _time_launches(torch, stream, launch, reps, warm), "eager"
+        g.replay()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        g.replay()
+        b.record(stream)
+        torch.cuda.synchronize()
+    return a.elapsed_time(b) * 1e3 / reps, "graph"
+
+
 def other_rows(torch, q4, synth, peak_hbm):
     """Each remaining hot-path row on its own configuration's shape: the GEMV
     of every format at batch 1 (NVFP4 also at batch 4 and 8), dequant and
     repack.  Every launch reads a different weight copy (working set > L2);
-    CUDA events on the launching stream.  Bytes are the row's algorithmic
+    CUDA events on the launching stream, the GEMV rows' launches replayed as
+    one CUDA graph.  Bytes are the row's algorithmic
     bytes: packed weights (q4_packed_bytes) + x + y for a GEMV, packed +
     f32 output for dequant, packed in + packed out for repack."""
     stream = torch.cuda.Stream()
@@ -793,11 +823,11 @@ def other_rows(torch, q4, synth, peak_hbm):
         def launch(i):
             c = cps[i % len(cps)]
             q4.q4_gemv(fmt, c["w"], c["scales"], auxes[i % len(cps)], x, y, M, N, K, stream=stream)
-        us = _time_launches(torch, stream, launch)
+        us, how = _time_graph(torch, stream, launch)
         moved = packed + x.numel() * x.element_size() + y.numel() * 4
         rows.append({"row": tag, "shape": f"{N}x{K}", "M": M, "us_per_launch": round(us, 2),
                      "GBps": round(moved / us / 1e3, 1), "frac_hbm": round(moved / us / 1e3 / peak_hbm, 4),
-                     "path": q4.q4_last_gemv_path()})
+                     "path": q4.q4_last_gemv_path(), "timing": how})
 
     gemv_row("a1 NVFP4 GEMV", "nvfp4", 14336, 4096, 4, 5, dict(row_scale=True), q4.Q4_DT_BF16)
     gemv_row("a1 NVFP4 GEMV", "nvfp4", 14336, 4096, 8, 5, dict(row_scale=True), q4.Q4_DT_BF16)
@@ -817,12 +847,13 @@ def other_rows(torch, q4, synth, peak_hbm):
     x = torch.from_numpy(np.ascontiguousarray(xb).view(np.int16)).cuda().view(torch.bfloat16)
     y = torch.empty((M, N), dtype=torch.float32, device="cuda")
     aux = q4.make_aux(scale2=layer["scale2"], x_dtype=q4.Q4_DT_BF16, fmt="nvfp4")
-    us = _time_launches(torch, stream, lambda i: q4.q4_gemv_a16q8(cps[i % len(cps)]["w"], cps[i % len(cps)]["scales"],
-                                                                  aux, x, y, M, N, K, stream=stream))
+    us, how = _time_graph(torch, stream, lambda i: q4.q4_gemv_a16q8(cps[i % len(cps)]["w"],
+                                                                    cps[i % len(cps)]["scales"], aux, x, y, M, N, K,
+                                                                    stream=stream))
     moved = packed + x.numel() * 2 + y.numel() * 4
     rows.append({"row": A16Q8_ROW, "shape": f"{N}x{K}", "M": M, "us_per_launch": round(us, 2),
                  "GBps": round(moved / us / 1e3, 1), "frac_hbm": round(moved / us / 1e3 / peak_hbm, 4),
-                 "path": q4.q4_last_gemv_path()})
+                 "path": q4.q4_last_gemv_path(), "timing": how})
     del cps
     torch.cuda.empty_cache()
 
@@ -840,9 +871,10 @@ def other_rows(torch, q4, synth, peak_hbm):
     moved = packed + x.numel() * 2 + y.numel() * 4
 
     def lane_row(tag, fn, nbytes=moved, path=True):
-        us = _time_launches(torch, stream, fn)
+        us, how = _time_graph(torch, stream, fn)
         row = {"row": tag, "shape": f"{N}x{K}", "M": M, "us_per_launch": round(us, 2),
-               "GBps": round(nbytes / us / 1e3, 1), "frac_hbm": round(nbytes / us / 1e3 / peak_hbm, 4)}
+               "GBps": round(nbytes / us / 1e3, 1), "frac_hbm": round(nbytes / us / 1e3 / peak_hbm, 4),
+               "timing": how}
         if path:
             row["path"] = q4.q4_last_gemv_path()
         rows.append(row)
@@ -866,12 +898,13 @@ def other_rows(torch, q4, synth, peak_hbm):
     _, qxf = synth.draw_x(1, 4096, config=1, matrix=5, dtype="f32")
     qx = torch.from_numpy(np.ascontiguousarray(qxf, np.float32)).cuda()
     qy = torch.empty((1, 4096), dtype=torch.float32, device="cuda")
-    us = _time_launches(torch, stream, lambda i: q4.q4_gemv_q4k_q8(qcps[i % len(qcps)]["w"], None, qx, qy, 1, 4096,
-                                                                    4096, stream=stream))
+    us, how = _time_graph(torch, stream, lambda i: q4.q4_gemv_q4k_q8(qcps[i % len(qcps)]["w"], None, qx, qy, 1,
+                                                                      4096, 4096, stream=stream))
     qmoved = qpacked + qx.numel() * 4 + qy.numel() * 4
     rows.append({"row": "f2 Q4_K x Q8 (W4A8) GEMV, integer sub-block sums", "shape": "4096x4096", "M": 1,
                  "us_per_launch": round(us, 2), "GBps": round(qmoved / us / 1e3, 1),
-                 "frac_hbm": round(qmoved / us / 1e3 / peak_hbm, 4), "path": q4.q4_last_gemv_path()})
+                 "frac_hbm": round(qmoved / us / 1e3 / peak_hbm, 4), "path": q4.q4_last_gemv_path(),
+                 "timing": how})
     del qcps
     torch.cuda.empty_cache()
     # f3: the GPU quantizers on the 14336x4096 layer (f32 W in, packed out)
@@ -955,6 +988,9 @@ def other_rows(torch, q4, synth, peak_hbm):
     del cps
     torch.cuda.empty_cache()
     return {"l2": "each launch reads a different weight copy; working set >= 256 MB per row",
+            "timing": "CUDA events around 200 launches: for the GEMV rows one CUDA graph of the 200 launches "
+                      "(no host launch gaps, as the headline step; a row's 'timing' says 'eager' if its calls "
+                      "could not be captured), for the others launch by launch",
             "peak_hbm_GBps": peak_hbm, "entries": rows}
 
 

@@ -52,7 +52,9 @@ constexpr int AQ_SC = AQ_ROWS * AQ_KS / 16;           // 2 KB of E4M3 scales
 constexpr int AQ_STAGE = AQ_PAY + AQ_SC;
 constexpr int AQ_MAX_NS = 6;
 constexpr int AQ_XQ = 656;                            // staged codes per block and row: 4 x 144 B, padded to 16 mod 128
-constexpr int AQ_SMEM_CAP = 112 * 1024;
+// Shared memory per CTA: two CTAs per SM, or three (batch 1 where three ring stages
+// still fit: more decode warps per scheduler, measured faster) within 74 KB.
+constexpr int aq_smem_cap(int ctas) { return ctas == 3 ? 74 * 1024 : 112 * 1024; }
 constexpr long long AQ_WAIT = 1LL << 31;
 static_assert(AQ_STAGE % 1024 == 0, "stages stay 1024-byte aligned");
 
@@ -125,8 +127,8 @@ __device__ __forceinline__ void aq_load8(const __nv_bfloat16 *p, float (&v)[8]) 
     }
 }
 
-template <typename XT, int MB>
-__global__ void __launch_bounds__(AQ_THREADS, 2)
+template <typename XT, int MB, int CTAS>
+__global__ void __launch_bounds__(AQ_THREADS, CTAS)
 gemv_a16q8_tc(const __grid_constant__ AqMaps maps, const __grid_constant__ AqArgs a) {
     extern __shared__ uint8_t smem_raw[];
     __shared__ uint64_t full[AQ_MAX_NS], empty[AQ_MAX_NS];
@@ -186,42 +188,70 @@ gemv_a16q8_tc(const __grid_constant__ AqMaps maps, const __grid_constant__ AqArg
     const XT *xp = reinterpret_cast<const XT *>(a.x);
     const uint32_t xs_w = smem_u32(ring + L.xs) + (uint32_t)(warp * nst * MB * AQ_XQ);
     float *as_w = reinterpret_cast<float *>(ring + L.as) + warp * nst * MB;
-    for (int s = 0; s < nst; s++) {
-        const int b = warp + AQ_WARPS * s;
-        if (b >= nb) break;
+    for (int s0 = 0; s0 < nst; s0 += 2) {
+        // two of the warp's blocks at a time: their loads and shuffle chains overlap
+        float v[2][MB][8];
 #pragma unroll
-        for (int m = 0; m < MB; m++) {
-            float v[8];
-            aq_load8(xp + (int64_t)m * a.K + (int64_t)b * 256 + lane * 8, v);
-            float amax = 0.0f, val = 0.0f;
-            int idx = 0x7fffffff;
+        for (int p = 0; p < 2; p++) {
+            const int b = warp + AQ_WARPS * (s0 + p);
+            const bool have = s0 + p < nst && b < nb;
 #pragma unroll
-            for (int i = 0; i < 8; i++) {
-                const float av = fabsf(v[i]);
-                if (av > amax) { amax = av; val = v[i]; idx = lane * 8 + i; }
+            for (int m = 0; m < MB; m++) {
+                if (have) {
+                    aq_load8(xp + (int64_t)m * a.K + (int64_t)b * 256 + lane * 8, v[p][m]);
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 8; i++) v[p][m][i] = 0.0f;
+                }
+            }
+        }
+        float amax[2][MB], val[2][MB];
+        int idx[2][MB];
+#pragma unroll
+        for (int p = 0; p < 2; p++)
+#pragma unroll
+            for (int m = 0; m < MB; m++) {
+                amax[p][m] = 0.0f, val[p][m] = 0.0f, idx[p][m] = 0x7fffffff;
+#pragma unroll
+                for (int i = 0; i < 8; i++) {
+                    const float av = fabsf(v[p][m][i]);
+                    if (av > amax[p][m]) { amax[p][m] = av; val[p][m] = v[p][m][i]; idx[p][m] = lane * 8 + i; }
+                }
             }
 #pragma unroll
-            for (int off = 16; off > 0; off >>= 1) {   // largest magnitude, first index on ties
-                const float oa = __shfl_xor_sync(0xffffffffu, amax, off);
-                const float ov = __shfl_xor_sync(0xffffffffu, val, off);
-                const int oi = __shfl_xor_sync(0xffffffffu, idx, off);
-                if (oa > amax || (oa == amax && oi < idx)) { amax = oa; val = ov; idx = oi; }
-            }
-            const float iscale = __fdiv_rn(-127.0f, val);
-            const bool live = isfinite(iscale);         // zero (or vanishing) block: codes 0, scale 0
-            uint32_t h[4];
+        for (int off = 16; off > 0; off >>= 1)          // largest magnitude, first index on ties
 #pragma unroll
-            for (int i = 0; i < 4; i++) {
-                int c0 = live ? __float2int_rn(__fmul_rn(v[2 * i], iscale)) : 0;
-                int c1 = live ? __float2int_rn(__fmul_rn(v[2 * i + 1], iscale)) : 0;
-                c0 = (int)(int8_t)(uint8_t)((c0 > 127 ? 127 : c0) & 0xff);     // the 8-bit code the contract keeps
-                c1 = (int)(int8_t)(uint8_t)((c1 > 127 ? 127 : c1) & 0xff);
-                h[i] = h2bits(__int2half_rn(2 * c0), __int2half_rn(2 * c1));   // 2 q8: the MMA sums q1 q8
+            for (int p = 0; p < 2; p++)
+#pragma unroll
+                for (int m = 0; m < MB; m++) {
+                    const float oa = __shfl_xor_sync(0xffffffffu, amax[p][m], off);
+                    const float ov = __shfl_xor_sync(0xffffffffu, val[p][m], off);
+                    const int oi = __shfl_xor_sync(0xffffffffu, idx[p][m], off);
+                    if (oa > amax[p][m] || (oa == amax[p][m] && oi < idx[p][m])) {
+                        amax[p][m] = oa; val[p][m] = ov; idx[p][m] = oi;
+                    }
+                }
+#pragma unroll
+        for (int p = 0; p < 2; p++) {
+            const int s = s0 + p, b = warp + AQ_WARPS * s;
+            if (s >= nst || b >= nb) break;
+#pragma unroll
+            for (int m = 0; m < MB; m++) {
+                const float iscale = __fdiv_rn(-127.0f, val[p][m]);
+                const bool live = isfinite(iscale);     // zero (or vanishing) block: codes 0, scale 0
+                uint32_t h[4];
+#pragma unroll
+                for (int i = 0; i < 4; i++) {
+                    int c0 = live ? __float2int_rn(__fmul_rn(v[p][m][2 * i], iscale)) : 0;
+                    int c1 = live ? __float2int_rn(__fmul_rn(v[p][m][2 * i + 1], iscale)) : 0;
+                    c0 = (int)(int8_t)(uint8_t)((c0 > 127 ? 127 : c0) & 0xff);     // the 8-bit code the contract keeps
+                    c1 = (int)(int8_t)(uint8_t)((c1 > 127 ? 127 : c1) & 0xff);
+                    h[i] = h2bits(__int2half_rn(2 * c0), __int2half_rn(2 * c1));   // 2 q8: the MMA sums q1 q8
+                }
+                sts128(xs_w + (uint32_t)((s * MB + m) * AQ_XQ + (lane >> 3) * 144 + (lane & 7) * 16),
+                       make_uint4(h[0], h[1], h[2], h[3]));
+                if (lane == 0) as_w[s * MB + m] = live ? __fdiv_rn(1.0f, iscale) : 0.0f;
             }
-            // k = 256 b + 8 lane ..: quarter lane >> 3 of the block, 16 bytes at 16 (lane & 7)
-            sts128(xs_w + (uint32_t)((s * MB + m) * AQ_XQ + (lane >> 3) * 144 + (lane & 7) * 16),
-                   make_uint4(h[0], h[1], h[2], h[3]));
-            if (lane == 0) as_w[s * MB + m] = live ? __fdiv_rn(1.0f, iscale) : 0.0f;
         }
     }
     __syncwarp();
@@ -327,33 +357,33 @@ struct AqPlan {
     int nb, nst, NS, smem;
 };
 
-bool aq_plan(int64_t K, int mb, AqPlan &p) {
+bool aq_plan(int64_t K, int mb, int ctas, AqPlan &p) {
     if (K % 256 != 0 || K <= 0 || K > (1LL << 24)) return false;
     p.nb = (int)(K / 256);
     p.nst = (p.nb + AQ_WARPS - 1) / AQ_WARPS;
     const AqLayout L0 = aq_layout(0, p.nst, p.nb, mb);
-    const int ns = (AQ_SMEM_CAP - 1024 - L0.total) / AQ_STAGE;
+    const int ns = (aq_smem_cap(ctas) - 1024 - L0.total) / AQ_STAGE;
     if (ns < 3) return false;
     p.NS = ns < AQ_MAX_NS ? ns : AQ_MAX_NS;
     p.smem = 1024 + aq_layout(p.NS, p.nst, p.nb, mb).total;
     return true;
 }
 
-template <typename XT, int MB>
+template <typename XT, int MB, int CTAS>
 cudaError_t aq_run(const AqMaps &maps, const AqArgs &a, int smem, cudaStream_t s) {
-    auto kern = gemv_a16q8_tc<XT, MB>;
+    auto kern = gemv_a16q8_tc<XT, MB, CTAS>;
     static bool attr_set[64] = {};
     static int per_sm[64] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (!attr_set[dev & 63]) {
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, AQ_SMEM_CAP);
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, aq_smem_cap(CTAS));
         if (e != cudaSuccess) return e;
         e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
         if (e != cudaSuccess) return e;
         int b = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, kern, AQ_THREADS, AQ_SMEM_CAP) != cudaSuccess || b < 1)
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, kern, AQ_THREADS, aq_smem_cap(CTAS)) != cudaSuccess || b < 1)
             b = 1;
         per_sm[dev & 63] = b;
         attr_set[dev & 63] = true;
@@ -400,13 +430,14 @@ bool gemv_a16q8_tc_eligible(const Tensor &t, int64_t M) {
     if (t.fmt != Q4_NVFP4 || M < 1 || M > 2 || t.K % 256 != 0 || t.N < 1 || t.N > (1LL << 30)) return false;
     if ((((uintptr_t)t.w | (uintptr_t)t.scales) & 15) != 0 || encode_fn() == nullptr) return false;
     AqPlan p;
-    return aq_plan(t.K, (int)M, p);
+    return aq_plan(t.K, (int)M, 2, p);
 }
 
 cudaError_t launch_gemv_a16q8_tc(const Tensor &t, const void *x, q4_dtype xd, float *y, int64_t M, cudaStream_t s) {
     AqPlan p;
     AqMaps maps;
-    if (M < 1 || M > 2 || !aq_plan(t.K, (int)M, p) || !aq_encode(maps, t)) return cudaErrorInvalidValue;
+    const bool three = M == 1 && aq_plan(t.K, 1, 3, p);
+    if (M < 1 || M > 2 || (!three && !aq_plan(t.K, (int)M, 2, p)) || !aq_encode(maps, t)) return cudaErrorInvalidValue;
     AqArgs a;
     a.x = x;
     a.y = y;
@@ -418,8 +449,12 @@ cudaError_t launch_gemv_a16q8_tc(const Tensor &t, const void *x, q4_dtype xd, fl
     a.NS = p.NS;
     a.scale2 = t.scale2;
     if (M == 2)
-        return xd == Q4_DT_BF16 ? aq_run<__nv_bfloat16, 2>(maps, a, p.smem, s) : aq_run<float, 2>(maps, a, p.smem, s);
-    return xd == Q4_DT_BF16 ? aq_run<__nv_bfloat16, 1>(maps, a, p.smem, s) : aq_run<float, 1>(maps, a, p.smem, s);
+        return xd == Q4_DT_BF16 ? aq_run<__nv_bfloat16, 2, 2>(maps, a, p.smem, s)
+                                : aq_run<float, 2, 2>(maps, a, p.smem, s);
+    if (three)
+        return xd == Q4_DT_BF16 ? aq_run<__nv_bfloat16, 1, 3>(maps, a, p.smem, s)
+                                : aq_run<float, 1, 3>(maps, a, p.smem, s);
+    return xd == Q4_DT_BF16 ? aq_run<__nv_bfloat16, 1, 2>(maps, a, p.smem, s) : aq_run<float, 1, 2>(maps, a, p.smem, s);
 }
 
 int a16tc_read_and_clear_error() {

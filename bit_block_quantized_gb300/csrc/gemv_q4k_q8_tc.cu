@@ -185,48 +185,78 @@ gemv_q4k_q8_tc(const __grid_constant__ CUtensorMap wmap, const __grid_constant__
         // lane l holds k = 8l .. 8l+7: chunk l >> 3, the low (0) or high (1) nibble half, code words i0, i0 + 1
         const int tq = lane >> 3, half = (lane >> 2) & 1, i0 = 2 * (lane & 3);
         const float f = half ? 0.0625f : 1.0f;
-        for (int s = 0; s < nst; s++) {
-            const int u = warp + KT_WARPS * s;
-            if (u >= nsb) break;
+        // P of the warp's super-blocks at a time, their loads and shuffle chains overlapped: two,
+        // but one for f32 x at batch 1 (measured faster: two f32 blocks hold 16 values per lane)
+        constexpr int P = (sizeof(XT) == 4 && MB == 1) ? 1 : 2;
+        for (int s0 = 0; s0 < nst; s0 += P) {
+            float v[P][MB][8];
 #pragma unroll
-            for (int m = 0; m < MB; m++) {
-                float v[8];
-                kt_load8(xp + (int64_t)m * a.K + (int64_t)u * 256 + lane * 8, v);
-                float amax = 0.0f, val = 0.0f;
-                int idx = 0x7fffffff;
+            for (int p = 0; p < P; p++) {
+                const int u = warp + KT_WARPS * (s0 + p);
+                const bool have = s0 + p < nst && u < nsb;
 #pragma unroll
-                for (int i = 0; i < 8; i++) {
-                    const float av = fabsf(v[i]);
-                    if (av > amax) { amax = av; val = v[i]; idx = lane * 8 + i; }
+                for (int m = 0; m < MB; m++) {
+                    if (have) {
+                        kt_load8(xp + (int64_t)m * a.K + (int64_t)u * 256 + lane * 8, v[p][m]);
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 8; i++) v[p][m][i] = 0.0f;
+                    }
+                }
+            }
+            float amax[P][MB], val[P][MB];
+            int idx[P][MB];
+#pragma unroll
+            for (int p = 0; p < P; p++)
+#pragma unroll
+                for (int m = 0; m < MB; m++) {
+                    amax[p][m] = 0.0f, val[p][m] = 0.0f, idx[p][m] = 0x7fffffff;
+#pragma unroll
+                    for (int i = 0; i < 8; i++) {
+                        const float av = fabsf(v[p][m][i]);
+                        if (av > amax[p][m]) { amax[p][m] = av; val[p][m] = v[p][m][i]; idx[p][m] = lane * 8 + i; }
+                    }
                 }
 #pragma unroll
-                for (int off = 16; off > 0; off >>= 1) {   // largest magnitude, first index on ties
-                    const float oa = __shfl_xor_sync(0xffffffffu, amax, off);
-                    const float ov = __shfl_xor_sync(0xffffffffu, val, off);
-                    const int oi = __shfl_xor_sync(0xffffffffu, idx, off);
-                    if (oa > amax || (oa == amax && oi < idx)) { amax = oa; val = ov; idx = oi; }
-                }
-                const float iscale = __fdiv_rn(-127.0f, val);
-                const bool live = isfinite(iscale);         // zero (or vanishing) block: codes 0, scale 0
-                int c[8], ssum = 0;
+            for (int off = 16; off > 0; off >>= 1)      // largest magnitude, first index on ties
 #pragma unroll
-                for (int i = 0; i < 8; i++) {
-                    int ci = live ? __float2int_rn(__fmul_rn(v[i], iscale)) : 0;
-                    ci = (int)(int8_t)(uint8_t)((ci > 127 ? 127 : ci) & 0xff);   // the 8-bit code the contract keeps
-                    c[i] = ci;
-                    ssum += ci;
-                }
-                ssum += __shfl_xor_sync(0xffffffffu, ssum, 1);   // the sub-block's lanes 4j .. 4j+3
-                ssum += __shfl_xor_sync(0xffffffffu, ssum, 2);
+                for (int p = 0; p < P; p++)
 #pragma unroll
-                for (int q = 0; q < 2; q++) {
-                    // B pairs (k, k+2) and (k+1, k+3) of code word i0 + q as f16 (exact; /16 for high nibbles)
-                    const uint32_t h02 = h2bits(__float2half_rn((float)c[4 * q] * f), __float2half_rn((float)c[4 * q + 2] * f));
-                    const uint32_t h13 = h2bits(__float2half_rn((float)c[4 * q + 1] * f), __float2half_rn((float)c[4 * q + 3] * f));
-                    kt_sts64(xs_w + (uint32_t)(s * KT_XU + (tq * 8 + i0 + q) * 32 + m * 16 + half * 8), h02, h13);
+                    for (int m = 0; m < MB; m++) {
+                        const float oa = __shfl_xor_sync(0xffffffffu, amax[p][m], off);
+                        const float ov = __shfl_xor_sync(0xffffffffu, val[p][m], off);
+                        const int oi = __shfl_xor_sync(0xffffffffu, idx[p][m], off);
+                        if (oa > amax[p][m] || (oa == amax[p][m] && oi < idx[p][m])) {
+                            amax[p][m] = oa; val[p][m] = ov; idx[p][m] = oi;
+                        }
+                    }
+#pragma unroll
+            for (int p = 0; p < P; p++) {
+                const int s = s0 + p, u = warp + KT_WARPS * s;
+                if (s >= nst || u >= nsb) break;
+#pragma unroll
+                for (int m = 0; m < MB; m++) {
+                    const float iscale = __fdiv_rn(-127.0f, val[p][m]);
+                    const bool live = isfinite(iscale);     // zero (or vanishing) block: codes 0, scale 0
+                    int c[8], ssum = 0;
+#pragma unroll
+                    for (int i = 0; i < 8; i++) {
+                        int ci = live ? __float2int_rn(__fmul_rn(v[p][m][i], iscale)) : 0;
+                        ci = (int)(int8_t)(uint8_t)((ci > 127 ? 127 : ci) & 0xff);   // the 8-bit code the contract keeps
+                        c[i] = ci;
+                        ssum += ci;
+                    }
+                    ssum += __shfl_xor_sync(0xffffffffu, ssum, 1);   // the sub-block's lanes 4j .. 4j+3
+                    ssum += __shfl_xor_sync(0xffffffffu, ssum, 2);
+#pragma unroll
+                    for (int q = 0; q < 2; q++) {
+                        const uint32_t h02 = h2bits(__float2half_rn((float)c[4 * q] * f), __float2half_rn((float)c[4 * q + 2] * f));
+                        const uint32_t h13 = h2bits(__float2half_rn((float)c[4 * q + 1] * f), __float2half_rn((float)c[4 * q + 3] * f));
+                        kt_sts64(xs_w + (uint32_t)(s * KT_XU + (tq * 8 + i0 + q) * 32 + m * 16 + half * 8), h02, h13);
+                    }
+                    if ((lane & 3) == 0) bs_w[(s * MB + m) * 8 + (lane >> 2)] = ssum;
+                    if (lane == 0) as_w[s * MB + m] = live ? __fdiv_rn(1.0f, iscale) : 0.0f;
                 }
-                if ((lane & 3) == 0) bs_w[(s * MB + m) * 8 + (lane >> 2)] = ssum;
-                if (lane == 0) as_w[s * MB + m] = live ? __fdiv_rn(1.0f, iscale) : 0.0f;
             }
         }
     }

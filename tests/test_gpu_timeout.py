@@ -98,7 +98,10 @@ def test_chain_grid_barrier_times_out_then_recovers_after_rezeroing():
     ys = [torch.zeros((1, L["N"]), device="cuda") for L in layers]
     groups = [[("nvfp4", d["w"], d["scales"], aux_for(L, d, x_dtype=torch.bfloat16), x, y, L["N"], 4096)]
               for L, d, y in zip(layers, ds, ys)]
-    sync = torch.zeros(2, dtype=torch.int32, device="cuda")
+    # A barrier no arrival can complete: the count starts far above the grid size, so no CTA
+    # is the last to arrive and every CTA's bounded spin runs out (with a one-clock limit it
+    # would otherwise race the arrivals: CTAs with equal work can all arrive before any checks).
+    sync = torch.tensor([1 << 30, 0], dtype=torch.int32, device="cuda")
     assert q4.q4_set_wait_limit(1) == q4.Q4_OK
     q4.q4_gemv_chain(groups, 1, sync=sync)
     assert q4.q4_last_gemv_path() == "gemv_tma_chain"
