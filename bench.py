@@ -769,13 +769,14 @@ def _time_launches(torch, stream, launch, reps=200, warm=10):
     return a.elapsed_time(b) * 1e3 / reps
 
 
-def _time_graph(torch, stream, launch, reps=200, warm=10):
-    """Average device time per launch with the `reps` launches captured into
-    one CUDA graph and replayed between the two events (on `stream`), so no
-    host launch gap enters the time: how the headline step is timed.  For the
-    GEMV rows, whose calls allocate nothing and never synchronize.  If the
-    capture fails the launches are issued one by one instead.  Returns
-    (us per launch, "graph" or "eager")."""
+def _time_graph(torch, stream, launch, reps=200, warm=10, cells=5):
+    """Device time per launch with the `reps` launches captured into one CUDA
+    graph, replayed `cells` times, each replay between its own two events (on
+    `stream`), so no host launch gap enters the time: how the headline step is
+    timed.  For the GEMV rows, whose calls allocate nothing and never
+    synchronize.  If the capture fails the launches are issued one by one
+    instead.  Returns (median us per launch over the cells, "graph" or
+    "eager", coefficient of variation over the cells or None)."""
     with torch.cuda.stream(stream):
         for i in range(warm):
             launch(i)
@@ -787,15 +788,21 @@ def _time_graph(torch, stream, launch, reps=200, warm=10):
                     launch(i)
         except Exception:
             torch.cuda.synchronize()
-            return _time_launches(torch, stream, launch, reps, warm), "eager"
+            return _time_launches(torch, stream, launch, reps, warm), "eager", None
         g.replay()
         torch.cuda.synchronize()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        g.replay()
-        b.record(stream)
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(cells)]
+        for a, b in ev:
+            a.record(stream)
+            g.replay()
+            b.record(stream)
         torch.cuda.synchronize()
-    return a.elapsed_time(b) * 1e3 / reps, "graph"
+    us = [a.elapsed_time(b) * 1e3 / reps for a, b in ev]
+    return statistics.median(us), "graph", statistics.pstdev(us) / statistics.mean(us)
+
+
+def _cv(v):
+    return None if v is None else round(v, 4)
 
 
 def other_rows(torch, q4, synth, peak_hbm):
@@ -829,11 +836,11 @@ def other_rows(torch, q4, synth, peak_hbm):
         def launch(i):
             c = cps[i % len(cps)]
             q4.q4_gemv(fmt, c["w"], c["scales"], auxes[i % len(cps)], x, y, M, N, K, stream=stream)
-        us, how = _time_graph(torch, stream, launch)
+        us, how, cv = _time_graph(torch, stream, launch)
         moved = packed + x.numel() * x.element_size() + y.numel() * 4
         rows.append({"row": tag, "shape": f"{N}x{K}", "M": M, "us_per_launch": round(us, 2),
                      "GBps": round(moved / us / 1e3, 1), "frac_hbm": round(moved / us / 1e3 / peak_hbm, 4),
-                     "path": q4.q4_last_gemv_path(), "timing": how})
+                     "path": q4.q4_last_gemv_path(), "timing": how, "cv": _cv(cv)})
 
     gemv_row("a1 NVFP4 GEMV", "nvfp4", 14336, 4096, 4, 5, dict(row_scale=True), q4.Q4_DT_BF16)
     gemv_row("a1 NVFP4 GEMV", "nvfp4", 14336, 4096, 8, 5, dict(row_scale=True), q4.Q4_DT_BF16)
@@ -853,13 +860,13 @@ def other_rows(torch, q4, synth, peak_hbm):
     x = torch.from_numpy(np.ascontiguousarray(xb).view(np.int16)).cuda().view(torch.bfloat16)
     y = torch.empty((M, N), dtype=torch.float32, device="cuda")
     aux = q4.make_aux(scale2=layer["scale2"], x_dtype=q4.Q4_DT_BF16, fmt="nvfp4")
-    us, how = _time_graph(torch, stream, lambda i: q4.q4_gemv_a16q8(cps[i % len(cps)]["w"],
+    us, how, cv = _time_graph(torch, stream, lambda i: q4.q4_gemv_a16q8(cps[i % len(cps)]["w"],
                                                                     cps[i % len(cps)]["scales"], aux, x, y, M, N, K,
                                                                     stream=stream))
     moved = packed + x.numel() * 2 + y.numel() * 4
     rows.append({"row": A16Q8_ROW, "shape": f"{N}x{K}", "M": M, "us_per_launch": round(us, 2),
                  "GBps": round(moved / us / 1e3, 1), "frac_hbm": round(moved / us / 1e3 / peak_hbm, 4),
-                 "path": q4.q4_last_gemv_path(), "timing": how})
+                 "path": q4.q4_last_gemv_path(), "timing": how, "cv": _cv(cv)})
     del cps
     torch.cuda.empty_cache()
 
@@ -877,10 +884,10 @@ def other_rows(torch, q4, synth, peak_hbm):
     moved = packed + x.numel() * 2 + y.numel() * 4
 
     def lane_row(tag, fn, nbytes=moved, path=True):
-        us, how = _time_graph(torch, stream, fn)
+        us, how, cv = _time_graph(torch, stream, fn)
         row = {"row": tag, "shape": f"{N}x{K}", "M": M, "us_per_launch": round(us, 2),
                "GBps": round(nbytes / us / 1e3, 1), "frac_hbm": round(nbytes / us / 1e3 / peak_hbm, 4),
-               "timing": how}
+               "timing": how, "cv": _cv(cv)}
         if path:
             row["path"] = q4.q4_last_gemv_path()
         rows.append(row)
@@ -904,13 +911,13 @@ def other_rows(torch, q4, synth, peak_hbm):
     _, qxf = synth.draw_x(1, 4096, config=1, matrix=5, dtype="f32")
     qx = torch.from_numpy(np.ascontiguousarray(qxf, np.float32)).cuda()
     qy = torch.empty((1, 4096), dtype=torch.float32, device="cuda")
-    us, how = _time_graph(torch, stream, lambda i: q4.q4_gemv_q4k_q8(qcps[i % len(qcps)]["w"], None, qx, qy, 1,
+    us, how, cv = _time_graph(torch, stream, lambda i: q4.q4_gemv_q4k_q8(qcps[i % len(qcps)]["w"], None, qx, qy, 1,
                                                                       4096, 4096, stream=stream))
     qmoved = qpacked + qx.numel() * 4 + qy.numel() * 4
     rows.append({"row": "f2 Q4_K x Q8 (W4A8) GEMV, integer sub-block sums", "shape": "4096x4096", "M": 1,
                  "us_per_launch": round(us, 2), "GBps": round(qmoved / us / 1e3, 1),
                  "frac_hbm": round(qmoved / us / 1e3 / peak_hbm, 4), "path": q4.q4_last_gemv_path(),
-                 "timing": how})
+                 "timing": how, "cv": _cv(cv)})
     del qcps
     torch.cuda.empty_cache()
     # f3: the GPU quantizers on the 14336x4096 layer (f32 W in, packed out)
@@ -995,8 +1002,9 @@ def other_rows(torch, q4, synth, peak_hbm):
     torch.cuda.empty_cache()
     return {"l2": "each launch reads a different weight copy; working set >= 256 MB per row",
             "timing": "CUDA events around 200 launches: for the GEMV rows one CUDA graph of the 200 launches "
-                      "(no host launch gaps, as the headline step; a row's 'timing' says 'eager' if its calls "
-                      "could not be captured), for the others launch by launch",
+                      "replayed 5 times, each between its own events, the median reported with the coefficient "
+                      "of variation 'cv' (no host launch gaps, as the headline step; a row's 'timing' says 'eager' "
+                      "if its calls could not be captured), for the others launch by launch",
             "peak_hbm_GBps": peak_hbm, "entries": rows}
 
 
@@ -1094,17 +1102,22 @@ def layer_set_sweep(torch, q4, peak_hbm, batches=SWEEP_BATCHES, formats=SWEEP_FO
                 for _ in range(3):
                     g.replay()
                 torch.cuda.synchronize()
-                reps = 10
-                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                a.record(stream)
-                for _ in range(reps):
-                    g.replay()
-                b.record(stream)
+                # five cells of two back-to-back replays each, every cell between its own events
+                reps, cells = 2, 5
+                ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                      for _ in range(cells)]
+                for a, b in ev:
+                    a.record(stream)
+                    for _ in range(reps):
+                        g.replay()
+                    b.record(stream)
                 torch.cuda.synchronize()
-            us = a.elapsed_time(b) * 1e3 / (reps * ncopies)
+            cell_us = [a.elapsed_time(b) * 1e3 / (reps * ncopies) for a, b in ev]
+            us = statistics.median(cell_us)
             gbs = layer_bytes / us / 1e3
             out.append({"fmt": fmt, "M": M, "us_per_layer": round(us, 2), "GBps": round(gbs, 1),
                         "frac_hbm": round(gbs / peak_hbm, 4),
+                        "cv": round(statistics.pstdev(cell_us) / statistics.mean(cell_us), 4),
                         "tokens_equivalent_per_s": round(1e6 / (LAYERS * us), 1),
                         "paths": sorted(set(paths))})
             del xs, ys
@@ -1118,6 +1131,8 @@ def layer_set_sweep(torch, q4, peak_hbm, batches=SWEEP_BATCHES, formats=SWEEP_FO
             "l2": "each layer pass reads a different weight copy (copies > 4 x L2)",
             "launch": "per layer: q4_gemv_grouped(q, k, v), q4_gemv(o), q4_gemv_grouped(gate, up), q4_gemv(down); "
                       "one CUDA graph over the copies",
+            "timing": "per cell the median over 5 timed repetitions (each two replays of the graph between its own "
+                      "CUDA events), with the coefficient of variation over the 5",
             "peak_hbm_GBps": peak_hbm, "entries": out}
 
 
