@@ -29,6 +29,8 @@
 // q9 adds in 64 bits, the four lanes of a row add their block sums, and the
 // block's pinned f32 steps go to a per-row list that one thread per row sums
 // in block order at the end of the tile.  One or two batch rows per launch.
+// Two CTAs share an SM, or three at batch 1 where three ring stages still fit
+// in 74 KB (K <= 4352): more decode warps per scheduler, measured faster.
 #include <cuda.h>
 
 #include "q4_internal.cuh"
